@@ -1,0 +1,18 @@
+"""GB300-native (sm_103a) exact scaled-dot-product attention forward.
+
+The compute path is the C-ABI library ``libattn.so`` built from ``csrc/``
+(declared in ``include/attn.h``); :mod:`.binding` marshals torch tensors into
+it.  Importing this package loads nothing: the library is opened on first use
+and a missing library raises instead of falling back to anything else.
+"""
+
+from .binding import (  # noqa: F401
+    AttnError,
+    attn_fwd,
+    attn_fwd_host,
+    attn_get_device_status,
+    attn_last_error,
+    fwd,
+    library_path,
+    load_library,
+)

@@ -1,0 +1,143 @@
+"""ctypes binding of libattn.so (declared in include/attn.h).
+
+Argument marshalling only: torch tensors supply device pointers and the
+current CUDA stream; every step of the attention forward runs in the library's
+kernels.  There is no fallback: if the library cannot be loaded, or a call
+returns an error status, :class:`AttnError` is raised.
+"""
+
+from __future__ import annotations
+
+import ctypes
+import math
+import os
+import threading
+
+import torch
+
+_PKG = os.path.dirname(os.path.abspath(__file__))
+
+ATTN_OK = 0
+ATTN_ERR_INVALID_ARG = 1
+ATTN_ERR_UNSUPPORTED = 2
+ATTN_ERR_CUDA = 3
+ATTN_ERR_TIMEOUT = 4
+ATTN_DTYPE_F16 = 0
+ATTN_DTYPE_BF16 = 1
+
+EXPORTED = ("attn_fwd", "attn_fwd_host", "attn_last_error", "attn_get_device_status",
+            "attn_version")
+
+_DTYPE_CODE = {torch.float16: ATTN_DTYPE_F16, torch.bfloat16: ATTN_DTYPE_BF16}
+
+
+class AttnError(RuntimeError):
+    def __init__(self, status: int, message: str):
+        super().__init__(f"attn status {status}: {message}")
+        self.status = status
+        self.message = message
+
+
+_lib = None
+_lock = threading.Lock()
+
+
+def library_path() -> str:
+    return os.environ.get("ATTN_LIBRARY", os.path.join(_PKG, "libattn.so"))
+
+
+def load_library() -> ctypes.CDLL:
+    """Open libattn.so (once) and declare its signatures."""
+    global _lib
+    with _lock:
+        if _lib is not None:
+            return _lib
+        path = library_path()
+        if not os.path.exists(path):
+            raise AttnError(ATTN_ERR_UNSUPPORTED,
+                            f"{path} is missing; build it with exact_attention_53_gb300.build.build()")
+        lib = ctypes.CDLL(path)
+        i64, vp, i32 = ctypes.c_int64, ctypes.c_void_p, ctypes.c_int
+        lib.attn_fwd.argtypes = [vp, vp, vp, vp, vp, i64, i64, i64, i64, i64, i32,
+                                 ctypes.c_float, i32, vp]
+        lib.attn_fwd.restype = i32
+        lib.attn_fwd_host.argtypes = [vp] * 10 + [i64, i64, i64, i64, i64, i32, ctypes.c_float,
+                                                  i32, vp]
+        lib.attn_fwd_host.restype = i32
+        lib.attn_last_error.argtypes = []
+        lib.attn_last_error.restype = ctypes.c_char_p
+        lib.attn_get_device_status.argtypes = [vp]
+        lib.attn_get_device_status.restype = i32
+        lib.attn_version.argtypes = []
+        lib.attn_version.restype = i32
+        _lib = lib
+        return lib
+
+
+def attn_last_error() -> str:
+    return load_library().attn_last_error().decode()
+
+
+def _check(status: int) -> None:
+    if status != ATTN_OK:
+        raise AttnError(status, attn_last_error())
+
+
+def _stream_handle(stream) -> int | None:
+    if stream is None:
+        return torch.cuda.current_stream().cuda_stream
+    if isinstance(stream, torch.cuda.Stream):
+        return stream.cuda_stream
+    return int(stream)
+
+
+def attn_fwd(q, k, v, o, lse, B, H, S_q, S_k, d, causal, scale, dtype, stream=None) -> None:
+    """Enqueue the forward; q, k, v, o, lse are tensors or raw device pointers."""
+    lib = load_library()
+    ptr = lambda t: t.data_ptr() if isinstance(t, torch.Tensor) else t  # noqa: E731
+    _check(lib.attn_fwd(ptr(q), ptr(k), ptr(v), ptr(o), ptr(lse), B, H, S_q, S_k, d,
+                        int(causal), float(scale), int(dtype), _stream_handle(stream)))
+
+
+def attn_fwd_host(q_host, k_host, v_host, o_host, lse_host, q_dev, k_dev, v_dev, o_dev, lse_dev,
+                  B, H, S_q, S_k, d, causal, scale, dtype, stream=None) -> None:
+    """Enqueue host→device copies, the forward, and device→host copies of O and LSE."""
+    lib = load_library()
+    ptr = lambda t: t.data_ptr() if isinstance(t, torch.Tensor) else t  # noqa: E731
+    _check(lib.attn_fwd_host(ptr(q_host), ptr(k_host), ptr(v_host), ptr(o_host), ptr(lse_host),
+                             ptr(q_dev), ptr(k_dev), ptr(v_dev), ptr(o_dev), ptr(lse_dev),
+                             B, H, S_q, S_k, d, int(causal), float(scale), int(dtype),
+                             _stream_handle(stream)))
+
+
+def attn_get_device_status(stream=None) -> None:
+    """Synchronise and raise AttnError(ATTN_ERR_TIMEOUT) if a kernel's wait ran out."""
+    _check(load_library().attn_get_device_status(_stream_handle(stream)))
+
+
+def fwd(q: torch.Tensor, k: torch.Tensor, v: torch.Tensor, causal: bool = False,
+        scale: float | None = None, out: torch.Tensor | None = None,
+        lse: torch.Tensor | None = None):
+    """O, LSE for contiguous CUDA tensors q [B,H,S_q,d], k, v [B,H,S_k,d].
+
+    ``scale`` defaults to 1/sqrt(d).  Outputs are allocated with torch unless
+    given.  Returns ``(o, lse)``; work is enqueued on the current stream.
+    """
+    if q.dim() != 4 or k.dim() != 4 or v.dim() != 4:
+        raise AttnError(ATTN_ERR_INVALID_ARG, "q, k, v must be 4-D [B,H,S,d]")
+    if not (q.is_contiguous() and k.is_contiguous() and v.is_contiguous()):
+        raise AttnError(ATTN_ERR_INVALID_ARG, "q, k, v must be contiguous")
+    if q.dtype != k.dtype or q.dtype != v.dtype or q.dtype not in _DTYPE_CODE:
+        raise AttnError(ATTN_ERR_UNSUPPORTED, "q, k, v must share dtype float16 or bfloat16")
+    B, H, S_q, d = q.shape
+    if k.shape[:2] != (B, H) or k.shape[3] != d or v.shape != k.shape:
+        raise AttnError(ATTN_ERR_INVALID_ARG, f"shape mismatch q{tuple(q.shape)} k{tuple(k.shape)} v{tuple(v.shape)}")
+    S_k = k.shape[2]
+    if scale is None:
+        scale = 1.0 / math.sqrt(d)
+    if out is None:
+        out = torch.empty_like(q)
+    if lse is None:
+        lse = torch.empty((B, H, S_q), dtype=torch.float32, device=q.device)
+    attn_fwd(q, k, v, out, lse, B, H, S_q, S_k, d, causal, scale, _DTYPE_CODE[q.dtype])
+    return out, lse

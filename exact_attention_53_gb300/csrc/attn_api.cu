@@ -1,0 +1,290 @@
+// C ABI of libattn.so: argument validation, TMA descriptor encoding, kernel
+// selection and launch.  Declared in include/attn.h.
+//
+// Validation mirrors the page's validate_config (oxicuda-dnn 0.1.8 hopper.rs):
+// head_dim must be one of SUPPORTED_HEAD_DIMS, the element type f16 or bf16,
+// and every failure names the offending field.  Problem sizes, pointers and the
+// scale are checked here as well, because the library takes raw pointers.
+#include <cudaTypedefs.h>
+
+#include <atomic>
+#include <cmath>
+#include <cstdarg>
+#include <cstdio>
+#include <cstring>
+#include <mutex>
+
+#include "attn.h"
+#include "attn_launch.h"
+
+namespace {
+
+constexpr int kVersion = 10000;  // 1.0.0
+constexpr int kMaxDevices = 64;
+constexpr int64_t kMaxSeq = int64_t(1) << 22;
+
+thread_local char g_msg[512] = "";
+
+attn_status_t fail(attn_status_t s, const char* fmt, ...) {
+    va_list ap;
+    va_start(ap, fmt);
+    vsnprintf(g_msg, sizeof(g_msg), fmt, ap);
+    va_end(ap);
+    return s;
+}
+
+attn_status_t ok() {
+    g_msg[0] = '\0';
+    return ATTN_OK;
+}
+
+// Set (bit per role) by a kernel whose bounded wait ran out.
+__device__ unsigned int g_attn_status;
+
+std::atomic<int> g_device_checked[kMaxDevices];          // 0 unknown, 1 ok, 2 unsupported
+std::atomic<unsigned int*> g_status_ptr[kMaxDevices];
+
+PFN_cuTensorMapEncodeTiled_v12000 encode_fn() {
+    static PFN_cuTensorMapEncodeTiled_v12000 fn = nullptr;
+    static std::once_flag once;
+    std::call_once(once, [] {
+        void* p = nullptr;
+        cudaDriverEntryPointQueryResult q{};
+        if (cudaGetDriverEntryPointByVersion("cuTensorMapEncodeTiled", &p, 12000,
+                                             cudaEnableDefault, &q) == cudaSuccess &&
+            q == cudaDriverEntryPointSuccess)
+            fn = reinterpret_cast<PFN_cuTensorMapEncodeTiled_v12000>(p);
+    });
+    return fn;
+}
+
+bool overlaps(const void* a, size_t na, const void* b, size_t nb) {
+    const uintptr_t x = reinterpret_cast<uintptr_t>(a), y = reinterpret_cast<uintptr_t>(b);
+    return x < y + nb && y < x + na;
+}
+
+bool aligned(const void* p, size_t n) { return (reinterpret_cast<uintptr_t>(p) % n) == 0; }
+
+struct Problem {
+    int64_t B, H, S_q, S_k, d;
+    bool causal;
+    float scale;
+    attn_dtype_t dtype;
+    size_t q_bytes, kv_bytes, o_bytes, lse_bytes;
+};
+
+attn_status_t validate_sizes(Problem& p, int64_t B, int64_t H, int64_t S_q, int64_t S_k,
+                             int64_t d, int causal, float scale, attn_dtype_t dtype) {
+    if (B < 1) return fail(ATTN_ERR_INVALID_ARG, "B must be >= 1, got %lld", (long long)B);
+    if (H < 1) return fail(ATTN_ERR_INVALID_ARG, "H must be >= 1, got %lld", (long long)H);
+    if (S_q < 1) return fail(ATTN_ERR_INVALID_ARG, "S_q must be >= 1, got %lld", (long long)S_q);
+    if (S_k < 1) return fail(ATTN_ERR_INVALID_ARG, "S_k must be >= 1, got %lld", (long long)S_k);
+    if (d < 1) return fail(ATTN_ERR_INVALID_ARG, "d must be >= 1, got %lld", (long long)d);
+    if (d != 64 && d != 128 && d != 256)
+        return fail(ATTN_ERR_UNSUPPORTED, "head_dim d=%lld not supported; must be one of [64, 128, 256]",
+                    (long long)d);
+    if (dtype != ATTN_DTYPE_F16 && dtype != ATTN_DTYPE_BF16)
+        return fail(ATTN_ERR_UNSUPPORTED, "dtype must be ATTN_DTYPE_F16 (0) or ATTN_DTYPE_BF16 (1), got %d",
+                    (int)dtype);
+    if (causal != 0 && causal != 1)
+        return fail(ATTN_ERR_INVALID_ARG, "causal must be 0 or 1, got %d", causal);
+    if (!std::isfinite(scale))
+        return fail(ATTN_ERR_INVALID_ARG, "scale must be finite");
+    if (scale < 0.f)
+        return fail(ATTN_ERR_UNSUPPORTED, "scale must be >= 0, got %g", (double)scale);
+    if (B * H > INT32_MAX || B > INT32_MAX || H > INT32_MAX)
+        return fail(ATTN_ERR_INVALID_ARG, "B*H = %lld exceeds 2^31-1", (long long)(B * H));
+    if (S_q > kMaxSeq) return fail(ATTN_ERR_INVALID_ARG, "S_q=%lld exceeds 2^22", (long long)S_q);
+    if (S_k > kMaxSeq) return fail(ATTN_ERR_INVALID_ARG, "S_k=%lld exceeds 2^22", (long long)S_k);
+    p.B = B; p.H = H; p.S_q = S_q; p.S_k = S_k; p.d = d;
+    p.causal = causal != 0;
+    p.scale = scale;
+    p.dtype = dtype;
+    const size_t bh = static_cast<size_t>(B * H);
+    p.q_bytes = bh * static_cast<size_t>(S_q) * static_cast<size_t>(d) * 2;
+    p.kv_bytes = bh * static_cast<size_t>(S_k) * static_cast<size_t>(d) * 2;
+    p.o_bytes = p.q_bytes;
+    p.lse_bytes = bh * static_cast<size_t>(S_q) * 4;
+    return ATTN_OK;
+}
+
+attn_status_t validate_device_ptrs(const Problem& p, const void* q, const void* k, const void* v,
+                                   const void* o, const void* lse) {
+    if (!q) return fail(ATTN_ERR_INVALID_ARG, "q is null");
+    if (!k) return fail(ATTN_ERR_INVALID_ARG, "k is null");
+    if (!v) return fail(ATTN_ERR_INVALID_ARG, "v is null");
+    if (!o) return fail(ATTN_ERR_INVALID_ARG, "o is null");
+    if (!lse) return fail(ATTN_ERR_INVALID_ARG, "lse is null");
+    if (!aligned(q, 16)) return fail(ATTN_ERR_INVALID_ARG, "q is not 16-byte aligned");
+    if (!aligned(k, 16)) return fail(ATTN_ERR_INVALID_ARG, "k is not 16-byte aligned");
+    if (!aligned(v, 16)) return fail(ATTN_ERR_INVALID_ARG, "v is not 16-byte aligned");
+    if (!aligned(o, 16)) return fail(ATTN_ERR_INVALID_ARG, "o is not 16-byte aligned");
+    if (!aligned(lse, 4)) return fail(ATTN_ERR_INVALID_ARG, "lse is not 4-byte aligned");
+    if (overlaps(o, p.o_bytes, q, p.q_bytes)) return fail(ATTN_ERR_INVALID_ARG, "o overlaps q");
+    if (overlaps(o, p.o_bytes, k, p.kv_bytes)) return fail(ATTN_ERR_INVALID_ARG, "o overlaps k");
+    if (overlaps(o, p.o_bytes, v, p.kv_bytes)) return fail(ATTN_ERR_INVALID_ARG, "o overlaps v");
+    if (overlaps(lse, p.lse_bytes, q, p.q_bytes)) return fail(ATTN_ERR_INVALID_ARG, "lse overlaps q");
+    if (overlaps(lse, p.lse_bytes, k, p.kv_bytes)) return fail(ATTN_ERR_INVALID_ARG, "lse overlaps k");
+    if (overlaps(lse, p.lse_bytes, v, p.kv_bytes)) return fail(ATTN_ERR_INVALID_ARG, "lse overlaps v");
+    if (overlaps(lse, p.lse_bytes, o, p.o_bytes)) return fail(ATTN_ERR_INVALID_ARG, "lse overlaps o");
+    return ATTN_OK;
+}
+
+// The kernels are built for sm_103a only; check the current device once.
+attn_status_t check_device(int* dev_out) {
+    int dev = 0;
+    cudaError_t e = cudaGetDevice(&dev);
+    if (e != cudaSuccess) return fail(ATTN_ERR_CUDA, "cudaGetDevice: %s", cudaGetErrorString(e));
+    if (dev < 0 || dev >= kMaxDevices) return fail(ATTN_ERR_UNSUPPORTED, "device ordinal %d", dev);
+    int state = g_device_checked[dev].load(std::memory_order_acquire);
+    if (state == 0) {
+        int major = 0, minor = 0;
+        e = cudaDeviceGetAttribute(&major, cudaDevAttrComputeCapabilityMajor, dev);
+        if (e == cudaSuccess) e = cudaDeviceGetAttribute(&minor, cudaDevAttrComputeCapabilityMinor, dev);
+        if (e != cudaSuccess) return fail(ATTN_ERR_CUDA, "cudaDeviceGetAttribute: %s", cudaGetErrorString(e));
+        state = (major == 10 && minor == 3) ? 1 : 2;
+        g_device_checked[dev].store(state, std::memory_order_release);
+        if (state == 1) {
+            void* sp = nullptr;
+            e = cudaGetSymbolAddress(&sp, g_attn_status);
+            if (e != cudaSuccess) {
+                g_device_checked[dev].store(0);
+                return fail(ATTN_ERR_CUDA, "cudaGetSymbolAddress(status): %s", cudaGetErrorString(e));
+            }
+            g_status_ptr[dev].store(static_cast<unsigned int*>(sp));
+        }
+    }
+    if (state != 1)
+        return fail(ATTN_ERR_UNSUPPORTED, "device %d is not an sm_103 GPU; this library is built for sm_103a only", dev);
+    *dev_out = dev;
+    return ATTN_OK;
+}
+
+attn_status_t encode_rows(CUtensorMap* map, const void* base, const Problem& p, int64_t S,
+                          const char* name) {
+    auto fn = encode_fn();
+    if (!fn) return fail(ATTN_ERR_CUDA, "cuTensorMapEncodeTiled is unavailable from the driver");
+    // Dimensions innermost first: (d, S, B·H); box 64 elements (128 bytes) × 128 rows.
+    cuuint64_t dims[3] = {static_cast<cuuint64_t>(p.d), static_cast<cuuint64_t>(S),
+                          static_cast<cuuint64_t>(p.B * p.H)};
+    cuuint64_t strides[2] = {static_cast<cuuint64_t>(p.d * 2), static_cast<cuuint64_t>(S * p.d * 2)};
+    cuuint32_t box[3] = {64, static_cast<cuuint32_t>(attn::kBlockM), 1};
+    cuuint32_t estr[3] = {1, 1, 1};
+    CUresult r = fn(map,
+                    p.dtype == ATTN_DTYPE_BF16 ? CU_TENSOR_MAP_DATA_TYPE_BFLOAT16
+                                               : CU_TENSOR_MAP_DATA_TYPE_FLOAT16,
+                    3, const_cast<void*>(base), dims, strides, box, estr,
+                    CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B,
+                    CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
+    if (r != CUDA_SUCCESS) return fail(ATTN_ERR_CUDA, "cuTensorMapEncodeTiled(%s) failed with %d", name, (int)r);
+    return ATTN_OK;
+}
+
+using LaunchFn = cudaError_t (*)(const attn::FwdArgs&, cudaStream_t);
+
+LaunchFn pick(int64_t d, bool bf16, bool causal) {
+#define ATTN_PICK(D)                                                                   \
+    if (d == D) {                                                                      \
+        if (bf16) return causal ? attn::launch_attn_fwd<D, true, true>                 \
+                                : attn::launch_attn_fwd<D, true, false>;               \
+        return causal ? attn::launch_attn_fwd<D, false, true>                          \
+                      : attn::launch_attn_fwd<D, false, false>;                        \
+    }
+    ATTN_PICK(64)
+    ATTN_PICK(128)
+    ATTN_PICK(256)
+#undef ATTN_PICK
+    return nullptr;
+}
+
+attn_status_t launch_checked(const Problem& p, const void* q, const void* k, const void* v,
+                             void* o, float* lse, cudaStream_t stream) {
+    int dev = 0;
+    attn_status_t s = check_device(&dev);
+    if (s != ATTN_OK) return s;
+    attn::FwdArgs a;
+    if ((s = encode_rows(&a.tm_q, q, p, p.S_q, "q")) != ATTN_OK) return s;
+    if ((s = encode_rows(&a.tm_k, k, p, p.S_k, "k")) != ATTN_OK) return s;
+    if ((s = encode_rows(&a.tm_v, v, p, p.S_k, "v")) != ATTN_OK) return s;
+    a.o = o;
+    a.lse = lse;
+    a.S_q = static_cast<int32_t>(p.S_q);
+    a.S_k = static_cast<int32_t>(p.S_k);
+    a.BH = static_cast<int32_t>(p.B * p.H);
+    a.scale_log2 = static_cast<float>(static_cast<double>(p.scale) * 1.4426950408889634);
+    a.status = g_status_ptr[dev].load();
+    LaunchFn fn = pick(p.d, p.dtype == ATTN_DTYPE_BF16, p.causal);
+    if (!fn) return fail(ATTN_ERR_UNSUPPORTED, "no kernel for d=%lld", (long long)p.d);
+    cudaError_t e = fn(a, stream);
+    if (e != cudaSuccess) return fail(ATTN_ERR_CUDA, "kernel launch: %s", cudaGetErrorString(e));
+    return ok();
+}
+
+}  // namespace
+
+extern "C" {
+
+attn_status_t attn_fwd(const void* q, const void* k, const void* v, void* o, float* lse,
+                       int64_t B, int64_t H, int64_t S_q, int64_t S_k, int64_t d, int causal,
+                       float scale, attn_dtype_t dtype, struct CUstream_st* stream) {
+    Problem p;
+    attn_status_t s = validate_sizes(p, B, H, S_q, S_k, d, causal, scale, dtype);
+    if (s != ATTN_OK) return s;
+    if ((s = validate_device_ptrs(p, q, k, v, o, lse)) != ATTN_OK) return s;
+    return launch_checked(p, q, k, v, o, lse, stream);
+}
+
+attn_status_t attn_fwd_host(const void* q_host, const void* k_host, const void* v_host,
+                            void* o_host, float* lse_host, void* q_dev, void* k_dev, void* v_dev,
+                            void* o_dev, float* lse_dev, int64_t B, int64_t H, int64_t S_q,
+                            int64_t S_k, int64_t d, int causal, float scale, attn_dtype_t dtype,
+                            struct CUstream_st* stream) {
+    Problem p;
+    attn_status_t s = validate_sizes(p, B, H, S_q, S_k, d, causal, scale, dtype);
+    if (s != ATTN_OK) return s;
+    if (!q_host) return fail(ATTN_ERR_INVALID_ARG, "q_host is null");
+    if (!k_host) return fail(ATTN_ERR_INVALID_ARG, "k_host is null");
+    if (!v_host) return fail(ATTN_ERR_INVALID_ARG, "v_host is null");
+    if (!o_host) return fail(ATTN_ERR_INVALID_ARG, "o_host is null");
+    if (!lse_host) return fail(ATTN_ERR_INVALID_ARG, "lse_host is null");
+    if ((s = validate_device_ptrs(p, q_dev, k_dev, v_dev, o_dev, lse_dev)) != ATTN_OK) return s;
+    if (overlaps(q_dev, p.q_bytes, k_dev, p.kv_bytes) || overlaps(q_dev, p.q_bytes, v_dev, p.kv_bytes) ||
+        overlaps(k_dev, p.kv_bytes, v_dev, p.kv_bytes))
+        return fail(ATTN_ERR_INVALID_ARG, "q_dev, k_dev and v_dev must not overlap (they are copy targets)");
+    int dev = 0;
+    if ((s = check_device(&dev)) != ATTN_OK) return s;
+    cudaError_t e;
+    if ((e = cudaMemcpyAsync(q_dev, q_host, p.q_bytes, cudaMemcpyHostToDevice, stream)) != cudaSuccess ||
+        (e = cudaMemcpyAsync(k_dev, k_host, p.kv_bytes, cudaMemcpyHostToDevice, stream)) != cudaSuccess ||
+        (e = cudaMemcpyAsync(v_dev, v_host, p.kv_bytes, cudaMemcpyHostToDevice, stream)) != cudaSuccess)
+        return fail(ATTN_ERR_CUDA, "host-to-device copy: %s", cudaGetErrorString(e));
+    if ((s = launch_checked(p, q_dev, k_dev, v_dev, o_dev, lse_dev, stream)) != ATTN_OK) return s;
+    if ((e = cudaMemcpyAsync(o_host, o_dev, p.o_bytes, cudaMemcpyDeviceToHost, stream)) != cudaSuccess ||
+        (e = cudaMemcpyAsync(lse_host, lse_dev, p.lse_bytes, cudaMemcpyDeviceToHost, stream)) != cudaSuccess)
+        return fail(ATTN_ERR_CUDA, "device-to-host copy: %s", cudaGetErrorString(e));
+    return ok();
+}
+
+const char* attn_last_error(void) { return g_msg; }
+
+attn_status_t attn_get_device_status(struct CUstream_st* stream) {
+    cudaError_t e = cudaStreamSynchronize(stream);
+    if (e != cudaSuccess) return fail(ATTN_ERR_CUDA, "cudaStreamSynchronize: %s", cudaGetErrorString(e));
+    int dev = 0;
+    attn_status_t s = check_device(&dev);
+    if (s != ATTN_OK) return s;
+    unsigned int v = 0;
+    e = cudaMemcpyFromSymbol(&v, g_attn_status, sizeof(v));
+    if (e != cudaSuccess) return fail(ATTN_ERR_CUDA, "reading status: %s", cudaGetErrorString(e));
+    if (v == 0) return ok();
+    const unsigned int zero = 0;
+    e = cudaMemcpyToSymbol(g_attn_status, &zero, sizeof(zero));
+    if (e != cudaSuccess) return fail(ATTN_ERR_CUDA, "clearing status: %s", cudaGetErrorString(e));
+    return fail(ATTN_ERR_TIMEOUT, "a bounded wait ran out in:%s%s%s%s%s", (v & 1u) ? " producer" : "",
+                (v & 2u) ? " mma" : "", (v & 4u) ? " softmax" : "", (v & 8u) ? " epilogue" : "",
+                (v & 16u) ? " drain" : "");
+}
+
+int attn_version(void) { return kVersion; }
+
+}  // extern "C"

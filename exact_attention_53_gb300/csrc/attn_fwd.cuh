@@ -1,0 +1,486 @@
+// Exact scaled-dot-product attention forward for sm_103a.
+//
+// What it computes (oxicuda-dnn 0.1.8 hopper.rs, doc comment of
+// FlashAttention3Plan::generate_forward): per key/value tile, S = Q·Kᵀ, an
+// online softmax with a running row maximum m and row sum l, causal masking of
+// future keys, O_acc += P·V, and after the last tile O = O_acc / l together
+// with the log-sum-exp m + log l.  The S_q × S_k score matrix never leaves the
+// SM.
+//
+// How it maps onto Blackwell:
+//   * One CTA owns one (batch·head, query block).  A query block is two
+//     128-row query tiles for d = 64/128, one tile for d = 256.
+//   * Warp roles: 4 softmax warps per query tile (one row per thread, the
+//     warp's TMEM lane quarter), one TMA producer warp, one MMA-issuing warp.
+//   * K and V tiles (128 keys × d, 128-byte swizzled) stream through an
+//     NS-slot shared-memory ring, handed over with full/empty mbarriers.
+//   * S = Q·Kᵀ and O += P·V are tcgen05.mma (M = 128, fp32 accumulate) into
+//     tensor memory.  Softmax reads S with tcgen05.ld, writes P (fp16/bf16)
+//     back over the upper half of the S columns with tcgen05.st, and the PV
+//     MMA takes P straight from tensor memory.
+//   * The running maximum used for exponentiation is only raised when a row's
+//     maximum grows by more than 2^8 (kRescaleLog2); O and l then share the
+//     same stale maximum, so O / l is unchanged.  This skips almost all O
+//     rescales without approximating anything.
+//   * Causal: key tiles entirely above the diagonal are never loaded or
+//     computed; only tiles that straddle it (or the ragged end of the keys)
+//     take the masked path.  Query blocks are issued heaviest first.
+#pragma once
+
+#include <cuda_bf16.h>
+#include <cuda_fp16.h>
+
+#include "attn_launch.h"
+#include "sm100.cuh"
+
+namespace attn {
+
+// Status bits written when a bounded wait runs out.
+enum : unsigned int {
+    kStatusProducer = 1u,
+    kStatusMma = 2u,
+    kStatusSoftmax = 4u,
+    kStatusEpilogue = 8u,
+    kStatusDrain = 16u,
+};
+
+constexpr float kRescaleLog2 = 8.0f;
+constexpr float kLn2 = 0.693147180559945309f;
+
+template <int D>
+struct FwdTile {
+    static constexpr int BM = kBlockM;
+    static constexpr int BN = kBlockN;
+    static constexpr int TILES = q_tiles_per_cta(D);
+    static constexpr int CHUNKS = D / 64;                 // 128-byte swizzle atoms along d
+    static constexpr int ATOM_ROWS_BYTES = 128;           // one row of one atom
+    static constexpr int Q_CHUNK_BYTES = BM * ATOM_ROWS_BYTES;
+    static constexpr int KV_CHUNK_BYTES = BN * ATOM_ROWS_BYTES;
+    static constexpr int Q_TILE_BYTES = BM * D * 2;
+    static constexpr int KV_TILE_BYTES = BN * D * 2;
+    static constexpr int NS = D == 64 ? 8 : (D == 128 ? 4 : 2);
+    static constexpr int TILE_BYTES = TILES * Q_TILE_BYTES + NS * KV_TILE_BYTES;
+    static constexpr int NUM_BARS = 1 + 2 * NS + 2 + 2 + 2 + 1;
+    static constexpr int SMEM_BYTES = 1024 + TILE_BYTES + NUM_BARS * 8 + 16;
+    static constexpr int SOFTMAX_WARPS = 4 * TILES;
+    static constexpr int PRODUCER_WARP = SOFTMAX_WARPS;
+    static constexpr int MMA_WARP = SOFTMAX_WARPS + 1;
+    static constexpr int THREADS = 32 * (SOFTMAX_WARPS + 2);
+    // tensor memory columns: S buffers 0 and 1, then one O accumulator per tile
+    static constexpr uint32_t TMEM_COLS = 512;
+    static constexpr uint32_t S_STRIDE = 128;             // S buffer b at column b * 128
+    static constexpr uint32_t P_OFF = 64;                 // P (16-bit, packed) over S cols 64..127
+    static constexpr uint32_t O_COL = 256;
+    static_assert(SMEM_BYTES <= 232448, "shared memory budget");
+    static_assert(O_COL + TILES * D <= TMEM_COLS, "tensor memory budget");
+};
+
+// Number of key tiles query tile t of a block starting at row q0 visits.
+template <bool CAUSAL>
+__device__ __forceinline__ int kv_tiles_for(int row_begin, int S_q, int S_k) {
+    if (row_begin >= S_q) return 0;
+    int n = (S_k + kBlockN - 1) / kBlockN;
+    if (CAUSAL) {
+        const int last_row = min(row_begin + kBlockM, S_q) - 1;
+        n = min(n, last_row / kBlockN + 1);
+    }
+    return n;
+}
+
+template <int D, bool BF16, bool CAUSAL>
+__global__ void __launch_bounds__(FwdTile<D>::THREADS, 1)
+    attn_fwd_kernel(const __grid_constant__ CUtensorMap tm_q,
+                    const __grid_constant__ CUtensorMap tm_k,
+                    const __grid_constant__ CUtensorMap tm_v, void* __restrict__ o_ptr,
+                    float* __restrict__ lse_ptr, int S_q, int S_k, float scale_log2,
+                    unsigned int* __restrict__ status) {
+    using T = FwdTile<D>;
+    using namespace sm100;
+
+    extern __shared__ uint8_t smem_raw[];
+    const uint32_t raw_addr = smem_u32(smem_raw);
+    uint8_t* smem = smem_raw + ((1024u - (raw_addr & 1023u)) & 1023u);
+    uint8_t* sQ = smem;
+    uint8_t* sKV = smem + T::TILES * T::Q_TILE_BYTES;
+    uint64_t* bars = reinterpret_cast<uint64_t*>(smem + T::TILE_BYTES);
+    uint64_t* q_full = bars;
+    uint64_t* kv_full = bars + 1;
+    uint64_t* kv_empty = kv_full + T::NS;
+    uint64_t* s_full = kv_empty + T::NS;      // [2] S buffer b written
+    uint64_t* p_full = s_full + 2;            // [2] P in buffer b written (+ O rescaled)
+    uint64_t* o_done = p_full + 2;            // [2] PV MMAs of tile t finished
+    uint64_t* drain = o_done + 2;             // every MMA of the CTA finished
+    uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(drain + 1);
+    volatile int* abort_flag = reinterpret_cast<volatile int*>(tmem_slot + 1);
+
+    const int warp = threadIdx.x >> 5;
+    const int lane = threadIdx.x & 31;
+    const int bh = blockIdx.x;
+    const int n_qblk = gridDim.y;
+    const int qblk = CAUSAL ? (n_qblk - 1 - static_cast<int>(blockIdx.y))
+                            : static_cast<int>(blockIdx.y);
+    const int q0 = qblk * T::BM * T::TILES;
+
+    const int n_kv0 = kv_tiles_for<CAUSAL>(q0, S_q, S_k);
+    const int n_kv1 = T::TILES == 2 ? kv_tiles_for<CAUSAL>(q0 + T::BM, S_q, S_k) : 0;
+    const int n_max = max(n_kv0, n_kv1);
+
+    if (threadIdx.x == 0) {
+        mbar_init(q_full, 1);
+        for (int s = 0; s < T::NS; ++s) {
+            mbar_init(&kv_full[s], 1);
+            mbar_init(&kv_empty[s], 1);
+        }
+        for (int b = 0; b < 2; ++b) {
+            mbar_init(&s_full[b], 1);
+            mbar_init(&p_full[b], 128);
+            mbar_init(&o_done[b], 1);
+        }
+        mbar_init(drain, 1);
+        *abort_flag = 0;
+        fence_mbar_init();
+        asm volatile("fence.proxy.async.shared::cta;" ::: "memory");
+    }
+    if (warp == 0) {
+        tmem_alloc(tmem_slot, T::TMEM_COLS);
+        tmem_relinquish();
+    }
+    tc_fence_before();
+    __syncthreads();
+    tc_fence_after();
+    const uint32_t tmem = *tmem_slot;
+
+    if (warp == T::PRODUCER_WARP) {
+        // ------------------------------------------------------------ TMA producer
+        if (lane == 0 && n_max > 0) {
+            tma_prefetch_desc(&tm_q);
+            tma_prefetch_desc(&tm_k);
+            tma_prefetch_desc(&tm_v);
+            mbar_arrive_expect_tx(q_full, T::TILES * T::Q_TILE_BYTES);
+            for (int t = 0; t < T::TILES; ++t)
+                for (int c = 0; c < T::CHUNKS; ++c)
+                    tma_load_3d(sQ + (t * T::CHUNKS + c) * T::Q_CHUNK_BYTES, &tm_q, q_full,
+                                c * 64, q0 + t * T::BM, bh);
+            int idx = 0;
+            bool ok = true;
+            auto issue = [&](const CUtensorMap* map, int j) {
+                if (!ok) return;
+                const int slot = idx % T::NS;
+                ok = mbar_wait(&kv_empty[slot], ((idx / T::NS) & 1) ^ 1, abort_flag, status,
+                               kStatusProducer);
+                if (!ok) return;
+                mbar_arrive_expect_tx(&kv_full[slot], T::KV_TILE_BYTES);
+                uint8_t* dst = sKV + slot * T::KV_TILE_BYTES;
+                for (int c = 0; c < T::CHUNKS; ++c)
+                    tma_load_3d(dst + c * T::KV_CHUNK_BYTES, map, &kv_full[slot], c * 64,
+                                j * T::BN, bh);
+                ++idx;
+            };
+            // Load order is the MMA warp's consumption order.
+            if (T::TILES == 2) {
+                for (int j = 0; j < n_max; ++j) {
+                    issue(&tm_k, j);
+                    issue(&tm_v, j);
+                }
+            } else {
+                issue(&tm_k, 0);
+                if (n_max > 1) issue(&tm_k, 1);
+                for (int j = 0; j < n_max; ++j) {
+                    issue(&tm_v, j);
+                    if (j + 2 < n_max) issue(&tm_k, j + 2);
+                }
+            }
+            if (*abort_flag) {
+                // Let every copy this thread started land before the CTA exits.
+                const uint64_t t0 = global_timer_ns();
+                for (int i = max(0, idx - T::NS); i < idx; ++i) {
+                    const uint32_t a = smem_u32(&kv_full[i % T::NS]);
+                    while (!mbar_try_wait(a, (i / T::NS) & 1)) {
+                        if (global_timer_ns() - t0 > kWaitLimitNs) {
+                            atomicOr(status, kStatusDrain);
+                            break;
+                        }
+                    }
+                }
+                const uint32_t a = smem_u32(q_full);
+                while (!mbar_try_wait(a, 0)) {
+                    if (global_timer_ns() - t0 > kWaitLimitNs) {
+                        atomicOr(status, kStatusDrain);
+                        break;
+                    }
+                }
+            }
+        }
+    } else if (warp == T::MMA_WARP) {
+        // ------------------------------------------------------------ MMA issuer
+        if (lane == 0 && n_max > 0) {
+            constexpr uint32_t id_s = idesc_f16(128, T::BN, BF16, false, false);
+            constexpr uint32_t id_o = idesc_f16(128, D, BF16, false, true);
+            const uint32_t q_base = smem_u32(sQ);
+            const uint32_t kv_base = smem_u32(sKV);
+            bool ok = mbar_wait(q_full, 0, abort_flag, status, kStatusMma);
+            tc_fence_after();
+            int acq = 0;
+            auto acquire = [&](int& slot) {
+                if (!ok) return;
+                slot = acq % T::NS;
+                ok = mbar_wait(&kv_full[slot], (acq / T::NS) & 1, abort_flag, status, kStatusMma);
+                ++acq;
+                tc_fence_after();
+            };
+            auto wait_p = [&](int b, uint32_t parity) {
+                if (!ok) return;
+                ok = mbar_wait(&p_full[b], parity, abort_flag, status, kStatusMma);
+                tc_fence_after();
+            };
+            // S_b = Q_t · K(slot)ᵀ : M = 128, N = BN, K = D in steps of 16
+            auto mma_qk = [&](int t, int slot, int b) {
+                const uint32_t qa = q_base + t * T::Q_TILE_BYTES;
+                const uint32_t ka = kv_base + slot * T::KV_TILE_BYTES;
+#pragma unroll
+                for (int kk = 0; kk < D / 16; ++kk) {
+                    const uint32_t off = (kk >> 2) * T::Q_CHUNK_BYTES + (kk & 3) * 32;
+                    const uint32_t koff = (kk >> 2) * T::KV_CHUNK_BYTES + (kk & 3) * 32;
+                    mma_ss(tmem + b * T::S_STRIDE, sdesc_sw128(qa + off, 16, 1024),
+                           sdesc_sw128(ka + koff, 16, 1024), id_s, kk > 0);
+                }
+            };
+            // O_t (+)= P_b · V(slot) : M = 128, N = D, K = BN in steps of 16
+            auto mma_pv = [&](int t, int slot, int b, bool acc) {
+                const uint32_t va = kv_base + slot * T::KV_TILE_BYTES;
+#pragma unroll
+                for (int kk = 0; kk < T::BN / 16; ++kk) {
+                    mma_ts(tmem + T::O_COL + t * D, tmem + b * T::S_STRIDE + T::P_OFF + kk * 8,
+                           sdesc_sw128(va + kk * 16 * 128, T::KV_CHUNK_BYTES, 1024), id_o,
+                           (acc || kk > 0) ? 1u : 0u);
+                }
+            };
+            if (T::TILES == 2) {
+                const int n0 = n_kv0, n1 = n_kv1;
+                int kslot = 0, vslot = 0;
+                acquire(kslot);
+                if (ok) {
+                    if (n0 > 0) { mma_qk(0, kslot, 0); tc_commit(&s_full[0]); }
+                    if (n1 > 0) { mma_qk(1, kslot, 1); tc_commit(&s_full[1]); }
+                    tc_commit(&kv_empty[kslot]);
+                }
+                for (int j = 0; j < n_max && ok; ++j) {
+                    const bool has_next = j + 1 < n_max;
+                    acquire(vslot);
+                    if (j < n0) {
+                        wait_p(0, j & 1);
+                        if (!ok) break;
+                        mma_pv(0, vslot, 0, j > 0);
+                        if (j == n0 - 1) tc_commit(&o_done[0]);
+                    }
+                    if (has_next) acquire(kslot);
+                    if (!ok) break;
+                    if (j + 1 < n0) { mma_qk(0, kslot, 0); tc_commit(&s_full[0]); }
+                    if (j < n1) {
+                        wait_p(1, j & 1);
+                        if (!ok) break;
+                        mma_pv(1, vslot, 1, j > 0);
+                        if (j == n1 - 1) tc_commit(&o_done[1]);
+                    }
+                    tc_commit(&kv_empty[vslot]);
+                    if (j + 1 < n1) { mma_qk(1, kslot, 1); tc_commit(&s_full[1]); }
+                    if (has_next) tc_commit(&kv_empty[kslot]);
+                }
+            } else {
+                const int n = n_kv0;
+                int slot = 0;
+                acquire(slot);
+                if (ok) { mma_qk(0, slot, 0); tc_commit(&s_full[0]); tc_commit(&kv_empty[slot]); }
+                if (n > 1) {
+                    acquire(slot);
+                    if (ok) { mma_qk(0, slot, 1); tc_commit(&s_full[1]); tc_commit(&kv_empty[slot]); }
+                }
+                for (int j = 0; j < n && ok; ++j) {
+                    const int b = j & 1;
+                    int vslot = 0;
+                    acquire(vslot);
+                    wait_p(b, (j >> 1) & 1);
+                    if (!ok) break;
+                    mma_pv(0, vslot, b, j > 0);
+                    tc_commit(&o_done[0]);
+                    tc_commit(&kv_empty[vslot]);
+                    if (j + 2 < n) {
+                        acquire(slot);
+                        if (!ok) break;
+                        mma_qk(0, slot, b);
+                        tc_commit(&s_full[b]);
+                        tc_commit(&kv_empty[slot]);
+                    }
+                }
+            }
+            // Every MMA of this CTA has finished once `drain` flips.
+            tc_commit(drain);
+            const uint32_t a = smem_u32(drain);
+            const uint64_t t0 = global_timer_ns();
+            while (!mbar_try_wait(a, 0)) {
+                if (global_timer_ns() - t0 > kWaitLimitNs) {
+                    atomicOr(status, kStatusDrain);
+                    *abort_flag = 1;
+                    break;
+                }
+            }
+        }
+    } else {
+        // ------------------------------------------------------------ softmax warps
+        const int t = T::TILES == 2 ? (warp >> 2) : 0;
+        const int wq = warp & 3;                      // TMEM lane quarter of this warp
+        const int row = wq * 32 + lane;
+        const int row_begin = q0 + t * T::BM;
+        const int q_idx = row_begin + row;
+        const int n = t == 0 ? n_kv0 : n_kv1;
+        const uint32_t lane_base = tmem + (static_cast<uint32_t>(wq * 32) << 16);
+        float m = -INFINITY;                          // running max, log2 units (scale folded)
+        float l = 0.f;                                // running sum of exp2(x - m)
+        bool ok = true;
+
+        for (int j = 0; j < n; ++j) {
+            const int b = T::TILES == 2 ? t : (j & 1);
+            const uint32_t parity = T::TILES == 2 ? (j & 1) : ((j >> 1) & 1);
+            ok = mbar_wait(&s_full[b], parity, abort_flag, status, kStatusSoftmax);
+            ok = __all_sync(0xffffffffu, ok);
+            if (!ok) break;
+            tc_fence_after();
+
+            uint32_t sa[64], sb[64];
+            tmem_ld64(lane_base + b * T::S_STRIDE, sa);
+            tmem_ld64(lane_base + b * T::S_STRIDE + 64, sb);
+            float s[128];
+#pragma unroll
+            for (int c = 0; c < 64; ++c) {
+                s[c] = __uint_as_float(sa[c]);
+                s[64 + c] = __uint_as_float(sb[c]);
+            }
+
+            const int kv0 = j * T::BN;
+            const bool masked = (CAUSAL && kv0 + T::BN - 1 > row_begin) || (kv0 + T::BN > S_k);
+            // keys kv0 + c with c < lim are visible to this row
+            const int lim = masked ? max(0, min(S_k, CAUSAL ? q_idx + 1 : S_k) - kv0) : T::BN;
+
+            float mx = -INFINITY;
+            if (!masked) {
+#pragma unroll
+                for (int c = 0; c < 128; ++c) mx = fmaxf(mx, s[c]);
+            } else {
+#pragma unroll
+                for (int c = 0; c < 128; ++c) mx = c < lim ? fmaxf(mx, s[c]) : mx;
+            }
+            const float m_tile = (mx == -INFINITY) ? -INFINITY : mx * scale_log2;
+            const float m_new = fmaxf(m, m_tile);
+            bool rescale = false;
+            float alpha = 1.f;
+            if (m == -INFINITY) {
+                m = m_new;                             // nothing accumulated yet
+            } else if (m_new - m > kRescaleLog2) {
+                alpha = ex2_approx(m - m_new);
+                m = m_new;
+                l *= alpha;
+                rescale = true;
+            }
+            const float neg_m = (m == -INFINITY) ? 0.f : -m;
+
+            uint32_t pk[64];
+            float rs0 = 0.f, rs1 = 0.f;
+#pragma unroll
+            for (int c = 0; c < 128; c += 2) {
+                float p0 = ex2_approx(fmaf(s[c], scale_log2, neg_m));
+                float p1 = ex2_approx(fmaf(s[c + 1], scale_log2, neg_m));
+                if (masked) {
+                    p0 = c < lim ? p0 : 0.f;
+                    p1 = c + 1 < lim ? p1 : 0.f;
+                }
+                rs0 += p0;
+                rs1 += p1;
+                pk[c >> 1] = BF16 ? pack_bf16(p0, p1) : pack_f16(p0, p1);
+            }
+            l += rs0 + rs1;
+
+            tmem_st32(lane_base + b * T::S_STRIDE + T::P_OFF, pk);
+            tmem_st32(lane_base + b * T::S_STRIDE + T::P_OFF + 32, pk + 32);
+
+            if (T::TILES == 1 && j > 0) {
+                // O holds PV up to key tile j-1 only once that MMA has finished.
+                ok = mbar_wait(&o_done[0], (j - 1) & 1, abort_flag, status, kStatusSoftmax);
+                ok = __all_sync(0xffffffffu, ok);
+                if (!ok) break;
+                tc_fence_after();
+            }
+            if (__any_sync(0xffffffffu, rescale)) {
+                const uint32_t o_base = lane_base + T::O_COL + t * D;
+#pragma unroll 1
+                for (int cc = 0; cc < D; cc += 32) {
+                    uint32_t r[32];
+                    tmem_ld32(o_base + cc, r);
+#pragma unroll
+                    for (int i = 0; i < 32; ++i) r[i] = __float_as_uint(__uint_as_float(r[i]) * alpha);
+                    tmem_st32(o_base + cc, r);
+                }
+            }
+            tmem_st_wait();
+            tc_fence_before();
+            mbar_arrive(&p_full[b]);
+        }
+
+        if (ok && n > 0) {
+            const uint32_t parity = T::TILES == 2 ? 0u : static_cast<uint32_t>((n - 1) & 1);
+            ok = mbar_wait(&o_done[T::TILES == 2 ? t : 0], parity, abort_flag, status,
+                           kStatusEpilogue);
+            ok = __all_sync(0xffffffffu, ok);
+            if (ok) {
+                tc_fence_after();
+                const float inv_l = 1.f / l;
+                const bool store = q_idx < S_q;
+                const size_t row_off = (static_cast<size_t>(bh) * S_q + q_idx);
+                uint4* dst = reinterpret_cast<uint4*>(static_cast<uint16_t*>(o_ptr) + row_off * D);
+                const uint32_t o_base = lane_base + T::O_COL + t * D;
+#pragma unroll 1
+                for (int cc = 0; cc < D; cc += 32) {
+                    uint32_t r[32];
+                    tmem_ld32(o_base + cc, r);
+                    uint32_t w[16];
+#pragma unroll
+                    for (int i = 0; i < 16; ++i) {
+                        const float a = __uint_as_float(r[2 * i]) * inv_l;
+                        const float c = __uint_as_float(r[2 * i + 1]) * inv_l;
+                        w[i] = BF16 ? pack_bf16(a, c) : pack_f16(a, c);
+                    }
+                    if (store) {
+#pragma unroll
+                        for (int i = 0; i < 4; ++i)
+                            dst[cc / 8 + i] = make_uint4(w[4 * i], w[4 * i + 1], w[4 * i + 2],
+                                                         w[4 * i + 3]);
+                    }
+                }
+                if (store) lse_ptr[row_off] = (m + log2f(l)) * kLn2;
+            }
+        }
+    }
+
+    tc_fence_before();
+    __syncthreads();
+    if (warp == 0) {
+        tc_fence_after();
+        tmem_dealloc(tmem, T::TMEM_COLS);
+    }
+}
+
+template <int D, bool BF16, bool CAUSAL>
+cudaError_t launch_attn_fwd(const FwdArgs& a, cudaStream_t stream) {
+    using T = FwdTile<D>;
+    auto kernel = attn_fwd_kernel<D, BF16, CAUSAL>;
+    cudaError_t err = cudaFuncSetAttribute(kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                           T::SMEM_BYTES);
+    if (err != cudaSuccess) return err;
+    const int rows_per_cta = T::BM * T::TILES;
+    const int n_qblk = (a.S_q + rows_per_cta - 1) / rows_per_cta;
+    dim3 grid(static_cast<unsigned>(a.BH), static_cast<unsigned>(n_qblk), 1);
+    kernel<<<grid, T::THREADS, T::SMEM_BYTES, stream>>>(a.tm_q, a.tm_k, a.tm_v, a.o, a.lse, a.S_q,
+                                                         a.S_k, a.scale_log2, a.status);
+    return cudaGetLastError();
+}
+
+}  // namespace attn

@@ -1,0 +1,116 @@
+/*
+ * attn.h — C ABI of the GB300 (sm_103a) exact attention forward library
+ * (libattn.so).
+ *
+ * The operation (oxicuda-dnn 0.1.8, src/attn/flash_attn/hopper.rs, doc comment
+ * of FlashAttention3Plan::generate_forward, and the kernel parameter list
+ * built there):
+ *
+ *     S      = scale · Q · Kᵀ                 per (b, h), S_q × S_k
+ *     S[i,j] = −∞ for j > i                   when causal (top-left aligned)
+ *     O      = softmax_rows(S) · V
+ *     LSE_i  = ln Σ_j exp(S[i,j])             natural log, scale included
+ *
+ * computed tile by tile with an online softmax, so the S_q × S_k matrix never
+ * reaches device memory.
+ *
+ * Layout.  Q is [B, H, S_q, d]; K and V are [B, H, S_k, d]; O is [B, H, S_q, d];
+ * all dense row-major (d contiguous) in the element type `dtype`.  LSE is
+ * [B, H, S_q] fp32.  d ∈ {64, 128, 256} (SUPPORTED_HEAD_DIMS on the page).
+ *
+ * Ownership.  The caller owns every buffer.  The library allocates no memory,
+ * keeps no pointer after a call returns, and enqueues all device work on
+ * `stream` (NULL = the legacy default stream); calls return before the work
+ * completes.
+ *
+ * Errors.  Argument checks happen on the host before anything is enqueued and
+ * return a status; attn_last_error() then describes the offending argument
+ * by name (as the page's validate_config does).  A kernel whose internal
+ * bounded wait runs out does not hang: it returns early, and the next
+ * attn_get_device_status() reports ATTN_ERR_TIMEOUT.
+ */
+#ifndef ATTN_GB300_ATTN_H_
+#define ATTN_GB300_ATTN_H_
+
+#include <stdint.h>
+
+#ifdef __cplusplus
+extern "C" {
+#endif
+
+struct CUstream_st; /* cudaStream_t is `struct CUstream_st*` */
+
+typedef enum {
+    ATTN_DTYPE_F16 = 0,
+    ATTN_DTYPE_BF16 = 1
+} attn_dtype_t;
+
+typedef enum {
+    ATTN_OK = 0,
+    ATTN_ERR_INVALID_ARG = 1, /* null or misaligned pointer, size < 1, overlap, non-finite scale, size too large */
+    ATTN_ERR_UNSUPPORTED = 2, /* head_dim not in {64,128,256}, dtype not f16/bf16, negative scale, no sm_103 device */
+    ATTN_ERR_CUDA = 3,        /* a CUDA runtime or driver call failed (message has the CUDA error) */
+    ATTN_ERR_TIMEOUT = 4      /* a kernel's bounded internal wait ran out (reported by attn_get_device_status) */
+} attn_status_t;
+
+/*
+ * attn_fwd — enqueue the attention forward on `stream`.
+ *
+ *   q, k, v  device pointers, 16-byte aligned, element type `dtype`:
+ *            q [B,H,S_q,d], k and v [B,H,S_k,d]
+ *   o        device pointer, 16-byte aligned, [B,H,S_q,d] in `dtype`; written
+ *   lse      device pointer, 4-byte aligned, [B,H,S_q] fp32; written
+ *   B, H     batch and heads, >= 1, B·H <= 2^31 − 1
+ *   S_q, S_k query and key lengths, 1 .. 2^24 (need not be tile multiples)
+ *   d        head dimension: 64, 128 or 256
+ *   causal   0 or 1; 1 masks key j for query i when j > i (top-left)
+ *   scale    multiplier of Q·Kᵀ, finite and >= 0 (1/sqrt(d) is the usual)
+ *   stream   CUDA stream
+ *
+ * o and lse must not overlap q, k, v or each other.  Returns ATTN_OK once the
+ * kernel is enqueued.
+ */
+attn_status_t attn_fwd(const void* q, const void* k, const void* v, void* o, float* lse,
+                       int64_t B, int64_t H, int64_t S_q, int64_t S_k, int64_t d, int causal,
+                       float scale, attn_dtype_t dtype, struct CUstream_st* stream);
+
+/*
+ * attn_fwd_host — the same forward, for inputs and outputs in HOST memory.
+ *
+ * Enqueues on `stream`: copies of q_host, k_host, v_host into the caller's
+ * device buffers q_dev, k_dev, v_dev; attn_fwd on them into o_dev, lse_dev;
+ * copies of o_dev, lse_dev back into o_host, lse_host.  Host buffers should be
+ * page-locked for the copies to be asynchronous.  Shapes, alignment and
+ * argument rules are those of attn_fwd (device buffers as there; host buffers
+ * non-null).  The results are in o_host / lse_host once the stream has
+ * reached this point (e.g. after cudaStreamSynchronize).
+ */
+attn_status_t attn_fwd_host(const void* q_host, const void* k_host, const void* v_host,
+                            void* o_host, float* lse_host, void* q_dev, void* k_dev, void* v_dev,
+                            void* o_dev, float* lse_dev, int64_t B, int64_t H, int64_t S_q,
+                            int64_t S_k, int64_t d, int causal, float scale, attn_dtype_t dtype,
+                            struct CUstream_st* stream);
+
+/*
+ * attn_last_error — message for the last non-OK status returned on this host
+ * thread ("" if none).  The string stays valid until the next call on this
+ * thread.
+ */
+const char* attn_last_error(void);
+
+/*
+ * attn_get_device_status — synchronise `stream`, then read and clear the
+ * current device's status word.  ATTN_OK if every kernel since the last read
+ * finished its waits; ATTN_ERR_TIMEOUT if one ran out (the message names the
+ * role that gave up); ATTN_ERR_CUDA if the synchronisation itself failed.
+ */
+attn_status_t attn_get_device_status(struct CUstream_st* stream);
+
+/* attn_version — library version, major·10000 + minor·100 + patch. */
+int attn_version(void);
+
+#ifdef __cplusplus
+}
+#endif
+
+#endif /* ATTN_GB300_ATTN_H_ */
