@@ -1,0 +1,373 @@
+"""Benchmark of the attention forward: TFLOP/s on the d=128, S=4096 workload.
+
+One step = one forward over the whole batch in each masking mode: a full
+(non-causal) launch and a causal launch on the same seeded inputs
+(B=2, H=32, S_q=S_k=4096, d=128, bf16, scale=1/sqrt(128); Q, K ~ N(0,1),
+V ~ U(-1,1)).  FLOPs per step = 4·B·H·S²·d (full) + half of that (causal).
+
+Prints one JSON line (rank 0).  ``value`` is device-timed throughput with
+inputs resident in HBM; ``e2e`` is the same metric through the host-buffer C
+entry point, copies included; ``roofline`` is for the dominant launch (the
+full one); ``cpu_baseline`` times the fp64 oracle on a bounded sample.
+
+``--impl reference`` times the fp64 CPU oracle instead (there is no runnable
+reference implementation: the attention page is Rust that emits PTX for
+sm_90, with its kernel body absent).
+"""
+
+from __future__ import annotations
+
+import argparse
+import json
+import math
+import os
+import statistics
+import subprocess
+import sys
+import threading
+import time
+
+ROOT = os.path.dirname(os.path.abspath(__file__))
+if ROOT not in sys.path:
+    sys.path.insert(0, ROOT)
+
+WORKLOAD = "c3"
+METRIC = "attention fwd TFLOP/s (bf16, causal & non-causal) and % of GB300 dense peak"
+FALLBACK_PEAKS = {"hbm_gbs": 6800.0, "bf16_tflops": 1900.0, "bf16_tflops_sustained": 1700.0}
+
+
+def _env_int(name, default):
+    try:
+        return int(os.environ.get(name, default))
+    except ValueError:
+        return default
+
+
+def load_peaks():
+    path = os.path.join(ROOT, "MEASURED_PEAKS.json")
+    try:
+        with open(path) as f:
+            p = json.load(f)
+        return p, "measured"
+    except (OSError, ValueError):
+        return dict(FALLBACK_PEAKS), "fallback"
+
+
+class ClockSampler:
+    """nvidia-smi clock / throttle-reason samples every 200 ms while running."""
+
+    FIELDS = ("clocks.sm,clocks.max.sm,power.draw,clocks_event_reasons.hw_slowdown,"
+              "clocks_event_reasons.hw_thermal_slowdown,clocks_event_reasons.sw_thermal_slowdown,"
+              "clocks_event_reasons.sw_power_cap")
+
+    def __init__(self, device_index: int):
+        self.samples = []
+        self.proc = None
+        self.dev = device_index
+
+    def start(self):
+        try:
+            self.proc = subprocess.Popen(
+                ["nvidia-smi", f"--query-gpu={self.FIELDS}", "--format=csv,noheader,nounits",
+                 "-i", str(self.dev), "-lms", "200"],
+                stdout=subprocess.PIPE, stderr=subprocess.DEVNULL, text=True)
+        except OSError:
+            self.proc = None
+            return
+        self.thread = threading.Thread(target=self._read, daemon=True)
+        self.thread.start()
+
+    def _read(self):
+        for line in self.proc.stdout:
+            parts = [x.strip() for x in line.split(",")]
+            if len(parts) < 7:
+                continue
+            try:
+                self.samples.append((time.time(), float(parts[0]), float(parts[1]), parts[3:7]))
+            except ValueError:
+                continue
+
+    def stop(self):
+        if self.proc is not None:
+            self.proc.terminate()
+            try:
+                self.proc.wait(timeout=5)
+            except subprocess.TimeoutExpired:
+                self.proc.kill()
+
+    def summary(self, t0, t1):
+        win = [s for s in self.samples if t0 - 0.25 <= s[0] <= t1 + 0.25] or self.samples
+        if not win:
+            return {"sm_mhz": None, "sm_max_mhz": None, "reasons": ["no samples"], "samples": 0}
+        names = ["hw_slowdown", "hw_thermal_slowdown", "sw_thermal_slowdown", "sw_power_cap"]
+        reasons = sorted({names[i] for s in win for i, v in enumerate(s[3]) if v.lower() == "active"})
+        return {"sm_mhz": statistics.median(s[1] for s in win),
+                "sm_max_mhz": max(s[2] for s in win), "reasons": reasons, "samples": len(win)}
+
+
+def kernel_source_digest() -> str:
+    """sha256 over the kernel sources; ties recorded DRAM traffic to the code it was taken on."""
+    import hashlib
+    h = hashlib.sha256()
+    csrc = os.path.join(ROOT, "exact_attention_53_gb300", "csrc")
+    for name in sorted(os.listdir(csrc)):
+        if name.endswith((".cu", ".cuh", ".h")):
+            with open(os.path.join(csrc, name), "rb") as f:
+                h.update(name.encode() + b"\0" + f.read())
+    return h.hexdigest()
+
+
+def measured_traffic(key: str):
+    """DRAM bytes per launch from the committed ncu summary, or None if the kernel changed since."""
+    path = os.path.join(ROOT, "profiles", "traffic.json")
+    try:
+        with open(path) as f:
+            rec = json.load(f)
+    except (OSError, ValueError):
+        return None
+    if rec.get("kernel_source_sha256") != kernel_source_digest():
+        return None
+    return rec.get(key)
+
+
+def cpu_baseline(budget_s: float = 12.0):
+    """The fp64 oracle, as it stands, on whole heads of the workload until the budget is spent."""
+    import numpy as np  # noqa: F401
+
+    import oracle
+    from exact_attention_53_gb300.workloads import WORKLOADS, workload_qkv
+
+    w = WORKLOADS[WORKLOAD]
+    q, k, v = workload_qkv(w)
+    flops = 0.0
+    heads = 0
+    t0 = time.perf_counter()
+    while True:
+        b, h = divmod(heads % (w.B * w.H), w.H)
+        causal = heads % 2 == 1
+        oracle.attention_forward(q[b:b + 1, h:h + 1], k[b:b + 1, h:h + 1], v[b:b + 1, h:h + 1],
+                                 causal=causal, scale=w.scale)
+        flops += 4.0 * w.S_q * w.S_k * w.d / (2 if causal else 1)
+        heads += 1
+        if time.perf_counter() - t0 >= budget_s:
+            break
+    dt = time.perf_counter() - t0
+    return {"value": flops / dt / 1e12, "unit": "TFLOP/s", "cores": os.cpu_count(),
+            "kind": "oracle",
+            "sample": f"{heads} whole (b,h) heads of {WORKLOAD} (B=2,H=32,S=4096,d=128), "
+                      f"alternating full/causal, fp64 numpy, {dt:.1f} s"}
+
+
+def run_reference(args, rank, world):
+    """The fp64 oracle on the host cores, K timed steps of one head pair each."""
+    if rank != 0:
+        return
+    import oracle
+    from exact_attention_53_gb300.workloads import WORKLOADS, workload_qkv
+
+    w = WORKLOADS[WORKLOAD]
+    q, k, v = workload_qkv(w)
+
+    def step(i):
+        b, h = divmod(i % (w.B * w.H), w.H)
+        sl = (slice(b, b + 1), slice(h, h + 1))
+        for causal in (False, True):
+            oracle.attention_forward(q[sl], k[sl], v[sl], causal=causal, scale=w.scale)
+
+    for i in range(args.warmup):
+        step(i)
+    t0 = time.perf_counter()
+    for i in range(args.steps):
+        step(args.warmup + i)
+    dt = time.perf_counter() - t0
+    flops_step = 4.0 * w.S_q * w.S_k * w.d * 1.5
+    value = flops_step * args.steps / dt / 1e12
+    sample = f"per step one (b,h) head of {WORKLOAD}, full + causal, fp64 numpy oracle"
+    print(json.dumps({
+        "impl": "reference", "metric": METRIC, "value": value, "unit": "TFLOP/s",
+        "n_gpus": args.gpus, "steps": args.steps, "warmup": args.warmup,
+        "ms_per_step": dt * 1e3 / args.steps, "higher_is_better": True, "scaling": "weak",
+        "vs_baseline": None, "dtype": "f64", "data": "synthetic",
+        "config": {"workload": f"{WORKLOAD}: one head per step of B=2,H=32,S_q=S_k=4096,d=128"},
+        "cpu_baseline": {"value": value, "unit": "TFLOP/s", "cores": os.cpu_count(),
+                         "kind": "oracle", "sample": sample},
+        "e2e": {"value": value, "unit": "TFLOP/s", "h2d_bytes_per_step": 0,
+                "d2h_bytes_per_step": 0},
+    }), flush=True)
+
+
+def run_gpu(args, rank, world):
+    import torch
+
+    from exact_attention_53_gb300 import attn_fwd, attn_fwd_host, attn_get_device_status
+    from exact_attention_53_gb300.binding import ATTN_DTYPE_BF16, load_library
+    from exact_attention_53_gb300.build import build
+    from exact_attention_53_gb300.workloads import WORKLOADS, workload_qkv
+
+    local = _env_int("LOCAL_RANK", 0)
+    dev = torch.device("cuda", local)
+    torch.cuda.set_device(dev)
+    if rank == 0 or world == 1:
+        build()
+    if world > 1:
+        torch.distributed.barrier()
+    load_library()
+
+    w = WORKLOADS[WORKLOAD]
+    B, H, S_q, S_k, d = w.B, w.H, w.S_q, w.S_k, w.d
+    q_h, k_h, v_h = workload_qkv(w)
+    q, k, v = q_h.to(dev), k_h.to(dev), v_h.to(dev)
+    o = torch.empty_like(q)
+    lse = torch.empty((B, H, S_q), dtype=torch.float32, device=dev)
+    stream = torch.cuda.current_stream(dev)
+    flops = {False: w.flops(False), True: w.flops(True)}
+    flops_step = flops[False] + flops[True]
+
+    def launch(causal):
+        attn_fwd(q, k, v, o, lse, B, H, S_q, S_k, d, int(causal), w.scale, ATTN_DTYPE_BF16, stream)
+
+    def barrier():
+        if world > 1:
+            torch.distributed.barrier()
+        torch.cuda.synchronize(dev)
+
+    sampler = ClockSampler(local)
+    sampler.start()
+    # Untimed warm-up: at least W steps, and at least ~0.4 s so the clocks have
+    # ramped and the sampler has seen the GPU under this load.
+    t_w = time.time()
+    warm = 0
+    while warm < args.warmup or time.time() - t_w < 0.4:
+        launch(False)
+        launch(True)
+        warm += 1
+        if warm % 8 == 0:
+            torch.cuda.synchronize(dev)
+    attn_get_device_status(stream)
+    barrier()
+
+    ev = [[torch.cuda.Event(enable_timing=True) for _ in range(3)] for _ in range(args.steps)]
+    t_wall0 = time.time()
+    start = torch.cuda.Event(enable_timing=True)
+    end = torch.cuda.Event(enable_timing=True)
+    start.record(stream)
+    for i in range(args.steps):
+        ev[i][0].record(stream)
+        launch(False)
+        ev[i][1].record(stream)
+        launch(True)
+        ev[i][2].record(stream)
+    end.record(stream)
+    barrier()
+    t_wall1 = time.time()
+    total_ms = start.elapsed_time(end)
+    full_ms = [e[0].elapsed_time(e[1]) for e in ev]
+    causal_ms = [e[1].elapsed_time(e[2]) for e in ev]
+    attn_get_device_status(stream)
+
+    if world > 1:
+        t = torch.tensor([total_ms], device=dev, dtype=torch.float64)
+        torch.distributed.all_reduce(t, op=torch.distributed.ReduceOp.MAX)
+        total_ms = float(t.item())
+    value = flops_step * args.steps * world / (total_ms * 1e-3) / 1e12
+
+    # ---- e2e: host buffers in, host buffers out, through attn_fwd_host
+    qp, kp, vp = q_h.pin_memory(), k_h.pin_memory(), v_h.pin_memory()
+    op = torch.empty_like(qp).pin_memory()
+    lp = torch.empty((B, H, S_q), dtype=torch.float32).pin_memory()
+    q2, k2, v2 = torch.empty_like(q), torch.empty_like(k), torch.empty_like(v)
+
+    def e2e_launch(causal):
+        attn_fwd_host(qp, kp, vp, op, lp, q2, k2, v2, o, lse, B, H, S_q, S_k, d, int(causal),
+                      w.scale, ATTN_DTYPE_BF16, stream)
+
+    for _ in range(args.warmup):
+        e2e_launch(False)
+        e2e_launch(True)
+    barrier()
+    e0 = torch.cuda.Event(enable_timing=True)
+    e1 = torch.cuda.Event(enable_timing=True)
+    e0.record(stream)
+    for _ in range(args.steps):
+        e2e_launch(False)
+        e2e_launch(True)
+    e1.record(stream)
+    barrier()
+    e2e_ms = e0.elapsed_time(e1)
+    if world > 1:
+        t = torch.tensor([e2e_ms], device=dev, dtype=torch.float64)
+        torch.distributed.all_reduce(t, op=torch.distributed.ReduceOp.MAX)
+        e2e_ms = float(t.item())
+    e2e_value = flops_step * args.steps * world / (e2e_ms * 1e-3) / 1e12
+    in_bytes = q.numel() * 2 + k.numel() * 2 + v.numel() * 2
+    out_bytes = o.numel() * 2 + lse.numel() * 4
+    sampler.stop()
+
+    if rank != 0:
+        return
+    peaks, peak_src = load_peaks()
+    peak = float(peaks.get("bf16_tflops", FALLBACK_PEAKS["bf16_tflops"]))
+    full_avg = statistics.mean(full_ms)
+    causal_avg = statistics.mean(causal_ms)
+    achieved = flops[False] / (full_avg * 1e-3) / 1e12
+    achieved_c = flops[True] / (causal_avg * 1e-3) / 1e12
+    clocks = sampler.summary(t_wall0, t_wall1)
+    traffic = measured_traffic("attn_fwd_d128_bf16_full_c3")
+    line = {
+        "metric": METRIC, "value": value, "unit": "TFLOP/s", "n_gpus": world,
+        "steps": args.steps, "warmup": args.warmup, "warmup_steps_run": warm,
+        "ms_per_step": total_ms / args.steps,
+        "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "bf16",
+        "data": "synthetic",
+        "config": {"workload": f"{WORKLOAD}: B={B} H={H} S_q=S_k={S_q} d={d} bf16, one full + one "
+                               f"causal forward per step, scale=1/sqrt(128), Q,K~N(0,1) V~U(-1,1)",
+                   "global_batch": B * world, "seq_len": S_q,
+                   "parallelism": f"replicas x{world}" if world > 1 else "single GPU",
+                   "l2": "inputs larger than L2 (Q+K+V = 201 MB > 129 MB), no flush"},
+        "modes": {"full": {"ms": full_avg, "tflops": achieved, "frac_of_peak": achieved / peak},
+                  "causal": {"ms": causal_avg, "tflops": achieved_c,
+                             "frac_of_peak": achieved_c / peak}},
+        "roofline": {"bound": "tensor", "achieved": achieved, "peak": peak, "unit": "TFLOP/s",
+                     "frac": achieved / peak, "traffic": traffic,
+                     "kernel": "attn_fwd_kernel<128,bf16,full>",
+                     "peak_source": f"{peak_src} bf16 burst (MEASURED_PEAKS.json bf16_tflops)"
+                     if peak_src == "measured" else "fallback 1.9 PFLOP/s"},
+        "e2e": {"value": e2e_value, "unit": "TFLOP/s", "h2d_bytes_per_step": 2 * in_bytes,
+                "d2h_bytes_per_step": 2 * out_bytes},
+        "gpu_launches": 2 * args.steps,
+        "clocks": clocks,
+    }
+    if not args.no_cpu_baseline and world == 1:
+        line["cpu_baseline"] = cpu_baseline()
+    print(json.dumps(line), flush=True)
+
+
+def main():
+    ap = argparse.ArgumentParser(description=__doc__.split("\n")[0])
+    ap.add_argument("--gpus", type=int, default=1)
+    ap.add_argument("--steps", type=int, default=50)
+    ap.add_argument("--warmup", type=int, default=5)
+    ap.add_argument("--impl", choices=["ours", "reference"], default="ours")
+    ap.add_argument("--no-cpu-baseline", action="store_true",
+                    help="skip the ~12 s oracle timing on the host cores")
+    args = ap.parse_args()
+    args.warmup = max(3, args.warmup)   # at least three untimed warm-up steps
+    world = _env_int("WORLD_SIZE", 1)
+    rank = _env_int("RANK", 0)
+    if args.impl == "reference":
+        run_reference(args, rank, world)
+        return
+    if world > 1:
+        import torch
+        torch.cuda.set_device(_env_int("LOCAL_RANK", 0))
+        torch.distributed.init_process_group("nccl")
+    try:
+        run_gpu(args, rank, world)
+    finally:
+        if world > 1:
+            import torch
+            torch.distributed.destroy_process_group()
+
+
+if __name__ == "__main__":
+    main()

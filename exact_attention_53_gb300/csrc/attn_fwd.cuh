@@ -30,6 +30,8 @@
 #include <cuda_bf16.h>
 #include <cuda_fp16.h>
 
+#include <algorithm>
+
 #include "attn_launch.h"
 #include "sm100.cuh"
 
@@ -63,9 +65,17 @@ struct FwdTile {
     static constexpr int NUM_BARS = 1 + 2 * NS + 2 + 2 + 2 + 1;
     static constexpr int SMEM_BYTES = 1024 + TILE_BYTES + NUM_BARS * 8 + 16;
     static constexpr int SOFTMAX_WARPS = 4 * TILES;
-    static constexpr int PRODUCER_WARP = SOFTMAX_WARPS;
+    static constexpr int PRODUCER_WARP = SOFTMAX_WARPS;       // first warp of the aux warpgroup
     static constexpr int MMA_WARP = SOFTMAX_WARPS + 1;
-    static constexpr int THREADS = 32 * (SOFTMAX_WARPS + 2);
+    static constexpr int THREADS = 32 * (SOFTMAX_WARPS + 4);  // + one aux warpgroup
+    // Register split (TILES == 2): 12 warps put 3 on each SM sub-partition, so
+    // the launch gets 168 registers a thread (16384 / 3 warps / 32, rounded to
+    // 8).  The aux warpgroup gives most of its share to the softmax ones:
+    // 2·216 + 72 = 3·168 (72 is the least the aux roles need without spills).
+    static constexpr int LAUNCH_REGS = 168;
+    static constexpr int SOFTMAX_REGS = 216;
+    static constexpr int AUX_REGS = 72;
+    static_assert(TILES == 1 || 2 * SOFTMAX_REGS + AUX_REGS <= 3 * LAUNCH_REGS, "register split");
     // tensor memory columns: S buffers 0 and 1, then one O accumulator per tile
     static constexpr uint32_t TMEM_COLS = 512;
     static constexpr uint32_t S_STRIDE = 128;             // S buffer b at column b * 128
@@ -92,8 +102,8 @@ __global__ void __launch_bounds__(FwdTile<D>::THREADS, 1)
     attn_fwd_kernel(const __grid_constant__ CUtensorMap tm_q,
                     const __grid_constant__ CUtensorMap tm_k,
                     const __grid_constant__ CUtensorMap tm_v, void* __restrict__ o_ptr,
-                    float* __restrict__ lse_ptr, int S_q, int S_k, float scale_log2,
-                    unsigned int* __restrict__ status) {
+                    float* __restrict__ lse_ptr, int S_q, int S_k, int BH, int n_qblk,
+                    int head_group, float scale_log2, unsigned int* __restrict__ status) {
     using T = FwdTile<D>;
     using namespace sm100;
 
@@ -115,10 +125,28 @@ __global__ void __launch_bounds__(FwdTile<D>::THREADS, 1)
 
     const int warp = threadIdx.x >> 5;
     const int lane = threadIdx.x & 31;
-    const int bh = blockIdx.x;
-    const int n_qblk = gridDim.y;
-    const int qblk = CAUSAL ? (n_qblk - 1 - static_cast<int>(blockIdx.y))
-                            : static_cast<int>(blockIdx.y);
+    // Linear block index -> (head, query block).  Full attention: the query
+    // blocks of one head are adjacent, so the CTAs resident at a time share a
+    // few heads' K/V in L2.  Causal: heads go in groups of `head_group` (sized
+    // so a group's K/V fits in L2) and within a group the heaviest query
+    // blocks of all its heads go first, which keeps the tail short.
+    int bh, qblk;
+    {
+        const int L = static_cast<int>(blockIdx.x);
+        if (CAUSAL) {
+            const int per_group = head_group * n_qblk;
+            const int g = L / per_group;
+            const int r = L - g * per_group;
+            const int g0 = g * head_group;
+            const int gsz = min(head_group, BH - g0);
+            const int qi = r / gsz;
+            bh = g0 + (r - qi * gsz);
+            qblk = n_qblk - 1 - qi;
+        } else {
+            bh = L / n_qblk;
+            qblk = L - bh * n_qblk;
+        }
+    }
     const int q0 = qblk * T::BM * T::TILES;
 
     const int n_kv0 = kv_tiles_for<CAUSAL>(q0, S_q, S_k);
@@ -150,7 +178,20 @@ __global__ void __launch_bounds__(FwdTile<D>::THREADS, 1)
     tc_fence_after();
     const uint32_t tmem = *tmem_slot;
 
-    if (warp == T::PRODUCER_WARP) {
+    // Each branch below ends in its own copy of the teardown, so no code runs
+    // under two different register budgets.
+    auto teardown = [&]() {
+        tc_fence_before();
+        __syncthreads();
+        if (warp == 0) {
+            tc_fence_after();
+            tmem_dealloc(tmem, T::TMEM_COLS);
+        }
+    };
+
+    if (warp >= T::SOFTMAX_WARPS) {
+      if (T::TILES == 2) regs_shrink<T::AUX_REGS>();
+      if (warp == T::PRODUCER_WARP) {
         // ------------------------------------------------------------ TMA producer
         if (lane == 0 && n_max > 0) {
             tma_prefetch_desc(&tm_q);
@@ -325,7 +366,10 @@ __global__ void __launch_bounds__(FwdTile<D>::THREADS, 1)
                 }
             }
         }
+      }
+      teardown();
     } else {
+        if (T::TILES == 2) regs_grow<T::SOFTMAX_REGS>();
         // ------------------------------------------------------------ softmax warps
         const int t = T::TILES == 2 ? (warp >> 2) : 0;
         const int wq = warp & 3;                      // TMEM lane quarter of this warp
@@ -361,13 +405,21 @@ __global__ void __launch_bounds__(FwdTile<D>::THREADS, 1)
             // keys kv0 + c with c < lim are visible to this row
             const int lim = masked ? max(0, min(S_k, CAUSAL ? q_idx + 1 : S_k) - kv0) : T::BN;
 
-            float mx = -INFINITY;
-            if (!masked) {
+            if (masked) {
 #pragma unroll
-                for (int c = 0; c < 128; ++c) mx = fmaxf(mx, s[c]);
-            } else {
+                for (int c = 0; c < 128; ++c) s[c] = c < lim ? s[c] : -INFINITY;
+            }
+            // row maximum: 8 independent chains of 3-input maxima
+            float mx;
+            {
+                float a[8];
 #pragma unroll
-                for (int c = 0; c < 128; ++c) mx = c < lim ? fmaxf(mx, s[c]) : mx;
+                for (int i = 0; i < 8; ++i) a[i] = fmaxf(s[2 * i], s[2 * i + 1]);
+#pragma unroll
+                for (int c = 16; c < 128; c += 16)
+#pragma unroll
+                    for (int i = 0; i < 8; ++i) a[i] = fmax3(a[i], s[c + i], s[c + 8 + i]);
+                mx = fmax3(fmax3(a[0], a[1], a[2]), fmax3(a[3], a[4], a[5]), fmaxf(a[6], a[7]));
             }
             const float m_tile = (mx == -INFINITY) ? -INFINITY : mx * scale_log2;
             const float m_new = fmaxf(m, m_tile);
@@ -383,21 +435,30 @@ __global__ void __launch_bounds__(FwdTile<D>::THREADS, 1)
             }
             const float neg_m = (m == -INFINITY) ? 0.f : -m;
 
+            // p = 2^(s·scale·log2e − m), two lanes at a time on the packed fp32 pipe
             uint32_t pk[64];
-            float rs0 = 0.f, rs1 = 0.f;
+            const float2 sl2 = make_float2(scale_log2, scale_log2);
+            const float2 nm = make_float2(neg_m, neg_m);
+            float2 acc[4] = {make_float2(0.f, 0.f), make_float2(0.f, 0.f), make_float2(0.f, 0.f),
+                             make_float2(0.f, 0.f)};
 #pragma unroll
             for (int c = 0; c < 128; c += 2) {
-                float p0 = ex2_approx(fmaf(s[c], scale_log2, neg_m));
-                float p1 = ex2_approx(fmaf(s[c + 1], scale_log2, neg_m));
+                const float2 x = __ffma2_rn(make_float2(s[c], s[c + 1]), sl2, nm);
+                float p0 = ex2_approx(x.x);
+                float p1 = ex2_approx(x.y);
                 if (masked) {
                     p0 = c < lim ? p0 : 0.f;
                     p1 = c + 1 < lim ? p1 : 0.f;
                 }
-                rs0 += p0;
-                rs1 += p1;
+                acc[(c >> 1) & 3] = __fadd2_rn(acc[(c >> 1) & 3], make_float2(p0, p1));
                 pk[c >> 1] = BF16 ? pack_bf16(p0, p1) : pack_f16(p0, p1);
             }
-            l += rs0 + rs1;
+            {
+                const float2 a01 = __fadd2_rn(acc[0], acc[1]);
+                const float2 a23 = __fadd2_rn(acc[2], acc[3]);
+                const float2 t = __fadd2_rn(a01, a23);
+                l += t.x + t.y;
+            }
 
             tmem_st32(lane_base + b * T::S_STRIDE + T::P_OFF, pk);
             tmem_st32(lane_base + b * T::S_STRIDE + T::P_OFF + 32, pk + 32);
@@ -458,13 +519,7 @@ __global__ void __launch_bounds__(FwdTile<D>::THREADS, 1)
                 if (store) lse_ptr[row_off] = (m + log2f(l)) * kLn2;
             }
         }
-    }
-
-    tc_fence_before();
-    __syncthreads();
-    if (warp == 0) {
-        tc_fence_after();
-        tmem_dealloc(tmem, T::TMEM_COLS);
+        teardown();
     }
 }
 
@@ -475,11 +530,28 @@ cudaError_t launch_attn_fwd(const FwdArgs& a, cudaStream_t stream) {
     cudaError_t err = cudaFuncSetAttribute(kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
                                            T::SMEM_BYTES);
     if (err != cudaSuccess) return err;
+    if (T::TILES == 2) {
+        // The warpgroup register split assumes the launch grants LAUNCH_REGS a
+        // thread; refuse to launch a build where it does not (it would stall).
+        cudaFuncAttributes fa;
+        err = cudaFuncGetAttributes(&fa, kernel);
+        if (err != cudaSuccess) return err;
+        if (fa.numRegs != T::LAUNCH_REGS) return cudaErrorInvalidConfiguration;
+    }
+    int head_group = 1;
+    if (CAUSAL) {
+        const long long kv_head_bytes = 2LL * a.S_k * D * 2;
+        const long long budget = 48LL << 20;
+        head_group = static_cast<int>(std::max(1LL, std::min<long long>(a.BH, budget / kv_head_bytes)));
+    }
     const int rows_per_cta = T::BM * T::TILES;
     const int n_qblk = (a.S_q + rows_per_cta - 1) / rows_per_cta;
-    dim3 grid(static_cast<unsigned>(a.BH), static_cast<unsigned>(n_qblk), 1);
+    const long long blocks = static_cast<long long>(a.BH) * n_qblk;
+    if (blocks > 0x7fffffffLL) return cudaErrorInvalidConfiguration;
+    dim3 grid(static_cast<unsigned>(blocks), 1, 1);
     kernel<<<grid, T::THREADS, T::SMEM_BYTES, stream>>>(a.tm_q, a.tm_k, a.tm_v, a.o, a.lse, a.S_q,
-                                                         a.S_k, a.scale_log2, a.status);
+                                                         a.S_k, a.BH, n_qblk, head_group,
+                                                         a.scale_log2, a.status);
     return cudaGetLastError();
 }
 

@@ -230,7 +230,27 @@ __device__ __forceinline__ void tmem_st_wait() {
 #undef ATTN_R8
 #undef ATTN_W8
 
+// ---------------------------------------------------------------- registers
+// Per-warpgroup register budget changes (all 128 threads of the warpgroup
+// execute the same instruction).  The sum over warpgroups must not exceed the
+// registers the CTA was launched with.
+template <int N>
+__device__ __forceinline__ void regs_grow() {
+    asm volatile("setmaxnreg.inc.sync.aligned.u32 %0;" ::"n"(N));
+}
+template <int N>
+__device__ __forceinline__ void regs_shrink() {
+    asm volatile("setmaxnreg.dec.sync.aligned.u32 %0;" ::"n"(N));
+}
+
 // ---------------------------------------------------------------- math
+// Three-input maximum (one instruction on sm_100 family).
+__device__ __forceinline__ float fmax3(float a, float b, float c) {
+    float r;
+    asm("max.f32 %0, %1, %2, %3;" : "=f"(r) : "f"(a), "f"(b), "f"(c));
+    return r;
+}
+
 __device__ __forceinline__ float ex2_approx(float x) {
     float y;
     asm("ex2.approx.ftz.f32 %0, %1;" : "=f"(y) : "f"(x));

@@ -1,0 +1,131 @@
+"""Host-side tests of the C ABI (no GPU needed).
+
+The library must load, export every function include/attn.h declares, and
+reject bad arguments with the documented status before touching the device,
+with a message naming the offending field (as the page's validate_config does:
+oxicuda-dnn 0.1.8 hopper.rs, validate_config and its tests).
+"""
+
+import ctypes
+import os
+import re
+
+import pytest
+
+from exact_attention_53_gb300 import binding
+from exact_attention_53_gb300.build import build
+
+ROOT = os.path.dirname(os.path.dirname(os.path.abspath(__file__)))
+HEADER = os.path.join(ROOT, "include", "attn.h")
+
+A = 1 << 20          # a fake, 16-byte aligned "device" address; never dereferenced
+MB = 1 << 24
+
+
+@pytest.fixture(scope="module")
+def lib():
+    build()
+    return binding.load_library()
+
+
+def _declared_functions():
+    text = open(HEADER).read()
+    text = re.sub(r"/\*.*?\*/", "", text, flags=re.S)
+    return sorted(set(re.findall(r"^\s*[a-z_][\w \*]*?\b(attn_\w+)\s*\(", text, flags=re.M)))
+
+
+def test_header_declares_the_boundary():
+    names = _declared_functions()
+    assert names == sorted(["attn_fwd", "attn_fwd_host", "attn_last_error",
+                            "attn_get_device_status", "attn_version"])
+
+
+def test_library_exports_every_declared_symbol(lib):
+    for name in _declared_functions():
+        assert hasattr(lib, name), name
+    assert set(binding.EXPORTED) == set(_declared_functions())
+    assert lib.attn_version() == 10000
+
+
+def _fwd(lib, q=A, k=A + MB, v=A + 2 * MB, o=A + 3 * MB, lse=A + 4 * MB, B=1, H=2, S_q=128,
+         S_k=128, d=128, causal=0, scale=0.125, dtype=1):
+    return lib.attn_fwd(q, k, v, o, lse, B, H, S_q, S_k, d, causal, scale, dtype, None)
+
+
+CASES = [
+    (dict(q=0), binding.ATTN_ERR_INVALID_ARG, "q is null"),
+    (dict(k=0), binding.ATTN_ERR_INVALID_ARG, "k is null"),
+    (dict(v=0), binding.ATTN_ERR_INVALID_ARG, "v is null"),
+    (dict(o=0), binding.ATTN_ERR_INVALID_ARG, "o is null"),
+    (dict(lse=0), binding.ATTN_ERR_INVALID_ARG, "lse is null"),
+    (dict(B=0), binding.ATTN_ERR_INVALID_ARG, "B must be"),
+    (dict(H=-1), binding.ATTN_ERR_INVALID_ARG, "H must be"),
+    (dict(S_q=0), binding.ATTN_ERR_INVALID_ARG, "S_q must be"),
+    (dict(S_k=0), binding.ATTN_ERR_INVALID_ARG, "S_k must be"),
+    (dict(d=0), binding.ATTN_ERR_INVALID_ARG, "d must be"),
+    (dict(d=96), binding.ATTN_ERR_UNSUPPORTED, "head_dim"),
+    (dict(d=512), binding.ATTN_ERR_UNSUPPORTED, "head_dim"),
+    (dict(dtype=2), binding.ATTN_ERR_UNSUPPORTED, "dtype"),
+    (dict(causal=2), binding.ATTN_ERR_INVALID_ARG, "causal"),
+    (dict(scale=float("nan")), binding.ATTN_ERR_INVALID_ARG, "scale"),
+    (dict(scale=float("inf")), binding.ATTN_ERR_INVALID_ARG, "scale"),
+    (dict(scale=-0.5), binding.ATTN_ERR_UNSUPPORTED, "scale"),
+    (dict(q=A + 8), binding.ATTN_ERR_INVALID_ARG, "q is not 16-byte aligned"),
+    (dict(k=A + MB + 2), binding.ATTN_ERR_INVALID_ARG, "k is not 16-byte aligned"),
+    (dict(o=A + 3 * MB + 4), binding.ATTN_ERR_INVALID_ARG, "o is not 16-byte aligned"),
+    (dict(lse=A + 4 * MB + 2), binding.ATTN_ERR_INVALID_ARG, "lse is not 4-byte aligned"),
+    (dict(o=A + 64), binding.ATTN_ERR_INVALID_ARG, "o overlaps q"),
+    (dict(lse=A + 2 * MB + 16), binding.ATTN_ERR_INVALID_ARG, "lse overlaps v"),
+    (dict(lse=A + 3 * MB + 1024), binding.ATTN_ERR_INVALID_ARG, "lse overlaps o"),
+    (dict(S_q=(1 << 22) + 1), binding.ATTN_ERR_INVALID_ARG, "S_q"),
+    (dict(S_k=(1 << 22) + 1, k=A + 8 * MB, v=A + 16 * MB * 256), binding.ATTN_ERR_INVALID_ARG, "S_k"),
+    (dict(B=1 << 16, H=1 << 16), binding.ATTN_ERR_INVALID_ARG, "B*H"),
+]
+
+
+@pytest.mark.parametrize("kw,status,msg", CASES, ids=[c[2] for c in CASES])
+def test_validation_rejects_before_device_work(lib, kw, status, msg):
+    assert _fwd(lib, **kw) == status
+    assert msg in lib.attn_last_error().decode()
+
+
+def test_host_entry_point_checks_host_pointers(lib):
+    dev = [A, A + MB, A + 2 * MB, A + 3 * MB, A + 4 * MB]
+    host = [A + 10 * MB, A + 11 * MB, A + 12 * MB, A + 13 * MB, A + 14 * MB]
+    for i, name in enumerate(["q_host", "k_host", "v_host", "o_host", "lse_host"]):
+        h = list(host)
+        h[i] = 0
+        st = lib.attn_fwd_host(*h, *dev, 1, 2, 128, 128, 128, 0, 0.125, 1, None)
+        assert st == binding.ATTN_ERR_INVALID_ARG
+        assert name in lib.attn_last_error().decode()
+    d2 = list(dev)
+    d2[1] = A + 64          # k_dev overlapping q_dev
+    st = lib.attn_fwd_host(*host, *d2, 1, 2, 128, 128, 128, 0, 0.125, 1, None)
+    assert st == binding.ATTN_ERR_INVALID_ARG
+
+
+def test_valid_call_without_gpu_reports_cuda_error(lib):
+    """With no usable device, a valid call fails cleanly with ATTN_ERR_CUDA/UNSUPPORTED."""
+    import torch
+    if torch.cuda.is_available():
+        pytest.skip("a GPU is present")
+    st = _fwd(lib)
+    assert st in (binding.ATTN_ERR_CUDA, binding.ATTN_ERR_UNSUPPORTED)
+    assert lib.attn_last_error().decode()
+
+
+def test_python_wrapper_raises_on_bad_input(lib):
+    import torch
+    q = torch.zeros(1, 1, 8, 64, dtype=torch.float32)
+    with pytest.raises(binding.AttnError):
+        binding.fwd(q, q, q)
+    with pytest.raises(binding.AttnError):
+        binding.fwd(q[0], q[0], q[0])
+
+
+def test_missing_library_raises(monkeypatch, tmp_path):
+    monkeypatch.setattr(binding, "_lib", None)
+    monkeypatch.setenv("ATTN_LIBRARY", str(tmp_path / "nope.so"))
+    with pytest.raises(binding.AttnError, match="missing"):
+        binding.load_library()
+    monkeypatch.setattr(binding, "_lib", None)
