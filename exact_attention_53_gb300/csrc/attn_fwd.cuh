@@ -191,9 +191,12 @@ __global__ void __launch_bounds__(FwdTile<D>::THREADS, 1)
 
     if (warp >= T::SOFTMAX_WARPS) {
       if (T::TILES == 2) regs_shrink<T::AUX_REGS>();
-      if (warp == T::PRODUCER_WARP) {
+      // Both aux roles run warp-uniform loops (waits on every lane); only the
+      // TMA / MMA / commit instructions themselves are issued by one lane.
+      if (warp == T::PRODUCER_WARP && n_max > 0) {
         // ------------------------------------------------------------ TMA producer
-        if (lane == 0 && n_max > 0) {
+        const bool leader = elect_one();
+        if (leader) {
             tma_prefetch_desc(&tm_q);
             tma_prefetch_desc(&tm_k);
             tma_prefetch_desc(&tm_v);
@@ -202,170 +205,181 @@ __global__ void __launch_bounds__(FwdTile<D>::THREADS, 1)
                 for (int c = 0; c < T::CHUNKS; ++c)
                     tma_load_3d(sQ + (t * T::CHUNKS + c) * T::Q_CHUNK_BYTES, &tm_q, q_full,
                                 c * 64, q0 + t * T::BM, bh);
-            int idx = 0;
-            bool ok = true;
-            auto issue = [&](const CUtensorMap* map, int j) {
-                if (!ok) return;
-                const int slot = idx % T::NS;
-                ok = mbar_wait(&kv_empty[slot], ((idx / T::NS) & 1) ^ 1, abort_flag, status,
-                               kStatusProducer);
-                if (!ok) return;
+        }
+        __syncwarp();
+        int idx = 0;
+        bool ok = true;
+        auto issue = [&](const CUtensorMap* map, int j) {
+            if (!ok) return;
+            const int slot = idx % T::NS;
+            ok = mbar_wait(&kv_empty[slot], ((idx / T::NS) & 1) ^ 1, abort_flag, status,
+                           kStatusProducer);
+            ok = __all_sync(0xffffffffu, ok);
+            if (!ok) return;
+            if (leader) {
                 mbar_arrive_expect_tx(&kv_full[slot], T::KV_TILE_BYTES);
                 uint8_t* dst = sKV + slot * T::KV_TILE_BYTES;
+#pragma unroll
                 for (int c = 0; c < T::CHUNKS; ++c)
                     tma_load_3d(dst + c * T::KV_CHUNK_BYTES, map, &kv_full[slot], c * 64,
                                 j * T::BN, bh);
-                ++idx;
-            };
-            // Load order is the MMA warp's consumption order.
-            if (T::TILES == 2) {
-                for (int j = 0; j < n_max; ++j) {
-                    issue(&tm_k, j);
-                    issue(&tm_v, j);
-                }
-            } else {
-                issue(&tm_k, 0);
-                if (n_max > 1) issue(&tm_k, 1);
-                for (int j = 0; j < n_max; ++j) {
-                    issue(&tm_v, j);
-                    if (j + 2 < n_max) issue(&tm_k, j + 2);
-                }
             }
-            if (*abort_flag) {
-                // Let every copy this thread started land before the CTA exits.
-                const uint64_t t0 = global_timer_ns();
-                for (int i = max(0, idx - T::NS); i < idx; ++i) {
-                    const uint32_t a = smem_u32(&kv_full[i % T::NS]);
-                    while (!mbar_try_wait(a, (i / T::NS) & 1)) {
-                        if (global_timer_ns() - t0 > kWaitLimitNs) {
-                            atomicOr(status, kStatusDrain);
-                            break;
-                        }
-                    }
-                }
-                const uint32_t a = smem_u32(q_full);
-                while (!mbar_try_wait(a, 0)) {
+            __syncwarp();
+            ++idx;
+        };
+        // Load order is the MMA warp's consumption order.
+        if (T::TILES == 2) {
+            for (int j = 0; j < n_max; ++j) {
+                issue(&tm_k, j);
+                issue(&tm_v, j);
+            }
+        } else {
+            issue(&tm_k, 0);
+            if (n_max > 1) issue(&tm_k, 1);
+            for (int j = 0; j < n_max; ++j) {
+                issue(&tm_v, j);
+                if (j + 2 < n_max) issue(&tm_k, j + 2);
+            }
+        }
+        if (*abort_flag && leader) {
+            // Let every copy this CTA started land before it exits.
+            const uint64_t t0 = global_timer_ns();
+            for (int i = max(0, idx - T::NS); i < idx; ++i) {
+                const uint32_t a = smem_u32(&kv_full[i % T::NS]);
+                while (!mbar_try_wait(a, (i / T::NS) & 1)) {
                     if (global_timer_ns() - t0 > kWaitLimitNs) {
                         atomicOr(status, kStatusDrain);
                         break;
                     }
                 }
             }
-        }
-    } else if (warp == T::MMA_WARP) {
-        // ------------------------------------------------------------ MMA issuer
-        if (lane == 0 && n_max > 0) {
-            constexpr uint32_t id_s = idesc_f16(128, T::BN, BF16, false, false);
-            constexpr uint32_t id_o = idesc_f16(128, D, BF16, false, true);
-            const uint32_t q_base = smem_u32(sQ);
-            const uint32_t kv_base = smem_u32(sKV);
-            bool ok = mbar_wait(q_full, 0, abort_flag, status, kStatusMma);
-            tc_fence_after();
-            int acq = 0;
-            auto acquire = [&](int& slot) {
-                if (!ok) return;
-                slot = acq % T::NS;
-                ok = mbar_wait(&kv_full[slot], (acq / T::NS) & 1, abort_flag, status, kStatusMma);
-                ++acq;
-                tc_fence_after();
-            };
-            auto wait_p = [&](int b, uint32_t parity) {
-                if (!ok) return;
-                ok = mbar_wait(&p_full[b], parity, abort_flag, status, kStatusMma);
-                tc_fence_after();
-            };
-            // S_b = Q_t · K(slot)ᵀ : M = 128, N = BN, K = D in steps of 16
-            auto mma_qk = [&](int t, int slot, int b) {
-                const uint32_t qa = q_base + t * T::Q_TILE_BYTES;
-                const uint32_t ka = kv_base + slot * T::KV_TILE_BYTES;
-#pragma unroll
-                for (int kk = 0; kk < D / 16; ++kk) {
-                    const uint32_t off = (kk >> 2) * T::Q_CHUNK_BYTES + (kk & 3) * 32;
-                    const uint32_t koff = (kk >> 2) * T::KV_CHUNK_BYTES + (kk & 3) * 32;
-                    mma_ss(tmem + b * T::S_STRIDE, sdesc_sw128(qa + off, 16, 1024),
-                           sdesc_sw128(ka + koff, 16, 1024), id_s, kk > 0);
-                }
-            };
-            // O_t (+)= P_b · V(slot) : M = 128, N = D, K = BN in steps of 16
-            auto mma_pv = [&](int t, int slot, int b, bool acc) {
-                const uint32_t va = kv_base + slot * T::KV_TILE_BYTES;
-#pragma unroll
-                for (int kk = 0; kk < T::BN / 16; ++kk) {
-                    mma_ts(tmem + T::O_COL + t * D, tmem + b * T::S_STRIDE + T::P_OFF + kk * 8,
-                           sdesc_sw128(va + kk * 16 * 128, T::KV_CHUNK_BYTES, 1024), id_o,
-                           (acc || kk > 0) ? 1u : 0u);
-                }
-            };
-            if (T::TILES == 2) {
-                const int n0 = n_kv0, n1 = n_kv1;
-                int kslot = 0, vslot = 0;
-                acquire(kslot);
-                if (ok) {
-                    if (n0 > 0) { mma_qk(0, kslot, 0); tc_commit(&s_full[0]); }
-                    if (n1 > 0) { mma_qk(1, kslot, 1); tc_commit(&s_full[1]); }
-                    tc_commit(&kv_empty[kslot]);
-                }
-                for (int j = 0; j < n_max && ok; ++j) {
-                    const bool has_next = j + 1 < n_max;
-                    acquire(vslot);
-                    if (j < n0) {
-                        wait_p(0, j & 1);
-                        if (!ok) break;
-                        mma_pv(0, vslot, 0, j > 0);
-                        if (j == n0 - 1) tc_commit(&o_done[0]);
-                    }
-                    if (has_next) acquire(kslot);
-                    if (!ok) break;
-                    if (j + 1 < n0) { mma_qk(0, kslot, 0); tc_commit(&s_full[0]); }
-                    if (j < n1) {
-                        wait_p(1, j & 1);
-                        if (!ok) break;
-                        mma_pv(1, vslot, 1, j > 0);
-                        if (j == n1 - 1) tc_commit(&o_done[1]);
-                    }
-                    tc_commit(&kv_empty[vslot]);
-                    if (j + 1 < n1) { mma_qk(1, kslot, 1); tc_commit(&s_full[1]); }
-                    if (has_next) tc_commit(&kv_empty[kslot]);
-                }
-            } else {
-                const int n = n_kv0;
-                int slot = 0;
-                acquire(slot);
-                if (ok) { mma_qk(0, slot, 0); tc_commit(&s_full[0]); tc_commit(&kv_empty[slot]); }
-                if (n > 1) {
-                    acquire(slot);
-                    if (ok) { mma_qk(0, slot, 1); tc_commit(&s_full[1]); tc_commit(&kv_empty[slot]); }
-                }
-                for (int j = 0; j < n && ok; ++j) {
-                    const int b = j & 1;
-                    int vslot = 0;
-                    acquire(vslot);
-                    wait_p(b, (j >> 1) & 1);
-                    if (!ok) break;
-                    mma_pv(0, vslot, b, j > 0);
-                    tc_commit(&o_done[0]);
-                    tc_commit(&kv_empty[vslot]);
-                    if (j + 2 < n) {
-                        acquire(slot);
-                        if (!ok) break;
-                        mma_qk(0, slot, b);
-                        tc_commit(&s_full[b]);
-                        tc_commit(&kv_empty[slot]);
-                    }
-                }
-            }
-            // Every MMA of this CTA has finished once `drain` flips.
-            tc_commit(drain);
-            const uint32_t a = smem_u32(drain);
-            const uint64_t t0 = global_timer_ns();
+            const uint32_t a = smem_u32(q_full);
             while (!mbar_try_wait(a, 0)) {
                 if (global_timer_ns() - t0 > kWaitLimitNs) {
                     atomicOr(status, kStatusDrain);
-                    *abort_flag = 1;
                     break;
                 }
             }
         }
+        __syncwarp();
+      } else if (warp == T::MMA_WARP && n_max > 0) {
+        // ------------------------------------------------------------ MMA issuer
+        constexpr uint32_t id_s = idesc_f16(128, T::BN, BF16, false, false);
+        constexpr uint32_t id_o = idesc_f16(128, D, BF16, false, true);
+        const uint32_t q_base = smem_u32(sQ);
+        const uint32_t kv_base = smem_u32(sKV);
+        bool ok = mbar_wait(q_full, 0, abort_flag, status, kStatusMma);
+        ok = __all_sync(0xffffffffu, ok);
+        tc_fence_after();
+        int acq = 0;
+        auto acquire = [&](int& slot) {
+            if (!ok) return;
+            slot = acq % T::NS;
+            ok = mbar_wait(&kv_full[slot], (acq / T::NS) & 1, abort_flag, status, kStatusMma);
+            ok = __all_sync(0xffffffffu, ok);
+            ++acq;
+            tc_fence_after();
+        };
+        auto wait_p = [&](int b, uint32_t parity) {
+            if (!ok) return;
+            ok = mbar_wait(&p_full[b], parity, abort_flag, status, kStatusMma);
+            ok = __all_sync(0xffffffffu, ok);
+            tc_fence_after();
+        };
+        // S_b = Q_t · K(slot)ᵀ : M = 128, N = BN, K = D in steps of 16
+        auto mma_qk = [&](int t, int slot, int b) {
+            const uint32_t qa = q_base + t * T::Q_TILE_BYTES;
+            const uint32_t ka = kv_base + slot * T::KV_TILE_BYTES;
+#pragma unroll
+            for (int kk = 0; kk < D / 16; ++kk) {
+                const uint32_t off = (kk >> 2) * T::Q_CHUNK_BYTES + (kk & 3) * 32;
+                const uint32_t koff = (kk >> 2) * T::KV_CHUNK_BYTES + (kk & 3) * 32;
+                mma_ss_warp(tmem + b * T::S_STRIDE, sdesc_sw128(qa + off, 16, 1024),
+                            sdesc_sw128(ka + koff, 16, 1024), id_s, kk > 0);
+            }
+        };
+        // O_t (+)= P_b · V(slot) : M = 128, N = D, K = BN in steps of 16
+        auto mma_pv = [&](int t, int slot, int b, bool acc) {
+            const uint32_t va = kv_base + slot * T::KV_TILE_BYTES;
+#pragma unroll
+            for (int kk = 0; kk < T::BN / 16; ++kk) {
+                mma_ts_warp(tmem + T::O_COL + t * D, tmem + b * T::S_STRIDE + T::P_OFF + kk * 8,
+                            sdesc_sw128(va + kk * 16 * 128, T::KV_CHUNK_BYTES, 1024), id_o,
+                            (acc || kk > 0) ? 1u : 0u);
+            }
+        };
+        if (T::TILES == 2) {
+            const int n0 = n_kv0, n1 = n_kv1;
+            int kslot = 0, vslot = 0;
+            acquire(kslot);
+            if (ok) {
+                if (n0 > 0) { mma_qk(0, kslot, 0); tc_commit_warp(&s_full[0]); }
+                if (n1 > 0) { mma_qk(1, kslot, 1); tc_commit_warp(&s_full[1]); }
+                tc_commit_warp(&kv_empty[kslot]);
+            }
+            for (int j = 0; j < n_max && ok; ++j) {
+                const bool has_next = j + 1 < n_max;
+                acquire(vslot);
+                if (j < n0) {
+                    wait_p(0, j & 1);
+                    if (!ok) break;
+                    mma_pv(0, vslot, 0, j > 0);
+                    if (j == n0 - 1) tc_commit_warp(&o_done[0]);
+                }
+                if (has_next) acquire(kslot);
+                if (!ok) break;
+                if (j + 1 < n0) { mma_qk(0, kslot, 0); tc_commit_warp(&s_full[0]); }
+                if (j < n1) {
+                    wait_p(1, j & 1);
+                    if (!ok) break;
+                    mma_pv(1, vslot, 1, j > 0);
+                    if (j == n1 - 1) tc_commit_warp(&o_done[1]);
+                }
+                tc_commit_warp(&kv_empty[vslot]);
+                if (j + 1 < n1) { mma_qk(1, kslot, 1); tc_commit_warp(&s_full[1]); }
+                if (has_next) tc_commit_warp(&kv_empty[kslot]);
+            }
+        } else {
+            const int n = n_kv0;
+            int slot = 0;
+            acquire(slot);
+            if (ok) { mma_qk(0, slot, 0); tc_commit_warp(&s_full[0]); tc_commit_warp(&kv_empty[slot]); }
+            if (n > 1) {
+                acquire(slot);
+                if (ok) { mma_qk(0, slot, 1); tc_commit_warp(&s_full[1]); tc_commit_warp(&kv_empty[slot]); }
+            }
+            for (int j = 0; j < n && ok; ++j) {
+                const int b = j & 1;
+                int vslot = 0;
+                acquire(vslot);
+                wait_p(b, (j >> 1) & 1);
+                if (!ok) break;
+                mma_pv(0, vslot, b, j > 0);
+                tc_commit_warp(&o_done[0]);
+                tc_commit_warp(&kv_empty[vslot]);
+                if (j + 2 < n) {
+                    acquire(slot);
+                    if (!ok) break;
+                    mma_qk(0, slot, b);
+                    tc_commit_warp(&s_full[b]);
+                    tc_commit_warp(&kv_empty[slot]);
+                }
+            }
+        }
+        // Every MMA of this CTA has finished once `drain` flips.
+        tc_commit_warp(drain);
+        const uint32_t a = smem_u32(drain);
+        const uint64_t t0 = global_timer_ns();
+        while (!mbar_try_wait(a, 0)) {
+            if (global_timer_ns() - t0 > kWaitLimitNs) {
+                if (elect_one()) {
+                    atomicOr(status, kStatusDrain);
+                    *abort_flag = 1;
+                }
+                break;
+            }
+        }
+        __syncwarp();
       }
       teardown();
     } else {
