@@ -97,6 +97,56 @@ __device__ __forceinline__ int kv_tiles_for(int row_begin, int S_q, int S_k) {
     return n;
 }
 
+// Row maximum of one 128-score row: 8 independent chains of 3-input maxima.
+// MASKED: scores at c >= lim are excluded (they become −∞).  The masked and
+// unmasked forms are separate instantiations so the unmasked path carries no
+// per-element compare/select.
+template <bool MASKED>
+__device__ __forceinline__ float row_max128(float (&s)[128], int lim) {
+    using namespace sm100;
+    if (MASKED) {
+#pragma unroll
+        for (int c = 0; c < 128; ++c) s[c] = c < lim ? s[c] : -INFINITY;
+    }
+    float a[8];
+#pragma unroll
+    for (int i = 0; i < 8; ++i) a[i] = fmaxf(s[2 * i], s[2 * i + 1]);
+#pragma unroll
+    for (int c = 16; c < 128; c += 16)
+#pragma unroll
+        for (int i = 0; i < 8; ++i) a[i] = fmax3(a[i], s[c + i], s[c + 8 + i]);
+    return fmax3(fmax3(a[0], a[1], a[2]), fmax3(a[3], a[4], a[5]), fmaxf(a[6], a[7]));
+}
+
+// p = 2^(s·scale_log2 − m) for one row, packed to 16-bit pairs in `pk`;
+// returns Σ p (fp32).  Two lanes at a time on the packed fp32 pipe.
+// MASKED: p = 0 for c >= lim.
+template <bool MASKED, bool BF16>
+__device__ __forceinline__ float exp_pack128(const float (&s)[128], int lim, float scale_log2,
+                                             float neg_m, uint32_t (&pk)[64]) {
+    using namespace sm100;
+    const float2 sl2 = make_float2(scale_log2, scale_log2);
+    const float2 nm = make_float2(neg_m, neg_m);
+    float2 acc[4] = {make_float2(0.f, 0.f), make_float2(0.f, 0.f), make_float2(0.f, 0.f),
+                     make_float2(0.f, 0.f)};
+#pragma unroll
+    for (int c = 0; c < 128; c += 2) {
+        const float2 x = __ffma2_rn(make_float2(s[c], s[c + 1]), sl2, nm);
+        float p0 = ex2_approx(x.x);
+        float p1 = ex2_approx(x.y);
+        if (MASKED) {
+            p0 = c < lim ? p0 : 0.f;
+            p1 = c + 1 < lim ? p1 : 0.f;
+        }
+        acc[(c >> 1) & 3] = __fadd2_rn(acc[(c >> 1) & 3], make_float2(p0, p1));
+        pk[c >> 1] = BF16 ? pack_bf16(p0, p1) : pack_f16(p0, p1);
+    }
+    const float2 a01 = __fadd2_rn(acc[0], acc[1]);
+    const float2 a23 = __fadd2_rn(acc[2], acc[3]);
+    const float2 t = __fadd2_rn(a01, a23);
+    return t.x + t.y;
+}
+
 template <int D, bool BF16, bool CAUSAL>
 __global__ void __launch_bounds__(FwdTile<D>::THREADS, 1)
     attn_fwd_kernel(const __grid_constant__ CUtensorMap tm_q,
@@ -419,22 +469,7 @@ __global__ void __launch_bounds__(FwdTile<D>::THREADS, 1)
             // keys kv0 + c with c < lim are visible to this row
             const int lim = masked ? max(0, min(S_k, CAUSAL ? q_idx + 1 : S_k) - kv0) : T::BN;
 
-            if (masked) {
-#pragma unroll
-                for (int c = 0; c < 128; ++c) s[c] = c < lim ? s[c] : -INFINITY;
-            }
-            // row maximum: 8 independent chains of 3-input maxima
-            float mx;
-            {
-                float a[8];
-#pragma unroll
-                for (int i = 0; i < 8; ++i) a[i] = fmaxf(s[2 * i], s[2 * i + 1]);
-#pragma unroll
-                for (int c = 16; c < 128; c += 16)
-#pragma unroll
-                    for (int i = 0; i < 8; ++i) a[i] = fmax3(a[i], s[c + i], s[c + 8 + i]);
-                mx = fmax3(fmax3(a[0], a[1], a[2]), fmax3(a[3], a[4], a[5]), fmaxf(a[6], a[7]));
-            }
+            const float mx = masked ? row_max128<true>(s, lim) : row_max128<false>(s, lim);
             const float m_tile = (mx == -INFINITY) ? -INFINITY : mx * scale_log2;
             const float m_new = fmaxf(m, m_tile);
             bool rescale = false;
@@ -449,30 +484,11 @@ __global__ void __launch_bounds__(FwdTile<D>::THREADS, 1)
             }
             const float neg_m = (m == -INFINITY) ? 0.f : -m;
 
-            // p = 2^(s·scale·log2e − m), two lanes at a time on the packed fp32 pipe
             uint32_t pk[64];
-            const float2 sl2 = make_float2(scale_log2, scale_log2);
-            const float2 nm = make_float2(neg_m, neg_m);
-            float2 acc[4] = {make_float2(0.f, 0.f), make_float2(0.f, 0.f), make_float2(0.f, 0.f),
-                             make_float2(0.f, 0.f)};
-#pragma unroll
-            for (int c = 0; c < 128; c += 2) {
-                const float2 x = __ffma2_rn(make_float2(s[c], s[c + 1]), sl2, nm);
-                float p0 = ex2_approx(x.x);
-                float p1 = ex2_approx(x.y);
-                if (masked) {
-                    p0 = c < lim ? p0 : 0.f;
-                    p1 = c + 1 < lim ? p1 : 0.f;
-                }
-                acc[(c >> 1) & 3] = __fadd2_rn(acc[(c >> 1) & 3], make_float2(p0, p1));
-                pk[c >> 1] = BF16 ? pack_bf16(p0, p1) : pack_f16(p0, p1);
-            }
-            {
-                const float2 a01 = __fadd2_rn(acc[0], acc[1]);
-                const float2 a23 = __fadd2_rn(acc[2], acc[3]);
-                const float2 t = __fadd2_rn(a01, a23);
-                l += t.x + t.y;
-            }
+            if (masked)
+                l += exp_pack128<true, BF16>(s, lim, scale_log2, neg_m, pk);
+            else
+                l += exp_pack128<false, BF16>(s, lim, scale_log2, neg_m, pk);
 
             tmem_st32(lane_base + b * T::S_STRIDE + T::P_OFF, pk);
             tmem_st32(lane_base + b * T::S_STRIDE + T::P_OFF + 32, pk + 32);
