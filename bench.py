@@ -105,6 +105,22 @@ class ClockSampler:
                 "sm_max_mhz": max(s[2] for s in win), "reasons": reasons, "samples": len(win)}
 
 
+def max_over_ranks(value: float, world: int, device=None) -> float:
+    """The largest `value` over all ranks (the job time is the slowest rank's)."""
+    if world <= 1:
+        return float(value)
+    import torch
+    t = torch.tensor([float(value)], dtype=torch.float64,
+                     device=device if device is not None else "cpu")
+    torch.distributed.all_reduce(t, op=torch.distributed.ReduceOp.MAX)
+    return float(t.item())
+
+
+def replica_throughput(flops_per_step: float, steps: int, world: int, max_ms: float) -> float:
+    """Whole-job TFLOP/s when every rank runs its own replica of the workload."""
+    return flops_per_step * steps * world / (max_ms * 1e-3) / 1e12
+
+
 def kernel_source_digest() -> str:
     """sha256 over the kernel sources; ties recorded DRAM traffic to the code it was taken on."""
     import hashlib
@@ -265,11 +281,8 @@ def run_gpu(args, rank, world):
     causal_ms = [e[1].elapsed_time(e[2]) for e in ev]
     attn_get_device_status(stream)
 
-    if world > 1:
-        t = torch.tensor([total_ms], device=dev, dtype=torch.float64)
-        torch.distributed.all_reduce(t, op=torch.distributed.ReduceOp.MAX)
-        total_ms = float(t.item())
-    value = flops_step * args.steps * world / (total_ms * 1e-3) / 1e12
+    total_ms = max_over_ranks(total_ms, world, dev)
+    value = replica_throughput(flops_step, args.steps, world, total_ms)
 
     # ---- e2e: host buffers in, host buffers out, through attn_fwd_host
     qp, kp, vp = q_h.pin_memory(), k_h.pin_memory(), v_h.pin_memory()
@@ -294,11 +307,8 @@ def run_gpu(args, rank, world):
     e1.record(stream)
     barrier()
     e2e_ms = e0.elapsed_time(e1)
-    if world > 1:
-        t = torch.tensor([e2e_ms], device=dev, dtype=torch.float64)
-        torch.distributed.all_reduce(t, op=torch.distributed.ReduceOp.MAX)
-        e2e_ms = float(t.item())
-    e2e_value = flops_step * args.steps * world / (e2e_ms * 1e-3) / 1e12
+    e2e_ms = max_over_ranks(e2e_ms, world, dev)
+    e2e_value = replica_throughput(flops_step, args.steps, world, e2e_ms)
     in_bytes = q.numel() * 2 + k.numel() * 2 + v.numel() * 2
     out_bytes = o.numel() * 2 + lse.numel() * 4
     sampler.stop()

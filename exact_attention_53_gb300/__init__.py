@@ -10,6 +10,7 @@ from .binding import (  # noqa: F401
     AttnError,
     attn_fwd,
     attn_fwd_host,
+    attn_fwd_plan,
     attn_get_device_status,
     attn_last_error,
     fwd,

@@ -25,8 +25,18 @@ ATTN_ERR_TIMEOUT = 4
 ATTN_DTYPE_F16 = 0
 ATTN_DTYPE_BF16 = 1
 
-EXPORTED = ("attn_fwd", "attn_fwd_host", "attn_last_error", "attn_get_device_status",
-            "attn_version")
+EXPORTED = ("attn_fwd", "attn_fwd_host", "attn_fwd_plan", "attn_last_error",
+            "attn_get_device_status", "attn_version")
+
+
+class AttnPlan(ctypes.Structure):
+    """Mirror of attn_plan_t (include/attn.h)."""
+    _fields_ = [("block_m", ctypes.c_int64), ("block_n", ctypes.c_int64),
+                ("q_tiles", ctypes.c_int64), ("kv_tiles", ctypes.c_int64),
+                ("q_tiles_per_cta", ctypes.c_int64), ("bh", ctypes.c_int64),
+                ("ctas", ctypes.c_int64), ("threads", ctypes.c_int32),
+                ("smem_bytes", ctypes.c_int32), ("tmem_cols", ctypes.c_int32),
+                ("kv_stages", ctypes.c_int32)]
 
 _DTYPE_CODE = {torch.float16: ATTN_DTYPE_F16, torch.bfloat16: ATTN_DTYPE_BF16}
 
@@ -64,6 +74,8 @@ def load_library() -> ctypes.CDLL:
         lib.attn_fwd_host.argtypes = [vp] * 10 + [i64, i64, i64, i64, i64, i32, ctypes.c_float,
                                                   i32, vp]
         lib.attn_fwd_host.restype = i32
+        lib.attn_fwd_plan.argtypes = [i64, i64, i64, i64, i64, i32, i32, ctypes.POINTER(AttnPlan)]
+        lib.attn_fwd_plan.restype = i32
         lib.attn_last_error.argtypes = []
         lib.attn_last_error.restype = ctypes.c_char_p
         lib.attn_get_device_status.argtypes = [vp]
@@ -108,6 +120,14 @@ def attn_fwd_host(q_host, k_host, v_host, o_host, lse_host, q_dev, k_dev, v_dev,
                              ptr(q_dev), ptr(k_dev), ptr(v_dev), ptr(o_dev), ptr(lse_dev),
                              B, H, S_q, S_k, d, int(causal), float(scale), int(dtype),
                              _stream_handle(stream)))
+
+
+def attn_fwd_plan(B, H, S_q, S_k, d, causal, dtype) -> AttnPlan:
+    """The launch attn_fwd would use (host-only, no device needed)."""
+    plan = AttnPlan()
+    _check(load_library().attn_fwd_plan(B, H, S_q, S_k, d, int(causal), int(dtype),
+                                        ctypes.byref(plan)))
+    return plan
 
 
 def attn_get_device_status(stream=None) -> None:

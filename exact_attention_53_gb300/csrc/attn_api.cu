@@ -180,6 +180,28 @@ attn_status_t encode_rows(CUtensorMap* map, const void* base, const Problem& p, 
     return ATTN_OK;
 }
 
+template <int D>
+void fill_plan_d(const Problem& p, attn_plan_t* out) {
+    using T = attn::FwdTile<D>;
+    out->block_m = T::BM;
+    out->block_n = T::BN;
+    out->q_tiles = (p.S_q + T::BM - 1) / T::BM;
+    out->kv_tiles = (p.S_k + T::BN - 1) / T::BN;
+    out->q_tiles_per_cta = T::TILES;
+    out->bh = p.B * p.H;
+    out->ctas = out->bh * ((out->q_tiles + T::TILES - 1) / T::TILES);
+    out->threads = T::THREADS;
+    out->smem_bytes = T::SMEM_BYTES;
+    out->tmem_cols = static_cast<int32_t>(T::TMEM_COLS);
+    out->kv_stages = T::NS;
+}
+
+void fill_plan(const Problem& p, attn_plan_t* out) {
+    if (p.d == 64) fill_plan_d<64>(p, out);
+    else if (p.d == 128) fill_plan_d<128>(p, out);
+    else fill_plan_d<256>(p, out);
+}
+
 using LaunchFn = cudaError_t (*)(const attn::FwdArgs&, cudaStream_t);
 
 LaunchFn pick(int64_t d, bool bf16, bool causal) {
@@ -262,6 +284,16 @@ attn_status_t attn_fwd_host(const void* q_host, const void* k_host, const void* 
     if ((e = cudaMemcpyAsync(o_host, o_dev, p.o_bytes, cudaMemcpyDeviceToHost, stream)) != cudaSuccess ||
         (e = cudaMemcpyAsync(lse_host, lse_dev, p.lse_bytes, cudaMemcpyDeviceToHost, stream)) != cudaSuccess)
         return fail(ATTN_ERR_CUDA, "device-to-host copy: %s", cudaGetErrorString(e));
+    return ok();
+}
+
+attn_status_t attn_fwd_plan(int64_t B, int64_t H, int64_t S_q, int64_t S_k, int64_t d, int causal,
+                            attn_dtype_t dtype, attn_plan_t* plan) {
+    if (!plan) return fail(ATTN_ERR_INVALID_ARG, "plan is null");
+    Problem p;
+    attn_status_t s = validate_sizes(p, B, H, S_q, S_k, d, causal, 1.0f, dtype);
+    if (s != ATTN_OK) return s;
+    fill_plan(p, plan);
     return ok();
 }
 

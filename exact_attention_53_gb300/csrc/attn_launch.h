@@ -30,6 +30,44 @@ constexpr int kBlockN = 128;
 // tensor memory.
 __host__ __device__ constexpr int q_tiles_per_cta(int d) { return d == 256 ? 1 : 2; }
 
+// Static plan of one kernel instantiation: tiles, warp roles, shared and
+// tensor memory.  Shared by the kernel and the host (attn_fwd_plan).
+template <int D>
+struct FwdTile {
+    static constexpr int BM = kBlockM;
+    static constexpr int BN = kBlockN;
+    static constexpr int TILES = q_tiles_per_cta(D);
+    static constexpr int CHUNKS = D / 64;                 // 128-byte swizzle atoms along d
+    static constexpr int ATOM_ROWS_BYTES = 128;           // one row of one atom
+    static constexpr int Q_CHUNK_BYTES = BM * ATOM_ROWS_BYTES;
+    static constexpr int KV_CHUNK_BYTES = BN * ATOM_ROWS_BYTES;
+    static constexpr int Q_TILE_BYTES = BM * D * 2;
+    static constexpr int KV_TILE_BYTES = BN * D * 2;
+    static constexpr int NS = D == 64 ? 8 : (D == 128 ? 4 : 2);
+    static constexpr int TILE_BYTES = TILES * Q_TILE_BYTES + NS * KV_TILE_BYTES;
+    static constexpr int NUM_BARS = 1 + 2 * NS + 2 + 2 + 2 + 1;
+    static constexpr int SMEM_BYTES = 1024 + TILE_BYTES + NUM_BARS * 8 + 16;
+    static constexpr int SOFTMAX_WARPS = 4 * TILES;
+    static constexpr int PRODUCER_WARP = SOFTMAX_WARPS;       // first warp of the aux warpgroup
+    static constexpr int MMA_WARP = SOFTMAX_WARPS + 1;
+    static constexpr int THREADS = 32 * (SOFTMAX_WARPS + 4);  // + one aux warpgroup
+    // Register split (TILES == 2): 12 warps put 3 on each SM sub-partition, so
+    // the launch gets 168 registers a thread (16384 / 3 warps / 32, rounded to
+    // 8).  The aux warpgroup gives most of its share to the softmax ones:
+    // 2·216 + 72 = 3·168 (72 is the least the aux roles need without spills).
+    static constexpr int LAUNCH_REGS = 168;
+    static constexpr int SOFTMAX_REGS = 216;
+    static constexpr int AUX_REGS = 72;
+    static_assert(TILES == 1 || 2 * SOFTMAX_REGS + AUX_REGS <= 3 * LAUNCH_REGS, "register split");
+    // tensor memory columns: S buffers 0 and 1, then one O accumulator per tile
+    static constexpr uint32_t TMEM_COLS = 512;
+    static constexpr uint32_t S_STRIDE = 128;             // S buffer b at column b * 128
+    static constexpr uint32_t P_OFF = 64;                 // P (16-bit, packed) over S cols 64..127
+    static constexpr uint32_t O_COL = 256;
+    static_assert(SMEM_BYTES <= 232448, "shared memory budget");
+    static_assert(O_COL + TILES * D <= TMEM_COLS, "tensor memory budget");
+};
+
 template <int D, bool BF16, bool CAUSAL>
 cudaError_t launch_attn_fwd(const FwdArgs& args, cudaStream_t stream);
 

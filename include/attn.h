@@ -54,6 +54,34 @@ typedef enum {
 } attn_status_t;
 
 /*
+ * attn_plan_t — how attn_fwd would launch a problem (see attn_fwd_plan).
+ * The page's plan object (FlashAttention3Plan::launch_params and
+ * ::shared_memory_bytes) reports the same kind of figures for its design.
+ */
+typedef struct {
+    int64_t block_m;          /* query rows per tile (128) */
+    int64_t block_n;          /* keys per key/value tile (128) */
+    int64_t q_tiles;          /* ceil(S_q / block_m): query tiles per (b, h) */
+    int64_t kv_tiles;         /* ceil(S_k / block_n): key tiles per (b, h) */
+    int64_t q_tiles_per_cta;  /* 2 for d <= 128 (ping-pong), 1 for d = 256 */
+    int64_t bh;               /* B·H */
+    int64_t ctas;             /* grid size: bh · ceil(q_tiles / q_tiles_per_cta) */
+    int32_t threads;          /* threads per CTA */
+    int32_t smem_bytes;       /* dynamic shared memory per CTA */
+    int32_t tmem_cols;        /* tensor-memory columns allocated per CTA */
+    int32_t kv_stages;        /* slots in the K/V shared-memory ring */
+} attn_plan_t;
+
+/*
+ * attn_fwd_plan — fill *plan with the launch attn_fwd would use for these
+ * sizes.  Host-only: validates the same size/dtype/scale-free arguments as
+ * attn_fwd (same statuses and messages) and touches no device.  plan must
+ * be non-null.
+ */
+attn_status_t attn_fwd_plan(int64_t B, int64_t H, int64_t S_q, int64_t S_k, int64_t d, int causal,
+                            attn_dtype_t dtype, attn_plan_t* plan);
+
+/*
  * attn_fwd — enqueue the attention forward on `stream`.
  *
  *   q, k, v  device pointers, 16-byte aligned, element type `dtype`:
@@ -61,7 +89,7 @@ typedef enum {
  *   o        device pointer, 16-byte aligned, [B,H,S_q,d] in `dtype`; written
  *   lse      device pointer, 4-byte aligned, [B,H,S_q] fp32; written
  *   B, H     batch and heads, >= 1, B·H <= 2^31 − 1
- *   S_q, S_k query and key lengths, 1 .. 2^24 (need not be tile multiples)
+ *   S_q, S_k query and key lengths, 1 .. 2^22 (need not be tile multiples)
  *   d        head dimension: 64, 128 or 256
  *   causal   0 or 1; 1 masks key j for query i when j > i (top-left)
  *   scale    multiplier of Q·Kᵀ, finite and >= 0 (1/sqrt(d) is the usual)

@@ -36,7 +36,7 @@ def _declared_functions():
 
 def test_header_declares_the_boundary():
     names = _declared_functions()
-    assert names == sorted(["attn_fwd", "attn_fwd_host", "attn_last_error",
+    assert names == sorted(["attn_fwd", "attn_fwd_host", "attn_fwd_plan", "attn_last_error",
                             "attn_get_device_status", "attn_version"])
 
 
@@ -129,3 +129,47 @@ def test_missing_library_raises(monkeypatch, tmp_path):
     with pytest.raises(binding.AttnError, match="missing"):
         binding.load_library()
     monkeypatch.setattr(binding, "_lib", None)
+
+
+GOLDEN = os.path.join(ROOT, "tests", "golden", "launch_grid_cases.txt")
+
+
+def _golden_rows():
+    rows = []
+    for line in open(GOLDEN):
+        line = line.strip()
+        if line and not line.startswith("#"):
+            rows.append(tuple(int(x) for x in line.split()))
+    return rows
+
+
+@pytest.mark.parametrize("row", _golden_rows(), ids=lambda r: "x".join(map(str, r)))
+def test_plan_matches_page_launch_grid(lib, row):
+    """The query-tile count and head count agree with the page's launch_params cases."""
+    S_q, S_k, B, H, q_tiles, bh = row
+    for d in (64, 128):
+        plan = binding.attn_fwd_plan(B, H, S_q, S_k, d, 0, binding.ATTN_DTYPE_F16)
+        assert plan.block_m == 128
+        assert plan.q_tiles == q_tiles
+        assert plan.bh == bh
+        assert plan.ctas == bh * -(-q_tiles // plan.q_tiles_per_cta)
+
+
+def test_plan_resources_fit_the_sm():
+    build()
+    for d in (64, 128, 256):
+        for causal in (0, 1):
+            p = binding.attn_fwd_plan(2, 3, 1000, 700, d, causal, binding.ATTN_DTYPE_BF16)
+            assert p.smem_bytes <= 232448
+            assert p.tmem_cols <= 512
+            assert p.threads % 128 == 0
+            assert p.kv_tiles == 6 and p.q_tiles == 8
+            assert p.q_tiles_per_cta == (1 if d == 256 else 2)
+
+
+def test_plan_validates_like_fwd(lib):
+    with pytest.raises(binding.AttnError, match="head_dim"):
+        binding.attn_fwd_plan(1, 1, 16, 16, 80, 0, binding.ATTN_DTYPE_BF16)
+    with pytest.raises(binding.AttnError, match="S_q must be"):
+        binding.attn_fwd_plan(1, 1, 0, 16, 64, 0, binding.ATTN_DTYPE_BF16)
+    assert lib.attn_fwd_plan(1, 1, 16, 16, 64, 0, 1, None) == binding.ATTN_ERR_INVALID_ARG
