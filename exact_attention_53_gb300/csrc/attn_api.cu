@@ -228,6 +228,7 @@ attn_status_t launch_checked(const Problem& p, const void* q, const void* k, con
     if ((s = encode_rows(&a.tm_q, q, p, p.S_q, "q")) != ATTN_OK) return s;
     if ((s = encode_rows(&a.tm_k, k, p, p.S_k, "k")) != ATTN_OK) return s;
     if ((s = encode_rows(&a.tm_v, v, p, p.S_k, "v")) != ATTN_OK) return s;
+    if ((s = encode_rows(&a.tm_o, o, p, p.S_q, "o")) != ATTN_OK) return s;
     a.o = o;
     a.lse = lse;
     a.S_q = static_cast<int32_t>(p.S_q);

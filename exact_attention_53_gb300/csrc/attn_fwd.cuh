@@ -85,15 +85,18 @@ __device__ __forceinline__ float row_max128(float (&s)[128], int lim) {
 
 // p = 2^(s·scale_log2 − m) for one row, packed to 16-bit pairs in `pk`;
 // returns Σ p (fp32).  Two lanes at a time on the packed fp32 pipe.
-// MASKED: p = 0 for c >= lim.
-template <bool MASKED, bool BF16>
+// MASKED: p = 0 for c >= lim.  TRACK: also returns in *xmax the largest
+// exponent s·scale_log2 − m over the visible keys (a maximum taken alongside
+// the exponentials, on another pipe).
+template <bool MASKED, bool BF16, bool TRACK>
 __device__ __forceinline__ float exp_pack128(const float (&s)[128], int lim, float scale_log2,
-                                             float neg_m, uint32_t (&pk)[64]) {
+                                             float neg_m, uint32_t (&pk)[64], float* xmax) {
     using namespace sm100;
     const float2 sl2 = make_float2(scale_log2, scale_log2);
     const float2 nm = make_float2(neg_m, neg_m);
     float2 acc[4] = {make_float2(0.f, 0.f), make_float2(0.f, 0.f), make_float2(0.f, 0.f),
                      make_float2(0.f, 0.f)};
+    float mx[4] = {-INFINITY, -INFINITY, -INFINITY, -INFINITY};
 #pragma unroll
     for (int c = 0; c < 128; c += 2) {
         const float2 x = __ffma2_rn(make_float2(s[c], s[c + 1]), sl2, nm);
@@ -103,9 +106,18 @@ __device__ __forceinline__ float exp_pack128(const float (&s)[128], int lim, flo
             p0 = c < lim ? p0 : 0.f;
             p1 = c + 1 < lim ? p1 : 0.f;
         }
+        if (TRACK) {
+            if (MASKED) {
+                mx[(c >> 1) & 3] = fmax3(mx[(c >> 1) & 3], c < lim ? x.x : -INFINITY,
+                                         c + 1 < lim ? x.y : -INFINITY);
+            } else {
+                mx[(c >> 1) & 3] = fmax3(mx[(c >> 1) & 3], x.x, x.y);
+            }
+        }
         acc[(c >> 1) & 3] = __fadd2_rn(acc[(c >> 1) & 3], make_float2(p0, p1));
         pk[c >> 1] = BF16 ? pack_bf16(p0, p1) : pack_f16(p0, p1);
     }
+    if (TRACK) *xmax = fmaxf(fmax3(mx[0], mx[1], mx[2]), mx[3]);
     const float2 a01 = __fadd2_rn(acc[0], acc[1]);
     const float2 a23 = __fadd2_rn(acc[2], acc[3]);
     const float2 t = __fadd2_rn(a01, a23);
@@ -116,7 +128,8 @@ template <int D, bool BF16, bool CAUSAL>
 __global__ void __launch_bounds__(FwdTile<D>::THREADS, 1)
     attn_fwd_kernel(const __grid_constant__ CUtensorMap tm_q,
                     const __grid_constant__ CUtensorMap tm_k,
-                    const __grid_constant__ CUtensorMap tm_v, void* __restrict__ o_ptr,
+                    const __grid_constant__ CUtensorMap tm_v,
+                    const __grid_constant__ CUtensorMap tm_o,
                     float* __restrict__ lse_ptr, int S_q, int S_k, int BH, int n_qblk,
                     int head_group, float scale_log2, unsigned int* __restrict__ status) {
     using T = FwdTile<D>;
@@ -132,10 +145,11 @@ __global__ void __launch_bounds__(FwdTile<D>::THREADS, 1)
     uint64_t* kv_full = bars + 1;
     uint64_t* kv_empty = kv_full + T::NS;
     uint64_t* s_full = kv_empty + T::NS;      // [2] S buffer b written
-    uint64_t* p_full = s_full + 2;            // [2] P in buffer b written (+ O rescaled)
+    uint64_t* p_full = s_full + 2;            // [2] P in buffer b written (+ O rescaled), per warp
     uint64_t* o_done = p_full + 2;            // [2] PV MMAs of tile t finished
     uint64_t* drain = o_done + 2;             // every MMA of the CTA finished
-    uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(drain + 1);
+    uint64_t* epi_bar = drain + 1;            // [2] O tile t staged in shared memory (per warp)
+    uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(epi_bar + 2);
     volatile int* abort_flag = reinterpret_cast<volatile int*>(tmem_slot + 1);
 
     const int warp = threadIdx.x >> 5;
@@ -176,10 +190,12 @@ __global__ void __launch_bounds__(FwdTile<D>::THREADS, 1)
         }
         for (int b = 0; b < 2; ++b) {
             mbar_init(&s_full[b], 1);
-            mbar_init(&p_full[b], 128);
+            mbar_init(&p_full[b], 4);           // one arrival per softmax warp
             mbar_init(&o_done[b], 1);
         }
         mbar_init(drain, 1);
+        mbar_init(&epi_bar[0], 4);
+        mbar_init(&epi_bar[1], 4);
         *abort_flag = 0;
         fence_mbar_init();
         asm volatile("fence.proxy.async.shared::cta;" ::: "memory");
@@ -302,24 +318,38 @@ __global__ void __launch_bounds__(FwdTile<D>::THREADS, 1)
             tc_fence_after();
         };
         // S_b = Q_t · K(slot)ᵀ : M = 128, N = BN, K = D in steps of 16
+        // Descriptors are built once; a K step moves the start address, which
+        // lives in the low 14 bits of the low word (addr >> 4, < 2^14 for any
+        // shared-memory address), so stepping is a 32-bit add without carries.
+        const uint64_t qk_desc = sdesc_sw128(q_base, 16, 1024);
+        const uint64_t kk_desc = sdesc_sw128(kv_base, 16, 1024);
+        const uint64_t v_desc = sdesc_sw128(kv_base, T::KV_CHUNK_BYTES, 1024);
+        const uint32_t q_lo = static_cast<uint32_t>(qk_desc);
+        const uint32_t q_hi = static_cast<uint32_t>(qk_desc >> 32);
+        const uint32_t k_lo = static_cast<uint32_t>(kk_desc);
+        const uint32_t k_hi = static_cast<uint32_t>(kk_desc >> 32);
+        const uint32_t v_lo = static_cast<uint32_t>(v_desc);
+        const uint32_t v_hi = static_cast<uint32_t>(v_desc >> 32);
+        // S_b = Q_t · K(slot)ᵀ : M = 128, N = BN, K = D in steps of 16
         auto mma_qk = [&](int t, int slot, int b) {
-            const uint32_t qa = q_base + t * T::Q_TILE_BYTES;
-            const uint32_t ka = kv_base + slot * T::KV_TILE_BYTES;
+            const uint32_t qa = q_lo + ((t * T::Q_TILE_BYTES) >> 4);
+            const uint32_t ka = k_lo + ((slot * T::KV_TILE_BYTES) >> 4);
 #pragma unroll
             for (int kk = 0; kk < D / 16; ++kk) {
-                const uint32_t off = (kk >> 2) * T::Q_CHUNK_BYTES + (kk & 3) * 32;
-                const uint32_t koff = (kk >> 2) * T::KV_CHUNK_BYTES + (kk & 3) * 32;
-                mma_ss_warp(tmem + b * T::S_STRIDE, sdesc_sw128(qa + off, 16, 1024),
-                            sdesc_sw128(ka + koff, 16, 1024), id_s, kk > 0);
+                const uint32_t off = ((kk >> 2) * T::Q_CHUNK_BYTES + (kk & 3) * 32) >> 4;
+                const uint32_t koff = ((kk >> 2) * T::KV_CHUNK_BYTES + (kk & 3) * 32) >> 4;
+                mma_ss_warp(tmem + b * T::S_STRIDE, qa + off, q_hi, ka + koff, k_hi, id_s,
+                            kk > 0 ? 1u : 0u);
             }
         };
         // O_t (+)= P_b · V(slot) : M = 128, N = D, K = BN in steps of 16
         auto mma_pv = [&](int t, int slot, int b, bool acc) {
-            const uint32_t va = kv_base + slot * T::KV_TILE_BYTES;
+            const uint32_t va = v_lo + ((slot * T::KV_TILE_BYTES) >> 4);
+            const uint32_t pa = tmem + b * T::S_STRIDE + T::P_OFF;
+            const uint32_t oa = tmem + T::O_COL + t * D;
 #pragma unroll
             for (int kk = 0; kk < T::BN / 16; ++kk) {
-                mma_ts_warp(tmem + T::O_COL + t * D, tmem + b * T::S_STRIDE + T::P_OFF + kk * 8,
-                            sdesc_sw128(va + kk * 16 * 128, T::KV_CHUNK_BYTES, 1024), id_o,
+                mma_ts_warp(oa, pa + kk * 8, va + ((kk * 16 * 128) >> 4), v_hi, id_o,
                             (acc || kk > 0) ? 1u : 0u);
             }
         };
@@ -434,26 +464,49 @@ __global__ void __launch_bounds__(FwdTile<D>::THREADS, 1)
             // keys kv0 + c with c < lim are visible to this row
             const int lim = masked ? max(0, min(S_k, CAUSAL ? q_idx + 1 : S_k) - kv0) : T::BN;
 
-            const float mx = masked ? row_max128<true>(s, lim) : row_max128<false>(s, lim);
-            const float m_tile = (mx == -INFINITY) ? -INFINITY : mx * scale_log2;
-            const float m_new = fmaxf(m, m_tile);
+            uint32_t pk[64];
             bool rescale = false;
             float alpha = 1.f;
             if (m == -INFINITY) {
-                m = m_new;                             // nothing accumulated yet
-            } else if (m_new - m > kRescaleLog2) {
-                alpha = ex2_approx(m - m_new);
-                m = m_new;
-                l *= alpha;
-                rescale = true;
+                // First visible tile of this row: the maximum has to come first.
+                const float mx = masked ? row_max128<true>(s, lim) : row_max128<false>(s, lim);
+                m = (mx == -INFINITY) ? -INFINITY : mx * scale_log2;
+                const float neg_m = (m == -INFINITY) ? 0.f : -m;
+                l = masked ? exp_pack128<true, BF16, false>(s, lim, scale_log2, neg_m, pk, nullptr)
+                           : exp_pack128<false, BF16, false>(s, lim, scale_log2, neg_m, pk, nullptr);
+            } else {
+                // Exponentiate against the running maximum and take this tile's
+                // maximum exponent alongside.  A row whose maximum grew by more
+                // than 2^kRescaleLog2 (rare) re-reads its scores from TMEM (P has
+                // not been written over them yet) and is redone against the new
+                // maximum, so the result equals the max-first order exactly.
+                float xmax;
+                float lsum = masked
+                    ? exp_pack128<true, BF16, true>(s, lim, scale_log2, -m, pk, &xmax)
+                    : exp_pack128<false, BF16, true>(s, lim, scale_log2, -m, pk, &xmax);
+                if (__any_sync(0xffffffffu, xmax > kRescaleLog2)) {
+                    uint32_t ra[64], rb[64];
+                    tmem_ld64(lane_base + b * T::S_STRIDE, ra);
+                    tmem_ld64(lane_base + b * T::S_STRIDE + 64, rb);
+                    if (xmax > kRescaleLog2) {
+#pragma unroll
+                        for (int c = 0; c < 64; ++c) {
+                            s[c] = __uint_as_float(ra[c]);
+                            s[64 + c] = __uint_as_float(rb[c]);
+                        }
+                        const float mx = masked ? row_max128<true>(s, lim) : row_max128<false>(s, lim);
+                        const float m_tile = mx * scale_log2;
+                        alpha = ex2_approx(m - m_tile);
+                        m = m_tile;
+                        l *= alpha;
+                        rescale = true;
+                        lsum = masked
+                            ? exp_pack128<true, BF16, false>(s, lim, scale_log2, -m, pk, nullptr)
+                            : exp_pack128<false, BF16, false>(s, lim, scale_log2, -m, pk, nullptr);
+                    }
+                }
+                l += lsum;
             }
-            const float neg_m = (m == -INFINITY) ? 0.f : -m;
-
-            uint32_t pk[64];
-            if (masked)
-                l += exp_pack128<true, BF16>(s, lim, scale_log2, neg_m, pk);
-            else
-                l += exp_pack128<false, BF16>(s, lim, scale_log2, neg_m, pk);
 
             tmem_st32(lane_base + b * T::S_STRIDE + T::P_OFF, pk);
             tmem_st32(lane_base + b * T::S_STRIDE + T::P_OFF + 32, pk + 32);
@@ -476,9 +529,12 @@ __global__ void __launch_bounds__(FwdTile<D>::THREADS, 1)
                     tmem_st32(o_base + cc, r);
                 }
             }
+            // Each lane's TMEM stores are complete (wait::st) and fenced; after the
+            // warp converges one lane publishes them for the whole warp.
             tmem_st_wait();
             tc_fence_before();
-            mbar_arrive(&p_full[b]);
+            __syncwarp();
+            if (lane == 0) mbar_arrive(&p_full[b]);
         }
 
         if (ok && n > 0) {
@@ -488,10 +544,11 @@ __global__ void __launch_bounds__(FwdTile<D>::THREADS, 1)
             ok = __all_sync(0xffffffffu, ok);
             if (ok) {
                 tc_fence_after();
+                // O / l in the output dtype, staged through this tile's Q area
+                // (its last Q·Kᵀ finished before the last P·V) in the 128-byte
+                // swizzled layout the O tensor map stores from.
                 const float inv_l = 1.f / l;
-                const bool store = q_idx < S_q;
-                const size_t row_off = (static_cast<size_t>(bh) * S_q + q_idx);
-                uint4* dst = reinterpret_cast<uint4*>(static_cast<uint16_t*>(o_ptr) + row_off * D);
+                uint8_t* sO = sQ + t * T::Q_TILE_BYTES;
                 const uint32_t o_base = lane_base + T::O_COL + t * D;
 #pragma unroll 1
                 for (int cc = 0; cc < D; cc += 32) {
@@ -504,14 +561,32 @@ __global__ void __launch_bounds__(FwdTile<D>::THREADS, 1)
                         const float c = __uint_as_float(r[2 * i + 1]) * inv_l;
                         w[i] = BF16 ? pack_bf16(a, c) : pack_f16(a, c);
                     }
-                    if (store) {
+                    uint8_t* rowp = sO + (cc / 64) * T::Q_CHUNK_BYTES + row * 128;
 #pragma unroll
-                        for (int i = 0; i < 4; ++i)
-                            dst[cc / 8 + i] = make_uint4(w[4 * i], w[4 * i + 1], w[4 * i + 2],
-                                                         w[4 * i + 3]);
+                    for (int i = 0; i < 4; ++i) {
+                        const int unit = ((cc & 63) / 8) + i;          // 16-byte unit in the row
+                        *reinterpret_cast<uint4*>(rowp + ((unit ^ (row & 7)) * 16)) =
+                            make_uint4(w[4 * i], w[4 * i + 1], w[4 * i + 2], w[4 * i + 3]);
                     }
                 }
-                if (store) lse_ptr[row_off] = (m + log2f(l)) * kLn2;
+                // Every warp publishes its rows; the first warp's leader stores
+                // the tile once all four have (a bounded wait, like every other).
+                fence_proxy_async_smem();
+                __syncwarp();
+                if (lane == 0) mbar_arrive(&epi_bar[t]);
+                if (wq == 0) {
+                    bool staged = mbar_wait(&epi_bar[t], 0, abort_flag, status, kStatusEpilogue);
+                    staged = __all_sync(0xffffffffu, staged);
+                    if (staged && elect_one()) {
+                        for (int c = 0; c < T::CHUNKS; ++c)
+                            tma_store_3d(&tm_o, sO + c * T::Q_CHUNK_BYTES, c * 64, row_begin, bh);
+                        bulk_commit_group();
+                        bulk_wait_all();
+                    }
+                    __syncwarp();
+                }
+                if (q_idx < S_q)
+                    lse_ptr[static_cast<size_t>(bh) * S_q + q_idx] = (m + log2f(l)) * kLn2;
             }
         }
         teardown();
@@ -544,7 +619,7 @@ cudaError_t launch_attn_fwd(const FwdArgs& a, cudaStream_t stream) {
     const long long blocks = static_cast<long long>(a.BH) * n_qblk;
     if (blocks > 0x7fffffffLL) return cudaErrorInvalidConfiguration;
     dim3 grid(static_cast<unsigned>(blocks), 1, 1);
-    kernel<<<grid, T::THREADS, T::SMEM_BYTES, stream>>>(a.tm_q, a.tm_k, a.tm_v, a.o, a.lse, a.S_q,
+    kernel<<<grid, T::THREADS, T::SMEM_BYTES, stream>>>(a.tm_q, a.tm_k, a.tm_v, a.tm_o, a.lse, a.S_q,
                                                          a.S_k, a.BH, n_qblk, head_group,
                                                          a.scale_log2, a.status);
     return cudaGetLastError();

@@ -12,6 +12,7 @@ struct FwdArgs {
     CUtensorMap tm_q;       // [B·H, S_q, d] rows of Q, box 64 × 128
     CUtensorMap tm_k;       // [B·H, S_k, d] rows of K, box 64 × 128
     CUtensorMap tm_v;       // [B·H, S_k, d] rows of V, box 64 × 128
+    CUtensorMap tm_o;       // [B·H, S_q, d] rows of O, box 64 × 128 (stores)
     void* o;                // [B, H, S_q, d], same dtype as Q
     float* lse;             // [B, H, S_q] fp32, natural log
     int32_t S_q;
@@ -45,7 +46,7 @@ struct FwdTile {
     static constexpr int KV_TILE_BYTES = BN * D * 2;
     static constexpr int NS = D == 64 ? 8 : (D == 128 ? 4 : 2);
     static constexpr int TILE_BYTES = TILES * Q_TILE_BYTES + NS * KV_TILE_BYTES;
-    static constexpr int NUM_BARS = 1 + 2 * NS + 2 + 2 + 2 + 1;
+    static constexpr int NUM_BARS = 1 + 2 * NS + 2 + 2 + 2 + 1 + 2;
     static constexpr int SMEM_BYTES = 1024 + TILE_BYTES + NUM_BARS * 8 + 16;
     static constexpr int SOFTMAX_WARPS = 4 * TILES;
     static constexpr int PRODUCER_WARP = SOFTMAX_WARPS;       // first warp of the aux warpgroup
