@@ -43,6 +43,7 @@ __device__ unsigned int g_attn_status;
 
 std::atomic<int> g_device_checked[kMaxDevices];          // 0 unknown, 1 ok, 2 unsupported
 std::atomic<unsigned int*> g_status_ptr[kMaxDevices];
+std::atomic<int> g_num_sms[kMaxDevices];
 
 PFN_cuTensorMapEncodeTiled_v12000 encode_fn() {
     static PFN_cuTensorMapEncodeTiled_v12000 fn = nullptr;
@@ -142,6 +143,10 @@ attn_status_t check_device(int* dev_out) {
         e = cudaDeviceGetAttribute(&major, cudaDevAttrComputeCapabilityMajor, dev);
         if (e == cudaSuccess) e = cudaDeviceGetAttribute(&minor, cudaDevAttrComputeCapabilityMinor, dev);
         if (e != cudaSuccess) return fail(ATTN_ERR_CUDA, "cudaDeviceGetAttribute: %s", cudaGetErrorString(e));
+        int sms = 0;
+        e = cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev);
+        if (e != cudaSuccess) return fail(ATTN_ERR_CUDA, "cudaDeviceGetAttribute: %s", cudaGetErrorString(e));
+        g_num_sms[dev].store(sms);
         state = (major == 10 && minor == 3) ? 1 : 2;
         g_device_checked[dev].store(state, std::memory_order_release);
         if (state == 1) {
@@ -236,6 +241,7 @@ attn_status_t launch_checked(const Problem& p, const void* q, const void* k, con
     a.BH = static_cast<int32_t>(p.B * p.H);
     a.scale_log2 = static_cast<float>(static_cast<double>(p.scale) * 1.4426950408889634);
     a.status = g_status_ptr[dev].load();
+    a.num_sms = g_num_sms[dev].load();
     LaunchFn fn = pick(p.d, p.dtype == ATTN_DTYPE_BF16, p.causal);
     if (!fn) return fail(ATTN_ERR_UNSUPPORTED, "no kernel for d=%lld", (long long)p.d);
     cudaError_t e = fn(a, stream);

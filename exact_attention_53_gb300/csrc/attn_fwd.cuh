@@ -124,6 +124,35 @@ __device__ __forceinline__ float exp_pack128(const float (&s)[128], int lim, flo
     return t.x + t.y;
 }
 
+// Work unit L (one (batch·head, query block)) -> head and first query row.
+// Full attention: the query blocks of one head are adjacent, so the units in
+// flight at a time share a few heads' K/V in L2.  Causal: heads go in groups
+// of `head_group` (sized so a group's K/V fits in L2) and within a group the
+// heaviest query blocks of all its heads go first, which keeps the tail short.
+template <bool CAUSAL, int ROWS_PER_UNIT>
+__device__ __forceinline__ void unit_coords(int L, int BH, int n_qblk, int head_group, int& bh,
+                                            int& q0) {
+    int qblk;
+    if (CAUSAL) {
+        const int per_group = head_group * n_qblk;
+        const int g = L / per_group;
+        const int r = L - g * per_group;
+        const int g0 = g * head_group;
+        const int gsz = min(head_group, BH - g0);
+        const int qi = r / gsz;
+        bh = g0 + (r - qi * gsz);
+        qblk = n_qblk - 1 - qi;
+    } else {
+        bh = L / n_qblk;
+        qblk = L - bh * n_qblk;
+    }
+    q0 = qblk * ROWS_PER_UNIT;
+}
+
+// Persistent kernel: CTA c processes units c, c + gridDim.x, ...  Every
+// mbarrier phase and the K/V ring position carry over from one unit to the
+// next, so the next unit's Q load and first Q·Kᵀ overlap the current unit's
+// last P·V and epilogue.
 template <int D, bool BF16, bool CAUSAL>
 __global__ void __launch_bounds__(FwdTile<D>::THREADS, 1)
     attn_fwd_kernel(const __grid_constant__ CUtensorMap tm_q,
@@ -134,56 +163,43 @@ __global__ void __launch_bounds__(FwdTile<D>::THREADS, 1)
                     int head_group, float scale_log2, unsigned int* __restrict__ status) {
     using T = FwdTile<D>;
     using namespace sm100;
+    constexpr int ROWS = T::BM * T::TILES;                 // query rows per unit
 
     extern __shared__ uint8_t smem_raw[];
     const uint32_t raw_addr = smem_u32(smem_raw);
     uint8_t* smem = smem_raw + ((1024u - (raw_addr & 1023u)) & 1023u);
     uint8_t* sQ = smem;
-    uint8_t* sKV = smem + T::TILES * T::Q_TILE_BYTES;
+    uint8_t* sKV = sQ + T::TILES * T::Q_TILE_BYTES;
+    uint8_t* sO = sKV + T::NS * T::KV_TILE_BYTES;           // O staging for TMA stores
     uint64_t* bars = reinterpret_cast<uint64_t*>(smem + T::TILE_BYTES);
-    uint64_t* q_full = bars;
-    uint64_t* kv_full = bars + 1;
+    uint64_t* q_full = bars;                 // Q of the current unit landed
+    uint64_t* q_empty = q_full + 1;          // last Q·Kᵀ of the unit finished
+    uint64_t* kv_full = q_empty + 1;
     uint64_t* kv_empty = kv_full + T::NS;
-    uint64_t* s_full = kv_empty + T::NS;      // [2] S buffer b written
-    uint64_t* p_full = s_full + 2;            // [2] P in buffer b written (+ O rescaled), per warp
-    uint64_t* o_done = p_full + 2;            // [2] PV MMAs of tile t finished
-    uint64_t* drain = o_done + 2;             // every MMA of the CTA finished
-    uint64_t* epi_bar = drain + 1;            // [2] O tile t staged in shared memory (per warp)
-    uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(epi_bar + 2);
+    uint64_t* s_full = kv_empty + T::NS;     // [2] S buffer b written
+    uint64_t* p_full = s_full + 2;           // [2] P in buffer b written (+ O rescaled), per warp
+    uint64_t* o_done = p_full + 2;           // [2] last P·V of tile t (TILES == 1: every P·V)
+    uint64_t* drain = o_done + 2;            // every MMA of the CTA finished
+    uint64_t* epi_bar = drain + 1;           // [2] O rows of tile t staged, per warp
+    uint64_t* stage_free = epi_bar + 2;      // staging buffer read by its TMA store
+    uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(stage_free + 1);
     volatile int* abort_flag = reinterpret_cast<volatile int*>(tmem_slot + 1);
 
     const int warp = threadIdx.x >> 5;
     const int lane = threadIdx.x & 31;
-    // Linear block index -> (head, query block).  Full attention: the query
-    // blocks of one head are adjacent, so the CTAs resident at a time share a
-    // few heads' K/V in L2.  Causal: heads go in groups of `head_group` (sized
-    // so a group's K/V fits in L2) and within a group the heaviest query
-    // blocks of all its heads go first, which keeps the tail short.
-    int bh, qblk;
-    {
-        const int L = static_cast<int>(blockIdx.x);
-        if (CAUSAL) {
-            const int per_group = head_group * n_qblk;
-            const int g = L / per_group;
-            const int r = L - g * per_group;
-            const int g0 = g * head_group;
-            const int gsz = min(head_group, BH - g0);
-            const int qi = r / gsz;
-            bh = g0 + (r - qi * gsz);
-            qblk = n_qblk - 1 - qi;
-        } else {
-            bh = L / n_qblk;
-            qblk = L - bh * n_qblk;
-        }
-    }
-    const int q0 = qblk * T::BM * T::TILES;
-
-    const int n_kv0 = kv_tiles_for<CAUSAL>(q0, S_q, S_k);
-    const int n_kv1 = T::TILES == 2 ? kv_tiles_for<CAUSAL>(q0 + T::BM, S_q, S_k) : 0;
-    const int n_max = max(n_kv0, n_kv1);
+    const int n_units = BH * n_qblk;
+    // Units are handed out in rounds of gridDim.x, in serpentine order (CTA c
+    // takes position c of even rounds and gridDim.x-1-c of odd ones), so a CTA
+    // that got a heavy unit in one round gets a light one in the next.
+    auto unit_of_round = [&](int r) {
+        const int G = static_cast<int>(gridDim.x);
+        const int c = static_cast<int>(blockIdx.x);
+        return r * G + ((r & 1) ? (G - 1 - c) : c);
+    };
 
     if (threadIdx.x == 0) {
         mbar_init(q_full, 1);
+        mbar_init(q_empty, 1);
         for (int s = 0; s < T::NS; ++s) {
             mbar_init(&kv_full[s], 1);
             mbar_init(&kv_empty[s], 1);
@@ -192,13 +208,13 @@ __global__ void __launch_bounds__(FwdTile<D>::THREADS, 1)
             mbar_init(&s_full[b], 1);
             mbar_init(&p_full[b], 4);           // one arrival per softmax warp
             mbar_init(&o_done[b], 1);
+            mbar_init(&epi_bar[b], 4);
         }
         mbar_init(drain, 1);
-        mbar_init(&epi_bar[0], 4);
-        mbar_init(&epi_bar[1], 4);
+        mbar_init(stage_free, 1);
         *abort_flag = 0;
         fence_mbar_init();
-        asm volatile("fence.proxy.async.shared::cta;" ::: "memory");
+        fence_proxy_async_smem();
     }
     if (warp == 0) {
         tmem_alloc(tmem_slot, T::TMEM_COLS);
@@ -224,23 +240,21 @@ __global__ void __launch_bounds__(FwdTile<D>::THREADS, 1)
       if (T::TILES == 2) regs_shrink<T::AUX_REGS>();
       // Both aux roles run warp-uniform loops (waits on every lane); only the
       // TMA / MMA / commit instructions themselves are issued by one lane.
-      if (warp == T::PRODUCER_WARP && n_max > 0) {
+      if (warp == T::PRODUCER_WARP) {
         // ------------------------------------------------------------ TMA producer
         const bool leader = elect_one();
         if (leader) {
             tma_prefetch_desc(&tm_q);
             tma_prefetch_desc(&tm_k);
             tma_prefetch_desc(&tm_v);
-            mbar_arrive_expect_tx(q_full, T::TILES * T::Q_TILE_BYTES);
-            for (int t = 0; t < T::TILES; ++t)
-                for (int c = 0; c < T::CHUNKS; ++c)
-                    tma_load_3d(sQ + (t * T::CHUNKS + c) * T::Q_CHUNK_BYTES, &tm_q, q_full,
-                                c * 64, q0 + t * T::BM, bh);
+            tma_prefetch_desc(&tm_o);
         }
         __syncwarp();
-        int idx = 0;
+        int idx = 0;                          // K/V ring position, across units
+        int uq = 0;                           // units started by this CTA
+        int q_loads = 0;                      // Q loads issued
         bool ok = true;
-        auto issue = [&](const CUtensorMap* map, int j) {
+        auto issue = [&](const CUtensorMap* map, int j, int bh) {
             if (!ok) return;
             const int slot = idx % T::NS;
             ok = mbar_wait(&kv_empty[slot], ((idx / T::NS) & 1) ^ 1, abort_flag, status,
@@ -258,18 +272,41 @@ __global__ void __launch_bounds__(FwdTile<D>::THREADS, 1)
             __syncwarp();
             ++idx;
         };
-        // Load order is the MMA warp's consumption order.
-        if (T::TILES == 2) {
-            for (int j = 0; j < n_max; ++j) {
-                issue(&tm_k, j);
-                issue(&tm_v, j);
+        for (int r = 0; r * static_cast<int>(gridDim.x) < n_units && ok; ++r) {
+            const int L = unit_of_round(r);
+            if (L >= n_units) continue;
+            int bh, q0;
+            unit_coords<CAUSAL, ROWS>(L, BH, n_qblk, head_group, bh, q0);
+            const int n0 = kv_tiles_for<CAUSAL>(q0, S_q, S_k);
+            const int n1 = T::TILES == 2 ? kv_tiles_for<CAUSAL>(q0 + T::BM, S_q, S_k) : 0;
+            const int n_max = max(n0, n1);
+            const int uq_now = uq++;
+            // Q of this unit once the previous unit's last Q·Kᵀ is done.
+            ok = mbar_wait(q_empty, (uq_now & 1) ^ 1, abort_flag, status, kStatusProducer);
+            ok = __all_sync(0xffffffffu, ok);
+            if (!ok) break;
+            if (leader) {
+                mbar_arrive_expect_tx(q_full, T::TILES * T::Q_TILE_BYTES);
+                for (int t = 0; t < T::TILES; ++t)
+                    for (int c = 0; c < T::CHUNKS; ++c)
+                        tma_load_3d(sQ + (t * T::CHUNKS + c) * T::Q_CHUNK_BYTES, &tm_q, q_full,
+                                    c * 64, q0 + t * T::BM, bh);
             }
-        } else {
-            issue(&tm_k, 0);
-            if (n_max > 1) issue(&tm_k, 1);
-            for (int j = 0; j < n_max; ++j) {
-                issue(&tm_v, j);
-                if (j + 2 < n_max) issue(&tm_k, j + 2);
+            __syncwarp();
+            ++q_loads;
+            // K/V in the MMA warp's consumption order.
+            if (T::TILES == 2) {
+                for (int j = 0; j < n_max; ++j) {
+                    issue(&tm_k, j, bh);
+                    issue(&tm_v, j, bh);
+                }
+            } else {
+                issue(&tm_k, 0, bh);
+                if (n_max > 1) issue(&tm_k, 1, bh);
+                for (int j = 0; j < n_max; ++j) {
+                    issue(&tm_v, j, bh);
+                    if (j + 2 < n_max) issue(&tm_k, j + 2, bh);
+                }
             }
         }
         if (*abort_flag && leader) {
@@ -284,25 +321,28 @@ __global__ void __launch_bounds__(FwdTile<D>::THREADS, 1)
                     }
                 }
             }
-            const uint32_t a = smem_u32(q_full);
-            while (!mbar_try_wait(a, 0)) {
-                if (global_timer_ns() - t0 > kWaitLimitNs) {
-                    atomicOr(status, kStatusDrain);
-                    break;
+            if (q_loads > 0) {
+                const uint32_t a = smem_u32(q_full);
+                const uint32_t last = static_cast<uint32_t>(q_loads - 1) & 1u;
+                while (!mbar_try_wait(a, last)) {
+                    if (global_timer_ns() - t0 > kWaitLimitNs) {
+                        atomicOr(status, kStatusDrain);
+                        break;
+                    }
                 }
             }
         }
         __syncwarp();
-      } else if (warp == T::MMA_WARP && n_max > 0) {
+      } else if (warp == T::MMA_WARP) {
         // ------------------------------------------------------------ MMA issuer
         constexpr uint32_t id_s = idesc_f16(128, T::BN, BF16, false, false);
         constexpr uint32_t id_o = idesc_f16(128, D, BF16, false, true);
         const uint32_t q_base = smem_u32(sQ);
         const uint32_t kv_base = smem_u32(sKV);
-        bool ok = mbar_wait(q_full, 0, abort_flag, status, kStatusMma);
-        ok = __all_sync(0xffffffffu, ok);
-        tc_fence_after();
-        int acq = 0;
+        bool ok = true;
+        int acq = 0;                          // K/V ring position, across units
+        uint32_t pc0 = 0, pc1 = 0;            // P handoffs consumed per buffer
+        int uq = 0;
         auto acquire = [&](int& slot) {
             if (!ok) return;
             slot = acq % T::NS;
@@ -311,13 +351,13 @@ __global__ void __launch_bounds__(FwdTile<D>::THREADS, 1)
             ++acq;
             tc_fence_after();
         };
-        auto wait_p = [&](int b, uint32_t parity) {
+        auto wait_p = [&](int b) {
             if (!ok) return;
-            ok = mbar_wait(&p_full[b], parity, abort_flag, status, kStatusMma);
+            ok = mbar_wait(&p_full[b], (b ? pc1 : pc0) & 1, abort_flag, status, kStatusMma);
             ok = __all_sync(0xffffffffu, ok);
+            if (b) ++pc1; else ++pc0;
             tc_fence_after();
         };
-        // S_b = Q_t · K(slot)ᵀ : M = 128, N = BN, K = D in steps of 16
         // Descriptors are built once; a K step moves the start address, which
         // lives in the low 14 bits of the low word (addr >> 4, < 2^14 for any
         // shared-memory address), so stepping is a 32-bit add without carries.
@@ -353,62 +393,86 @@ __global__ void __launch_bounds__(FwdTile<D>::THREADS, 1)
                             (acc || kk > 0) ? 1u : 0u);
             }
         };
-        if (T::TILES == 2) {
-            const int n0 = n_kv0, n1 = n_kv1;
-            int kslot = 0, vslot = 0;
-            acquire(kslot);
-            if (ok) {
+        int gs = 0;                           // TILES == 1: S/PV steps across units
+        for (int r = 0; r * static_cast<int>(gridDim.x) < n_units && ok; ++r) {
+            const int L = unit_of_round(r);
+            if (L >= n_units) continue;
+            int bh, q0;
+            unit_coords<CAUSAL, ROWS>(L, BH, n_qblk, head_group, bh, q0);
+            const int n0 = kv_tiles_for<CAUSAL>(q0, S_q, S_k);
+            const int n1 = T::TILES == 2 ? kv_tiles_for<CAUSAL>(q0 + T::BM, S_q, S_k) : 0;
+            const int n_max = max(n0, n1);
+            ok = mbar_wait(q_full, uq & 1, abort_flag, status, kStatusMma);
+            ++uq;
+            ok = __all_sync(0xffffffffu, ok);
+            tc_fence_after();
+            if (!ok) break;
+            if (T::TILES == 2) {
+                int kslot = 0, vslot = 0;
+                acquire(kslot);
+                if (!ok) break;
                 if (n0 > 0) { mma_qk(0, kslot, 0); tc_commit_warp(&s_full[0]); }
                 if (n1 > 0) { mma_qk(1, kslot, 1); tc_commit_warp(&s_full[1]); }
                 tc_commit_warp(&kv_empty[kslot]);
-            }
-            for (int j = 0; j < n_max && ok; ++j) {
-                const bool has_next = j + 1 < n_max;
-                acquire(vslot);
-                if (j < n0) {
-                    wait_p(0, j & 1);
+                if (n_max == 1) tc_commit_warp(q_empty);
+                for (int j = 0; j < n_max && ok; ++j) {
+                    const bool has_next = j + 1 < n_max;
+                    acquire(vslot);
+                    if (j < n0) {
+                        wait_p(0);
+                        if (!ok) break;
+                        mma_pv(0, vslot, 0, j > 0);
+                        if (j == n0 - 1) tc_commit_warp(&o_done[0]);
+                    }
+                    if (has_next) acquire(kslot);
                     if (!ok) break;
-                    mma_pv(0, vslot, 0, j > 0);
-                    if (j == n0 - 1) tc_commit_warp(&o_done[0]);
+                    if (j + 1 < n0) { mma_qk(0, kslot, 0); tc_commit_warp(&s_full[0]); }
+                    if (j < n1) {
+                        wait_p(1);
+                        if (!ok) break;
+                        mma_pv(1, vslot, 1, j > 0);
+                        if (j == n1 - 1) tc_commit_warp(&o_done[1]);
+                    }
+                    tc_commit_warp(&kv_empty[vslot]);
+                    if (j + 1 < n1) { mma_qk(1, kslot, 1); tc_commit_warp(&s_full[1]); }
+                    if (has_next) tc_commit_warp(&kv_empty[kslot]);
+                    if (j + 2 == n_max) tc_commit_warp(q_empty);   // last Q·Kᵀ issued
                 }
-                if (has_next) acquire(kslot);
-                if (!ok) break;
-                if (j + 1 < n0) { mma_qk(0, kslot, 0); tc_commit_warp(&s_full[0]); }
-                if (j < n1) {
-                    wait_p(1, j & 1);
-                    if (!ok) break;
-                    mma_pv(1, vslot, 1, j > 0);
-                    if (j == n1 - 1) tc_commit_warp(&o_done[1]);
-                }
-                tc_commit_warp(&kv_empty[vslot]);
-                if (j + 1 < n1) { mma_qk(1, kslot, 1); tc_commit_warp(&s_full[1]); }
-                if (has_next) tc_commit_warp(&kv_empty[kslot]);
-            }
-        } else {
-            const int n = n_kv0;
-            int slot = 0;
-            acquire(slot);
-            if (ok) { mma_qk(0, slot, 0); tc_commit_warp(&s_full[0]); tc_commit_warp(&kv_empty[slot]); }
-            if (n > 1) {
+            } else {
+                const int n = n0;
+                int slot = 0;
                 acquire(slot);
-                if (ok) { mma_qk(0, slot, 1); tc_commit_warp(&s_full[1]); tc_commit_warp(&kv_empty[slot]); }
-            }
-            for (int j = 0; j < n && ok; ++j) {
-                const int b = j & 1;
-                int vslot = 0;
-                acquire(vslot);
-                wait_p(b, (j >> 1) & 1);
                 if (!ok) break;
-                mma_pv(0, vslot, b, j > 0);
-                tc_commit_warp(&o_done[0]);
-                tc_commit_warp(&kv_empty[vslot]);
-                if (j + 2 < n) {
+                mma_qk(0, slot, gs & 1);
+                tc_commit_warp(&s_full[gs & 1]);
+                tc_commit_warp(&kv_empty[slot]);
+                if (n > 1) {
                     acquire(slot);
                     if (!ok) break;
-                    mma_qk(0, slot, b);
-                    tc_commit_warp(&s_full[b]);
+                    mma_qk(0, slot, (gs + 1) & 1);
+                    tc_commit_warp(&s_full[(gs + 1) & 1]);
                     tc_commit_warp(&kv_empty[slot]);
                 }
+                if (n <= 2) tc_commit_warp(q_empty);
+                for (int j = 0; j < n && ok; ++j) {
+                    const int b = (gs + j) & 1;
+                    int vslot = 0;
+                    acquire(vslot);
+                    wait_p(b);
+                    if (!ok) break;
+                    mma_pv(0, vslot, b, j > 0);
+                    tc_commit_warp(&o_done[0]);
+                    tc_commit_warp(&kv_empty[vslot]);
+                    if (j + 2 < n) {
+                        acquire(slot);
+                        if (!ok) break;
+                        mma_qk(0, slot, b);
+                        tc_commit_warp(&s_full[b]);
+                        tc_commit_warp(&kv_empty[slot]);
+                        if (j + 3 == n) tc_commit_warp(q_empty);
+                    }
+                }
+                gs += n;
             }
         }
         // Every MMA of this CTA has finished once `drain` flips.
@@ -433,162 +497,202 @@ __global__ void __launch_bounds__(FwdTile<D>::THREADS, 1)
         const int t = T::TILES == 2 ? (warp >> 2) : 0;
         const int wq = warp & 3;                      // TMEM lane quarter of this warp
         const int row = wq * 32 + lane;
-        const int row_begin = q0 + t * T::BM;
-        const int q_idx = row_begin + row;
-        const int n = t == 0 ? n_kv0 : n_kv1;
         const uint32_t lane_base = tmem + (static_cast<uint32_t>(wq * 32) << 16);
-        float m = -INFINITY;                          // running max, log2 units (scale folded)
-        float l = 0.f;                                // running sum of exp2(x - m)
         bool ok = true;
+        uint32_t sc = 0;                              // S tiles consumed by this warpgroup
+        uint32_t oc = 0;                              // o_done phases consumed
+        uint32_t round = 0;                           // staging rounds of the whole CTA
+        uint32_t my_rounds = 0;                       // staging rounds of this warpgroup
+        bool stored = false;                          // this thread issued TMA stores
 
-        for (int j = 0; j < n; ++j) {
-            const int b = T::TILES == 2 ? t : (j & 1);
-            const uint32_t parity = T::TILES == 2 ? (j & 1) : ((j >> 1) & 1);
-            ok = mbar_wait(&s_full[b], parity, abort_flag, status, kStatusSoftmax);
-            ok = __all_sync(0xffffffffu, ok);
-            if (!ok) break;
-            tc_fence_after();
+        for (int r = 0; r * static_cast<int>(gridDim.x) < n_units && ok; ++r) {
+            const int L = unit_of_round(r);
+            if (L >= n_units) continue;
+            int bh, q0;
+            unit_coords<CAUSAL, ROWS>(L, BH, n_qblk, head_group, bh, q0);
+            const int n0 = kv_tiles_for<CAUSAL>(q0, S_q, S_k);
+            const int n1 = T::TILES == 2 ? kv_tiles_for<CAUSAL>(q0 + T::BM, S_q, S_k) : 0;
+            const int n = t == 0 ? n0 : n1;
+            const int row_begin = q0 + t * T::BM;
+            const int q_idx = row_begin + row;
+            float m = -INFINITY;                      // running max, log2 units (scale folded)
+            float l = 0.f;                            // running sum of exp2(x - m)
 
-            uint32_t sa[64], sb[64];
-            tmem_ld64(lane_base + b * T::S_STRIDE, sa);
-            tmem_ld64(lane_base + b * T::S_STRIDE + 64, sb);
-            float s[128];
-#pragma unroll
-            for (int c = 0; c < 64; ++c) {
-                s[c] = __uint_as_float(sa[c]);
-                s[64 + c] = __uint_as_float(sb[c]);
-            }
-
-            const int kv0 = j * T::BN;
-            const bool masked = (CAUSAL && kv0 + T::BN - 1 > row_begin) || (kv0 + T::BN > S_k);
-            // keys kv0 + c with c < lim are visible to this row
-            const int lim = masked ? max(0, min(S_k, CAUSAL ? q_idx + 1 : S_k) - kv0) : T::BN;
-
-            uint32_t pk[64];
-            bool rescale = false;
-            float alpha = 1.f;
-            if (m == -INFINITY) {
-                // First visible tile of this row: the maximum has to come first.
-                const float mx = masked ? row_max128<true>(s, lim) : row_max128<false>(s, lim);
-                m = (mx == -INFINITY) ? -INFINITY : mx * scale_log2;
-                const float neg_m = (m == -INFINITY) ? 0.f : -m;
-                l = masked ? exp_pack128<true, BF16, false>(s, lim, scale_log2, neg_m, pk, nullptr)
-                           : exp_pack128<false, BF16, false>(s, lim, scale_log2, neg_m, pk, nullptr);
-            } else {
-                // Exponentiate against the running maximum and take this tile's
-                // maximum exponent alongside.  A row whose maximum grew by more
-                // than 2^kRescaleLog2 (rare) re-reads its scores from TMEM (P has
-                // not been written over them yet) and is redone against the new
-                // maximum, so the result equals the max-first order exactly.
-                float xmax;
-                float lsum = masked
-                    ? exp_pack128<true, BF16, true>(s, lim, scale_log2, -m, pk, &xmax)
-                    : exp_pack128<false, BF16, true>(s, lim, scale_log2, -m, pk, &xmax);
-                if (__any_sync(0xffffffffu, xmax > kRescaleLog2)) {
-                    uint32_t ra[64], rb[64];
-                    tmem_ld64(lane_base + b * T::S_STRIDE, ra);
-                    tmem_ld64(lane_base + b * T::S_STRIDE + 64, rb);
-                    if (xmax > kRescaleLog2) {
-#pragma unroll
-                        for (int c = 0; c < 64; ++c) {
-                            s[c] = __uint_as_float(ra[c]);
-                            s[64 + c] = __uint_as_float(rb[c]);
-                        }
-                        const float mx = masked ? row_max128<true>(s, lim) : row_max128<false>(s, lim);
-                        const float m_tile = mx * scale_log2;
-                        alpha = ex2_approx(m - m_tile);
-                        m = m_tile;
-                        l *= alpha;
-                        rescale = true;
-                        lsum = masked
-                            ? exp_pack128<true, BF16, false>(s, lim, scale_log2, -m, pk, nullptr)
-                            : exp_pack128<false, BF16, false>(s, lim, scale_log2, -m, pk, nullptr);
-                    }
-                }
-                l += lsum;
-            }
-
-            tmem_st32(lane_base + b * T::S_STRIDE + T::P_OFF, pk);
-            tmem_st32(lane_base + b * T::S_STRIDE + T::P_OFF + 32, pk + 32);
-
-            if (T::TILES == 1 && j > 0) {
-                // O holds PV up to key tile j-1 only once that MMA has finished.
-                ok = mbar_wait(&o_done[0], (j - 1) & 1, abort_flag, status, kStatusSoftmax);
+            for (int j = 0; j < n; ++j) {
+                // TILES == 2: S buffer t, one S per step.  TILES == 1: the two
+                // buffers alternate; sc counts steps across units.
+                const int b = T::TILES == 2 ? t : static_cast<int>(sc & 1);
+                const uint32_t parity = T::TILES == 2 ? (sc & 1) : ((sc >> 1) & 1);
+                ok = mbar_wait(&s_full[b], parity, abort_flag, status, kStatusSoftmax);
                 ok = __all_sync(0xffffffffu, ok);
                 if (!ok) break;
                 tc_fence_after();
-            }
-            if (__any_sync(0xffffffffu, rescale)) {
-                const uint32_t o_base = lane_base + T::O_COL + t * D;
-#pragma unroll 1
-                for (int cc = 0; cc < D; cc += 32) {
-                    uint32_t r[32];
-                    tmem_ld32(o_base + cc, r);
-#pragma unroll
-                    for (int i = 0; i < 32; ++i) r[i] = __float_as_uint(__uint_as_float(r[i]) * alpha);
-                    tmem_st32(o_base + cc, r);
-                }
-            }
-            // Each lane's TMEM stores are complete (wait::st) and fenced; after the
-            // warp converges one lane publishes them for the whole warp.
-            tmem_st_wait();
-            tc_fence_before();
-            __syncwarp();
-            if (lane == 0) mbar_arrive(&p_full[b]);
-        }
+                ++sc;
 
-        if (ok && n > 0) {
-            const uint32_t parity = T::TILES == 2 ? 0u : static_cast<uint32_t>((n - 1) & 1);
-            ok = mbar_wait(&o_done[T::TILES == 2 ? t : 0], parity, abort_flag, status,
-                           kStatusEpilogue);
-            ok = __all_sync(0xffffffffu, ok);
-            if (ok) {
-                tc_fence_after();
-                // O / l in the output dtype, staged through this tile's Q area
-                // (its last Q·Kᵀ finished before the last P·V) in the 128-byte
-                // swizzled layout the O tensor map stores from.
-                const float inv_l = 1.f / l;
-                uint8_t* sO = sQ + t * T::Q_TILE_BYTES;
-                const uint32_t o_base = lane_base + T::O_COL + t * D;
+                uint32_t sa[64], sb[64];
+                tmem_ld64(lane_base + b * T::S_STRIDE, sa);
+                tmem_ld64(lane_base + b * T::S_STRIDE + 64, sb);
+                float s[128];
+#pragma unroll
+                for (int c = 0; c < 64; ++c) {
+                    s[c] = __uint_as_float(sa[c]);
+                    s[64 + c] = __uint_as_float(sb[c]);
+                }
+
+                const int kv0 = j * T::BN;
+                const bool masked = (CAUSAL && kv0 + T::BN - 1 > row_begin) || (kv0 + T::BN > S_k);
+                // keys kv0 + c with c < lim are visible to this row
+                const int lim = masked ? max(0, min(S_k, CAUSAL ? q_idx + 1 : S_k) - kv0) : T::BN;
+
+                uint32_t pk[64];
+                bool rescale = false;
+                float alpha = 1.f;
+                if (m == -INFINITY) {
+                    // First visible tile of this row: the maximum has to come first.
+                    const float mx = masked ? row_max128<true>(s, lim) : row_max128<false>(s, lim);
+                    m = (mx == -INFINITY) ? -INFINITY : mx * scale_log2;
+                    const float neg_m = (m == -INFINITY) ? 0.f : -m;
+                    l = masked ? exp_pack128<true, BF16, false>(s, lim, scale_log2, neg_m, pk, nullptr)
+                               : exp_pack128<false, BF16, false>(s, lim, scale_log2, neg_m, pk, nullptr);
+                } else {
+                    // Exponentiate against the running maximum and take this tile's
+                    // maximum exponent alongside.  A row whose maximum grew by more
+                    // than 2^kRescaleLog2 (rare) re-reads its scores from TMEM (P has
+                    // not been written over them yet) and is redone against the new
+                    // maximum, so the result equals the max-first order exactly.
+                    float xmax;
+                    float lsum = masked
+                        ? exp_pack128<true, BF16, true>(s, lim, scale_log2, -m, pk, &xmax)
+                        : exp_pack128<false, BF16, true>(s, lim, scale_log2, -m, pk, &xmax);
+                    if (__any_sync(0xffffffffu, xmax > kRescaleLog2)) {
+                        uint32_t ra[64], rb[64];
+                        tmem_ld64(lane_base + b * T::S_STRIDE, ra);
+                        tmem_ld64(lane_base + b * T::S_STRIDE + 64, rb);
+                        if (xmax > kRescaleLog2) {
+#pragma unroll
+                            for (int c = 0; c < 64; ++c) {
+                                s[c] = __uint_as_float(ra[c]);
+                                s[64 + c] = __uint_as_float(rb[c]);
+                            }
+                            const float mx = masked ? row_max128<true>(s, lim) : row_max128<false>(s, lim);
+                            const float m_new = mx * scale_log2;
+                            alpha = ex2_approx(m - m_new);
+                            m = m_new;
+                            l *= alpha;
+                            rescale = true;
+                            lsum = masked
+                                ? exp_pack128<true, BF16, false>(s, lim, scale_log2, -m, pk, nullptr)
+                                : exp_pack128<false, BF16, false>(s, lim, scale_log2, -m, pk, nullptr);
+                        }
+                    }
+                    l += lsum;
+                }
+
+                tmem_st32(lane_base + b * T::S_STRIDE + T::P_OFF, pk);
+                tmem_st32(lane_base + b * T::S_STRIDE + T::P_OFF + 32, pk + 32);
+
+                if (T::TILES == 1 && j > 0) {
+                    // O holds PV up to key tile j-1 only once that MMA has finished.
+                    ok = mbar_wait(&o_done[0], oc & 1, abort_flag, status, kStatusSoftmax);
+                    ok = __all_sync(0xffffffffu, ok);
+                    if (!ok) break;
+                    ++oc;
+                    tc_fence_after();
+                }
+                if (__any_sync(0xffffffffu, rescale)) {
+                    const uint32_t o_base = lane_base + T::O_COL + t * D;
 #pragma unroll 1
-                for (int cc = 0; cc < D; cc += 32) {
-                    uint32_t r[32];
-                    tmem_ld32(o_base + cc, r);
-                    uint32_t w[16];
+                    for (int cc = 0; cc < D; cc += 32) {
+                        uint32_t r[32];
+                        tmem_ld32(o_base + cc, r);
 #pragma unroll
-                    for (int i = 0; i < 16; ++i) {
-                        const float a = __uint_as_float(r[2 * i]) * inv_l;
-                        const float c = __uint_as_float(r[2 * i + 1]) * inv_l;
-                        w[i] = BF16 ? pack_bf16(a, c) : pack_f16(a, c);
-                    }
-                    uint8_t* rowp = sO + (cc / 64) * T::Q_CHUNK_BYTES + row * 128;
-#pragma unroll
-                    for (int i = 0; i < 4; ++i) {
-                        const int unit = ((cc & 63) / 8) + i;          // 16-byte unit in the row
-                        *reinterpret_cast<uint4*>(rowp + ((unit ^ (row & 7)) * 16)) =
-                            make_uint4(w[4 * i], w[4 * i + 1], w[4 * i + 2], w[4 * i + 3]);
+                        for (int i = 0; i < 32; ++i) r[i] = __float_as_uint(__uint_as_float(r[i]) * alpha);
+                        tmem_st32(o_base + cc, r);
                     }
                 }
-                // Every warp publishes its rows; the first warp's leader stores
-                // the tile once all four have (a bounded wait, like every other).
-                fence_proxy_async_smem();
+                // Each lane's TMEM stores are complete (wait::st) and fenced; after the
+                // warp converges one lane publishes them for the whole warp.
+                tmem_st_wait();
+                tc_fence_before();
                 __syncwarp();
-                if (lane == 0) mbar_arrive(&epi_bar[t]);
-                if (wq == 0) {
-                    bool staged = mbar_wait(&epi_bar[t], 0, abort_flag, status, kStatusEpilogue);
-                    staged = __all_sync(0xffffffffu, staged);
-                    if (staged && elect_one()) {
-                        for (int c = 0; c < T::CHUNKS; ++c)
-                            tma_store_3d(&tm_o, sO + c * T::Q_CHUNK_BYTES, c * 64, row_begin, bh);
-                        bulk_commit_group();
-                        bulk_wait_all();
+                if (lane == 0) mbar_arrive(&p_full[b]);
+            }
+            if (!ok) break;
+
+            // ---------------------------------------------------------- epilogue
+            // Rounds of the staging buffer run in a fixed order over the CTA:
+            // tile 0's then tile 1's, unit after unit.
+            const uint32_t rounds_t0 = n0 > 0 ? T::STAGE_ROUNDS : 0;
+            const uint32_t rounds_t1 = (T::TILES == 2 && n1 > 0) ? T::STAGE_ROUNDS : 0;
+            if (n > 0) {
+                const uint32_t parity = T::TILES == 2 ? (oc & 1) : (oc & 1);
+                ok = mbar_wait(&o_done[t], parity, abort_flag, status, kStatusEpilogue);
+                ok = __all_sync(0xffffffffu, ok);
+                if (!ok) break;
+                ++oc;
+                tc_fence_after();
+                const float inv_l = 1.f / l;
+                const uint32_t o_base = lane_base + T::O_COL + t * D;
+                uint32_t r_idx = round + (t == 1 ? rounds_t0 : 0);
+                for (int rr = 0; rr < T::STAGE_ROUNDS; ++rr, ++r_idx) {
+                    // The staging buffer is free once the previous round's TMA store
+                    // has read it.
+                    if (r_idx > 0) {
+                        ok = mbar_wait(stage_free, (r_idx - 1) & 1, abort_flag, status,
+                                       kStatusEpilogue);
+                        ok = __all_sync(0xffffffffu, ok);
+                        if (!ok) break;
                     }
+#pragma unroll 1
+                    for (int cc = 0; cc < T::STAGE_CHUNKS * 64; cc += 32) {
+                        uint32_t r[32];
+                        tmem_ld32(o_base + rr * T::STAGE_CHUNKS * 64 + cc, r);
+                        uint32_t w[16];
+#pragma unroll
+                        for (int i = 0; i < 16; ++i) {
+                            const float a = __uint_as_float(r[2 * i]) * inv_l;
+                            const float c = __uint_as_float(r[2 * i + 1]) * inv_l;
+                            w[i] = BF16 ? pack_bf16(a, c) : pack_f16(a, c);
+                        }
+                        uint8_t* rowp = sO + (cc / 64) * T::Q_CHUNK_BYTES + row * 128;
+#pragma unroll
+                        for (int i = 0; i < 4; ++i) {
+                            const int unit = ((cc & 63) / 8) + i;      // 16-byte unit in the row
+                            *reinterpret_cast<uint4*>(rowp + ((unit ^ (row & 7)) * 16)) =
+                                make_uint4(w[4 * i], w[4 * i + 1], w[4 * i + 2], w[4 * i + 3]);
+                        }
+                    }
+                    // Every warp publishes its rows; the first warp's leader stores the
+                    // round once all four have (a bounded wait, like every other).
+                    fence_proxy_async_smem();
                     __syncwarp();
+                    if (lane == 0) mbar_arrive(&epi_bar[t]);
+                    if (wq == 0) {
+                        bool staged = mbar_wait(&epi_bar[t], my_rounds & 1, abort_flag, status,
+                                                kStatusEpilogue);
+                        staged = __all_sync(0xffffffffu, staged);
+                        if (staged && elect_one()) {
+                            for (int c = 0; c < T::STAGE_CHUNKS; ++c)
+                                tma_store_3d(&tm_o, sO + c * T::Q_CHUNK_BYTES,
+                                             (rr * T::STAGE_CHUNKS + c) * 64, row_begin, bh);
+                            bulk_commit_group();
+                            bulk_wait_read_all();
+                            mbar_arrive(stage_free);
+                            stored = true;
+                        }
+                        __syncwarp();
+                        ok = staged;
+                    }
+                    ++my_rounds;
+                    if (!ok) break;
                 }
+                if (!ok) break;
                 if (q_idx < S_q)
                     lse_ptr[static_cast<size_t>(bh) * S_q + q_idx] = (m + log2f(l)) * kLn2;
             }
+            round += rounds_t0 + rounds_t1;
         }
+        if (stored) bulk_wait_all();                  // O writes complete before exit
         teardown();
     }
 }
@@ -616,9 +720,10 @@ cudaError_t launch_attn_fwd(const FwdArgs& a, cudaStream_t stream) {
     }
     const int rows_per_cta = T::BM * T::TILES;
     const int n_qblk = (a.S_q + rows_per_cta - 1) / rows_per_cta;
-    const long long blocks = static_cast<long long>(a.BH) * n_qblk;
-    if (blocks > 0x7fffffffLL) return cudaErrorInvalidConfiguration;
-    dim3 grid(static_cast<unsigned>(blocks), 1, 1);
+    const long long units = static_cast<long long>(a.BH) * n_qblk;
+    if (units > 0x7fffffffLL) return cudaErrorInvalidConfiguration;
+    // One CTA per SM (each takes the whole of tensor memory), looping over units.
+    const int grid = static_cast<int>(std::min<long long>(units, a.num_sms));
     kernel<<<grid, T::THREADS, T::SMEM_BYTES, stream>>>(a.tm_q, a.tm_k, a.tm_v, a.tm_o, a.lse, a.S_q,
                                                          a.S_k, a.BH, n_qblk, head_group,
                                                          a.scale_log2, a.status);

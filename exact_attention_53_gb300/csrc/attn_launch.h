@@ -19,6 +19,7 @@ struct FwdArgs {
     int32_t S_k;
     int32_t BH;             // B·H
     float scale_log2;       // scale · log2(e), >= 0
+    int32_t num_sms;        // SMs of the device: the persistent grid size
     unsigned int* status;   // device status word (bit set on a wait that ran out)
 };
 
@@ -45,8 +46,13 @@ struct FwdTile {
     static constexpr int Q_TILE_BYTES = BM * D * 2;
     static constexpr int KV_TILE_BYTES = BN * D * 2;
     static constexpr int NS = D == 64 ? 8 : (D == 128 ? 4 : 2);
-    static constexpr int TILE_BYTES = TILES * Q_TILE_BYTES + NS * KV_TILE_BYTES;
-    static constexpr int NUM_BARS = 1 + 2 * NS + 2 + 2 + 2 + 1 + 2;
+    // O leaves through a staging buffer of up to two 64-column chunks (TMA
+    // store boxes), in STAGE_ROUNDS rounds per query tile.
+    static constexpr int STAGE_CHUNKS = CHUNKS < 2 ? CHUNKS : 2;
+    static constexpr int STAGE_ROUNDS = CHUNKS / STAGE_CHUNKS;
+    static constexpr int STAGE_BYTES = STAGE_CHUNKS * Q_CHUNK_BYTES;
+    static constexpr int TILE_BYTES = TILES * Q_TILE_BYTES + NS * KV_TILE_BYTES + STAGE_BYTES;
+    static constexpr int NUM_BARS = 2 + 2 * NS + 2 + 2 + 2 + 1 + 2 + 1;
     static constexpr int SMEM_BYTES = 1024 + TILE_BYTES + NUM_BARS * 8 + 16;
     static constexpr int SOFTMAX_WARPS = 4 * TILES;
     static constexpr int PRODUCER_WARP = SOFTMAX_WARPS;       // first warp of the aux warpgroup
