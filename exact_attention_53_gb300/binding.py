@@ -34,7 +34,7 @@ class AttnPlan(ctypes.Structure):
     _fields_ = [("block_m", ctypes.c_int64), ("block_n", ctypes.c_int64),
                 ("q_tiles", ctypes.c_int64), ("kv_tiles", ctypes.c_int64),
                 ("q_tiles_per_cta", ctypes.c_int64), ("bh", ctypes.c_int64),
-                ("ctas", ctypes.c_int64), ("threads", ctypes.c_int32),
+                ("units", ctypes.c_int64), ("threads", ctypes.c_int32),
                 ("smem_bytes", ctypes.c_int32), ("tmem_cols", ctypes.c_int32),
                 ("kv_stages", ctypes.c_int32)]
 

@@ -194,7 +194,7 @@ void fill_plan_d(const Problem& p, attn_plan_t* out) {
     out->kv_tiles = (p.S_k + T::BN - 1) / T::BN;
     out->q_tiles_per_cta = T::TILES;
     out->bh = p.B * p.H;
-    out->ctas = out->bh * ((out->q_tiles + T::TILES - 1) / T::TILES);
+    out->units = out->bh * ((out->q_tiles + T::TILES - 1) / T::TILES);
     out->threads = T::THREADS;
     out->smem_bytes = T::SMEM_BYTES;
     out->tmem_cols = static_cast<int32_t>(T::TMEM_COLS);

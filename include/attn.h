@@ -65,7 +65,8 @@ typedef struct {
     int64_t kv_tiles;         /* ceil(S_k / block_n): key tiles per (b, h) */
     int64_t q_tiles_per_cta;  /* 2 for d <= 128 (ping-pong), 1 for d = 256 */
     int64_t bh;               /* B·H */
-    int64_t ctas;             /* grid size: bh · ceil(q_tiles / q_tiles_per_cta) */
+    int64_t units;            /* work units, bh · ceil(q_tiles / q_tiles_per_cta); the launch
+                                 runs min(units, SM count) persistent CTAs over them */
     int32_t threads;          /* threads per CTA */
     int32_t smem_bytes;       /* dynamic shared memory per CTA */
     int32_t tmem_cols;        /* tensor-memory columns allocated per CTA */

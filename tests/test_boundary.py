@@ -152,7 +152,7 @@ def test_plan_matches_page_launch_grid(lib, row):
         assert plan.block_m == 128
         assert plan.q_tiles == q_tiles
         assert plan.bh == bh
-        assert plan.ctas == bh * -(-q_tiles // plan.q_tiles_per_cta)
+        assert plan.units == bh * -(-q_tiles // plan.q_tiles_per_cta)
 
 
 def test_plan_resources_fit_the_sm():
