@@ -11,9 +11,12 @@ from .binding import (  # noqa: F401
     attn_fwd,
     attn_fwd_host,
     attn_fwd_plan,
+    attn_fwd_splitkv,
+    attn_fwd_splitkv_plan,
     attn_get_device_status,
     attn_last_error,
     fwd,
+    fwd_splitkv,
     library_path,
     load_library,
 )

@@ -25,8 +25,8 @@ ATTN_ERR_TIMEOUT = 4
 ATTN_DTYPE_F16 = 0
 ATTN_DTYPE_BF16 = 1
 
-EXPORTED = ("attn_fwd", "attn_fwd_host", "attn_fwd_plan", "attn_last_error",
-            "attn_get_device_status", "attn_version")
+EXPORTED = ("attn_fwd", "attn_fwd_host", "attn_fwd_plan", "attn_fwd_splitkv_plan",
+            "attn_fwd_splitkv", "attn_last_error", "attn_get_device_status", "attn_version")
 
 
 class AttnPlan(ctypes.Structure):
@@ -76,6 +76,12 @@ def load_library() -> ctypes.CDLL:
         lib.attn_fwd_host.restype = i32
         lib.attn_fwd_plan.argtypes = [i64, i64, i64, i64, i64, i32, i32, ctypes.POINTER(AttnPlan)]
         lib.attn_fwd_plan.restype = i32
+        lib.attn_fwd_splitkv_plan.argtypes = [i64, i64, i64, i64, i64, i32, i64,
+                                              ctypes.POINTER(i64), ctypes.POINTER(i64)]
+        lib.attn_fwd_splitkv_plan.restype = i32
+        lib.attn_fwd_splitkv.argtypes = [vp, vp, vp, vp, vp, i64, i64, i64, i64, i64,
+                                         ctypes.c_float, i32, i64, vp, i64, vp]
+        lib.attn_fwd_splitkv.restype = i32
         lib.attn_last_error.argtypes = []
         lib.attn_last_error.restype = ctypes.c_char_p
         lib.attn_get_device_status.argtypes = [vp]
@@ -130,9 +136,40 @@ def attn_fwd_plan(B, H, S_q, S_k, d, causal, dtype) -> AttnPlan:
     return plan
 
 
+def attn_fwd_splitkv_plan(B, H, S_q, S_k, d, dtype, n_split=0) -> tuple[int, int]:
+    """(ranges used, workspace bytes) for the split-KV forward; n_split 0 = automatic."""
+    n_used, ws = ctypes.c_int64(), ctypes.c_int64()
+    _check(load_library().attn_fwd_splitkv_plan(B, H, S_q, S_k, d, int(dtype), int(n_split),
+                                                ctypes.byref(n_used), ctypes.byref(ws)))
+    return n_used.value, ws.value
+
+
+def attn_fwd_splitkv(q, k, v, o, lse, B, H, S_q, S_k, d, scale, dtype, n_split, workspace,
+                     workspace_bytes, stream=None) -> None:
+    """Enqueue the split-KV forward (full attention); tensors or raw device pointers."""
+    lib = load_library()
+    ptr = lambda t: t.data_ptr() if isinstance(t, torch.Tensor) else t  # noqa: E731
+    _check(lib.attn_fwd_splitkv(ptr(q), ptr(k), ptr(v), ptr(o), ptr(lse), B, H, S_q, S_k, d,
+                                float(scale), int(dtype), int(n_split), ptr(workspace),
+                                int(workspace_bytes), _stream_handle(stream)))
+
+
 def attn_get_device_status(stream=None) -> None:
     """Synchronise and raise AttnError(ATTN_ERR_TIMEOUT) if a kernel's wait ran out."""
     _check(load_library().attn_get_device_status(_stream_handle(stream)))
+
+
+def _check_qkv(q, k, v):
+    if q.dim() != 4 or k.dim() != 4 or v.dim() != 4:
+        raise AttnError(ATTN_ERR_INVALID_ARG, "q, k, v must be 4-D [B,H,S,d]")
+    if not (q.is_contiguous() and k.is_contiguous() and v.is_contiguous()):
+        raise AttnError(ATTN_ERR_INVALID_ARG, "q, k, v must be contiguous")
+    if q.dtype != k.dtype or q.dtype != v.dtype or q.dtype not in _DTYPE_CODE:
+        raise AttnError(ATTN_ERR_UNSUPPORTED, "q, k, v must share dtype float16 or bfloat16")
+    B, H, S_q, d = q.shape
+    if k.shape[:2] != (B, H) or k.shape[3] != d or v.shape != k.shape:
+        raise AttnError(ATTN_ERR_INVALID_ARG, f"shape mismatch q{tuple(q.shape)} k{tuple(k.shape)} v{tuple(v.shape)}")
+    return B, H, S_q, k.shape[2], d
 
 
 def fwd(q: torch.Tensor, k: torch.Tensor, v: torch.Tensor, causal: bool = False,
@@ -143,16 +180,7 @@ def fwd(q: torch.Tensor, k: torch.Tensor, v: torch.Tensor, causal: bool = False,
     ``scale`` defaults to 1/sqrt(d).  Outputs are allocated with torch unless
     given.  Returns ``(o, lse)``; work is enqueued on the current stream.
     """
-    if q.dim() != 4 or k.dim() != 4 or v.dim() != 4:
-        raise AttnError(ATTN_ERR_INVALID_ARG, "q, k, v must be 4-D [B,H,S,d]")
-    if not (q.is_contiguous() and k.is_contiguous() and v.is_contiguous()):
-        raise AttnError(ATTN_ERR_INVALID_ARG, "q, k, v must be contiguous")
-    if q.dtype != k.dtype or q.dtype != v.dtype or q.dtype not in _DTYPE_CODE:
-        raise AttnError(ATTN_ERR_UNSUPPORTED, "q, k, v must share dtype float16 or bfloat16")
-    B, H, S_q, d = q.shape
-    if k.shape[:2] != (B, H) or k.shape[3] != d or v.shape != k.shape:
-        raise AttnError(ATTN_ERR_INVALID_ARG, f"shape mismatch q{tuple(q.shape)} k{tuple(k.shape)} v{tuple(v.shape)}")
-    S_k = k.shape[2]
+    B, H, S_q, S_k, d = _check_qkv(q, k, v)
     if scale is None:
         scale = 1.0 / math.sqrt(d)
     if out is None:
@@ -160,4 +188,29 @@ def fwd(q: torch.Tensor, k: torch.Tensor, v: torch.Tensor, causal: bool = False,
     if lse is None:
         lse = torch.empty((B, H, S_q), dtype=torch.float32, device=q.device)
     attn_fwd(q, k, v, out, lse, B, H, S_q, S_k, d, causal, scale, _DTYPE_CODE[q.dtype])
+    return out, lse
+
+
+def fwd_splitkv(q: torch.Tensor, k: torch.Tensor, v: torch.Tensor, n_split: int = 0,
+                scale: float | None = None, workspace: torch.Tensor | None = None,
+                out: torch.Tensor | None = None, lse: torch.Tensor | None = None):
+    """Split-KV forward (full attention) of contiguous CUDA tensors; see :func:`fwd`.
+
+    ``n_split`` 0 lets the library choose.  The workspace is allocated with
+    torch unless given (a uint8 tensor of at least the planned size).
+    Returns ``(o, lse)``.
+    """
+    B, H, S_q, S_k, d = _check_qkv(q, k, v)
+    dtype = _DTYPE_CODE[q.dtype]
+    if scale is None:
+        scale = 1.0 / math.sqrt(d)
+    _, ws = attn_fwd_splitkv_plan(B, H, S_q, S_k, d, dtype, n_split)
+    if workspace is None:
+        workspace = torch.empty(max(ws, 16), dtype=torch.uint8, device=q.device)
+    if out is None:
+        out = torch.empty_like(q)
+    if lse is None:
+        lse = torch.empty((B, H, S_q), dtype=torch.float32, device=q.device)
+    attn_fwd_splitkv(q, k, v, out, lse, B, H, S_q, S_k, d, scale, dtype, n_split, workspace,
+                     workspace.numel() * workspace.element_size())
     return out, lse

@@ -1,7 +1,8 @@
 """Build libattn.so in-tree with nvcc for sm_103a.
 
-Each (head_dim, dtype, causal) instantiation of the kernel is compiled as its
-own object in parallel, then linked with the C-ABI layer into
+Each (head_dim, dtype, causal / split-KV) instantiation of the kernel is
+compiled as its own object in parallel, then linked with the merge kernel and
+the C-ABI layer into
 ``exact_attention_53_gb300/libattn.so``.  Objects go to ``_build/`` beside this
 file; an object is rebuilt only when a source or header is newer than it.
 """
@@ -24,7 +25,10 @@ LIB = os.path.join(PKG, "libattn.so")
 ARCH = ["-gencode", "arch=compute_103a,code=sm_103a"]
 FLAGS = ["-O3", "-std=c++17", "-lineinfo", "-Xcompiler", "-fPIC", "-I" + INCLUDE, "-I" + CSRC]
 
-INSTANCES = [(d, bf16, causal) for d in (64, 128, 256) for bf16 in (0, 1) for causal in (0, 1)]
+# (head_dim, bf16, causal, split): every masked/unmasked kernel, plus the
+# split-KV variant of full attention.
+INSTANCES = ([(d, bf16, causal, 0) for d in (64, 128, 256) for bf16 in (0, 1) for causal in (0, 1)]
+             + [(d, bf16, 0, 1) for d in (64, 128, 256) for bf16 in (0, 1)])
 
 
 def _nvcc() -> str:
@@ -57,20 +61,22 @@ def build(verbose: bool = False, jobs: int | None = None) -> str:
     nvcc = _nvcc()
     os.makedirs(BUILD, exist_ok=True)
     deps = _deps()
-    jobs = jobs or max(1, min(len(INSTANCES) + 1, os.cpu_count() or 4))
+    jobs = jobs or max(1, min(len(INSTANCES) + 2, os.cpu_count() or 4))
     steps = []
     objs = []
-    for d, bf16, causal in INSTANCES:
-        obj = os.path.join(BUILD, f"attn_fwd_d{d}_{'bf16' if bf16 else 'f16'}_{'causal' if causal else 'full'}.o")
+    for d, bf16, causal, split in INSTANCES:
+        mode = "split" if split else ("causal" if causal else "full")
+        obj = os.path.join(BUILD, f"attn_fwd_d{d}_{'bf16' if bf16 else 'f16'}_{mode}.o")
         objs.append(obj)
         if _stale(obj, deps):
             steps.append([nvcc, *ARCH, *FLAGS, f"-DATTN_D={d}", f"-DATTN_BF16={bf16}",
-                          f"-DATTN_CAUSAL={causal}", "-c", os.path.join(CSRC, "attn_inst.cu"),
-                          "-o", obj])
-    api_obj = os.path.join(BUILD, "attn_api.o")
-    objs.append(api_obj)
-    if _stale(api_obj, deps):
-        steps.append([nvcc, *ARCH, *FLAGS, "-c", os.path.join(CSRC, "attn_api.cu"), "-o", api_obj])
+                          f"-DATTN_CAUSAL={causal}", f"-DATTN_SPLIT={split}", "-c",
+                          os.path.join(CSRC, "attn_inst.cu"), "-o", obj])
+    for name in ("attn_api", "attn_combine"):
+        obj = os.path.join(BUILD, f"{name}.o")
+        objs.append(obj)
+        if _stale(obj, deps):
+            steps.append([nvcc, *ARCH, *FLAGS, "-c", os.path.join(CSRC, f"{name}.cu"), "-o", obj])
     if steps:
         if verbose:
             print(f"[build] compiling {len(steps)} objects with {jobs} jobs", file=sys.stderr)

@@ -7,6 +7,7 @@
 // scale are checked here as well, because the library takes raw pointers.
 #include <cudaTypedefs.h>
 
+#include <algorithm>
 #include <atomic>
 #include <cmath>
 #include <cstdarg>
@@ -212,10 +213,10 @@ using LaunchFn = cudaError_t (*)(const attn::FwdArgs&, cudaStream_t);
 LaunchFn pick(int64_t d, bool bf16, bool causal) {
 #define ATTN_PICK(D)                                                                   \
     if (d == D) {                                                                      \
-        if (bf16) return causal ? attn::launch_attn_fwd<D, true, true>                 \
-                                : attn::launch_attn_fwd<D, true, false>;               \
-        return causal ? attn::launch_attn_fwd<D, false, true>                          \
-                      : attn::launch_attn_fwd<D, false, false>;                        \
+        if (bf16) return causal ? attn::launch_attn_fwd<D, true, true, false>          \
+                                : attn::launch_attn_fwd<D, true, false, false>;        \
+        return causal ? attn::launch_attn_fwd<D, false, true, false>                   \
+                      : attn::launch_attn_fwd<D, false, false, false>;                 \
     }
     ATTN_PICK(64)
     ATTN_PICK(128)
@@ -224,12 +225,20 @@ LaunchFn pick(int64_t d, bool bf16, bool causal) {
     return nullptr;
 }
 
-attn_status_t launch_checked(const Problem& p, const void* q, const void* k, const void* v,
-                             void* o, float* lse, cudaStream_t stream) {
-    int dev = 0;
-    attn_status_t s = check_device(&dev);
-    if (s != ATTN_OK) return s;
-    attn::FwdArgs a;
+LaunchFn pick_split(int64_t d, bool bf16) {
+    if (d == 64) return bf16 ? attn::launch_attn_fwd<64, true, false, true>
+                             : attn::launch_attn_fwd<64, false, false, true>;
+    if (d == 128) return bf16 ? attn::launch_attn_fwd<128, true, false, true>
+                              : attn::launch_attn_fwd<128, false, false, true>;
+    if (d == 256) return bf16 ? attn::launch_attn_fwd<256, true, false, true>
+                              : attn::launch_attn_fwd<256, false, false, true>;
+    return nullptr;
+}
+
+// Maps, sizes and device words shared by every launch of problem p.
+attn_status_t fill_args(attn::FwdArgs& a, const Problem& p, int dev, const void* q, const void* k,
+                        const void* v, void* o, float* lse) {
+    attn_status_t s;
     if ((s = encode_rows(&a.tm_q, q, p, p.S_q, "q")) != ATTN_OK) return s;
     if ((s = encode_rows(&a.tm_k, k, p, p.S_k, "k")) != ATTN_OK) return s;
     if ((s = encode_rows(&a.tm_v, v, p, p.S_k, "v")) != ATTN_OK) return s;
@@ -242,11 +251,88 @@ attn_status_t launch_checked(const Problem& p, const void* q, const void* k, con
     a.scale_log2 = static_cast<float>(static_cast<double>(p.scale) * 1.4426950408889634);
     a.status = g_status_ptr[dev].load();
     a.num_sms = g_num_sms[dev].load();
+    a.n_split = 1;
+    a.kv_per_split = 0;
+    a.o_part = nullptr;
+    a.lse_part = nullptr;
+    return ATTN_OK;
+}
+
+attn_status_t launch_checked(const Problem& p, const void* q, const void* k, const void* v,
+                             void* o, float* lse, cudaStream_t stream) {
+    int dev = 0;
+    attn_status_t s = check_device(&dev);
+    if (s != ATTN_OK) return s;
+    attn::FwdArgs a;
+    if ((s = fill_args(a, p, dev, q, k, v, o, lse)) != ATTN_OK) return s;
     LaunchFn fn = pick(p.d, p.dtype == ATTN_DTYPE_BF16, p.causal);
     if (!fn) return fail(ATTN_ERR_UNSUPPORTED, "no kernel for d=%lld", (long long)p.d);
     cudaError_t e = fn(a, stream);
     if (e != cudaSuccess) return fail(ATTN_ERR_CUDA, "kernel launch: %s", cudaGetErrorString(e));
     return ok();
+}
+
+// ---------------------------------------------------------------- split-KV
+struct SplitPlan {
+    int64_t n_split;         // key ranges actually used (no range is empty)
+    int64_t kv_per_split;    // key tiles per range (the last may have fewer)
+    int64_t workspace_bytes; // 0 when n_split == 1 (the plain kernel runs)
+};
+
+// Split-KV units hold one 128-row query tile each.
+int64_t split_query_blocks(const Problem& p) { return (p.S_q + attn::kBlockM - 1) / attn::kBlockM; }
+
+// Requested (or, for 0, chosen) range count -> ranges, tiles per range, bytes.
+// Auto: the count whose persistent schedule (waves of num_sms units, a unit
+// costing its key tiles plus about one tile of setup) finishes first; ties go
+// to fewer ranges, which also keeps the merge pass small.
+attn_status_t split_plan(const Problem& p, int64_t n_req, int num_sms, SplitPlan* out) {
+    const int64_t n_kv = (p.S_k + attn::kBlockN - 1) / attn::kBlockN;
+    const int64_t base = p.B * p.H * split_query_blocks(p);
+    int64_t n = 1;
+    if (n_req > 0) {
+        n = std::min(n_req, n_kv);
+    } else {
+        double best = 0;
+        const int64_t cap = std::min<int64_t>(n_kv, 1024);
+        for (int64_t c = 1; c <= cap; ++c) {
+            const int64_t per = (n_kv + c - 1) / c;
+            const int64_t used = (n_kv + per - 1) / per;
+            const int64_t waves = (base * used + num_sms - 1) / num_sms;
+            const double cost = double(waves) * double(per + 1);
+            if (c == 1 || cost < best) {
+                best = cost;
+                n = used;
+            }
+        }
+    }
+    const int64_t per = (n_kv + n - 1) / n;
+    n = (n_kv + per - 1) / per;
+    if (base * n > INT32_MAX)
+        return fail(ATTN_ERR_INVALID_ARG, "n_split=%lld gives %lld work units, above 2^31-1",
+                    (long long)n, (long long)(base * n));
+    if (n > 1 && double(n) * double(p.B * p.H) * double(p.S_q) * double(p.d + 1) * 4.0 > 0x1p60)
+        return fail(ATTN_ERR_INVALID_ARG, "n_split=%lld needs a workspace above 2^60 bytes",
+                    (long long)n);
+    out->n_split = n;
+    out->kv_per_split = per;
+    out->workspace_bytes =
+        n > 1 ? n * p.B * p.H * p.S_q * (p.d + 1) * int64_t(sizeof(float)) : 0;
+    return ATTN_OK;
+}
+
+attn_status_t resolve_split(const Problem& p, int64_t n_split, SplitPlan* sp) {
+    if (n_split < 0)
+        return fail(ATTN_ERR_INVALID_ARG, "n_split must be >= 0 (0 = automatic), got %lld",
+                    (long long)n_split);
+    int sms = 0;
+    if (n_split == 0) {
+        int dev = 0;
+        attn_status_t s = check_device(&dev);
+        if (s != ATTN_OK) return s;
+        sms = g_num_sms[dev].load();
+    }
+    return split_plan(p, n_split, sms, sp);
 }
 
 }  // namespace
@@ -301,6 +387,62 @@ attn_status_t attn_fwd_plan(int64_t B, int64_t H, int64_t S_q, int64_t S_k, int6
     attn_status_t s = validate_sizes(p, B, H, S_q, S_k, d, causal, 1.0f, dtype);
     if (s != ATTN_OK) return s;
     fill_plan(p, plan);
+    return ok();
+}
+
+attn_status_t attn_fwd_splitkv_plan(int64_t B, int64_t H, int64_t S_q, int64_t S_k, int64_t d,
+                                    attn_dtype_t dtype, int64_t n_split, int64_t* n_split_used,
+                                    int64_t* workspace_bytes) {
+    if (!n_split_used) return fail(ATTN_ERR_INVALID_ARG, "n_split_used is null");
+    if (!workspace_bytes) return fail(ATTN_ERR_INVALID_ARG, "workspace_bytes is null");
+    Problem p;
+    attn_status_t s = validate_sizes(p, B, H, S_q, S_k, d, 0, 1.0f, dtype);
+    if (s != ATTN_OK) return s;
+    SplitPlan sp;
+    if ((s = resolve_split(p, n_split, &sp)) != ATTN_OK) return s;
+    *n_split_used = sp.n_split;
+    *workspace_bytes = sp.workspace_bytes;
+    return ok();
+}
+
+attn_status_t attn_fwd_splitkv(const void* q, const void* k, const void* v, void* o, float* lse,
+                               int64_t B, int64_t H, int64_t S_q, int64_t S_k, int64_t d,
+                               float scale, attn_dtype_t dtype, int64_t n_split, void* workspace,
+                               int64_t workspace_bytes, struct CUstream_st* stream) {
+    Problem p;
+    attn_status_t s = validate_sizes(p, B, H, S_q, S_k, d, 0, scale, dtype);
+    if (s != ATTN_OK) return s;
+    if ((s = validate_device_ptrs(p, q, k, v, o, lse)) != ATTN_OK) return s;
+    SplitPlan sp;
+    if ((s = resolve_split(p, n_split, &sp)) != ATTN_OK) return s;
+    if (sp.n_split == 1) return launch_checked(p, q, k, v, o, lse, stream);
+    if (!workspace) return fail(ATTN_ERR_INVALID_ARG, "workspace is null");
+    if (!aligned(workspace, 16)) return fail(ATTN_ERR_INVALID_ARG, "workspace is not 16-byte aligned");
+    if (workspace_bytes < sp.workspace_bytes)
+        return fail(ATTN_ERR_INVALID_ARG, "workspace_bytes=%lld is below the %lld bytes %lld ranges need",
+                    (long long)workspace_bytes, (long long)sp.workspace_bytes, (long long)sp.n_split);
+    const size_t wb = static_cast<size_t>(sp.workspace_bytes);
+    if (overlaps(workspace, wb, q, p.q_bytes)) return fail(ATTN_ERR_INVALID_ARG, "workspace overlaps q");
+    if (overlaps(workspace, wb, k, p.kv_bytes)) return fail(ATTN_ERR_INVALID_ARG, "workspace overlaps k");
+    if (overlaps(workspace, wb, v, p.kv_bytes)) return fail(ATTN_ERR_INVALID_ARG, "workspace overlaps v");
+    if (overlaps(workspace, wb, o, p.o_bytes)) return fail(ATTN_ERR_INVALID_ARG, "workspace overlaps o");
+    if (overlaps(workspace, wb, lse, p.lse_bytes)) return fail(ATTN_ERR_INVALID_ARG, "workspace overlaps lse");
+    int dev = 0;
+    if ((s = check_device(&dev)) != ATTN_OK) return s;
+    attn::FwdArgs a;
+    if ((s = fill_args(a, p, dev, q, k, v, o, lse)) != ATTN_OK) return s;
+    const int64_t rows = p.B * p.H * p.S_q;
+    a.n_split = static_cast<int32_t>(sp.n_split);
+    a.kv_per_split = static_cast<int32_t>(sp.kv_per_split);
+    a.o_part = static_cast<float*>(workspace);
+    a.lse_part = a.o_part + sp.n_split * rows * p.d;
+    LaunchFn fn = pick_split(p.d, p.dtype == ATTN_DTYPE_BF16);
+    if (!fn) return fail(ATTN_ERR_UNSUPPORTED, "no kernel for d=%lld", (long long)p.d);
+    cudaError_t e = fn(a, stream);
+    if (e != cudaSuccess) return fail(ATTN_ERR_CUDA, "kernel launch: %s", cudaGetErrorString(e));
+    e = attn::launch_attn_combine(a.o_part, a.lse_part, o, lse, a.n_split, rows,
+                                  static_cast<int>(p.d), p.dtype == ATTN_DTYPE_BF16, stream);
+    if (e != cudaSuccess) return fail(ATTN_ERR_CUDA, "combine launch: %s", cudaGetErrorString(e));
     return ok();
 }
 

@@ -153,15 +153,17 @@ __device__ __forceinline__ void unit_coords(int L, int BH, int n_qblk, int head_
 // mbarrier phase and the K/V ring position carry over from one unit to the
 // next, so the next unit's Q load and first Q·Kᵀ overlap the current unit's
 // last P·V and epilogue.
-template <int D, bool BF16, bool CAUSAL>
-__global__ void __launch_bounds__(FwdTile<D>::THREADS, 1)
+template <int D, bool BF16, bool CAUSAL, bool SPLIT>
+__global__ void __launch_bounds__(KernelTile<D, SPLIT>::THREADS, 1)
     attn_fwd_kernel(const __grid_constant__ CUtensorMap tm_q,
                     const __grid_constant__ CUtensorMap tm_k,
                     const __grid_constant__ CUtensorMap tm_v,
                     const __grid_constant__ CUtensorMap tm_o,
                     float* __restrict__ lse_ptr, int S_q, int S_k, int BH, int n_qblk,
-                    int head_group, float scale_log2, unsigned int* __restrict__ status) {
-    using T = FwdTile<D>;
+                    int head_group, float scale_log2, unsigned int* __restrict__ status,
+                    int n_split, int kv_per_split, float* __restrict__ o_part,
+                    float* __restrict__ lse_part) {
+    using T = KernelTile<D, SPLIT>;
     using namespace sm100;
     constexpr int ROWS = T::BM * T::TILES;                 // query rows per unit
 
@@ -187,7 +189,23 @@ __global__ void __launch_bounds__(FwdTile<D>::THREADS, 1)
 
     const int warp = threadIdx.x >> 5;
     const int lane = threadIdx.x & 31;
-    const int n_units = BH * n_qblk;
+    // SPLIT: every (head, query block) is cut into n_split work units along the
+    // keys (kv_per_split key tiles each); each writes O/l in fp32 and its own
+    // log-sum-exp to o_part / lse_part for attn_combine to merge.
+    const int n_units = BH * n_qblk * (SPLIT ? n_split : 1);
+    // Unit L -> head, first query row, key tiles of each query tile, first key tile, split.
+    auto unit_info = [&](int L, int& bh, int& q0, int& n0, int& n1, int& kb, int& sp) {
+        sp = SPLIT ? L % n_split : 0;
+        unit_coords<CAUSAL, ROWS>(SPLIT ? L / n_split : L, BH, n_qblk, head_group, bh, q0);
+        n0 = kv_tiles_for<CAUSAL>(q0, S_q, S_k);
+        n1 = T::TILES == 2 ? kv_tiles_for<CAUSAL>(q0 + T::BM, S_q, S_k) : 0;
+        kb = 0;
+        if (SPLIT) {
+            kb = sp * kv_per_split;
+            n0 = max(0, min(n0, kb + kv_per_split) - kb);
+            n1 = max(0, min(n1, kb + kv_per_split) - kb);
+        }
+    };
     // Units are handed out in rounds of gridDim.x, in serpentine order (CTA c
     // takes position c of even rounds and gridDim.x-1-c of odd ones), so a CTA
     // that got a heavy unit in one round gets a light one in the next.
@@ -275,10 +293,8 @@ __global__ void __launch_bounds__(FwdTile<D>::THREADS, 1)
         for (int r = 0; r * static_cast<int>(gridDim.x) < n_units && ok; ++r) {
             const int L = unit_of_round(r);
             if (L >= n_units) continue;
-            int bh, q0;
-            unit_coords<CAUSAL, ROWS>(L, BH, n_qblk, head_group, bh, q0);
-            const int n0 = kv_tiles_for<CAUSAL>(q0, S_q, S_k);
-            const int n1 = T::TILES == 2 ? kv_tiles_for<CAUSAL>(q0 + T::BM, S_q, S_k) : 0;
+            int bh, q0, n0, n1, kb, sp;
+            unit_info(L, bh, q0, n0, n1, kb, sp);
             const int n_max = max(n0, n1);
             const int uq_now = uq++;
             // Q of this unit once the previous unit's last Q·Kᵀ is done.
@@ -297,15 +313,15 @@ __global__ void __launch_bounds__(FwdTile<D>::THREADS, 1)
             // K/V in the MMA warp's consumption order.
             if (T::TILES == 2) {
                 for (int j = 0; j < n_max; ++j) {
-                    issue(&tm_k, j, bh);
-                    issue(&tm_v, j, bh);
+                    issue(&tm_k, kb + j, bh);
+                    issue(&tm_v, kb + j, bh);
                 }
             } else {
-                issue(&tm_k, 0, bh);
-                if (n_max > 1) issue(&tm_k, 1, bh);
+                issue(&tm_k, kb, bh);
+                if (n_max > 1) issue(&tm_k, kb + 1, bh);
                 for (int j = 0; j < n_max; ++j) {
-                    issue(&tm_v, j, bh);
-                    if (j + 2 < n_max) issue(&tm_k, j + 2, bh);
+                    issue(&tm_v, kb + j, bh);
+                    if (j + 2 < n_max) issue(&tm_k, kb + j + 2, bh);
                 }
             }
         }
@@ -397,10 +413,8 @@ __global__ void __launch_bounds__(FwdTile<D>::THREADS, 1)
         for (int r = 0; r * static_cast<int>(gridDim.x) < n_units && ok; ++r) {
             const int L = unit_of_round(r);
             if (L >= n_units) continue;
-            int bh, q0;
-            unit_coords<CAUSAL, ROWS>(L, BH, n_qblk, head_group, bh, q0);
-            const int n0 = kv_tiles_for<CAUSAL>(q0, S_q, S_k);
-            const int n1 = T::TILES == 2 ? kv_tiles_for<CAUSAL>(q0 + T::BM, S_q, S_k) : 0;
+            int bh, q0, n0, n1, kb, sp;
+            unit_info(L, bh, q0, n0, n1, kb, sp);
             const int n_max = max(n0, n1);
             ok = mbar_wait(q_full, uq & 1, abort_flag, status, kStatusMma);
             ++uq;
@@ -508,10 +522,8 @@ __global__ void __launch_bounds__(FwdTile<D>::THREADS, 1)
         for (int r = 0; r * static_cast<int>(gridDim.x) < n_units && ok; ++r) {
             const int L = unit_of_round(r);
             if (L >= n_units) continue;
-            int bh, q0;
-            unit_coords<CAUSAL, ROWS>(L, BH, n_qblk, head_group, bh, q0);
-            const int n0 = kv_tiles_for<CAUSAL>(q0, S_q, S_k);
-            const int n1 = T::TILES == 2 ? kv_tiles_for<CAUSAL>(q0 + T::BM, S_q, S_k) : 0;
+            int bh, q0, n0, n1, kb, sp;
+            unit_info(L, bh, q0, n0, n1, kb, sp);
             const int n = t == 0 ? n0 : n1;
             const int row_begin = q0 + t * T::BM;
             const int q_idx = row_begin + row;
@@ -539,7 +551,7 @@ __global__ void __launch_bounds__(FwdTile<D>::THREADS, 1)
                     s[64 + c] = __uint_as_float(sb[c]);
                 }
 
-                const int kv0 = j * T::BN;
+                const int kv0 = (kb + j) * T::BN;
                 const bool masked = (CAUSAL && kv0 + T::BN - 1 > row_begin) || (kv0 + T::BN > S_k);
                 // keys kv0 + c with c < lim are visible to this row
                 const int lim = masked ? max(0, min(S_k, CAUSAL ? q_idx + 1 : S_k) - kv0) : T::BN;
@@ -620,6 +632,36 @@ __global__ void __launch_bounds__(FwdTile<D>::THREADS, 1)
             if (!ok) break;
 
             // ---------------------------------------------------------- epilogue
+            if (SPLIT) {
+                // Partial result of this key range: O/l in fp32 and its LSE.
+                if (n > 0) {
+                    ok = mbar_wait(&o_done[t], oc & 1, abort_flag, status, kStatusEpilogue);
+                    ok = __all_sync(0xffffffffu, ok);
+                    if (!ok) break;
+                    ++oc;
+                    tc_fence_after();
+                    const float inv_l = 1.f / l;
+                    const bool store = q_idx < S_q;
+                    const size_t prow = (static_cast<size_t>(sp) * BH + bh) * S_q + q_idx;
+                    float4* dst = reinterpret_cast<float4*>(o_part + prow * D);
+                    const uint32_t o_base = lane_base + T::O_COL + t * D;
+#pragma unroll 1
+                    for (int cc = 0; cc < D; cc += 32) {
+                        uint32_t v[32];
+                        tmem_ld32(o_base + cc, v);
+                        if (store) {
+#pragma unroll
+                            for (int i = 0; i < 8; ++i)
+                                dst[cc / 4 + i] = make_float4(__uint_as_float(v[4 * i]) * inv_l,
+                                                              __uint_as_float(v[4 * i + 1]) * inv_l,
+                                                              __uint_as_float(v[4 * i + 2]) * inv_l,
+                                                              __uint_as_float(v[4 * i + 3]) * inv_l);
+                        }
+                    }
+                    if (store) lse_part[prow] = (m + log2f(l)) * kLn2;
+                }
+                continue;
+            }
             // Rounds of the staging buffer run in a fixed order over the CTA:
             // tile 0's then tile 1's, unit after unit.
             const uint32_t rounds_t0 = n0 > 0 ? T::STAGE_ROUNDS : 0;
@@ -697,10 +739,11 @@ __global__ void __launch_bounds__(FwdTile<D>::THREADS, 1)
     }
 }
 
-template <int D, bool BF16, bool CAUSAL>
+template <int D, bool BF16, bool CAUSAL, bool SPLIT>
 cudaError_t launch_attn_fwd(const FwdArgs& a, cudaStream_t stream) {
-    using T = FwdTile<D>;
-    auto kernel = attn_fwd_kernel<D, BF16, CAUSAL>;
+    using T = KernelTile<D, SPLIT>;
+    static_assert(!(SPLIT && CAUSAL), "split-KV is built for full attention only");
+    auto kernel = attn_fwd_kernel<D, BF16, CAUSAL, SPLIT>;
     cudaError_t err = cudaFuncSetAttribute(kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
                                            T::SMEM_BYTES);
     if (err != cudaSuccess) return err;
@@ -720,13 +763,15 @@ cudaError_t launch_attn_fwd(const FwdArgs& a, cudaStream_t stream) {
     }
     const int rows_per_cta = T::BM * T::TILES;
     const int n_qblk = (a.S_q + rows_per_cta - 1) / rows_per_cta;
-    const long long units = static_cast<long long>(a.BH) * n_qblk;
+    const int n_split = SPLIT ? a.n_split : 1;
+    const long long units = static_cast<long long>(a.BH) * n_qblk * n_split;
     if (units > 0x7fffffffLL) return cudaErrorInvalidConfiguration;
     // One CTA per SM (each takes the whole of tensor memory), looping over units.
     const int grid = static_cast<int>(std::min<long long>(units, a.num_sms));
     kernel<<<grid, T::THREADS, T::SMEM_BYTES, stream>>>(a.tm_q, a.tm_k, a.tm_v, a.tm_o, a.lse, a.S_q,
                                                          a.S_k, a.BH, n_qblk, head_group,
-                                                         a.scale_log2, a.status);
+                                                         a.scale_log2, a.status, n_split,
+                                                         a.kv_per_split, a.o_part, a.lse_part);
     return cudaGetLastError();
 }
 

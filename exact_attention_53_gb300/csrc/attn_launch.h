@@ -20,6 +20,11 @@ struct FwdArgs {
     int32_t BH;             // B·H
     float scale_log2;       // scale · log2(e), >= 0
     int32_t num_sms;        // SMs of the device: the persistent grid size
+    // split-KV only (launch_attn_fwd<..., SPLIT = true>)
+    int32_t n_split;        // key ranges per (head, query block)
+    int32_t kv_per_split;   // key tiles per range
+    float* o_part;          // [n_split, B·H, S_q, d] fp32: O/l of each range
+    float* lse_part;        // [n_split, B·H, S_q] fp32: LSE of each range
     unsigned int* status;   // device status word (bit set on a wait that ran out)
 };
 
@@ -34,11 +39,14 @@ __host__ __device__ constexpr int q_tiles_per_cta(int d) { return d == 256 ? 1 :
 
 // Static plan of one kernel instantiation: tiles, warp roles, shared and
 // tensor memory.  Shared by the kernel and the host (attn_fwd_plan).
-template <int D>
+// TILES_: query tiles per work unit (q_tiles_per_cta(D) for the one-pass
+// forward; 1 for split-KV, whose units are short and must not wait on a
+// second query tile that short queries leave empty).
+template <int D, int TILES_ = q_tiles_per_cta(D)>
 struct FwdTile {
     static constexpr int BM = kBlockM;
     static constexpr int BN = kBlockN;
-    static constexpr int TILES = q_tiles_per_cta(D);
+    static constexpr int TILES = TILES_;
     static constexpr int CHUNKS = D / 64;                 // 128-byte swizzle atoms along d
     static constexpr int ATOM_ROWS_BYTES = 128;           // one row of one atom
     static constexpr int Q_CHUNK_BYTES = BM * ATOM_ROWS_BYTES;
@@ -75,7 +83,17 @@ struct FwdTile {
     static_assert(O_COL + TILES * D <= TMEM_COLS, "tensor memory budget");
 };
 
-template <int D, bool BF16, bool CAUSAL>
+// The tile plan a kernel instantiation runs with.
+template <int D, bool SPLIT>
+using KernelTile = FwdTile<D, SPLIT ? 1 : q_tiles_per_cta(D)>;
+
+template <int D, bool BF16, bool CAUSAL, bool SPLIT>
 cudaError_t launch_attn_fwd(const FwdArgs& args, cudaStream_t stream);
+
+// Merge n_split partial results: LSE = ln Σ_s exp(LSE_s), O = Σ_s exp(LSE_s − LSE)·O_s,
+// written as the output dtype into o and as fp32 into lse.  rows = B·H·S_q.
+cudaError_t launch_attn_combine(const float* o_part, const float* lse_part, void* o, float* lse,
+                                int n_split, long long rows, int d, bool bf16,
+                                cudaStream_t stream);
 
 }  // namespace attn

@@ -7,10 +7,11 @@ inputs from it.  Inputs are drawn on the CPU in float32 from
 workload dtype, and only then copied to a device, so every consumer sees the
 same rounded values.
 
-The five named workloads follow the configurations the attention page's
+The five workloads c1..c5 follow the configurations the attention page's
 FlashAttention-3 plan is sized for (oxicuda-dnn 0.1.8 hopper.rs,
 ``SUPPORTED_HEAD_DIMS`` = 64/128/256 and ``default_for`` tile sizes), with the
-shapes, value distributions and seeds fixed here.
+shapes, value distributions and seeds fixed here; ``decode`` is the short-query,
+long-key shape the split-KV forward is for.
 """
 
 from __future__ import annotations
@@ -59,6 +60,10 @@ WORKLOADS = {
                    "normal2", "normal", 1004),
     "c5": Workload("c5", 2, 8, 8192, 8192, 256, "bf16", (False,), 1 / 16,
                    "normal", "normal", 1005),
+    # Decoding step against a long key cache: one query row per head and few
+    # heads, so B·H alone gives far fewer work units than SMs (split-KV).
+    "decode": Workload("decode", 2, 16, 1, 32768, 128, "bf16", (False,), 1 / math.sqrt(128),
+                       "normal", "normal", 1006),
 }
 
 TORCH_DTYPE = {"f16": torch.float16, "bf16": torch.bfloat16}

@@ -121,6 +121,60 @@ attn_status_t attn_fwd_host(const void* q_host, const void* k_host, const void* 
                             struct CUstream_st* stream);
 
 /*
+ * Split-KV forward (full attention, short S_q against long S_k).
+ *
+ * The same O and LSE as attn_fwd with causal = 0, computed with the keys of
+ * every (b, h, query block) cut into n_split ranges of whole 128-key tiles so
+ * that enough work units exist to fill the GPU when B·H·ceil(S_q/256) is small
+ * (decoding).  Each range writes its normalised partial output O_s (fp32) and
+ * its log-sum-exp LSE_s to the caller's workspace; a second kernel merges them
+ * with LSE = ln Σ_s exp(LSE_s), O = Σ_s exp(LSE_s − LSE)·O_s.  The merge uses
+ * only the LSE output the page's forward defines (oxicuda-dnn 0.1.8,
+ * src/attn/flash_attn/hopper.rs, FlashAttention3Plan::generate_forward, final
+ * step); the page itself has no split-KV scheme.  Rounding differs from
+ * attn_fwd (the partial outputs are rounded to fp32, not to the output
+ * dtype), within the same tolerance of the exact result.
+ *
+ * attn_fwd_splitkv_plan — ranges and workspace size for these sizes.
+ *   n_split          0 = automatic: the count whose schedule over the current
+ *                    device's SMs finishes first (queries the device); >= 1 =
+ *                    that many ranges, capped at ceil(S_k/128) and reduced
+ *                    so that no range is empty
+ *   *n_split_used    ranges attn_fwd_splitkv will use (1 = the plain kernel
+ *                    runs and no workspace is needed)
+ *   *workspace_bytes n_split_used · B·H·S_q · (d + 1) · 4, or 0 when
+ *                    n_split_used is 1
+ * Validates like attn_fwd; n_split < 0 and null outputs are
+ * ATTN_ERR_INVALID_ARG.  Only n_split = 0 touches the device.
+ */
+attn_status_t attn_fwd_splitkv_plan(int64_t B, int64_t H, int64_t S_q, int64_t S_k, int64_t d,
+                                    attn_dtype_t dtype, int64_t n_split, int64_t* n_split_used,
+                                    int64_t* workspace_bytes);
+
+/*
+ * attn_fwd_splitkv — enqueue the split-KV forward on `stream`.
+ *
+ *   q, k, v, o, lse, B, H, S_q, S_k, d, scale, dtype, stream  as attn_fwd
+ *                    (no causal argument: full attention only)
+ *   n_split          as attn_fwd_splitkv_plan (the same device must be
+ *                    current for n_split = 0, so both pick the same count)
+ *   workspace        device pointer, 16-byte aligned, at least the
+ *                    workspace_bytes attn_fwd_splitkv_plan reports; may be
+ *                    null when that is 0.  Owned by the caller; written
+ *                    before it is read on every call (nothing needs clearing),
+ *                    must not overlap q, k, v, o or lse, and must not be used
+ *                    by another call in flight at the same time
+ *   workspace_bytes  size of `workspace` in bytes
+ *
+ * Launches two kernels (ranges, then merge) in order on `stream`, or the
+ * attn_fwd kernel alone when one range is used.
+ */
+attn_status_t attn_fwd_splitkv(const void* q, const void* k, const void* v, void* o, float* lse,
+                               int64_t B, int64_t H, int64_t S_q, int64_t S_k, int64_t d,
+                               float scale, attn_dtype_t dtype, int64_t n_split, void* workspace,
+                               int64_t workspace_bytes, struct CUstream_st* stream);
+
+/*
  * attn_last_error — message for the last non-OK status returned on this host
  * thread ("" if none).  The string stays valid until the next call on this
  * thread.

@@ -36,8 +36,9 @@ def _declared_functions():
 
 def test_header_declares_the_boundary():
     names = _declared_functions()
-    assert names == sorted(["attn_fwd", "attn_fwd_host", "attn_fwd_plan", "attn_last_error",
-                            "attn_get_device_status", "attn_version"])
+    assert names == sorted(["attn_fwd", "attn_fwd_host", "attn_fwd_plan", "attn_fwd_splitkv_plan",
+                            "attn_fwd_splitkv", "attn_last_error", "attn_get_device_status",
+                            "attn_version"])
 
 
 def test_library_exports_every_declared_symbol(lib):
@@ -173,3 +174,62 @@ def test_plan_validates_like_fwd(lib):
     with pytest.raises(binding.AttnError, match="S_q must be"):
         binding.attn_fwd_plan(1, 1, 0, 16, 64, 0, binding.ATTN_DTYPE_BF16)
     assert lib.attn_fwd_plan(1, 1, 16, 16, 64, 0, 1, None) == binding.ATTN_ERR_INVALID_ARG
+
+
+# ------------------------------------------------------------------ split-KV
+
+
+@pytest.mark.parametrize("S_k,n_req,n_used", [
+    (128, 4, 1),            # one key tile: one range whatever is asked
+    (1000, 1, 1),
+    (1000, 3, 3),           # 8 tiles -> 3,3,2
+    (1000, 5, 4),           # 8 tiles: ceil(8/5)=2 per range -> 4 ranges, none empty
+    (1000, 8, 8),
+    (1000, 50, 8),          # capped at the tile count
+    (16384, 7, 7),          # 128 tiles: 19 per range -> 7 ranges
+    (16385, 128, 65),       # 129 tiles: 2 per range -> 65 ranges
+])
+def test_splitkv_plan_ranges_and_workspace(lib, S_k, n_req, n_used):
+    B, H, S_q, d = 2, 3, 37, 128
+    n, ws = binding.attn_fwd_splitkv_plan(B, H, S_q, S_k, d, binding.ATTN_DTYPE_BF16, n_req)
+    assert n == n_used
+    assert ws == (n * B * H * S_q * (d + 1) * 4 if n > 1 else 0)
+    tiles = -(-S_k // 128)
+    per = -(-tiles // n)
+    assert (n - 1) * per < tiles <= n * per      # every range holds at least one tile
+
+
+def _split(lib, q=A, k=A + MB, v=A + 2 * MB, o=A + 3 * MB, lse=A + 4 * MB, B=1, H=2, S_q=16,
+           S_k=4096, d=128, scale=0.125, dtype=1, n_split=4, ws=A + 8 * MB, ws_bytes=1 << 22):
+    return lib.attn_fwd_splitkv(q, k, v, o, lse, B, H, S_q, S_k, d, scale, dtype, n_split, ws,
+                                ws_bytes, None)
+
+
+SPLIT_CASES = [
+    (dict(n_split=-1), binding.ATTN_ERR_INVALID_ARG, "n_split must be"),
+    (dict(ws=0), binding.ATTN_ERR_INVALID_ARG, "workspace is null"),
+    (dict(ws=A + 8 * MB + 8), binding.ATTN_ERR_INVALID_ARG, "workspace is not 16-byte aligned"),
+    (dict(ws_bytes=4 * 2 * 16 * 129 * 4 - 1), binding.ATTN_ERR_INVALID_ARG, "workspace_bytes"),
+    (dict(ws=A + 64), binding.ATTN_ERR_INVALID_ARG, "workspace overlaps q"),
+    (dict(ws=A + 3 * MB), binding.ATTN_ERR_INVALID_ARG, "workspace overlaps o"),
+    (dict(ws=A + 4 * MB - 1024), binding.ATTN_ERR_INVALID_ARG, "workspace overlaps lse"),
+    (dict(d=96), binding.ATTN_ERR_UNSUPPORTED, "head_dim"),
+    (dict(q=0), binding.ATTN_ERR_INVALID_ARG, "q is null"),
+    (dict(o=A + 64), binding.ATTN_ERR_INVALID_ARG, "o overlaps q"),
+]
+
+
+@pytest.mark.parametrize("kw,status,msg", SPLIT_CASES, ids=[c[2] for c in SPLIT_CASES])
+def test_splitkv_validation_rejects_before_device_work(lib, kw, status, msg):
+    assert _split(lib, **kw) == status
+    assert msg in lib.attn_last_error().decode()
+
+
+def test_splitkv_plan_validates(lib):
+    with pytest.raises(binding.AttnError, match="n_split must be"):
+        binding.attn_fwd_splitkv_plan(1, 1, 16, 4096, 128, binding.ATTN_DTYPE_BF16, -2)
+    with pytest.raises(binding.AttnError, match="head_dim"):
+        binding.attn_fwd_splitkv_plan(1, 1, 16, 4096, 80, binding.ATTN_DTYPE_BF16, 2)
+    n = ctypes.c_int64()
+    assert lib.attn_fwd_splitkv_plan(1, 1, 16, 16, 64, 1, 1, None, ctypes.byref(n)) == \
+        binding.ATTN_ERR_INVALID_ARG
