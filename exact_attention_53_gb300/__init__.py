@@ -12,6 +12,7 @@ from .binding import (  # noqa: F401
     attn_fwd_host,
     attn_fwd_plan,
     attn_fwd_splitkv,
+    attn_fwd_splitkv_noalloc,
     attn_fwd_splitkv_plan,
     attn_get_device_status,
     attn_last_error,

@@ -26,7 +26,9 @@ ATTN_DTYPE_F16 = 0
 ATTN_DTYPE_BF16 = 1
 
 EXPORTED = ("attn_fwd", "attn_fwd_host", "attn_fwd_plan", "attn_fwd_splitkv_plan",
-            "attn_fwd_splitkv", "attn_last_error", "attn_get_device_status", "attn_version")
+            "attn_fwd_splitkv", "attn_fwd_splitkv_noalloc", "attn_last_error",
+            "attn_get_device_status", "attn_version")
+NOALLOC_SCRATCH_BYTES = 16 * 1024 * 1024    # ATTN_NOALLOC_SCRATCH_BYTES
 
 
 class AttnPlan(ctypes.Structure):
@@ -82,6 +84,9 @@ def load_library() -> ctypes.CDLL:
         lib.attn_fwd_splitkv.argtypes = [vp, vp, vp, vp, vp, i64, i64, i64, i64, i64,
                                          ctypes.c_float, i32, i64, vp, i64, vp]
         lib.attn_fwd_splitkv.restype = i32
+        lib.attn_fwd_splitkv_noalloc.argtypes = [vp, vp, vp, vp, vp, i64, i64, i64, i64, i64,
+                                                 ctypes.c_float, i32, i64, vp]
+        lib.attn_fwd_splitkv_noalloc.restype = i32
         lib.attn_last_error.argtypes = []
         lib.attn_last_error.restype = ctypes.c_char_p
         lib.attn_get_device_status.argtypes = [vp]
@@ -152,6 +157,16 @@ def attn_fwd_splitkv(q, k, v, o, lse, B, H, S_q, S_k, d, scale, dtype, n_split, 
     _check(lib.attn_fwd_splitkv(ptr(q), ptr(k), ptr(v), ptr(o), ptr(lse), B, H, S_q, S_k, d,
                                 float(scale), int(dtype), int(n_split), ptr(workspace),
                                 int(workspace_bytes), _stream_handle(stream)))
+
+
+def attn_fwd_splitkv_noalloc(q, k, v, o, lse, B, H, S_q, S_k, d, scale, dtype, n_split,
+                             stream=None) -> None:
+    """Enqueue the split-KV forward on the library's built-in scratch (no workspace)."""
+    lib = load_library()
+    ptr = lambda t: t.data_ptr() if isinstance(t, torch.Tensor) else t  # noqa: E731
+    _check(lib.attn_fwd_splitkv_noalloc(ptr(q), ptr(k), ptr(v), ptr(o), ptr(lse), B, H, S_q, S_k,
+                                        d, float(scale), int(dtype), int(n_split),
+                                        _stream_handle(stream)))
 
 
 def attn_get_device_status(stream=None) -> None:

@@ -61,7 +61,7 @@ def build(verbose: bool = False, jobs: int | None = None) -> str:
     nvcc = _nvcc()
     os.makedirs(BUILD, exist_ok=True)
     deps = _deps()
-    jobs = jobs or max(1, min(len(INSTANCES) + 2, os.cpu_count() or 4))
+    jobs = jobs or max(1, min(len(INSTANCES) + 3, os.cpu_count() or 4))
     steps = []
     objs = []
     for d, bf16, causal, split in INSTANCES:
@@ -72,7 +72,7 @@ def build(verbose: bool = False, jobs: int | None = None) -> str:
             steps.append([nvcc, *ARCH, *FLAGS, f"-DATTN_D={d}", f"-DATTN_BF16={bf16}",
                           f"-DATTN_CAUSAL={causal}", f"-DATTN_SPLIT={split}", "-c",
                           os.path.join(CSRC, "attn_inst.cu"), "-o", obj])
-    for name in ("attn_api", "attn_combine"):
+    for name in ("attn_api", "attn_combine", "attn_noalloc"):
         obj = os.path.join(BUILD, f"{name}.o")
         objs.append(obj)
         if _stale(obj, deps):

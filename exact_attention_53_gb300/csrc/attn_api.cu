@@ -45,6 +45,7 @@ __device__ unsigned int g_attn_status;
 std::atomic<int> g_device_checked[kMaxDevices];          // 0 unknown, 1 ok, 2 unsupported
 std::atomic<unsigned int*> g_status_ptr[kMaxDevices];
 std::atomic<int> g_num_sms[kMaxDevices];
+std::atomic<void*> g_noalloc_scratch[kMaxDevices];       // attn_fwd_splitkv_noalloc's scratch
 
 PFN_cuTensorMapEncodeTiled_v12000 encode_fn() {
     static PFN_cuTensorMapEncodeTiled_v12000 fn = nullptr;
@@ -435,6 +436,51 @@ attn_status_t attn_fwd_splitkv(const void* q, const void* k, const void* v, void
     a.n_split = static_cast<int32_t>(sp.n_split);
     a.kv_per_split = static_cast<int32_t>(sp.kv_per_split);
     a.o_part = static_cast<float*>(workspace);
+    a.lse_part = a.o_part + sp.n_split * rows * p.d;
+    LaunchFn fn = pick_split(p.d, p.dtype == ATTN_DTYPE_BF16);
+    if (!fn) return fail(ATTN_ERR_UNSUPPORTED, "no kernel for d=%lld", (long long)p.d);
+    cudaError_t e = fn(a, stream);
+    if (e != cudaSuccess) return fail(ATTN_ERR_CUDA, "kernel launch: %s", cudaGetErrorString(e));
+    e = attn::launch_attn_combine(a.o_part, a.lse_part, o, lse, a.n_split, rows,
+                                  static_cast<int>(p.d), p.dtype == ATTN_DTYPE_BF16, stream);
+    if (e != cudaSuccess) return fail(ATTN_ERR_CUDA, "combine launch: %s", cudaGetErrorString(e));
+    return ok();
+}
+
+attn_status_t attn_fwd_splitkv_noalloc(const void* q, const void* k, const void* v, void* o,
+                                       float* lse, int64_t B, int64_t H, int64_t S_q, int64_t S_k,
+                                       int64_t d, float scale, attn_dtype_t dtype, int64_t n_split,
+                                       struct CUstream_st* stream) {
+    Problem p;
+    attn_status_t s = validate_sizes(p, B, H, S_q, S_k, d, 0, scale, dtype);
+    if (s != ATTN_OK) return s;
+    if ((s = validate_device_ptrs(p, q, k, v, o, lse)) != ATTN_OK) return s;
+    SplitPlan sp;
+    if ((s = resolve_split(p, n_split, &sp)) != ATTN_OK) return s;
+    if (sp.workspace_bytes > int64_t(ATTN_NOALLOC_SCRATCH_BYTES))
+        return fail(ATTN_ERR_INVALID_ARG,
+                    "%lld ranges need %lld bytes of scratch, above the built-in %lld bytes; "
+                    "use a smaller n_split or attn_fwd_splitkv with a workspace",
+                    (long long)sp.n_split, (long long)sp.workspace_bytes,
+                    (long long)ATTN_NOALLOC_SCRATCH_BYTES);
+    if (sp.n_split == 1) return launch_checked(p, q, k, v, o, lse, stream);
+    int dev = 0;
+    if ((s = check_device(&dev)) != ATTN_OK) return s;
+    // The scratch's address on this device, looked up once with it current.
+    void* scratch = g_noalloc_scratch[dev].load(std::memory_order_acquire);
+    if (!scratch) {
+        cudaError_t e = attn::noalloc_scratch_address(&scratch);
+        if (e != cudaSuccess || !scratch)
+            return fail(ATTN_ERR_CUDA, "cudaGetSymbolAddress(split-KV scratch): %s",
+                        cudaGetErrorString(e));
+        g_noalloc_scratch[dev].store(scratch, std::memory_order_release);
+    }
+    attn::FwdArgs a;
+    if ((s = fill_args(a, p, dev, q, k, v, o, lse)) != ATTN_OK) return s;
+    const int64_t rows = p.B * p.H * p.S_q;
+    a.n_split = static_cast<int32_t>(sp.n_split);
+    a.kv_per_split = static_cast<int32_t>(sp.kv_per_split);
+    a.o_part = static_cast<float*>(scratch);
     a.lse_part = a.o_part + sp.n_split * rows * p.d;
     LaunchFn fn = pick_split(p.d, p.dtype == ATTN_DTYPE_BF16);
     if (!fn) return fail(ATTN_ERR_UNSUPPORTED, "no kernel for d=%lld", (long long)p.d);

@@ -96,4 +96,8 @@ cudaError_t launch_attn_combine(const float* o_part, const float* lse_part, void
                                 int n_split, long long rows, int d, bool bf16,
                                 cudaStream_t stream);
 
+// Device address of the built-in split-KV scratch (ATTN_NOALLOC_SCRATCH_BYTES
+// bytes, 256-byte aligned) on the current device.
+cudaError_t noalloc_scratch_address(void** ptr);
+
 }  // namespace attn

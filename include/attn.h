@@ -175,6 +175,46 @@ attn_status_t attn_fwd_splitkv(const void* q, const void* k, const void* v, void
                                int64_t workspace_bytes, struct CUstream_st* stream);
 
 /*
+ * attn_fwd_splitkv_noalloc — attn_fwd_splitkv without a caller workspace and
+ * without allocating anything.
+ *
+ * The page has no counterpart to this entry point: it is a library service.
+ * It is for callers that cannot allocate device memory on the call path:
+ * code that runs under a fixed, pre-reserved memory budget, or that holds no
+ * device allocator of its own (a plain C caller), or that must not call
+ * cudaMalloc/cudaFree between launches because cudaFree synchronises the
+ * device and either call can fail at run time.  Instead of a workspace the
+ * partial results go to a scratch array built into the library: a static
+ * device array of ATTN_NOALLOC_SCRATCH_BYTES (16 MiB) on each device, whose
+ * address is looked up once per device.
+ *
+ *   q, k, v, o, lse, B, H, S_q, S_k, d, scale, dtype, n_split, stream
+ *                    as attn_fwd_splitkv
+ *
+ * Sizes whose plan (attn_fwd_splitkv_plan with the same arguments) needs
+ * more than ATTN_NOALLOC_SCRATCH_BYTES of workspace are rejected with
+ * ATTN_ERR_INVALID_ARG before anything is enqueued; choose a smaller n_split
+ * or use attn_fwd_splitkv.  A plan of one range needs no scratch.
+ *
+ * First call on a device: it looks up the scratch's device address (a CUDA
+ * runtime call, cudaGetSymbolAddress, which may load the array's module) with
+ * that device current.  Make that first call before any stream capture
+ * starts; later calls on the device make no such lookup.
+ *
+ * Nothing in the scratch needs to start at zero: every call writes the
+ * partial results it reads.  The scratch is shared by every call on the
+ * device, so two calls whose work overlaps in time (different streams, or
+ * different host threads without ordering between their streams) race on it
+ * and may return wrong results; order them (one stream, or events).
+ */
+#define ATTN_NOALLOC_SCRATCH_BYTES (16 * 1024 * 1024)
+
+attn_status_t attn_fwd_splitkv_noalloc(const void* q, const void* k, const void* v, void* o,
+                                       float* lse, int64_t B, int64_t H, int64_t S_q, int64_t S_k,
+                                       int64_t d, float scale, attn_dtype_t dtype, int64_t n_split,
+                                       struct CUstream_st* stream);
+
+/*
  * attn_last_error — message for the last non-OK status returned on this host
  * thread ("" if none).  The string stays valid until the next call on this
  * thread.

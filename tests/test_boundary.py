@@ -37,8 +37,8 @@ def _declared_functions():
 def test_header_declares_the_boundary():
     names = _declared_functions()
     assert names == sorted(["attn_fwd", "attn_fwd_host", "attn_fwd_plan", "attn_fwd_splitkv_plan",
-                            "attn_fwd_splitkv", "attn_last_error", "attn_get_device_status",
-                            "attn_version"])
+                            "attn_fwd_splitkv", "attn_fwd_splitkv_noalloc", "attn_last_error",
+                            "attn_get_device_status", "attn_version"])
 
 
 def test_library_exports_every_declared_symbol(lib):
@@ -233,3 +233,21 @@ def test_splitkv_plan_validates(lib):
     n = ctypes.c_int64()
     assert lib.attn_fwd_splitkv_plan(1, 1, 16, 16, 64, 1, 1, None, ctypes.byref(n)) == \
         binding.ATTN_ERR_INVALID_ARG
+
+
+def test_noalloc_rejects_plans_above_the_built_in_scratch(lib):
+    """64 ranges of 4·32·256·129·4 bytes exceed the 16 MiB scratch: rejected on the host."""
+    B, H, S_q, S_k, d = 4, 32, 256, 16384, 128
+    n, ws = binding.attn_fwd_splitkv_plan(B, H, S_q, S_k, d, binding.ATTN_DTYPE_BF16, 64)
+    assert ws > binding.NOALLOC_SCRATCH_BYTES
+    st = lib.attn_fwd_splitkv_noalloc(A, A + (1 << 30), A + (2 << 30), A + (3 << 30),
+                                      A + (4 << 30), B, H, S_q, S_k, d, 0.125, 1, 64, None)
+    assert st == binding.ATTN_ERR_INVALID_ARG
+    msg = lib.attn_last_error().decode()
+    assert "scratch" in msg and str(binding.NOALLOC_SCRATCH_BYTES) in msg
+
+
+def test_noalloc_header_states_the_scratch_size():
+    text = open(HEADER).read()
+    m = re.search(r"#define ATTN_NOALLOC_SCRATCH_BYTES \((\d+) \* 1024 \* 1024\)", text)
+    assert m and int(m.group(1)) * 1024 * 1024 == binding.NOALLOC_SCRATCH_BYTES
