@@ -8,7 +8,9 @@ V ~ U(-1,1)).  FLOPs per step = 4·B·H·S²·d (full) + half of that (causal).
 Prints one JSON line (rank 0).  ``value`` is device-timed throughput with
 inputs resident in HBM; ``e2e`` is the same metric through the host-buffer C
 entry point, copies included; ``roofline`` is for the dominant launch (the
-full one); ``cpu_baseline`` times the fp64 oracle on a bounded sample.
+full one); ``cpu_baseline`` times the fp64 oracle on a bounded sample;
+``splitkv`` reports the split-KV forward on the decode workload (one query row
+per head against 32768 keys) in HBM GB/s, measured after the timed steps.
 
 ``--impl reference`` times the fp64 CPU oracle instead (there is no runnable
 reference implementation: the attention page is Rust that emits PTX for
@@ -212,6 +214,58 @@ def run_reference(args, rank, world):
     }), flush=True)
 
 
+def measure_splitkv(dev, stream, iters: int = 50):
+    """Split-KV forward on the decode workload: HBM GB/s, beside the one-pass kernel on it.
+
+    Algorithmic bytes per call = Q, K, V read once + O and LSE written once
+    (the partial results in the workspace are not counted).  K+V = 537 MB,
+    larger than L2, so no flush is needed between calls.
+    """
+    import torch
+
+    from exact_attention_53_gb300 import attn_fwd, attn_fwd_splitkv, attn_fwd_splitkv_plan
+    from exact_attention_53_gb300.binding import ATTN_DTYPE_BF16
+    from exact_attention_53_gb300.workloads import WORKLOADS, workload_qkv
+
+    w = WORKLOADS["decode"]
+    B, H, S_q, S_k, d = w.B, w.H, w.S_q, w.S_k, w.d
+    q, k, v = (t.to(dev) for t in workload_qkv(w))
+    o = torch.empty_like(q)
+    lse = torch.empty((B, H, S_q), dtype=torch.float32, device=dev)
+    n_split, ws = attn_fwd_splitkv_plan(B, H, S_q, S_k, d, ATTN_DTYPE_BF16, 0)
+    work = torch.empty(max(ws, 16), dtype=torch.uint8, device=dev)
+
+    def split():
+        attn_fwd_splitkv(q, k, v, o, lse, B, H, S_q, S_k, d, w.scale, ATTN_DTYPE_BF16, 0, work,
+                         ws, stream)
+
+    def one_pass():
+        attn_fwd(q, k, v, o, lse, B, H, S_q, S_k, d, 0, w.scale, ATTN_DTYPE_BF16, stream)
+
+    def timed(fn, n):
+        for _ in range(5):
+            fn()
+        torch.cuda.synchronize(dev)
+        ev = [(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True))
+              for _ in range(n)]
+        for a, b in ev:
+            a.record(stream)
+            fn()
+            b.record(stream)
+        torch.cuda.synchronize(dev)
+        return statistics.mean(a.elapsed_time(b) for a, b in ev)
+
+    split_ms = timed(split, iters)
+    one_ms = timed(one_pass, max(10, iters // 5))
+    by = w.io_bytes()
+    return {"workload": f"decode: B={B} H={H} S_q={S_q} S_k={S_k} d={d} bf16, full attention, "
+                        f"Q,K,V~N(0,1)",
+            "n_split": n_split, "workspace_bytes": ws, "bytes_per_call": by,
+            "ms": split_ms, "gbs": by / (split_ms * 1e-3) / 1e9,
+            "one_pass_ms": one_ms, "speedup_vs_one_pass": one_ms / split_ms,
+            "gpu_launches_per_call": 2 if n_split > 1 else 1, "calls_timed": iters}
+
+
 def run_gpu(args, rank, world):
     import torch
 
@@ -311,6 +365,8 @@ def run_gpu(args, rank, world):
     e2e_value = replica_throughput(flops_step, args.steps, world, e2e_ms)
     in_bytes = q.numel() * 2 + k.numel() * 2 + v.numel() * 2
     out_bytes = o.numel() * 2 + lse.numel() * 4
+    splitkv = measure_splitkv(dev, stream)
+    attn_get_device_status(stream)
     sampler.stop()
 
     if rank != 0:
@@ -347,6 +403,13 @@ def run_gpu(args, rank, world):
         "gpu_launches": 2 * args.steps,
         "clocks": clocks,
     }
+    hbm = float(peaks.get("hbm_gbs", FALLBACK_PEAKS["hbm_gbs"]))
+    splitkv["roofline"] = {"bound": "hbm", "achieved": splitkv["gbs"], "peak": hbm, "unit": "GB/s",
+                           "frac": splitkv["gbs"] / hbm,
+                           "traffic": measured_traffic("attn_fwd_splitkv_d128_bf16_decode"),
+                           "kernel": "attn_fwd_kernel<128,bf16,full,split> + attn_combine_kernel",
+                           "peak_source": f"{peak_src} copy bandwidth (hbm_gbs)"}
+    line["splitkv"] = splitkv
     if not args.no_cpu_baseline and world == 1:
         line["cpu_baseline"] = cpu_baseline()
     print(json.dumps(line), flush=True)
