@@ -8,6 +8,8 @@ and a missing library raises instead of falling back to anything else.
 
 from .binding import (  # noqa: F401
     AttnError,
+    attn_bwd,
+    attn_bwd_workspace_size,
     attn_fwd,
     attn_fwd_host,
     attn_fwd_plan,
@@ -16,6 +18,7 @@ from .binding import (  # noqa: F401
     attn_fwd_splitkv_plan,
     attn_get_device_status,
     attn_last_error,
+    bwd,
     fwd,
     fwd_splitkv,
     library_path,

@@ -26,8 +26,8 @@ ATTN_DTYPE_F16 = 0
 ATTN_DTYPE_BF16 = 1
 
 EXPORTED = ("attn_fwd", "attn_fwd_host", "attn_fwd_plan", "attn_fwd_splitkv_plan",
-            "attn_fwd_splitkv", "attn_fwd_splitkv_noalloc", "attn_last_error",
-            "attn_get_device_status", "attn_version")
+            "attn_fwd_splitkv", "attn_fwd_splitkv_noalloc", "attn_bwd_workspace_size", "attn_bwd",
+            "attn_last_error", "attn_get_device_status", "attn_version")
 NOALLOC_SCRATCH_BYTES = 16 * 1024 * 1024    # ATTN_NOALLOC_SCRATCH_BYTES
 
 
@@ -87,6 +87,11 @@ def load_library() -> ctypes.CDLL:
         lib.attn_fwd_splitkv_noalloc.argtypes = [vp, vp, vp, vp, vp, i64, i64, i64, i64, i64,
                                                  ctypes.c_float, i32, i64, vp]
         lib.attn_fwd_splitkv_noalloc.restype = i32
+        lib.attn_bwd_workspace_size.argtypes = [i64, i64, i64, i64, i64, i32, ctypes.POINTER(i64)]
+        lib.attn_bwd_workspace_size.restype = i32
+        lib.attn_bwd.argtypes = [vp] * 9 + [i64, i64, i64, i64, i64, i32, ctypes.c_float, i32, vp,
+                                            i64, vp]
+        lib.attn_bwd.restype = i32
         lib.attn_last_error.argtypes = []
         lib.attn_last_error.restype = ctypes.c_char_p
         lib.attn_get_device_status.argtypes = [vp]
@@ -169,6 +174,23 @@ def attn_fwd_splitkv_noalloc(q, k, v, o, lse, B, H, S_q, S_k, d, scale, dtype, n
                                         _stream_handle(stream)))
 
 
+def attn_bwd_workspace_size(B, H, S_q, S_k, d, dtype) -> int:
+    """Workspace bytes attn_bwd needs (host-only)."""
+    ws = ctypes.c_int64()
+    _check(load_library().attn_bwd_workspace_size(B, H, S_q, S_k, d, int(dtype), ctypes.byref(ws)))
+    return ws.value
+
+
+def attn_bwd(q, k, v, o, lse, dout, dq, dk, dv, B, H, S_q, S_k, d, causal, scale, dtype,
+             workspace, workspace_bytes, stream=None) -> None:
+    """Enqueue the backward; tensors or raw device pointers."""
+    lib = load_library()
+    ptr = lambda t: t.data_ptr() if isinstance(t, torch.Tensor) else t  # noqa: E731
+    _check(lib.attn_bwd(ptr(q), ptr(k), ptr(v), ptr(o), ptr(lse), ptr(dout), ptr(dq), ptr(dk),
+                        ptr(dv), B, H, S_q, S_k, d, int(causal), float(scale), int(dtype),
+                        ptr(workspace), int(workspace_bytes), _stream_handle(stream)))
+
+
 def attn_get_device_status(stream=None) -> None:
     """Synchronise and raise AttnError(ATTN_ERR_TIMEOUT) if a kernel's wait ran out."""
     _check(load_library().attn_get_device_status(_stream_handle(stream)))
@@ -229,3 +251,30 @@ def fwd_splitkv(q: torch.Tensor, k: torch.Tensor, v: torch.Tensor, n_split: int 
     attn_fwd_splitkv(q, k, v, out, lse, B, H, S_q, S_k, d, scale, dtype, n_split, workspace,
                      workspace.numel() * workspace.element_size())
     return out, lse
+
+
+def bwd(q: torch.Tensor, k: torch.Tensor, v: torch.Tensor, o: torch.Tensor, lse: torch.Tensor,
+        dout: torch.Tensor, causal: bool = False, scale: float | None = None,
+        workspace: torch.Tensor | None = None):
+    """dQ, dK, dV for contiguous CUDA tensors (the forward's q, k, v, o, lse and dO).
+
+    Outputs and (unless given) the workspace are allocated with torch; work is
+    enqueued on the current stream.  Returns ``(dq, dk, dv)``.
+    """
+    B, H, S_q, S_k, d = _check_qkv(q, k, v)
+    if o.shape != q.shape or dout.shape != q.shape or o.dtype != q.dtype or dout.dtype != q.dtype:
+        raise AttnError(ATTN_ERR_INVALID_ARG, "o and dout must match q in shape and dtype")
+    if not (o.is_contiguous() and dout.is_contiguous() and lse.is_contiguous()):
+        raise AttnError(ATTN_ERR_INVALID_ARG, "o, dout and lse must be contiguous")
+    if lse.dtype != torch.float32 or tuple(lse.shape) != (B, H, S_q):
+        raise AttnError(ATTN_ERR_INVALID_ARG, "lse must be float32 [B, H, S_q]")
+    dtype = _DTYPE_CODE[q.dtype]
+    if scale is None:
+        scale = 1.0 / math.sqrt(d)
+    ws = attn_bwd_workspace_size(B, H, S_q, S_k, d, dtype)
+    if workspace is None:
+        workspace = torch.empty(ws, dtype=torch.uint8, device=q.device)
+    dq, dk, dv = torch.empty_like(q), torch.empty_like(k), torch.empty_like(v)
+    attn_bwd(q, k, v, o, lse, dout, dq, dk, dv, B, H, S_q, S_k, d, causal, scale, dtype,
+             workspace, workspace.numel() * workspace.element_size())
+    return dq, dk, dv

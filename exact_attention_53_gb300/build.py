@@ -29,6 +29,8 @@ FLAGS = ["-O3", "-std=c++17", "-lineinfo", "-Xcompiler", "-fPIC", "-I" + INCLUDE
 # split-KV variant of full attention.
 INSTANCES = ([(d, bf16, causal, 0) for d in (64, 128, 256) for bf16 in (0, 1) for causal in (0, 1)]
              + [(d, bf16, 0, 1) for d in (64, 128, 256) for bf16 in (0, 1)])
+# (head_dim, bf16, causal) of the backward
+BWD_INSTANCES = [(d, bf16, causal) for d in (64, 128) for bf16 in (0, 1) for causal in (0, 1)]
 
 
 def _nvcc() -> str:
@@ -61,7 +63,7 @@ def build(verbose: bool = False, jobs: int | None = None) -> str:
     nvcc = _nvcc()
     os.makedirs(BUILD, exist_ok=True)
     deps = _deps()
-    jobs = jobs or max(1, min(len(INSTANCES) + 3, os.cpu_count() or 4))
+    jobs = jobs or max(1, min(len(INSTANCES) + len(BWD_INSTANCES) + 3, os.cpu_count() or 4))
     steps = []
     objs = []
     for d, bf16, causal, split in INSTANCES:
@@ -72,6 +74,13 @@ def build(verbose: bool = False, jobs: int | None = None) -> str:
             steps.append([nvcc, *ARCH, *FLAGS, f"-DATTN_D={d}", f"-DATTN_BF16={bf16}",
                           f"-DATTN_CAUSAL={causal}", f"-DATTN_SPLIT={split}", "-c",
                           os.path.join(CSRC, "attn_inst.cu"), "-o", obj])
+    for d, bf16, causal in BWD_INSTANCES:
+        obj = os.path.join(BUILD, f"attn_bwd_d{d}_{'bf16' if bf16 else 'f16'}_{'causal' if causal else 'full'}.o")
+        objs.append(obj)
+        if _stale(obj, deps):
+            steps.append([nvcc, *ARCH, *FLAGS, f"-DATTN_D={d}", f"-DATTN_BF16={bf16}",
+                          f"-DATTN_CAUSAL={causal}", "-c", os.path.join(CSRC, "attn_bwd_inst.cu"),
+                          "-o", obj])
     for name in ("attn_api", "attn_combine", "attn_noalloc"):
         obj = os.path.join(BUILD, f"{name}.o")
         objs.append(obj)

@@ -187,6 +187,26 @@ attn_status_t encode_rows(CUtensorMap* map, const void* base, const Problem& p, 
     return ATTN_OK;
 }
 
+// Rows of [B·H, S, d] as a 3-D map with a box of 64 columns × box_rows rows.
+attn_status_t encode_rows_box(CUtensorMap* map, const void* base, const Problem& p, int64_t S,
+                              uint32_t box_rows, const char* name) {
+    auto fn = encode_fn();
+    if (!fn) return fail(ATTN_ERR_CUDA, "cuTensorMapEncodeTiled is unavailable from the driver");
+    cuuint64_t dims[3] = {static_cast<cuuint64_t>(p.d), static_cast<cuuint64_t>(S),
+                          static_cast<cuuint64_t>(p.B * p.H)};
+    cuuint64_t strides[2] = {static_cast<cuuint64_t>(p.d * 2), static_cast<cuuint64_t>(S * p.d * 2)};
+    cuuint32_t box[3] = {64, box_rows, 1};
+    cuuint32_t estr[3] = {1, 1, 1};
+    CUresult r = fn(map,
+                    p.dtype == ATTN_DTYPE_BF16 ? CU_TENSOR_MAP_DATA_TYPE_BFLOAT16
+                                               : CU_TENSOR_MAP_DATA_TYPE_FLOAT16,
+                    3, const_cast<void*>(base), dims, strides, box, estr,
+                    CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B,
+                    CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
+    if (r != CUDA_SUCCESS) return fail(ATTN_ERR_CUDA, "cuTensorMapEncodeTiled(%s) failed with %d", name, (int)r);
+    return ATTN_OK;
+}
+
 template <int D>
 void fill_plan_d(const Problem& p, attn_plan_t* out) {
     using T = attn::FwdTile<D>;
@@ -334,6 +354,35 @@ attn_status_t resolve_split(const Problem& p, int64_t n_split, SplitPlan* sp) {
         sms = g_num_sms[dev].load();
     }
     return split_plan(p, n_split, sms, sp);
+}
+
+// ---------------------------------------------------------------- backward
+using BwdLaunchFn = cudaError_t (*)(const attn::BwdArgs&, cudaStream_t);
+
+BwdLaunchFn pick_bwd(int64_t d, bool bf16, bool causal) {
+#define ATTN_PICK_BWD(D)                                                              \
+    if (d == D) {                                                                     \
+        if (bf16) return causal ? attn::launch_attn_bwd<D, true, true>                \
+                                : attn::launch_attn_bwd<D, true, false>;              \
+        return causal ? attn::launch_attn_bwd<D, false, true>                         \
+                      : attn::launch_attn_bwd<D, false, false>;                       \
+    }
+    ATTN_PICK_BWD(64)
+    ATTN_PICK_BWD(128)
+#undef ATTN_PICK_BWD
+    return nullptr;
+}
+
+int64_t bwd_s_pad(const Problem& p) { return (p.S_q + 127) / 128 * 128; }
+
+int64_t bwd_workspace_bytes(const Problem& p) { return 2 * p.B * p.H * bwd_s_pad(p) * 4; }
+
+attn_status_t validate_bwd_head_dim(const Problem& p) {
+    if (p.d != 64 && p.d != 128)
+        return fail(ATTN_ERR_UNSUPPORTED,
+                    "head_dim d=%lld not supported by the backward; must be one of [64, 128]",
+                    (long long)p.d);
+    return ATTN_OK;
 }
 
 }  // namespace
@@ -492,6 +541,93 @@ attn_status_t attn_fwd_splitkv_noalloc(const void* q, const void* k, const void*
     return ok();
 }
 
+attn_status_t attn_bwd_workspace_size(int64_t B, int64_t H, int64_t S_q, int64_t S_k, int64_t d,
+                                      attn_dtype_t dtype, int64_t* workspace_bytes) {
+    if (!workspace_bytes) return fail(ATTN_ERR_INVALID_ARG, "workspace_bytes is null");
+    Problem p;
+    attn_status_t s = validate_sizes(p, B, H, S_q, S_k, d, 0, 1.0f, dtype);
+    if (s != ATTN_OK) return s;
+    if ((s = validate_bwd_head_dim(p)) != ATTN_OK) return s;
+    *workspace_bytes = bwd_workspace_bytes(p);
+    return ok();
+}
+
+attn_status_t attn_bwd(const void* q, const void* k, const void* v, const void* o,
+                       const float* lse, const void* dout, void* dq, void* dk, void* dv,
+                       int64_t B, int64_t H, int64_t S_q, int64_t S_k, int64_t d, int causal,
+                       float scale, attn_dtype_t dtype, void* workspace, int64_t workspace_bytes,
+                       struct CUstream_st* stream) {
+    Problem p;
+    attn_status_t s = validate_sizes(p, B, H, S_q, S_k, d, causal, scale, dtype);
+    if (s != ATTN_OK) return s;
+    if ((s = validate_bwd_head_dim(p)) != ATTN_OK) return s;
+    struct Buf {
+        const void* ptr;
+        size_t bytes;
+        size_t align;
+        const char* name;
+        bool written;
+    };
+    const size_t wb = static_cast<size_t>(bwd_workspace_bytes(p));
+    const Buf bufs[] = {
+        {q, p.q_bytes, 16, "q", false},          {k, p.kv_bytes, 16, "k", false},
+        {v, p.kv_bytes, 16, "v", false},         {o, p.o_bytes, 16, "o", false},
+        {lse, p.lse_bytes, 4, "lse", false},     {dout, p.o_bytes, 16, "dout", false},
+        {dq, p.q_bytes, 16, "dq", true},         {dk, p.kv_bytes, 16, "dk", true},
+        {dv, p.kv_bytes, 16, "dv", true},        {workspace, wb, 16, "workspace", true},
+    };
+    for (const Buf& b : bufs) {
+        if (!b.ptr) return fail(ATTN_ERR_INVALID_ARG, "%s is null", b.name);
+        if (!aligned(b.ptr, b.align))
+            return fail(ATTN_ERR_INVALID_ARG, "%s is not %zu-byte aligned", b.name, b.align);
+    }
+    if (workspace_bytes < static_cast<int64_t>(wb))
+        return fail(ATTN_ERR_INVALID_ARG, "workspace_bytes=%lld is below the %lld bytes needed",
+                    (long long)workspace_bytes, (long long)wb);
+    // Every written buffer must be disjoint from every other buffer.
+    for (const Buf& w : bufs) {
+        if (!w.written) continue;
+        for (const Buf& x : bufs) {
+            if (&x == &w) continue;
+            if (overlaps(w.ptr, w.bytes, x.ptr, x.bytes))
+                return fail(ATTN_ERR_INVALID_ARG, "%s overlaps %s", w.name, x.name);
+        }
+    }
+    int dev = 0;
+    if ((s = check_device(&dev)) != ATTN_OK) return s;
+    attn::BwdArgs a;
+    if ((s = encode_rows_box(&a.tm_k_fixed, k, p, p.S_k, 128, "k")) != ATTN_OK) return s;
+    if ((s = encode_rows_box(&a.tm_v_fixed, v, p, p.S_k, 128, "v")) != ATTN_OK) return s;
+    if ((s = encode_rows_box(&a.tm_q_step, q, p, p.S_q, 64, "q")) != ATTN_OK) return s;
+    if ((s = encode_rows_box(&a.tm_do_step, dout, p, p.S_q, 64, "dout")) != ATTN_OK) return s;
+    if ((s = encode_rows_box(&a.tm_q_fixed, q, p, p.S_q, 128, "q")) != ATTN_OK) return s;
+    if ((s = encode_rows_box(&a.tm_do_fixed, dout, p, p.S_q, 128, "dout")) != ATTN_OK) return s;
+    if ((s = encode_rows_box(&a.tm_k_step, k, p, p.S_k, 64, "k")) != ATTN_OK) return s;
+    if ((s = encode_rows_box(&a.tm_v_step, v, p, p.S_k, 64, "v")) != ATTN_OK) return s;
+    const int64_t s_pad = bwd_s_pad(p);
+    a.o = o;
+    a.dout = dout;
+    a.lse = lse;
+    a.lse2 = static_cast<float*>(workspace);
+    a.delta = a.lse2 + p.B * p.H * s_pad;
+    a.dq = dq;
+    a.dk = dk;
+    a.dv = dv;
+    a.S_q = static_cast<int32_t>(p.S_q);
+    a.S_k = static_cast<int32_t>(p.S_k);
+    a.BH = static_cast<int32_t>(p.B * p.H);
+    a.S_pad = static_cast<int32_t>(s_pad);
+    a.scale = p.scale;
+    a.scale_log2 = static_cast<float>(static_cast<double>(p.scale) * 1.4426950408889634);
+    a.num_sms = g_num_sms[dev].load();
+    a.status = g_status_ptr[dev].load();
+    BwdLaunchFn fn = pick_bwd(p.d, p.dtype == ATTN_DTYPE_BF16, p.causal);
+    if (!fn) return fail(ATTN_ERR_UNSUPPORTED, "no backward kernel for d=%lld", (long long)p.d);
+    cudaError_t e = fn(a, stream);
+    if (e != cudaSuccess) return fail(ATTN_ERR_CUDA, "backward launch: %s", cudaGetErrorString(e));
+    return ok();
+}
+
 const char* attn_last_error(void) { return g_msg; }
 
 attn_status_t attn_get_device_status(struct CUstream_st* stream) {
@@ -507,9 +643,11 @@ attn_status_t attn_get_device_status(struct CUstream_st* stream) {
     const unsigned int zero = 0;
     e = cudaMemcpyToSymbol(g_attn_status, &zero, sizeof(zero));
     if (e != cudaSuccess) return fail(ATTN_ERR_CUDA, "clearing status: %s", cudaGetErrorString(e));
-    return fail(ATTN_ERR_TIMEOUT, "a bounded wait ran out in:%s%s%s%s%s", (v & 1u) ? " producer" : "",
-                (v & 2u) ? " mma" : "", (v & 4u) ? " softmax" : "", (v & 8u) ? " epilogue" : "",
-                (v & 16u) ? " drain" : "");
+    return fail(ATTN_ERR_TIMEOUT, "a bounded wait ran out in:%s%s%s%s%s%s%s%s%s",
+                (v & 1u) ? " producer" : "", (v & 2u) ? " mma" : "", (v & 4u) ? " softmax" : "",
+                (v & 8u) ? " epilogue" : "", (v & 16u) ? " drain" : "",
+                (v & 32u) ? " bwd-producer" : "", (v & 64u) ? " bwd-mma" : "",
+                (v & 128u) ? " bwd-softmax" : "", (v & 256u) ? " bwd-drain" : "");
 }
 
 int attn_version(void) { return kVersion; }

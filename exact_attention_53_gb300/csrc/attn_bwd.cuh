@@ -1,0 +1,946 @@
+// Attention backward on sm_103a: tcgen05 MMAs with TMEM accumulators, TMA
+// loads into shared-memory rings, mbarrier handoffs, persistent CTAs.
+//
+// The steps are those of the page's backward (oxicuda-dnn 0.1.8,
+// src/attn/flash_attn/hopper.rs, doc comment of generate_backward): recompute
+// P from the forward's log-sum-exp, then dV = Pᵀ·dO, dP = dO·Vᵀ,
+// dS = P ∘ (dP − D) with D_i = rowsum(dO ∘ O), dQ = dS·K, dK = dSᵀ·Q (dQ and
+// dK times the softmax scale).  Three kernels:
+//
+//   attn_bwd_prep_kernel   D_i = Σ_c dO_ic·O_ic and LSE_i·log2(e), one row
+//                          per warp, into a workspace padded to whole tiles
+//                          (padding rows: D = 0, LSE = +inf, so P = 0 there);
+//   attn_bwd_dkdv_kernel   one unit = (head, 128 keys): loops over 64-row
+//                          query steps, Sᵀ = K·Qᵀ and dPᵀ = V·dOᵀ into TMEM,
+//                          Pᵀ and dSᵀ formed by four softmax warps (one key
+//                          row per thread), dV += Pᵀ·dO and dK += dSᵀ·Q with
+//                          Pᵀ / dSᵀ read from TMEM;
+//   attn_bwd_dq_kernel     one unit = (head, 128 queries): loops over 64-key
+//                          steps, S = Q·Kᵀ and dP = dO·Vᵀ, dS by the softmax
+//                          warps (one query row per thread), dQ += dS·K.
+//
+// dQ gets its own pass (it recomputes S and dP) instead of the page's f32
+// atomics, so every result is deterministic: no two CTAs ever add into the
+// same output.  Tensor memory holds two S buffers, two dP buffers and the
+// accumulators (dV and dK: 2·d columns; dQ: d), so head_dim is 64 or 128.
+#pragma once
+
+#include <cuda.h>
+#include <cuda_fp16.h>
+#include <cuda_runtime.h>
+
+#include <algorithm>
+#include <cstdint>
+
+#include "attn_launch.h"
+#include "sm100.cuh"
+
+namespace attn {
+
+// Status bits of the backward kernels (shared word with the forward).
+constexpr unsigned int kStatusBwdProducer = 1u << 5;
+constexpr unsigned int kStatusBwdMma = 1u << 6;
+constexpr unsigned int kStatusBwdSoftmax = 1u << 7;
+constexpr unsigned int kStatusBwdDrain = 1u << 8;
+
+template <int D>
+struct BwdTile {
+    static_assert(D == 64 || D == 128, "the backward is built for head_dim 64 and 128");
+    static constexpr int BU = 128;                    // rows of the unit's fixed operands
+    static constexpr int BS = 64;                     // rows per step
+    static constexpr int CHUNKS = D / 64;             // 128-byte swizzle atoms along d
+    static constexpr int BIG_CHUNK = BU * 128;        // one atom column of a 128-row tile
+    static constexpr int SMALL_CHUNK = BS * 128;      // of a 64-row tile
+    static constexpr int BIG_TILE = BU * D * 2;
+    static constexpr int SMALL_TILE = BS * D * 2;
+    static constexpr int NS = D == 64 ? 8 : 4;        // ring slots, two 64-row tiles each
+    static constexpr int SLOT_BYTES = 2 * SMALL_TILE;
+    static constexpr int STAT_FLOATS = 2 * BS;        // per slot: LSE·log2e and D of 64 rows
+    static constexpr int NUM_BARS = 2 + 2 * NS + 2 + 2 + 1 + 1;
+    static constexpr int TILE_BYTES = 2 * BIG_TILE + NS * SLOT_BYTES + NS * STAT_FLOATS * 4;
+    static constexpr int SMEM_BYTES = 1024 + TILE_BYTES + NUM_BARS * 8 + 16;
+    static constexpr int THREADS = 192;               // 4 softmax warps, producer, MMA
+    static constexpr int PRODUCER_WARP = 4;
+    static constexpr int MMA_WARP = 5;
+    static constexpr uint32_t TMEM_COLS = 512;
+    static constexpr uint32_t S_COL = 0;              // S buffer b at column 64·b (fp32)
+    static constexpr uint32_t DP_COL = 128;           // dP buffer b at 128 + 64·b
+    static constexpr uint32_t PK_OFF = 32;            // packed 16-bit results over cols 32..63
+    static constexpr uint32_t ACC_COL = 256;          // accumulators: 256 (+ D)
+    static_assert(SMEM_BYTES <= 232448, "shared memory budget");
+    static_assert(ACC_COL + 2 * D <= TMEM_COLS, "tensor memory budget");
+};
+
+// Unit L -> (head, tile).  Full attention: a head's tiles are adjacent, so the
+// units in flight share that head's step operands in L2.  Causal: heads in
+// groups of head_group, heaviest tiles of the group first (HEAVY_LOW: tile 0
+// is the heaviest, as for key tiles; otherwise the last tile is).
+template <bool CAUSAL, bool HEAVY_LOW>
+__device__ __forceinline__ void bwd_unit_coords(int L, int BH, int n_tiles, int head_group,
+                                                int& bh, int& tile) {
+    if (CAUSAL) {
+        const int per_group = head_group * n_tiles;
+        const int g = L / per_group;
+        const int r = L - g * per_group;
+        const int g0 = g * head_group;
+        const int gsz = min(head_group, BH - g0);
+        const int ti = r / gsz;
+        bh = g0 + (r - ti * gsz);
+        tile = HEAVY_LOW ? ti : n_tiles - 1 - ti;
+    } else {
+        bh = L / n_tiles;
+        tile = L - bh * n_tiles;
+    }
+}
+
+// Softmax-side work of one step for one row: P = 2^(s·scale·log2e − L) (0
+// where masked), dS = P·(dP − Dv); packs dS (and P when WANT_P) as 16-bit
+// pairs.  Per column c: lse2[c], dd[c] (COLUMN_STATS: one value per column,
+// read from shared memory; else the row's own, broadcast).  keep(c) tells
+// whether column c is visible.
+template <bool MASKED, bool BF16, bool WANT_P, bool COLUMN_STATS, typename Keep>
+__device__ __forceinline__ void grad_pack64(const uint32_t (&s)[64], const uint32_t (&dp)[64],
+                                            const float* lse2, const float* dd, float row_lse2,
+                                            float row_dd, float scale_log2, Keep keep,
+                                            uint32_t (&pk_p)[32], uint32_t (&pk_ds)[32]) {
+    using namespace sm100;
+#pragma unroll
+    for (int c = 0; c < 64; c += 4) {
+        float l[4], dv[4];
+        if (COLUMN_STATS) {
+            const float4 l4 = *reinterpret_cast<const float4*>(lse2 + c);
+            const float4 d4 = *reinterpret_cast<const float4*>(dd + c);
+            l[0] = l4.x; l[1] = l4.y; l[2] = l4.z; l[3] = l4.w;
+            dv[0] = d4.x; dv[1] = d4.y; dv[2] = d4.z; dv[3] = d4.w;
+        } else {
+#pragma unroll
+            for (int i = 0; i < 4; ++i) {
+                l[i] = row_lse2;
+                dv[i] = row_dd;
+            }
+        }
+        float p[4], g[4];
+#pragma unroll
+        for (int i = 0; i < 4; ++i) {
+            p[i] = ex2_approx(fmaf(__uint_as_float(s[c + i]), scale_log2, -l[i]));
+            if (MASKED) p[i] = keep(c + i) ? p[i] : 0.f;
+            g[i] = p[i] * (__uint_as_float(dp[c + i]) - dv[i]);
+        }
+        if (WANT_P) {
+            pk_p[c / 2] = BF16 ? pack_bf16(p[0], p[1]) : pack_f16(p[0], p[1]);
+            pk_p[c / 2 + 1] = BF16 ? pack_bf16(p[2], p[3]) : pack_f16(p[2], p[3]);
+        }
+        pk_ds[c / 2] = BF16 ? pack_bf16(g[0], g[1]) : pack_f16(g[0], g[1]);
+        pk_ds[c / 2 + 1] = BF16 ? pack_bf16(g[2], g[3]) : pack_f16(g[2], g[3]);
+    }
+}
+
+// Store one row of an fp32 TMEM accumulator (D columns at `taddr`) times
+// `mul` as 16-bit values to `dst` (D contiguous elements).
+template <int D, bool BF16>
+__device__ __forceinline__ void store_row_from_tmem(uint32_t taddr, float mul, void* dst,
+                                                    bool store) {
+    using namespace sm100;
+    uint4* out = reinterpret_cast<uint4*>(dst);
+#pragma unroll 1
+    for (int cc = 0; cc < D; cc += 32) {
+        uint32_t r[32];
+        tmem_ld32(taddr + cc, r);
+        if (store) {
+#pragma unroll
+            for (int i = 0; i < 4; ++i) {
+                uint32_t w[4];
+#pragma unroll
+                for (int k = 0; k < 4; ++k) {
+                    const float a = __uint_as_float(r[8 * i + 2 * k]) * mul;
+                    const float b = __uint_as_float(r[8 * i + 2 * k + 1]) * mul;
+                    w[k] = BF16 ? pack_bf16(a, b) : pack_f16(a, b);
+                }
+                out[cc / 8 + i] = make_uint4(w[0], w[1], w[2], w[3]);
+            }
+        }
+    }
+}
+
+// ============================================================== prep
+// delta[bh, i] = Σ_c dO[bh,i,c]·O[bh,i,c]; lse2[bh, i] = LSE[bh,i]·log2(e);
+// for i in [S_q, S_pad): delta = 0, lse2 = +inf.  One warp per padded row.
+template <int D, bool BF16>
+__global__ void __launch_bounds__(256) attn_bwd_prep_kernel(const uint16_t* __restrict__ o,
+                                                            const uint16_t* __restrict__ dout,
+                                                            const float* __restrict__ lse,
+                                                            float* __restrict__ lse2,
+                                                            float* __restrict__ delta, int S_q,
+                                                            int S_pad, long long rows_pad) {
+    constexpr int PER_LANE = D / 32;                  // 2 or 4 elements
+    const long long r = static_cast<long long>(blockIdx.x) * 8 + (threadIdx.x >> 5);
+    const int lane = threadIdx.x & 31;
+    if (r >= rows_pad) return;
+    const long long bh = r / S_pad;
+    const int i = static_cast<int>(r - bh * S_pad);
+    if (i >= S_q) {
+        if (lane == 0) {
+            delta[r] = 0.f;
+            lse2[r] = __int_as_float(0x7f800000);
+        }
+        return;
+    }
+    const size_t off = (static_cast<size_t>(bh) * S_q + i) * D + lane * PER_LANE;
+    float acc = 0.f;
+    uint32_t ow[PER_LANE / 2], dw[PER_LANE / 2];
+    if constexpr (PER_LANE == 2) {
+        ow[0] = *reinterpret_cast<const uint32_t*>(o + off);
+        dw[0] = *reinterpret_cast<const uint32_t*>(dout + off);
+    } else {
+        const uint2 a = *reinterpret_cast<const uint2*>(o + off);
+        const uint2 b = *reinterpret_cast<const uint2*>(dout + off);
+        ow[0] = a.x;
+        ow[1] = a.y;
+        dw[0] = b.x;
+        dw[1] = b.y;
+    }
+#pragma unroll
+    for (int w = 0; w < PER_LANE / 2; ++w) {
+        float o0, o1, d0, d1;
+        if (BF16) {
+            o0 = __uint_as_float(ow[w] << 16); o1 = __uint_as_float(ow[w] & 0xffff0000u);
+            d0 = __uint_as_float(dw[w] << 16); d1 = __uint_as_float(dw[w] & 0xffff0000u);
+        } else {
+            const __half2 oh = *reinterpret_cast<const __half2*>(&ow[w]);
+            const __half2 dh = *reinterpret_cast<const __half2*>(&dw[w]);
+            const float2 of = __half22float2(oh), df = __half22float2(dh);
+            o0 = of.x; o1 = of.y; d0 = df.x; d1 = df.y;
+        }
+        acc = fmaf(o0, d0, acc);
+        acc = fmaf(o1, d1, acc);
+    }
+#pragma unroll
+    for (int sh = 16; sh > 0; sh >>= 1) acc += __shfl_xor_sync(0xffffffffu, acc, sh);
+    if (lane == 0) {
+        delta[r] = acc;
+        lse2[r] = lse[static_cast<size_t>(bh) * S_q + i] * 1.4426950408889634f;
+    }
+}
+
+// ============================================================== dK, dV
+template <int D, bool BF16, bool CAUSAL>
+__global__ void __launch_bounds__(BwdTile<D>::THREADS, 1)
+    attn_bwd_dkdv_kernel(const __grid_constant__ CUtensorMap tm_k,    // box 64 × 128
+                         const __grid_constant__ CUtensorMap tm_v,    // box 64 × 128
+                         const __grid_constant__ CUtensorMap tm_q,    // box 64 × 64
+                         const __grid_constant__ CUtensorMap tm_do,   // box 64 × 64
+                         const float* __restrict__ lse2, const float* __restrict__ delta,
+                         uint16_t* __restrict__ dk, uint16_t* __restrict__ dv, int S_q, int S_k,
+                         int BH, int S_pad, int head_group, float scale, float scale_log2,
+                         unsigned int* __restrict__ status) {
+    using T = BwdTile<D>;
+    using namespace sm100;
+
+    extern __shared__ uint8_t smem_raw[];
+    const uint32_t raw_addr = smem_u32(smem_raw);
+    uint8_t* smem = smem_raw + ((1024u - (raw_addr & 1023u)) & 1023u);
+    uint8_t* sK = smem;
+    uint8_t* sV = sK + T::BIG_TILE;
+    uint8_t* sRing = sV + T::BIG_TILE;                // slot s: Q at s·SLOT, dO at +SMALL_TILE
+    float* sStat = reinterpret_cast<float*>(sRing + T::NS * T::SLOT_BYTES);
+    uint64_t* bars = reinterpret_cast<uint64_t*>(smem + T::TILE_BYTES);
+    uint64_t* kv_full = bars;
+    uint64_t* kv_empty = kv_full + 1;
+    uint64_t* slot_full = kv_empty + 1;
+    uint64_t* slot_empty = slot_full + T::NS;
+    uint64_t* s_full = slot_empty + T::NS;    // [2] Sᵀ and dPᵀ of buffer b computed
+    uint64_t* p_full = s_full + 2;            // [2] Pᵀ and dSᵀ of buffer b written (per warp)
+    uint64_t* acc_done = p_full + 2;          // dV and dK of the unit complete
+    uint64_t* drain = acc_done + 1;
+    uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(drain + 1);
+    volatile int* abort_flag = reinterpret_cast<volatile int*>(tmem_slot + 1);
+
+    const int warp = threadIdx.x >> 5;
+    const int lane = threadIdx.x & 31;
+    const int n_kt = (S_k + T::BU - 1) / T::BU;
+    const int n_qs = (S_q + T::BS - 1) / T::BS;
+    const int n_units = BH * n_kt;
+    // Query steps of key tile kt: causal skips query rows that see none of its keys.
+    auto unit_info = [&](int L, int& bh, int& kt, int& q_begin, int& n) {
+        bwd_unit_coords<CAUSAL, true>(L, BH, n_kt, head_group, bh, kt);
+        q_begin = CAUSAL ? min(n_qs, kt * (T::BU / T::BS)) : 0;
+        n = n_qs - q_begin;
+    };
+    auto unit_of_round = [&](int r) {
+        const int G = static_cast<int>(gridDim.x);
+        const int c = static_cast<int>(blockIdx.x);
+        return r * G + ((r & 1) ? (G - 1 - c) : c);
+    };
+
+    if (threadIdx.x == 0) {
+        mbar_init(kv_full, 1);
+        mbar_init(kv_empty, 1);
+        for (int s = 0; s < T::NS; ++s) {
+            mbar_init(&slot_full[s], 1);
+            mbar_init(&slot_empty[s], 1);
+        }
+        for (int b = 0; b < 2; ++b) {
+            mbar_init(&s_full[b], 1);
+            mbar_init(&p_full[b], 4);
+        }
+        mbar_init(acc_done, 1);
+        mbar_init(drain, 1);
+        *abort_flag = 0;
+        fence_mbar_init();
+        fence_proxy_async_smem();
+    }
+    if (warp == 0) {
+        tmem_alloc(tmem_slot, T::TMEM_COLS);
+        tmem_relinquish();
+    }
+    tc_fence_before();
+    __syncthreads();
+    tc_fence_after();
+    const uint32_t tmem = *tmem_slot;
+
+    if (warp == T::PRODUCER_WARP) {
+        // ------------------------------------------------------------ TMA producer
+        const bool leader = elect_one();
+        if (leader) {
+            tma_prefetch_desc(&tm_k);
+            tma_prefetch_desc(&tm_v);
+            tma_prefetch_desc(&tm_q);
+            tma_prefetch_desc(&tm_do);
+        }
+        __syncwarp();
+        bool ok = true;
+        int idx = 0;      // ring position, across units
+        int uk = 0;       // units with work started by this CTA
+        for (int r = 0; r * static_cast<int>(gridDim.x) < n_units && ok; ++r) {
+            const int L = unit_of_round(r);
+            if (L >= n_units) continue;
+            int bh, kt, q_begin, n;
+            unit_info(L, bh, kt, q_begin, n);
+            if (n == 0) continue;
+            ok = mbar_wait(kv_empty, (uk & 1) ^ 1, abort_flag, status, kStatusBwdProducer);
+            ok = __all_sync(0xffffffffu, ok);
+            if (!ok) break;
+            ++uk;
+            if (leader) {
+                mbar_arrive_expect_tx(kv_full, 2 * T::BIG_TILE);
+#pragma unroll
+                for (int c = 0; c < T::CHUNKS; ++c) {
+                    tma_load_3d(sK + c * T::BIG_CHUNK, &tm_k, kv_full, c * 64, kt * T::BU, bh);
+                    tma_load_3d(sV + c * T::BIG_CHUNK, &tm_v, kv_full, c * 64, kt * T::BU, bh);
+                }
+            }
+            __syncwarp();
+            for (int t = 0; t < n && ok; ++t) {
+                const int slot = idx % T::NS;
+                ok = mbar_wait(&slot_empty[slot], ((idx / T::NS) & 1) ^ 1, abort_flag, status,
+                               kStatusBwdProducer);
+                ok = __all_sync(0xffffffffu, ok);
+                if (!ok) break;
+                if (leader) {
+                    const int q0 = (q_begin + t) * T::BS;
+                    uint8_t* dst = sRing + slot * T::SLOT_BYTES;
+                    float* st = sStat + slot * T::STAT_FLOATS;
+                    const size_t soff = static_cast<size_t>(bh) * S_pad + q0;
+                    mbar_arrive_expect_tx(&slot_full[slot], T::SLOT_BYTES + T::STAT_FLOATS * 4);
+#pragma unroll
+                    for (int c = 0; c < T::CHUNKS; ++c) {
+                        tma_load_3d(dst + c * T::SMALL_CHUNK, &tm_q, &slot_full[slot], c * 64, q0,
+                                    bh);
+                        tma_load_3d(dst + T::SMALL_TILE + c * T::SMALL_CHUNK, &tm_do,
+                                    &slot_full[slot], c * 64, q0, bh);
+                    }
+                    bulk_load(st, lse2 + soff, T::BS * 4, &slot_full[slot]);
+                    bulk_load(st + T::BS, delta + soff, T::BS * 4, &slot_full[slot]);
+                }
+                __syncwarp();
+                ++idx;
+            }
+        }
+        if (*abort_flag && leader) {
+            // Let every copy this CTA started land before it exits.
+            const uint64_t t0 = global_timer_ns();
+            for (int i = max(0, idx - T::NS); i < idx; ++i) {
+                const uint32_t a = smem_u32(&slot_full[i % T::NS]);
+                while (!mbar_try_wait(a, (i / T::NS) & 1)) {
+                    if (global_timer_ns() - t0 > kWaitLimitNs) {
+                        atomicOr(status, kStatusBwdDrain);
+                        break;
+                    }
+                }
+            }
+            if (uk > 0) {
+                const uint32_t a = smem_u32(kv_full);
+                while (!mbar_try_wait(a, static_cast<uint32_t>(uk - 1) & 1u)) {
+                    if (global_timer_ns() - t0 > kWaitLimitNs) {
+                        atomicOr(status, kStatusBwdDrain);
+                        break;
+                    }
+                }
+            }
+        }
+        __syncwarp();
+    } else if (warp == T::MMA_WARP) {
+        // ------------------------------------------------------------ MMA issuer
+        constexpr uint32_t id_s = idesc_f16(128, T::BS, BF16, false, false);
+        constexpr uint32_t id_acc = idesc_f16(128, D, BF16, false, true);
+        const uint64_t k_desc = sdesc_sw128(smem_u32(sK), 16, 1024);
+        const uint64_t v_desc = sdesc_sw128(smem_u32(sV), 16, 1024);
+        const uint64_t rk_desc = sdesc_sw128(smem_u32(sRing), 16, 1024);            // K-major
+        const uint64_t rm_desc = sdesc_sw128(smem_u32(sRing), T::SMALL_CHUNK, 1024); // MN-major
+        const uint32_t k_lo = static_cast<uint32_t>(k_desc), k_hi = static_cast<uint32_t>(k_desc >> 32);
+        const uint32_t v_lo = static_cast<uint32_t>(v_desc), v_hi = static_cast<uint32_t>(v_desc >> 32);
+        const uint32_t rk_lo = static_cast<uint32_t>(rk_desc), rk_hi = static_cast<uint32_t>(rk_desc >> 32);
+        const uint32_t rm_lo = static_cast<uint32_t>(rm_desc), rm_hi = static_cast<uint32_t>(rm_desc >> 32);
+        bool ok = true;
+        int acq = 0;                 // ring position, across units
+        uint32_t gs = 0;             // steps issued, across units (S/dP buffer = gs & 1)
+        int uk = 0;
+        auto acquire = [&](int& slot) {
+            if (!ok) return;
+            slot = acq % T::NS;
+            ok = mbar_wait(&slot_full[slot], (acq / T::NS) & 1, abort_flag, status, kStatusBwdMma);
+            ok = __all_sync(0xffffffffu, ok);
+            ++acq;
+            tc_fence_after();
+        };
+        // Sᵀ_b = K·Q_slotᵀ and dPᵀ_b = V·dO_slotᵀ: M = 128 keys, N = 64 queries, K = D
+        auto mma_s = [&](int slot, int b) {
+            const uint32_t qoff = (slot * T::SLOT_BYTES) >> 4;
+            const uint32_t dooff = (slot * T::SLOT_BYTES + T::SMALL_TILE) >> 4;
+#pragma unroll
+            for (int kk = 0; kk < D / 16; ++kk) {
+                const uint32_t ao = ((kk >> 2) * T::BIG_CHUNK + (kk & 3) * 32) >> 4;
+                const uint32_t bo = ((kk >> 2) * T::SMALL_CHUNK + (kk & 3) * 32) >> 4;
+                mma_ss_warp(tmem + T::S_COL + b * 64, k_lo + ao, k_hi, rk_lo + qoff + bo, rk_hi,
+                            id_s, kk > 0 ? 1u : 0u);
+                mma_ss_warp(tmem + T::DP_COL + b * 64, v_lo + ao, v_hi, rk_lo + dooff + bo, rk_hi,
+                            id_s, kk > 0 ? 1u : 0u);
+            }
+        };
+        // dV += Pᵀ_b·dO_slot, dK += dSᵀ_b·Q_slot: M = 128 keys, N = D, K = 64 queries
+        auto mma_acc = [&](int slot, int b, bool acc) {
+            const uint32_t qoff = (slot * T::SLOT_BYTES) >> 4;
+            const uint32_t dooff = (slot * T::SLOT_BYTES + T::SMALL_TILE) >> 4;
+#pragma unroll
+            for (int kk = 0; kk < T::BS / 16; ++kk) {
+                const uint32_t bo = (kk * 16 * 128) >> 4;
+                mma_ts_warp(tmem + T::ACC_COL, tmem + T::S_COL + b * 64 + T::PK_OFF + kk * 8,
+                            rm_lo + dooff + bo, rm_hi, id_acc, (acc || kk > 0) ? 1u : 0u);
+                mma_ts_warp(tmem + T::ACC_COL + D, tmem + T::DP_COL + b * 64 + T::PK_OFF + kk * 8,
+                            rm_lo + qoff + bo, rm_hi, id_acc, (acc || kk > 0) ? 1u : 0u);
+            }
+        };
+        uint32_t pc0 = 0, pc1 = 0;
+        for (int r = 0; r * static_cast<int>(gridDim.x) < n_units && ok; ++r) {
+            const int L = unit_of_round(r);
+            if (L >= n_units) continue;
+            int bh, kt, q_begin, n;
+            unit_info(L, bh, kt, q_begin, n);
+            if (n == 0) continue;
+            ok = mbar_wait(kv_full, uk & 1, abort_flag, status, kStatusBwdMma);
+            ok = __all_sync(0xffffffffu, ok);
+            ++uk;
+            tc_fence_after();
+            if (!ok) break;
+            int sl = 0;
+            acquire(sl);
+            if (!ok) break;
+            mma_s(sl, gs & 1);
+            tc_commit_warp(&s_full[gs & 1]);
+            int sl_next = 0;
+            if (n > 1) {
+                acquire(sl_next);
+                if (!ok) break;
+                mma_s(sl_next, (gs + 1) & 1);
+                tc_commit_warp(&s_full[(gs + 1) & 1]);
+            }
+            if (n <= 2) tc_commit_warp(kv_empty);          // K and V no longer needed
+            int cur = sl, nxt = sl_next;
+            for (int t = 0; t < n && ok; ++t) {
+                const int b = static_cast<int>((gs + t) & 1);
+                ok = mbar_wait(&p_full[b], (b ? pc1 : pc0) & 1, abort_flag, status, kStatusBwdMma);
+                ok = __all_sync(0xffffffffu, ok);
+                if (b) ++pc1; else ++pc0;
+                tc_fence_after();
+                if (!ok) break;
+                mma_acc(cur, b, t > 0);
+                tc_commit_warp(&slot_empty[cur]);
+                int nn = 0;
+                if (t + 2 < n) {
+                    acquire(nn);
+                    if (!ok) break;
+                    mma_s(nn, b);
+                    tc_commit_warp(&s_full[b]);
+                    if (t + 3 == n) tc_commit_warp(kv_empty);
+                }
+                cur = nxt;
+                nxt = nn;
+            }
+            if (!ok) break;
+            tc_commit_warp(acc_done);
+            gs += static_cast<uint32_t>(n);
+        }
+        tc_commit_warp(drain);
+        const uint32_t a = smem_u32(drain);
+        const uint64_t t0 = global_timer_ns();
+        while (!mbar_try_wait(a, 0)) {
+            if (global_timer_ns() - t0 > kWaitLimitNs) {
+                if (elect_one()) {
+                    atomicOr(status, kStatusBwdDrain);
+                    *abort_flag = 1;
+                }
+                break;
+            }
+        }
+        __syncwarp();
+    } else if (warp < 4) {
+        // ------------------------------------------------------------ softmax warps
+        const int row = warp * 32 + lane;              // key row within the tile
+        const uint32_t lane_base = tmem + (static_cast<uint32_t>(warp * 32) << 16);
+        bool ok = true;
+        uint32_t gs = 0;
+        int uk = 0;
+        for (int r = 0; r * static_cast<int>(gridDim.x) < n_units && ok; ++r) {
+            const int L = unit_of_round(r);
+            if (L >= n_units) continue;
+            int bh, kt, q_begin, n;
+            unit_info(L, bh, kt, q_begin, n);
+            const int key = kt * T::BU + row;
+            const size_t out_off = (static_cast<size_t>(bh) * S_k + key) * D;
+            if (n == 0) {
+                // No query sees these keys: their gradients are zero.
+                if (key < S_k) {
+                    uint4* a = reinterpret_cast<uint4*>(dk + out_off);
+                    uint4* b = reinterpret_cast<uint4*>(dv + out_off);
+                    for (int i = 0; i < D / 8; ++i) {
+                        a[i] = make_uint4(0, 0, 0, 0);
+                        b[i] = make_uint4(0, 0, 0, 0);
+                    }
+                }
+                continue;
+            }
+            for (int t = 0; t < n; ++t) {
+                const uint32_t s = gs + static_cast<uint32_t>(t);
+                const int b = static_cast<int>(s & 1);
+                const int slot = static_cast<int>(s % T::NS);
+                ok = mbar_wait(&s_full[b], (s >> 1) & 1, abort_flag, status, kStatusBwdSoftmax);
+                if (ok) ok = mbar_wait(&slot_full[slot], (s / T::NS) & 1, abort_flag, status,
+                                       kStatusBwdSoftmax);
+                ok = __all_sync(0xffffffffu, ok);
+                if (!ok) break;
+                tc_fence_after();
+                uint32_t sv[64], dpv[64];
+                tmem_ld64(lane_base + T::S_COL + b * 64, sv);
+                tmem_ld64(lane_base + T::DP_COL + b * 64, dpv);
+                const float* st = sStat + slot * T::STAT_FLOATS;
+                const int q0 = (q_begin + t) * T::BS;
+                // key > query is masked; only steps that reach below the diagonal need it
+                const bool masked = CAUSAL && q0 < kt * T::BU + T::BU - 1;
+                uint32_t pk_p[32], pk_ds[32];
+                if (masked) {
+                    const int lim = key - q0;                  // visible iff c >= lim
+                    grad_pack64<true, BF16, true, true>(sv, dpv, st, st + T::BS, 0.f, 0.f,
+                                                        scale_log2,
+                                                        [&](int c) { return c >= lim; }, pk_p, pk_ds);
+                } else {
+                    grad_pack64<false, BF16, true, true>(sv, dpv, st, st + T::BS, 0.f, 0.f,
+                                                         scale_log2, [](int) { return true; },
+                                                         pk_p, pk_ds);
+                }
+                tmem_st32(lane_base + T::S_COL + b * 64 + T::PK_OFF, pk_p);
+                tmem_st32(lane_base + T::DP_COL + b * 64 + T::PK_OFF, pk_ds);
+                tmem_st_wait();
+                tc_fence_before();
+                __syncwarp();
+                if (lane == 0) mbar_arrive(&p_full[b]);
+            }
+            if (!ok) break;
+            gs += static_cast<uint32_t>(n);
+            ok = mbar_wait(acc_done, uk & 1, abort_flag, status, kStatusBwdSoftmax);
+            ok = __all_sync(0xffffffffu, ok);
+            ++uk;
+            if (!ok) break;
+            tc_fence_after();
+            const bool store = key < S_k;
+            store_row_from_tmem<D, BF16>(lane_base + T::ACC_COL, 1.f, dv + out_off, store);
+            store_row_from_tmem<D, BF16>(lane_base + T::ACC_COL + D, scale, dk + out_off, store);
+        }
+    }
+    tc_fence_before();
+    __syncthreads();
+    if (warp == 0) {
+        tc_fence_after();
+        tmem_dealloc(tmem, T::TMEM_COLS);
+    }
+}
+
+// ============================================================== dQ
+template <int D, bool BF16, bool CAUSAL>
+__global__ void __launch_bounds__(BwdTile<D>::THREADS, 1)
+    attn_bwd_dq_kernel(const __grid_constant__ CUtensorMap tm_q,    // box 64 × 128
+                       const __grid_constant__ CUtensorMap tm_do,   // box 64 × 128
+                       const __grid_constant__ CUtensorMap tm_k,    // box 64 × 64
+                       const __grid_constant__ CUtensorMap tm_v,    // box 64 × 64
+                       const float* __restrict__ lse2, const float* __restrict__ delta,
+                       uint16_t* __restrict__ dq, int S_q, int S_k, int BH, int S_pad,
+                       int head_group, float scale, float scale_log2,
+                       unsigned int* __restrict__ status) {
+    using T = BwdTile<D>;
+    using namespace sm100;
+
+    extern __shared__ uint8_t smem_raw[];
+    const uint32_t raw_addr = smem_u32(smem_raw);
+    uint8_t* smem = smem_raw + ((1024u - (raw_addr & 1023u)) & 1023u);
+    uint8_t* sQ = smem;
+    uint8_t* sdO = sQ + T::BIG_TILE;
+    uint8_t* sRing = sdO + T::BIG_TILE;                 // slot s: K at s·SLOT, V at +SMALL_TILE
+    uint64_t* bars = reinterpret_cast<uint64_t*>(smem + T::TILE_BYTES);
+    uint64_t* q_full = bars;
+    uint64_t* q_empty = q_full + 1;
+    uint64_t* slot_full = q_empty + 1;
+    uint64_t* slot_empty = slot_full + T::NS;
+    uint64_t* s_full = slot_empty + T::NS;
+    uint64_t* p_full = s_full + 2;
+    uint64_t* acc_done = p_full + 2;
+    uint64_t* drain = acc_done + 1;
+    uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(drain + 1);
+    volatile int* abort_flag = reinterpret_cast<volatile int*>(tmem_slot + 1);
+
+    const int warp = threadIdx.x >> 5;
+    const int lane = threadIdx.x & 31;
+    const int n_qt = (S_q + T::BU - 1) / T::BU;
+    const int n_ks = (S_k + T::BS - 1) / T::BS;
+    const int n_units = BH * n_qt;
+    auto unit_info = [&](int L, int& bh, int& qt, int& n) {
+        bwd_unit_coords<CAUSAL, false>(L, BH, n_qt, head_group, bh, qt);
+        n = n_ks;
+        if (CAUSAL) {
+            const int last_row = min(qt * T::BU + T::BU, S_q) - 1;
+            n = min(n_ks, last_row / T::BS + 1);
+        }
+    };
+    auto unit_of_round = [&](int r) {
+        const int G = static_cast<int>(gridDim.x);
+        const int c = static_cast<int>(blockIdx.x);
+        return r * G + ((r & 1) ? (G - 1 - c) : c);
+    };
+
+    if (threadIdx.x == 0) {
+        mbar_init(q_full, 1);
+        mbar_init(q_empty, 1);
+        for (int s = 0; s < T::NS; ++s) {
+            mbar_init(&slot_full[s], 1);
+            mbar_init(&slot_empty[s], 1);
+        }
+        for (int b = 0; b < 2; ++b) {
+            mbar_init(&s_full[b], 1);
+            mbar_init(&p_full[b], 4);
+        }
+        mbar_init(acc_done, 1);
+        mbar_init(drain, 1);
+        *abort_flag = 0;
+        fence_mbar_init();
+        fence_proxy_async_smem();
+    }
+    if (warp == 0) {
+        tmem_alloc(tmem_slot, T::TMEM_COLS);
+        tmem_relinquish();
+    }
+    tc_fence_before();
+    __syncthreads();
+    tc_fence_after();
+    const uint32_t tmem = *tmem_slot;
+
+    if (warp == T::PRODUCER_WARP) {
+        const bool leader = elect_one();
+        if (leader) {
+            tma_prefetch_desc(&tm_q);
+            tma_prefetch_desc(&tm_do);
+            tma_prefetch_desc(&tm_k);
+            tma_prefetch_desc(&tm_v);
+        }
+        __syncwarp();
+        bool ok = true;
+        int idx = 0;
+        int uq = 0;
+        for (int r = 0; r * static_cast<int>(gridDim.x) < n_units && ok; ++r) {
+            const int L = unit_of_round(r);
+            if (L >= n_units) continue;
+            int bh, qt, n;
+            unit_info(L, bh, qt, n);
+            ok = mbar_wait(q_empty, (uq & 1) ^ 1, abort_flag, status, kStatusBwdProducer);
+            ok = __all_sync(0xffffffffu, ok);
+            if (!ok) break;
+            ++uq;
+            if (leader) {
+                mbar_arrive_expect_tx(q_full, 2 * T::BIG_TILE);
+#pragma unroll
+                for (int c = 0; c < T::CHUNKS; ++c) {
+                    tma_load_3d(sQ + c * T::BIG_CHUNK, &tm_q, q_full, c * 64, qt * T::BU, bh);
+                    tma_load_3d(sdO + c * T::BIG_CHUNK, &tm_do, q_full, c * 64, qt * T::BU, bh);
+                }
+            }
+            __syncwarp();
+            for (int t = 0; t < n && ok; ++t) {
+                const int slot = idx % T::NS;
+                ok = mbar_wait(&slot_empty[slot], ((idx / T::NS) & 1) ^ 1, abort_flag, status,
+                               kStatusBwdProducer);
+                ok = __all_sync(0xffffffffu, ok);
+                if (!ok) break;
+                if (leader) {
+                    uint8_t* dst = sRing + slot * T::SLOT_BYTES;
+                    mbar_arrive_expect_tx(&slot_full[slot], T::SLOT_BYTES);
+#pragma unroll
+                    for (int c = 0; c < T::CHUNKS; ++c) {
+                        tma_load_3d(dst + c * T::SMALL_CHUNK, &tm_k, &slot_full[slot], c * 64,
+                                    t * T::BS, bh);
+                        tma_load_3d(dst + T::SMALL_TILE + c * T::SMALL_CHUNK, &tm_v,
+                                    &slot_full[slot], c * 64, t * T::BS, bh);
+                    }
+                }
+                __syncwarp();
+                ++idx;
+            }
+        }
+        if (*abort_flag && leader) {
+            const uint64_t t0 = global_timer_ns();
+            for (int i = max(0, idx - T::NS); i < idx; ++i) {
+                const uint32_t a = smem_u32(&slot_full[i % T::NS]);
+                while (!mbar_try_wait(a, (i / T::NS) & 1)) {
+                    if (global_timer_ns() - t0 > kWaitLimitNs) {
+                        atomicOr(status, kStatusBwdDrain);
+                        break;
+                    }
+                }
+            }
+            if (uq > 0) {
+                const uint32_t a = smem_u32(q_full);
+                while (!mbar_try_wait(a, static_cast<uint32_t>(uq - 1) & 1u)) {
+                    if (global_timer_ns() - t0 > kWaitLimitNs) {
+                        atomicOr(status, kStatusBwdDrain);
+                        break;
+                    }
+                }
+            }
+        }
+        __syncwarp();
+    } else if (warp == T::MMA_WARP) {
+        constexpr uint32_t id_s = idesc_f16(128, T::BS, BF16, false, false);
+        constexpr uint32_t id_acc = idesc_f16(128, D, BF16, false, true);
+        const uint64_t q_desc = sdesc_sw128(smem_u32(sQ), 16, 1024);
+        const uint64_t do_desc = sdesc_sw128(smem_u32(sdO), 16, 1024);
+        const uint64_t rk_desc = sdesc_sw128(smem_u32(sRing), 16, 1024);
+        const uint64_t rm_desc = sdesc_sw128(smem_u32(sRing), T::SMALL_CHUNK, 1024);
+        const uint32_t q_lo = static_cast<uint32_t>(q_desc), q_hi = static_cast<uint32_t>(q_desc >> 32);
+        const uint32_t do_lo = static_cast<uint32_t>(do_desc), do_hi = static_cast<uint32_t>(do_desc >> 32);
+        const uint32_t rk_lo = static_cast<uint32_t>(rk_desc), rk_hi = static_cast<uint32_t>(rk_desc >> 32);
+        const uint32_t rm_lo = static_cast<uint32_t>(rm_desc), rm_hi = static_cast<uint32_t>(rm_desc >> 32);
+        bool ok = true;
+        int acq = 0;
+        uint32_t gs = 0;
+        int uq = 0;
+        auto acquire = [&](int& slot) {
+            if (!ok) return;
+            slot = acq % T::NS;
+            ok = mbar_wait(&slot_full[slot], (acq / T::NS) & 1, abort_flag, status, kStatusBwdMma);
+            ok = __all_sync(0xffffffffu, ok);
+            ++acq;
+            tc_fence_after();
+        };
+        // S_b = Q·K_slotᵀ, dP_b = dO·V_slotᵀ: M = 128 queries, N = 64 keys, K = D
+        auto mma_s = [&](int slot, int b) {
+            const uint32_t koff = (slot * T::SLOT_BYTES) >> 4;
+            const uint32_t voff = (slot * T::SLOT_BYTES + T::SMALL_TILE) >> 4;
+#pragma unroll
+            for (int kk = 0; kk < D / 16; ++kk) {
+                const uint32_t ao = ((kk >> 2) * T::BIG_CHUNK + (kk & 3) * 32) >> 4;
+                const uint32_t bo = ((kk >> 2) * T::SMALL_CHUNK + (kk & 3) * 32) >> 4;
+                mma_ss_warp(tmem + T::S_COL + b * 64, q_lo + ao, q_hi, rk_lo + koff + bo, rk_hi,
+                            id_s, kk > 0 ? 1u : 0u);
+                mma_ss_warp(tmem + T::DP_COL + b * 64, do_lo + ao, do_hi, rk_lo + voff + bo, rk_hi,
+                            id_s, kk > 0 ? 1u : 0u);
+            }
+        };
+        // dQ += dS_b·K_slot: M = 128 queries, N = D, K = 64 keys
+        auto mma_acc = [&](int slot, int b, bool acc) {
+            const uint32_t koff = (slot * T::SLOT_BYTES) >> 4;
+#pragma unroll
+            for (int kk = 0; kk < T::BS / 16; ++kk) {
+                const uint32_t bo = (kk * 16 * 128) >> 4;
+                mma_ts_warp(tmem + T::ACC_COL, tmem + T::S_COL + b * 64 + T::PK_OFF + kk * 8,
+                            rm_lo + koff + bo, rm_hi, id_acc, (acc || kk > 0) ? 1u : 0u);
+            }
+        };
+        uint32_t pc0 = 0, pc1 = 0;
+        for (int r = 0; r * static_cast<int>(gridDim.x) < n_units && ok; ++r) {
+            const int L = unit_of_round(r);
+            if (L >= n_units) continue;
+            int bh, qt, n;
+            unit_info(L, bh, qt, n);
+            ok = mbar_wait(q_full, uq & 1, abort_flag, status, kStatusBwdMma);
+            ok = __all_sync(0xffffffffu, ok);
+            ++uq;
+            tc_fence_after();
+            if (!ok) break;
+            int sl = 0;
+            acquire(sl);
+            if (!ok) break;
+            mma_s(sl, gs & 1);
+            tc_commit_warp(&s_full[gs & 1]);
+            int sl_next = 0;
+            if (n > 1) {
+                acquire(sl_next);
+                if (!ok) break;
+                mma_s(sl_next, (gs + 1) & 1);
+                tc_commit_warp(&s_full[(gs + 1) & 1]);
+            }
+            if (n <= 2) tc_commit_warp(q_empty);           // Q and dO no longer needed
+            int cur = sl, nxt = sl_next;
+            for (int t = 0; t < n && ok; ++t) {
+                const int b = static_cast<int>((gs + t) & 1);
+                ok = mbar_wait(&p_full[b], (b ? pc1 : pc0) & 1, abort_flag, status, kStatusBwdMma);
+                ok = __all_sync(0xffffffffu, ok);
+                if (b) ++pc1; else ++pc0;
+                tc_fence_after();
+                if (!ok) break;
+                mma_acc(cur, b, t > 0);
+                tc_commit_warp(&slot_empty[cur]);
+                int nn = 0;
+                if (t + 2 < n) {
+                    acquire(nn);
+                    if (!ok) break;
+                    mma_s(nn, b);
+                    tc_commit_warp(&s_full[b]);
+                    if (t + 3 == n) tc_commit_warp(q_empty);
+                }
+                cur = nxt;
+                nxt = nn;
+            }
+            if (!ok) break;
+            tc_commit_warp(acc_done);
+            gs += static_cast<uint32_t>(n);
+        }
+        tc_commit_warp(drain);
+        const uint32_t a = smem_u32(drain);
+        const uint64_t t0 = global_timer_ns();
+        while (!mbar_try_wait(a, 0)) {
+            if (global_timer_ns() - t0 > kWaitLimitNs) {
+                if (elect_one()) {
+                    atomicOr(status, kStatusBwdDrain);
+                    *abort_flag = 1;
+                }
+                break;
+            }
+        }
+        __syncwarp();
+    } else if (warp < 4) {
+        const int row = warp * 32 + lane;                // query row within the tile
+        const uint32_t lane_base = tmem + (static_cast<uint32_t>(warp * 32) << 16);
+        bool ok = true;
+        uint32_t gs = 0;
+        int uq = 0;
+        for (int r = 0; r * static_cast<int>(gridDim.x) < n_units && ok; ++r) {
+            const int L = unit_of_round(r);
+            if (L >= n_units) continue;
+            int bh, qt, n;
+            unit_info(L, bh, qt, n);
+            const int q_idx = qt * T::BU + row;
+            const float row_lse2 = lse2[static_cast<size_t>(bh) * S_pad + q_idx];
+            const float row_dd = delta[static_cast<size_t>(bh) * S_pad + q_idx];
+            const int row_begin = qt * T::BU;
+            for (int t = 0; t < n; ++t) {
+                const uint32_t s = gs + static_cast<uint32_t>(t);
+                const int b = static_cast<int>(s & 1);
+                ok = mbar_wait(&s_full[b], (s >> 1) & 1, abort_flag, status, kStatusBwdSoftmax);
+                ok = __all_sync(0xffffffffu, ok);
+                if (!ok) break;
+                tc_fence_after();
+                uint32_t sv[64], dpv[64];
+                tmem_ld64(lane_base + T::S_COL + b * 64, sv);
+                tmem_ld64(lane_base + T::DP_COL + b * 64, dpv);
+                const int kv0 = t * T::BS;
+                const bool masked =
+                    (CAUSAL && kv0 + T::BS - 1 > row_begin) || (kv0 + T::BS > S_k);
+                uint32_t pk_p[32], pk_ds[32];
+                if (masked) {
+                    const int lim = min(S_k, CAUSAL ? q_idx + 1 : S_k) - kv0;  // visible iff c < lim
+                    grad_pack64<true, BF16, false, false>(sv, dpv, nullptr, nullptr, row_lse2,
+                                                          row_dd, scale_log2,
+                                                          [&](int c) { return c < lim; }, pk_p, pk_ds);
+                } else {
+                    grad_pack64<false, BF16, false, false>(sv, dpv, nullptr, nullptr, row_lse2,
+                                                           row_dd, scale_log2,
+                                                           [](int) { return true; }, pk_p, pk_ds);
+                }
+                tmem_st32(lane_base + T::S_COL + b * 64 + T::PK_OFF, pk_ds);
+                tmem_st_wait();
+                tc_fence_before();
+                __syncwarp();
+                if (lane == 0) mbar_arrive(&p_full[b]);
+            }
+            if (!ok) break;
+            gs += static_cast<uint32_t>(n);
+            ok = mbar_wait(acc_done, uq & 1, abort_flag, status, kStatusBwdSoftmax);
+            ok = __all_sync(0xffffffffu, ok);
+            ++uq;
+            if (!ok) break;
+            tc_fence_after();
+            store_row_from_tmem<D, BF16>(lane_base + T::ACC_COL, scale,
+                                         dq + (static_cast<size_t>(bh) * S_q + q_idx) * D,
+                                         q_idx < S_q);
+        }
+    }
+    tc_fence_before();
+    __syncthreads();
+    if (warp == 0) {
+        tc_fence_after();
+        tmem_dealloc(tmem, T::TMEM_COLS);
+    }
+}
+
+// ============================================================== launch
+template <int D, bool BF16, bool CAUSAL>
+cudaError_t launch_attn_bwd(const BwdArgs& a, cudaStream_t stream) {
+    using T = BwdTile<D>;
+    // D and LSE·log2e into the padded workspace.
+    const long long rows_pad = static_cast<long long>(a.BH) * a.S_pad;
+    const long long pblocks = (rows_pad + 7) / 8;
+    if (pblocks > 0x7fffffffLL) return cudaErrorInvalidConfiguration;
+    attn_bwd_prep_kernel<D, BF16><<<static_cast<unsigned>(pblocks), 256, 0, stream>>>(
+        static_cast<const uint16_t*>(a.o), static_cast<const uint16_t*>(a.dout), a.lse, a.lse2,
+        a.delta, a.S_q, a.S_pad, rows_pad);
+    cudaError_t err = cudaGetLastError();
+    if (err != cudaSuccess) return err;
+
+    const long long op_bytes = 2LL * D * 2;   // per row of one head: two operands
+    const long long group_bytes = 48LL << 20;
+
+    auto kdkdv = attn_bwd_dkdv_kernel<D, BF16, CAUSAL>;
+    err = cudaFuncSetAttribute(kdkdv, cudaFuncAttributeMaxDynamicSharedMemorySize, T::SMEM_BYTES);
+    if (err != cudaSuccess) return err;
+    const int n_kt = (a.S_k + T::BU - 1) / T::BU;
+    const long long units_kv = static_cast<long long>(a.BH) * n_kt;
+    if (units_kv > 0x7fffffffLL) return cudaErrorInvalidConfiguration;
+    const int hg_kv = static_cast<int>(std::max<long long>(1, group_bytes / (op_bytes * a.S_q)));
+    kdkdv<<<static_cast<int>(std::min<long long>(units_kv, a.num_sms)), T::THREADS, T::SMEM_BYTES,
+            stream>>>(a.tm_k_fixed, a.tm_v_fixed, a.tm_q_step, a.tm_do_step, a.lse2, a.delta,
+                      static_cast<uint16_t*>(a.dk), static_cast<uint16_t*>(a.dv), a.S_q, a.S_k,
+                      a.BH, a.S_pad, hg_kv, a.scale, a.scale_log2, a.status);
+    err = cudaGetLastError();
+    if (err != cudaSuccess) return err;
+
+    auto kdq = attn_bwd_dq_kernel<D, BF16, CAUSAL>;
+    err = cudaFuncSetAttribute(kdq, cudaFuncAttributeMaxDynamicSharedMemorySize, T::SMEM_BYTES);
+    if (err != cudaSuccess) return err;
+    const int n_qt = (a.S_q + T::BU - 1) / T::BU;
+    const long long units_q = static_cast<long long>(a.BH) * n_qt;
+    if (units_q > 0x7fffffffLL) return cudaErrorInvalidConfiguration;
+    const int hg_q = static_cast<int>(std::max<long long>(1, group_bytes / (op_bytes * a.S_k)));
+    kdq<<<static_cast<int>(std::min<long long>(units_q, a.num_sms)), T::THREADS, T::SMEM_BYTES,
+          stream>>>(a.tm_q_fixed, a.tm_do_fixed, a.tm_k_step, a.tm_v_step, a.lse2, a.delta,
+                    static_cast<uint16_t*>(a.dq), a.S_q, a.S_k, a.BH, a.S_pad, hg_q, a.scale,
+                    a.scale_log2, a.status);
+    return cudaGetLastError();
+}
+
+}  // namespace attn

@@ -96,6 +96,31 @@ cudaError_t launch_attn_combine(const float* o_part, const float* lse_part, void
                                 int n_split, long long rows, int d, bool bf16,
                                 cudaStream_t stream);
 
+// Backward launch contract (attn_bwd.cuh).  Fixed operands are the 128-row
+// tiles a unit keeps for all its steps (K, V for dK/dV; Q, dO for dQ); step
+// operands are the 64-row tiles it streams.
+struct BwdArgs {
+    CUtensorMap tm_k_fixed, tm_v_fixed;   // [B·H, S_k, d], box 64 × 128
+    CUtensorMap tm_q_step, tm_do_step;    // [B·H, S_q, d], box 64 × 64
+    CUtensorMap tm_q_fixed, tm_do_fixed;  // [B·H, S_q, d], box 64 × 128
+    CUtensorMap tm_k_step, tm_v_step;     // [B·H, S_k, d], box 64 × 64
+    const void* o;                        // forward output [B, H, S_q, d]
+    const void* dout;                     // dO [B, H, S_q, d]
+    const float* lse;                     // forward LSE [B, H, S_q], natural log
+    float* lse2;                          // workspace [B·H, S_pad]: LSE·log2(e)
+    float* delta;                         // workspace [B·H, S_pad]: rowsum(dO ∘ O)
+    void* dq;
+    void* dk;
+    void* dv;
+    int32_t S_q, S_k, BH, S_pad;          // S_pad = S_q rounded up to 128
+    float scale, scale_log2;
+    int32_t num_sms;
+    unsigned int* status;
+};
+
+template <int D, bool BF16, bool CAUSAL>
+cudaError_t launch_attn_bwd(const BwdArgs& args, cudaStream_t stream);
+
 // Device address of the built-in split-KV scratch (ATTN_NOALLOC_SCRATCH_BYTES
 // bytes, 256-byte aligned) on the current device.
 cudaError_t noalloc_scratch_address(void** ptr);

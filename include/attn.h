@@ -175,6 +175,49 @@ attn_status_t attn_fwd_splitkv(const void* q, const void* k, const void* v, void
                                int64_t workspace_bytes, struct CUstream_st* stream);
 
 /*
+ * Backward pass (oxicuda-dnn 0.1.8, src/attn/flash_attn/hopper.rs, doc comment
+ * of FlashAttention3Plan::generate_backward, and its parameter list q, k, v,
+ * o, do, lse, di, dq, dk, dv, sm_scale): with P recomputed from the saved LSE,
+ *
+ *     dV = Pᵀ·dO      dP = dO·Vᵀ      dS = P ∘ (dP − D),  D_i = Σ_c dO_ic·O_ic
+ *     dQ = scale·dS·K                 dK = scale·dSᵀ·Q
+ *
+ * (the gradients of Σ O ∘ dO for the forward above; the scale follows from the
+ * chain rule through scale·Q·Kᵀ).  dQ is produced by its own pass, not by
+ * atomic adds, so results are deterministic.  head_dim 64 or 128.
+ *
+ * attn_bwd_workspace_size — bytes of workspace attn_bwd needs:
+ * 2 · B·H · S_pad · 4 with S_pad = S_q rounded up to a multiple of 128 (the
+ * page's di vector and the LSE in base 2, padded to whole tiles).  Validates
+ * like attn_fwd (and head_dim ∈ {64, 128}); touches no device.
+ */
+attn_status_t attn_bwd_workspace_size(int64_t B, int64_t H, int64_t S_q, int64_t S_k, int64_t d,
+                                      attn_dtype_t dtype, int64_t* workspace_bytes);
+
+/*
+ * attn_bwd — enqueue the backward on `stream` (three kernels, in order).
+ *
+ *   q, k, v    the forward's inputs (layouts as attn_fwd), device, 16-byte aligned
+ *   o, lse     the forward's outputs for the same q, k, v, causal and scale
+ *              (o 16-byte aligned, lse 4-byte aligned)
+ *   dout       dO, the gradient of the loss with respect to o, [B,H,S_q,d]
+ *   dq, dk, dv outputs, [B,H,S_q,d], [B,H,S_k,d], [B,H,S_k,d] in `dtype`,
+ *              16-byte aligned; every element is written (key rows that no
+ *              query sees get zeros)
+ *   B .. dtype as attn_fwd; d ∈ {64, 128}
+ *   workspace  device, 16-byte aligned, at least attn_bwd_workspace_size
+ *              bytes; written before it is read (nothing needs clearing);
+ *              calls in flight at the same time need separate workspaces
+ *
+ * dq, dk, dv and workspace must not overlap each other or any input.
+ */
+attn_status_t attn_bwd(const void* q, const void* k, const void* v, const void* o,
+                       const float* lse, const void* dout, void* dq, void* dk, void* dv,
+                       int64_t B, int64_t H, int64_t S_q, int64_t S_k, int64_t d, int causal,
+                       float scale, attn_dtype_t dtype, void* workspace, int64_t workspace_bytes,
+                       struct CUstream_st* stream);
+
+/*
  * attn_fwd_splitkv_noalloc — attn_fwd_splitkv without a caller workspace and
  * without allocating anything.
  *
@@ -223,7 +266,7 @@ const char* attn_last_error(void);
 
 /*
  * attn_get_device_status — synchronise `stream`, then read and clear the
- * current device's status word.  ATTN_OK if every kernel since the last read
+ * current device's status word (shared by the forward and backward kernels).  ATTN_OK if every kernel since the last read
  * finished its waits; ATTN_ERR_TIMEOUT if one ran out (the message names the
  * role that gave up); ATTN_ERR_CUDA if the synchronisation itself failed.
  */

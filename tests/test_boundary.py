@@ -37,8 +37,9 @@ def _declared_functions():
 def test_header_declares_the_boundary():
     names = _declared_functions()
     assert names == sorted(["attn_fwd", "attn_fwd_host", "attn_fwd_plan", "attn_fwd_splitkv_plan",
-                            "attn_fwd_splitkv", "attn_fwd_splitkv_noalloc", "attn_last_error",
-                            "attn_get_device_status", "attn_version"])
+                            "attn_fwd_splitkv", "attn_fwd_splitkv_noalloc", "attn_bwd_workspace_size",
+                            "attn_bwd", "attn_last_error", "attn_get_device_status",
+                            "attn_version"])
 
 
 def test_library_exports_every_declared_symbol(lib):
@@ -251,3 +252,48 @@ def test_noalloc_header_states_the_scratch_size():
     text = open(HEADER).read()
     m = re.search(r"#define ATTN_NOALLOC_SCRATCH_BYTES \((\d+) \* 1024 \* 1024\)", text)
     assert m and int(m.group(1)) * 1024 * 1024 == binding.NOALLOC_SCRATCH_BYTES
+
+
+# ------------------------------------------------------------------ backward
+
+
+def test_bwd_workspace_size(lib):
+    assert binding.attn_bwd_workspace_size(2, 3, 300, 77, 128, binding.ATTN_DTYPE_BF16) == \
+        2 * 6 * 384 * 4
+    assert binding.attn_bwd_workspace_size(1, 1, 128, 1, 64, binding.ATTN_DTYPE_F16) == 2 * 128 * 4
+    with pytest.raises(binding.AttnError, match="backward"):
+        binding.attn_bwd_workspace_size(1, 1, 128, 128, 256, binding.ATTN_DTYPE_BF16)
+
+
+def _bwd(lib, **kw):
+    G = 1 << 24
+    args = dict(q=A, k=A + G, v=A + 2 * G, o=A + 3 * G, lse=A + 4 * G, dout=A + 5 * G,
+                dq=A + 6 * G, dk=A + 7 * G, dv=A + 8 * G, B=1, H=2, S_q=256, S_k=256, d=128,
+                causal=0, scale=0.125, dtype=1, ws=A + 9 * G, ws_bytes=1 << 20)
+    args.update(kw)
+    a = args
+    return lib.attn_bwd(a["q"], a["k"], a["v"], a["o"], a["lse"], a["dout"], a["dq"], a["dk"],
+                        a["dv"], a["B"], a["H"], a["S_q"], a["S_k"], a["d"], a["causal"],
+                        a["scale"], a["dtype"], a["ws"], a["ws_bytes"], None)
+
+
+BWD_CASES = [
+    (dict(d=256), binding.ATTN_ERR_UNSUPPORTED, "backward"),
+    (dict(d=96), binding.ATTN_ERR_UNSUPPORTED, "head_dim"),
+    (dict(dout=0), binding.ATTN_ERR_INVALID_ARG, "dout is null"),
+    (dict(dq=0), binding.ATTN_ERR_INVALID_ARG, "dq is null"),
+    (dict(ws=0), binding.ATTN_ERR_INVALID_ARG, "workspace is null"),
+    (dict(dk=A + (7 << 24) + 8), binding.ATTN_ERR_INVALID_ARG, "dk is not 16-byte aligned"),
+    (dict(lse=A + (4 << 24) + 2), binding.ATTN_ERR_INVALID_ARG, "lse is not 4-byte aligned"),
+    (dict(ws_bytes=2 * 2 * 256 * 4 - 1), binding.ATTN_ERR_INVALID_ARG, "workspace_bytes"),
+    (dict(dq=A + 64), binding.ATTN_ERR_INVALID_ARG, "dq overlaps q"),
+    (dict(dv=A + (7 << 24) + 1024), binding.ATTN_ERR_INVALID_ARG, "dk overlaps dv"),
+    (dict(ws=A + (8 << 24)), binding.ATTN_ERR_INVALID_ARG, "overlaps"),
+    (dict(causal=3), binding.ATTN_ERR_INVALID_ARG, "causal"),
+]
+
+
+@pytest.mark.parametrize("kw,status,msg", BWD_CASES, ids=[c[2] for c in BWD_CASES])
+def test_bwd_validation_rejects_before_device_work(lib, kw, status, msg):
+    assert _bwd(lib, **kw) == status
+    assert msg in lib.attn_last_error().decode()
