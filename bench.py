@@ -10,7 +10,9 @@ inputs resident in HBM; ``e2e`` is the same metric through the host-buffer C
 entry point, copies included; ``roofline`` is for the dominant launch (the
 full one); ``cpu_baseline`` times the fp64 oracle on a bounded sample;
 ``splitkv`` reports the split-KV forward on the decode workload (one query row
-per head against 32768 keys) in HBM GB/s, measured after the timed steps.
+per head against 32768 keys) in HBM GB/s, and ``backward`` the backward pass
+(dQ, dK, dV) on the same c3 inputs in TFLOP/s; both are measured after the
+timed steps and are not part of ``value``.
 
 ``--impl reference`` times the fp64 CPU oracle instead (there is no runnable
 reference implementation: the attention page is Rust that emits PTX for
@@ -266,6 +268,54 @@ def measure_splitkv(dev, stream, iters: int = 50):
             "gpu_launches_per_call": 2 if n_split > 1 else 1, "calls_timed": iters}
 
 
+def measure_bwd(dev, stream, w, q, k, v, iters: int = 10):
+    """Backward (dQ, dK, dV) on the benchmark workload, both masking modes.
+
+    FLOPs per call are counted as 2.5 forwards (the five S_q×S_k×d products
+    dV = Pᵀ·dO, dP = dO·Vᵀ, dQ = dS·K, dK = dSᵀ·Q and the recomputed Q·Kᵀ),
+    halved when causal; the kernels execute seven such products (dQ has its
+    own pass that recomputes Q·Kᵀ and dO·Vᵀ, so no atomics are needed).
+    """
+    import torch
+
+    from exact_attention_53_gb300 import attn_bwd, attn_bwd_workspace_size, attn_fwd
+    from exact_attention_53_gb300.binding import ATTN_DTYPE_BF16
+    from exact_attention_53_gb300.workloads import make_qkv
+
+    B, H, S_q, S_k, d = w.B, w.H, w.S_q, w.S_k, w.d
+    dout = make_qkv(B, H, S_q, 1, d, w.dtype, seed=w.seed + 100)[0].to(dev)
+    ws = attn_bwd_workspace_size(B, H, S_q, S_k, d, ATTN_DTYPE_BF16)
+    work = torch.empty(ws, dtype=torch.uint8, device=dev)
+    dq, dk, dv = torch.empty_like(q), torch.empty_like(k), torch.empty_like(v)
+    res = {}
+    for causal in (False, True):
+        o = torch.empty_like(q)
+        lse = torch.empty((B, H, S_q), dtype=torch.float32, device=dev)
+        attn_fwd(q, k, v, o, lse, B, H, S_q, S_k, d, int(causal), w.scale, ATTN_DTYPE_BF16, stream)
+
+        def call():
+            attn_bwd(q, k, v, o, lse, dout, dq, dk, dv, B, H, S_q, S_k, d, int(causal), w.scale,
+                     ATTN_DTYPE_BF16, work, ws, stream)
+
+        for _ in range(3):
+            call()
+        torch.cuda.synchronize(dev)
+        ev = [(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True))
+              for _ in range(iters)]
+        for a, b in ev:
+            a.record(stream)
+            call()
+            b.record(stream)
+        torch.cuda.synchronize(dev)
+        ms = statistics.mean(a.elapsed_time(b) for a, b in ev)
+        flops = 2.5 * w.flops(causal)
+        res["causal" if causal else "full"] = {"ms": ms, "tflops": flops / (ms * 1e-3) / 1e12}
+    res["flops_convention"] = "2.5 x forward (five S_q x S_k x d products), halved when causal"
+    res["gpu_launches_per_call"] = 3
+    res["calls_timed"] = iters
+    return res
+
+
 def run_gpu(args, rank, world):
     import torch
 
@@ -366,6 +416,7 @@ def run_gpu(args, rank, world):
     in_bytes = q.numel() * 2 + k.numel() * 2 + v.numel() * 2
     out_bytes = o.numel() * 2 + lse.numel() * 4
     splitkv = measure_splitkv(dev, stream)
+    backward = measure_bwd(dev, stream, w, q, k, v)
     attn_get_device_status(stream)
     sampler.stop()
 
@@ -410,6 +461,10 @@ def run_gpu(args, rank, world):
                            "kernel": "attn_fwd_kernel<128,bf16,full,split> + attn_combine_kernel",
                            "peak_source": f"{peak_src} copy bandwidth (hbm_gbs)"}
     line["splitkv"] = splitkv
+    for mode in ("full", "causal"):
+        backward[mode]["frac_of_peak"] = backward[mode]["tflops"] / peak
+    backward["workload"] = f"{WORKLOAD}: B={B} H={H} S_q=S_k={S_q} d={d} bf16, dO~N(0,1)"
+    line["backward"] = backward
     if not args.no_cpu_baseline and world == 1:
         line["cpu_baseline"] = cpu_baseline()
     print(json.dumps(line), flush=True)

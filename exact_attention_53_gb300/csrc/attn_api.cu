@@ -602,8 +602,6 @@ attn_status_t attn_bwd(const void* q, const void* k, const void* v, const void* 
     if ((s = encode_rows_box(&a.tm_do_step, dout, p, p.S_q, 64, "dout")) != ATTN_OK) return s;
     if ((s = encode_rows_box(&a.tm_q_fixed, q, p, p.S_q, 128, "q")) != ATTN_OK) return s;
     if ((s = encode_rows_box(&a.tm_do_fixed, dout, p, p.S_q, 128, "dout")) != ATTN_OK) return s;
-    if ((s = encode_rows_box(&a.tm_k_step, k, p, p.S_k, 64, "k")) != ATTN_OK) return s;
-    if ((s = encode_rows_box(&a.tm_v_step, v, p, p.S_k, 64, "v")) != ATTN_OK) return s;
     const int64_t s_pad = bwd_s_pad(p);
     a.o = o;
     a.dout = dout;

@@ -15,7 +15,7 @@
 //                          Pᵀ and dSᵀ formed by four softmax warps (one key
 //                          row per thread), dV += Pᵀ·dO and dK += dSᵀ·Q with
 //                          Pᵀ / dSᵀ read from TMEM;
-//   attn_bwd_dq_kernel     one unit = (head, 128 queries): loops over 64-key
+//   attn_bwd_dq_kernel     one unit = (head, 128 queries): loops over 128-key
 //                          steps, S = Q·Kᵀ and dP = dO·Vᵀ, dS by the softmax
 //                          warps (one query row per thread), dQ += dS·K.
 //
@@ -575,32 +575,67 @@ __global__ void __launch_bounds__(BwdTile<D>::THREADS, 1)
 }
 
 // ============================================================== dQ
+// 128-key steps, so every Q·Kᵀ / dO·Vᵀ MMA has N = 128.  Tensor memory: S in
+// two buffers (columns 0 and 128; dS overwrites the first 64 columns of its
+// own buffer as packed 16-bit pairs), one dP buffer (256) that the softmax
+// warps release as soon as they have read it, dQ at 384.  K and V arrive
+// through separate shared-memory rings.
+template <int D>
+struct DqTile {
+    static_assert(D == 64 || D == 128, "the backward is built for head_dim 64 and 128");
+    static constexpr int BU = 128;                    // query rows per unit
+    static constexpr int BS = 128;                    // keys per step
+    static constexpr int CHUNKS = D / 64;
+    static constexpr int CHUNK = 128 * 128;           // one atom column of a 128-row tile
+    static constexpr int TILE = 128 * D * 2;
+    // K and V stream through rings of their own: V of a step is free once its
+    // dP MMA is done, K only after the step's dQ MMA.
+    static constexpr int KS = D == 64 ? 5 : 3;        // K ring slots
+    static constexpr int VS = D == 64 ? 4 : 2;        // V ring slots
+    static constexpr int NUM_BARS = 2 + 2 * KS + 2 * VS + 2 + 1 + 2 + 1 + 1;
+    static constexpr int TILE_BYTES = 2 * TILE + (KS + VS) * TILE;
+    static constexpr int SMEM_BYTES = 1024 + TILE_BYTES + NUM_BARS * 8 + 16;
+    static constexpr int THREADS = 192;
+    static constexpr int PRODUCER_WARP = 4;
+    static constexpr int MMA_WARP = 5;
+    static constexpr uint32_t TMEM_COLS = 512;
+    static constexpr uint32_t S_COL = 0;              // S buffer b at 128·b
+    static constexpr uint32_t DP_COL = 256;
+    static constexpr uint32_t ACC_COL = 384;
+    static_assert(SMEM_BYTES <= 232448, "shared memory budget");
+    static_assert(ACC_COL + D <= TMEM_COLS, "tensor memory budget");
+};
+
 template <int D, bool BF16, bool CAUSAL>
-__global__ void __launch_bounds__(BwdTile<D>::THREADS, 1)
+__global__ void __launch_bounds__(DqTile<D>::THREADS, 1)
     attn_bwd_dq_kernel(const __grid_constant__ CUtensorMap tm_q,    // box 64 × 128
                        const __grid_constant__ CUtensorMap tm_do,   // box 64 × 128
-                       const __grid_constant__ CUtensorMap tm_k,    // box 64 × 64
-                       const __grid_constant__ CUtensorMap tm_v,    // box 64 × 64
+                       const __grid_constant__ CUtensorMap tm_k,    // box 64 × 128
+                       const __grid_constant__ CUtensorMap tm_v,    // box 64 × 128
                        const float* __restrict__ lse2, const float* __restrict__ delta,
                        uint16_t* __restrict__ dq, int S_q, int S_k, int BH, int S_pad,
                        int head_group, float scale, float scale_log2,
                        unsigned int* __restrict__ status) {
-    using T = BwdTile<D>;
+    using T = DqTile<D>;
     using namespace sm100;
 
     extern __shared__ uint8_t smem_raw[];
     const uint32_t raw_addr = smem_u32(smem_raw);
     uint8_t* smem = smem_raw + ((1024u - (raw_addr & 1023u)) & 1023u);
     uint8_t* sQ = smem;
-    uint8_t* sdO = sQ + T::BIG_TILE;
-    uint8_t* sRing = sdO + T::BIG_TILE;                 // slot s: K at s·SLOT, V at +SMALL_TILE
+    uint8_t* sdO = sQ + T::TILE;
+    uint8_t* sKr = sdO + T::TILE;                      // K ring
+    uint8_t* sVr = sKr + T::KS * T::TILE;              // V ring
     uint64_t* bars = reinterpret_cast<uint64_t*>(smem + T::TILE_BYTES);
     uint64_t* q_full = bars;
     uint64_t* q_empty = q_full + 1;
-    uint64_t* slot_full = q_empty + 1;
-    uint64_t* slot_empty = slot_full + T::NS;
-    uint64_t* s_full = slot_empty + T::NS;
-    uint64_t* p_full = s_full + 2;
+    uint64_t* k_full = q_empty + 1;
+    uint64_t* k_empty = k_full + T::KS;
+    uint64_t* v_full = k_empty + T::KS;
+    uint64_t* v_empty = v_full + T::VS;
+    uint64_t* s_full = v_empty + T::VS;      // [2] S_b and the dP of that step computed
+    uint64_t* dp_free = s_full + 2;          // the dP buffer has been read (per warp)
+    uint64_t* p_full = dp_free + 1;          // [2] dS written over S_b (per warp)
     uint64_t* acc_done = p_full + 2;
     uint64_t* drain = acc_done + 1;
     uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(drain + 1);
@@ -628,14 +663,19 @@ __global__ void __launch_bounds__(BwdTile<D>::THREADS, 1)
     if (threadIdx.x == 0) {
         mbar_init(q_full, 1);
         mbar_init(q_empty, 1);
-        for (int s = 0; s < T::NS; ++s) {
-            mbar_init(&slot_full[s], 1);
-            mbar_init(&slot_empty[s], 1);
+        for (int s = 0; s < T::KS; ++s) {
+            mbar_init(&k_full[s], 1);
+            mbar_init(&k_empty[s], 1);
+        }
+        for (int s = 0; s < T::VS; ++s) {
+            mbar_init(&v_full[s], 1);
+            mbar_init(&v_empty[s], 1);
         }
         for (int b = 0; b < 2; ++b) {
             mbar_init(&s_full[b], 1);
             mbar_init(&p_full[b], 4);
         }
+        mbar_init(dp_free, 4);
         mbar_init(acc_done, 1);
         mbar_init(drain, 1);
         *abort_flag = 0;
@@ -661,8 +701,27 @@ __global__ void __launch_bounds__(BwdTile<D>::THREADS, 1)
         }
         __syncwarp();
         bool ok = true;
-        int idx = 0;
+        int kidx = 0, vidx = 0;
         int uq = 0;
+        // One tile into ring slot idx % SLOTS once its previous use is released.
+        auto load = [&](const CUtensorMap* map, uint8_t* ring, uint64_t* full, uint64_t* empty,
+                        int slots, int& idx, int row, int bh) {
+            if (!ok) return;
+            const int slot = idx % slots;
+            ok = mbar_wait(&empty[slot], ((idx / slots) & 1) ^ 1, abort_flag, status,
+                           kStatusBwdProducer);
+            ok = __all_sync(0xffffffffu, ok);
+            if (!ok) return;
+            if (leader) {
+                mbar_arrive_expect_tx(&full[slot], T::TILE);
+#pragma unroll
+                for (int c = 0; c < T::CHUNKS; ++c)
+                    tma_load_3d(ring + slot * T::TILE + c * T::CHUNK, map, &full[slot], c * 64,
+                                row, bh);
+            }
+            __syncwarp();
+            ++idx;
+        };
         for (int r = 0; r * static_cast<int>(gridDim.x) < n_units && ok; ++r) {
             const int L = unit_of_round(r);
             if (L >= n_units) continue;
@@ -673,46 +732,34 @@ __global__ void __launch_bounds__(BwdTile<D>::THREADS, 1)
             if (!ok) break;
             ++uq;
             if (leader) {
-                mbar_arrive_expect_tx(q_full, 2 * T::BIG_TILE);
+                mbar_arrive_expect_tx(q_full, 2 * T::TILE);
 #pragma unroll
                 for (int c = 0; c < T::CHUNKS; ++c) {
-                    tma_load_3d(sQ + c * T::BIG_CHUNK, &tm_q, q_full, c * 64, qt * T::BU, bh);
-                    tma_load_3d(sdO + c * T::BIG_CHUNK, &tm_do, q_full, c * 64, qt * T::BU, bh);
+                    tma_load_3d(sQ + c * T::CHUNK, &tm_q, q_full, c * 64, qt * T::BU, bh);
+                    tma_load_3d(sdO + c * T::CHUNK, &tm_do, q_full, c * 64, qt * T::BU, bh);
                 }
             }
             __syncwarp();
             for (int t = 0; t < n && ok; ++t) {
-                const int slot = idx % T::NS;
-                ok = mbar_wait(&slot_empty[slot], ((idx / T::NS) & 1) ^ 1, abort_flag, status,
-                               kStatusBwdProducer);
-                ok = __all_sync(0xffffffffu, ok);
-                if (!ok) break;
-                if (leader) {
-                    uint8_t* dst = sRing + slot * T::SLOT_BYTES;
-                    mbar_arrive_expect_tx(&slot_full[slot], T::SLOT_BYTES);
-#pragma unroll
-                    for (int c = 0; c < T::CHUNKS; ++c) {
-                        tma_load_3d(dst + c * T::SMALL_CHUNK, &tm_k, &slot_full[slot], c * 64,
-                                    t * T::BS, bh);
-                        tma_load_3d(dst + T::SMALL_TILE + c * T::SMALL_CHUNK, &tm_v,
-                                    &slot_full[slot], c * 64, t * T::BS, bh);
-                    }
-                }
-                __syncwarp();
-                ++idx;
+                load(&tm_k, sKr, k_full, k_empty, T::KS, kidx, t * T::BS, bh);
+                load(&tm_v, sVr, v_full, v_empty, T::VS, vidx, t * T::BS, bh);
             }
         }
         if (*abort_flag && leader) {
             const uint64_t t0 = global_timer_ns();
-            for (int i = max(0, idx - T::NS); i < idx; ++i) {
-                const uint32_t a = smem_u32(&slot_full[i % T::NS]);
-                while (!mbar_try_wait(a, (i / T::NS) & 1)) {
-                    if (global_timer_ns() - t0 > kWaitLimitNs) {
-                        atomicOr(status, kStatusBwdDrain);
-                        break;
+            auto drain_ring = [&](uint64_t* full, int slots, int idx) {
+                for (int i = max(0, idx - slots); i < idx; ++i) {
+                    const uint32_t a = smem_u32(&full[i % slots]);
+                    while (!mbar_try_wait(a, (i / slots) & 1)) {
+                        if (global_timer_ns() - t0 > kWaitLimitNs) {
+                            atomicOr(status, kStatusBwdDrain);
+                            break;
+                        }
                     }
                 }
-            }
+            };
+            drain_ring(k_full, T::KS, kidx);
+            drain_ring(v_full, T::VS, vidx);
             if (uq > 0) {
                 const uint32_t a = smem_u32(q_full);
                 while (!mbar_try_wait(a, static_cast<uint32_t>(uq - 1) & 1u)) {
@@ -729,49 +776,67 @@ __global__ void __launch_bounds__(BwdTile<D>::THREADS, 1)
         constexpr uint32_t id_acc = idesc_f16(128, D, BF16, false, true);
         const uint64_t q_desc = sdesc_sw128(smem_u32(sQ), 16, 1024);
         const uint64_t do_desc = sdesc_sw128(smem_u32(sdO), 16, 1024);
-        const uint64_t rk_desc = sdesc_sw128(smem_u32(sRing), 16, 1024);
-        const uint64_t rm_desc = sdesc_sw128(smem_u32(sRing), T::SMALL_CHUNK, 1024);
+        const uint64_t kk_desc = sdesc_sw128(smem_u32(sKr), 16, 1024);          // K as K-major B
+        const uint64_t km_desc = sdesc_sw128(smem_u32(sKr), T::CHUNK, 1024);    // K as MN-major B
+        const uint64_t vk_desc = sdesc_sw128(smem_u32(sVr), 16, 1024);
         const uint32_t q_lo = static_cast<uint32_t>(q_desc), q_hi = static_cast<uint32_t>(q_desc >> 32);
         const uint32_t do_lo = static_cast<uint32_t>(do_desc), do_hi = static_cast<uint32_t>(do_desc >> 32);
-        const uint32_t rk_lo = static_cast<uint32_t>(rk_desc), rk_hi = static_cast<uint32_t>(rk_desc >> 32);
-        const uint32_t rm_lo = static_cast<uint32_t>(rm_desc), rm_hi = static_cast<uint32_t>(rm_desc >> 32);
+        const uint32_t kk_lo = static_cast<uint32_t>(kk_desc), kk_hi = static_cast<uint32_t>(kk_desc >> 32);
+        const uint32_t km_lo = static_cast<uint32_t>(km_desc), km_hi = static_cast<uint32_t>(km_desc >> 32);
+        const uint32_t vk_lo = static_cast<uint32_t>(vk_desc), vk_hi = static_cast<uint32_t>(vk_desc >> 32);
         bool ok = true;
-        int acq = 0;
-        uint32_t gs = 0;
+        int kacq = 0, vacq = 0;
+        uint32_t gs = 0;              // steps of all units so far (S buffer = step & 1)
         int uq = 0;
-        auto acquire = [&](int& slot) {
+        uint32_t dpf = 0;             // dp_free phases consumed
+        uint32_t pc0 = 0, pc1 = 0;
+        auto acquire = [&](uint64_t* full, int slots, int& acq, int& slot) {
             if (!ok) return;
-            slot = acq % T::NS;
-            ok = mbar_wait(&slot_full[slot], (acq / T::NS) & 1, abort_flag, status, kStatusBwdMma);
+            slot = acq % slots;
+            ok = mbar_wait(&full[slot], (acq / slots) & 1, abort_flag, status, kStatusBwdMma);
             ok = __all_sync(0xffffffffu, ok);
             ++acq;
             tc_fence_after();
         };
-        // S_b = Q·K_slotᵀ, dP_b = dO·V_slotᵀ: M = 128 queries, N = 64 keys, K = D
+        // S_b = Q·K_slotᵀ: M = 128 queries, N = 128 keys, K = D
         auto mma_s = [&](int slot, int b) {
-            const uint32_t koff = (slot * T::SLOT_BYTES) >> 4;
-            const uint32_t voff = (slot * T::SLOT_BYTES + T::SMALL_TILE) >> 4;
+            const uint32_t koff = (slot * T::TILE) >> 4;
 #pragma unroll
             for (int kk = 0; kk < D / 16; ++kk) {
-                const uint32_t ao = ((kk >> 2) * T::BIG_CHUNK + (kk & 3) * 32) >> 4;
-                const uint32_t bo = ((kk >> 2) * T::SMALL_CHUNK + (kk & 3) * 32) >> 4;
-                mma_ss_warp(tmem + T::S_COL + b * 64, q_lo + ao, q_hi, rk_lo + koff + bo, rk_hi,
-                            id_s, kk > 0 ? 1u : 0u);
-                mma_ss_warp(tmem + T::DP_COL + b * 64, do_lo + ao, do_hi, rk_lo + voff + bo, rk_hi,
+                const uint32_t o = ((kk >> 2) * T::CHUNK + (kk & 3) * 32) >> 4;
+                mma_ss_warp(tmem + T::S_COL + b * 128, q_lo + o, q_hi, kk_lo + koff + o, kk_hi,
                             id_s, kk > 0 ? 1u : 0u);
             }
         };
-        // dQ += dS_b·K_slot: M = 128 queries, N = D, K = 64 keys
+        // dP = dO·V_slotᵀ
+        auto mma_dp = [&](int slot) {
+            const uint32_t voff = (slot * T::TILE) >> 4;
+#pragma unroll
+            for (int kk = 0; kk < D / 16; ++kk) {
+                const uint32_t o = ((kk >> 2) * T::CHUNK + (kk & 3) * 32) >> 4;
+                mma_ss_warp(tmem + T::DP_COL, do_lo + o, do_hi, vk_lo + voff + o, vk_hi, id_s,
+                            kk > 0 ? 1u : 0u);
+            }
+        };
+        // dQ += dS_b·K_slot: M = 128 queries, N = D, K = 128 keys (dS packed in cols 0..63 of S_b)
         auto mma_acc = [&](int slot, int b, bool acc) {
-            const uint32_t koff = (slot * T::SLOT_BYTES) >> 4;
+            const uint32_t koff = (slot * T::TILE) >> 4;
 #pragma unroll
             for (int kk = 0; kk < T::BS / 16; ++kk) {
                 const uint32_t bo = (kk * 16 * 128) >> 4;
-                mma_ts_warp(tmem + T::ACC_COL, tmem + T::S_COL + b * 64 + T::PK_OFF + kk * 8,
-                            rm_lo + koff + bo, rm_hi, id_acc, (acc || kk > 0) ? 1u : 0u);
+                mma_ts_warp(tmem + T::ACC_COL, tmem + T::S_COL + b * 128 + kk * 8,
+                            km_lo + koff + bo, km_hi, id_acc, (acc || kk > 0) ? 1u : 0u);
             }
         };
-        uint32_t pc0 = 0, pc1 = 0;
+        auto wait_dp_free = [&]() {
+            if (!ok) return;
+            ok = mbar_wait(dp_free, dpf & 1, abort_flag, status, kStatusBwdMma);
+            ok = __all_sync(0xffffffffu, ok);
+            ++dpf;
+            tc_fence_after();
+        };
+        // The dP buffer is free for the first step of a unit once the previous
+        // unit's last step has released it (dpf counts releases; gs counts steps).
         for (int r = 0; r * static_cast<int>(gridDim.x) < n_units && ok; ++r) {
             const int L = unit_of_round(r);
             if (L >= n_units) continue;
@@ -782,36 +847,47 @@ __global__ void __launch_bounds__(BwdTile<D>::THREADS, 1)
             ++uq;
             tc_fence_after();
             if (!ok) break;
-            int sl = 0;
-            acquire(sl);
+            int cur = 0, nxt = 0, vs = 0;
+            acquire(k_full, T::KS, kacq, cur);
             if (!ok) break;
-            mma_s(sl, gs & 1);
+            mma_s(cur, gs & 1);
+            if (gs > 0) wait_dp_free();                    // previous step's dP read
+            acquire(v_full, T::VS, vacq, vs);
+            if (!ok) break;
+            mma_dp(vs);
+            tc_commit_warp(&v_empty[vs]);
             tc_commit_warp(&s_full[gs & 1]);
-            int sl_next = 0;
             if (n > 1) {
-                acquire(sl_next);
+                acquire(k_full, T::KS, kacq, nxt);
                 if (!ok) break;
-                mma_s(sl_next, (gs + 1) & 1);
-                tc_commit_warp(&s_full[(gs + 1) & 1]);
+                mma_s(nxt, (gs + 1) & 1);
             }
-            if (n <= 2) tc_commit_warp(q_empty);           // Q and dO no longer needed
-            int cur = sl, nxt = sl_next;
             for (int t = 0; t < n && ok; ++t) {
                 const int b = static_cast<int>((gs + t) & 1);
+                if (t + 1 < n) {
+                    // dP of the next step once the softmax warps have read this one's
+                    wait_dp_free();
+                    acquire(v_full, T::VS, vacq, vs);
+                    if (!ok) break;
+                    mma_dp(vs);
+                    tc_commit_warp(&v_empty[vs]);
+                    tc_commit_warp(&s_full[b ^ 1]);
+                    if (t + 2 == n) tc_commit_warp(q_empty);   // last use of Q and dO issued
+                } else if (n == 1) {
+                    tc_commit_warp(q_empty);
+                }
                 ok = mbar_wait(&p_full[b], (b ? pc1 : pc0) & 1, abort_flag, status, kStatusBwdMma);
                 ok = __all_sync(0xffffffffu, ok);
                 if (b) ++pc1; else ++pc0;
                 tc_fence_after();
                 if (!ok) break;
                 mma_acc(cur, b, t > 0);
-                tc_commit_warp(&slot_empty[cur]);
+                tc_commit_warp(&k_empty[cur]);
                 int nn = 0;
                 if (t + 2 < n) {
-                    acquire(nn);
+                    acquire(k_full, T::KS, kacq, nn);
                     if (!ok) break;
                     mma_s(nn, b);
-                    tc_commit_warp(&s_full[b]);
-                    if (t + 3 == n) tc_commit_warp(q_empty);
                 }
                 cur = nxt;
                 nxt = nn;
@@ -855,24 +931,38 @@ __global__ void __launch_bounds__(BwdTile<D>::THREADS, 1)
                 ok = __all_sync(0xffffffffu, ok);
                 if (!ok) break;
                 tc_fence_after();
-                uint32_t sv[64], dpv[64];
-                tmem_ld64(lane_base + T::S_COL + b * 64, sv);
-                tmem_ld64(lane_base + T::DP_COL + b * 64, dpv);
                 const int kv0 = t * T::BS;
                 const bool masked =
                     (CAUSAL && kv0 + T::BS - 1 > row_begin) || (kv0 + T::BS > S_k);
-                uint32_t pk_p[32], pk_ds[32];
-                if (masked) {
-                    const int lim = min(S_k, CAUSAL ? q_idx + 1 : S_k) - kv0;  // visible iff c < lim
-                    grad_pack64<true, BF16, false, false>(sv, dpv, nullptr, nullptr, row_lse2,
-                                                          row_dd, scale_log2,
-                                                          [&](int c) { return c < lim; }, pk_p, pk_ds);
-                } else {
-                    grad_pack64<false, BF16, false, false>(sv, dpv, nullptr, nullptr, row_lse2,
-                                                           row_dd, scale_log2,
-                                                           [](int) { return true; }, pk_p, pk_ds);
+                const int lim = masked ? min(S_k, CAUSAL ? q_idx + 1 : S_k) - kv0 : T::BS;
+                const uint32_t sb = lane_base + T::S_COL + b * 128;
+                // Two halves of 64 keys; dS of half h goes to columns 32h..32h+31
+                // of S_b, which have been read by then.
+#pragma unroll 1
+                for (int h = 0; h < 2; ++h) {
+                    uint32_t sv[64], dpv[64];
+                    tmem_ld64(sb + h * 64, sv);
+                    tmem_ld64(lane_base + T::DP_COL + h * 64, dpv);
+                    if (h == 1) {
+                        tc_fence_before();
+                        __syncwarp();
+                        if (lane == 0) mbar_arrive(dp_free);
+                    }
+                    uint32_t pk_p[32], pk_ds[32];
+                    const int hl = lim - h * 64;
+                    if (masked) {
+                        grad_pack64<true, BF16, false, false>(sv, dpv, nullptr, nullptr, row_lse2,
+                                                              row_dd, scale_log2,
+                                                              [&](int c) { return c < hl; }, pk_p,
+                                                              pk_ds);
+                    } else {
+                        grad_pack64<false, BF16, false, false>(sv, dpv, nullptr, nullptr,
+                                                               row_lse2, row_dd, scale_log2,
+                                                               [](int) { return true; }, pk_p,
+                                                               pk_ds);
+                    }
+                    tmem_st32(sb + h * 32, pk_ds);
                 }
-                tmem_st32(lane_base + T::S_COL + b * 64 + T::PK_OFF, pk_ds);
                 tmem_st_wait();
                 tc_fence_before();
                 __syncwarp();
@@ -929,15 +1019,16 @@ cudaError_t launch_attn_bwd(const BwdArgs& a, cudaStream_t stream) {
     err = cudaGetLastError();
     if (err != cudaSuccess) return err;
 
+    using TQ = DqTile<D>;
     auto kdq = attn_bwd_dq_kernel<D, BF16, CAUSAL>;
-    err = cudaFuncSetAttribute(kdq, cudaFuncAttributeMaxDynamicSharedMemorySize, T::SMEM_BYTES);
+    err = cudaFuncSetAttribute(kdq, cudaFuncAttributeMaxDynamicSharedMemorySize, TQ::SMEM_BYTES);
     if (err != cudaSuccess) return err;
-    const int n_qt = (a.S_q + T::BU - 1) / T::BU;
+    const int n_qt = (a.S_q + TQ::BU - 1) / TQ::BU;
     const long long units_q = static_cast<long long>(a.BH) * n_qt;
     if (units_q > 0x7fffffffLL) return cudaErrorInvalidConfiguration;
     const int hg_q = static_cast<int>(std::max<long long>(1, group_bytes / (op_bytes * a.S_k)));
-    kdq<<<static_cast<int>(std::min<long long>(units_q, a.num_sms)), T::THREADS, T::SMEM_BYTES,
-          stream>>>(a.tm_q_fixed, a.tm_do_fixed, a.tm_k_step, a.tm_v_step, a.lse2, a.delta,
+    kdq<<<static_cast<int>(std::min<long long>(units_q, a.num_sms)), TQ::THREADS, TQ::SMEM_BYTES,
+          stream>>>(a.tm_q_fixed, a.tm_do_fixed, a.tm_k_fixed, a.tm_v_fixed, a.lse2, a.delta,
                     static_cast<uint16_t*>(a.dq), a.S_q, a.S_k, a.BH, a.S_pad, hg_q, a.scale,
                     a.scale_log2, a.status);
     return cudaGetLastError();

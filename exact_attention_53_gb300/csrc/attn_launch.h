@@ -96,14 +96,13 @@ cudaError_t launch_attn_combine(const float* o_part, const float* lse_part, void
                                 int n_split, long long rows, int d, bool bf16,
                                 cudaStream_t stream);
 
-// Backward launch contract (attn_bwd.cuh).  Fixed operands are the 128-row
-// tiles a unit keeps for all its steps (K, V for dK/dV; Q, dO for dQ); step
-// operands are the 64-row tiles it streams.
+// Backward launch contract (attn_bwd.cuh).  The dK/dV kernel keeps 128-row K
+// and V tiles and streams 64-row Q and dO steps; the dQ kernel keeps 128-row
+// Q and dO tiles and streams 128-row K and V steps.
 struct BwdArgs {
     CUtensorMap tm_k_fixed, tm_v_fixed;   // [B·H, S_k, d], box 64 × 128
     CUtensorMap tm_q_step, tm_do_step;    // [B·H, S_q, d], box 64 × 64
     CUtensorMap tm_q_fixed, tm_do_fixed;  // [B·H, S_q, d], box 64 × 128
-    CUtensorMap tm_k_step, tm_v_step;     // [B·H, S_k, d], box 64 × 64
     const void* o;                        // forward output [B, H, S_q, d]
     const void* dout;                     // dO [B, H, S_q, d]
     const float* lse;                     // forward LSE [B, H, S_q], natural log

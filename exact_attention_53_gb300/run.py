@@ -3,6 +3,7 @@
     python -m exact_attention_53_gb300.run --workload c3 --causal 0 --iters 2
     python -m exact_attention_53_gb300.run --workload decode --split 0 --iters 2
     python -m exact_attention_53_gb300.run --split-sweep
+    python -m exact_attention_53_gb300.run --workload c3 --causal 1 --bwd --iters 3
 
 Inputs are the seeded synthetic ones of ``workloads``; the forward is
 launched ``--iters`` times on the current stream, then the device status is
@@ -10,6 +11,9 @@ checked.  Prints the device time per launch and the TFLOP/s (the best
 launch), or with ``--split N`` (split-KV, N ranges, 0 = automatic) the HBM
 GB/s of the algorithmic bytes.  ``--split-sweep`` times the split-KV forward
 over a grid of short-query shapes and range counts beside the one-pass kernel.
+``--bwd`` runs the forward once, then times the backward (dQ, dK, dV for a
+seeded dO) and prints TFLOP/s counted as 2.5 forwards (five S_q×S_k×d
+products).
 """
 
 from __future__ import annotations
@@ -18,7 +22,7 @@ import argparse
 
 import torch
 
-from . import attn_fwd_splitkv_plan, attn_get_device_status, fwd, fwd_splitkv
+from . import attn_fwd_splitkv_plan, attn_get_device_status, bwd, fwd, fwd_splitkv
 from .workloads import WORKLOADS, make_qkv, workload_qkv
 
 
@@ -69,6 +73,7 @@ def main(argv=None):
                     help="run the split-KV forward with this many ranges (0 = automatic)")
     ap.add_argument("--split-sweep", action="store_true",
                     help="time split-KV over short-query shapes and range counts")
+    ap.add_argument("--bwd", action="store_true", help="time the backward instead of the forward")
     args = ap.parse_args(argv)
     if args.split_sweep:
         split_sweep()
@@ -86,6 +91,19 @@ def main(argv=None):
     o = torch.empty_like(q)
     lse = torch.empty(q.shape[:3], dtype=torch.float32, device=dev)
     ev = [torch.cuda.Event(enable_timing=True) for _ in range(args.iters + 1)]
+    if args.bwd:
+        dout = make_qkv(q.shape[0], q.shape[1], w.S_q, 1, w.d, w.dtype, w.seed + 100)[0].to(dev)
+        fwd(q, k, v, causal=causal, scale=w.scale, out=o, lse=lse)
+        ev[0].record()
+        for i in range(args.iters):
+            bwd(q, k, v, o, lse, dout, causal=causal, scale=w.scale)
+            ev[i + 1].record()
+        attn_get_device_status()
+        ms = [ev[i].elapsed_time(ev[i + 1]) for i in range(args.iters)]
+        flops = 10.0 * bh * w.S_q * w.S_k * w.d / (2 if causal else 1)
+        print(f"{args.workload} bwd causal={int(causal)} B*H={bh}: per-call ms {['%.3f' % x for x in ms]}"
+              f" best {flops / min(ms) / 1e9:.1f} TFLOP/s")
+        return 0
     if args.split is not None:
         n, ws = attn_fwd_splitkv_plan(1 if args.heads else w.B, bh if args.heads else w.H, w.S_q,
                                       w.S_k, w.d, 1 if w.dtype == "bf16" else 0, args.split)
