@@ -125,15 +125,26 @@ def replica_throughput(flops_per_step: float, steps: int, world: int, max_ms: fl
     return flops_per_step * steps * world / (max_ms * 1e-3) / 1e12
 
 
-def kernel_source_digest() -> str:
-    """sha256 over the kernel sources; ties recorded DRAM traffic to the code it was taken on."""
+# Source files that make up each profiled kernel: a DRAM-traffic figure is
+# used only while these files are byte-identical to the ones it was taken on.
+FWD_SOURCES = ("attn_fwd.cuh", "attn_inst.cu", "attn_launch.h", "sm100.cuh")
+KERNEL_SOURCES = {
+    "attn_fwd_d128_bf16_full_c3": FWD_SOURCES,
+    "attn_fwd_d128_bf16_causal_c3": FWD_SOURCES,
+    "attn_fwd_splitkv_d128_bf16_decode": FWD_SOURCES + ("attn_combine.cu",),
+    "attn_bwd_d128_bf16_full_c3": ("attn_bwd.cuh", "attn_bwd_inst.cu", "attn_launch.h", "sm100.cuh"),
+    "attn_bwd_d128_bf16_causal_c3": ("attn_bwd.cuh", "attn_bwd_inst.cu", "attn_launch.h", "sm100.cuh"),
+}
+
+
+def kernel_source_digest(names) -> str:
+    """sha256 over the named kernel sources; ties recorded DRAM traffic to the code it was taken on."""
     import hashlib
     h = hashlib.sha256()
     csrc = os.path.join(ROOT, "exact_attention_53_gb300", "csrc")
-    for name in sorted(os.listdir(csrc)):
-        if name.endswith((".cu", ".cuh", ".h")):
-            with open(os.path.join(csrc, name), "rb") as f:
-                h.update(name.encode() + b"\0" + f.read())
+    for name in sorted(names):
+        with open(os.path.join(csrc, name), "rb") as f:
+            h.update(name.encode() + b"\0" + f.read())
     return h.hexdigest()
 
 
@@ -142,12 +153,12 @@ def measured_traffic(key: str):
     path = os.path.join(ROOT, "profiles", "traffic.json")
     try:
         with open(path) as f:
-            rec = json.load(f)
+            rec = json.load(f).get(key)
     except (OSError, ValueError):
         return None
-    if rec.get("kernel_source_sha256") != kernel_source_digest():
+    if not isinstance(rec, dict) or rec.get("sources_sha256") != kernel_source_digest(KERNEL_SOURCES[key]):
         return None
-    return rec.get(key)
+    return rec.get("bytes")
 
 
 def cpu_baseline(budget_s: float = 12.0):
@@ -463,6 +474,12 @@ def run_gpu(args, rank, world):
     line["splitkv"] = splitkv
     for mode in ("full", "causal"):
         backward[mode]["frac_of_peak"] = backward[mode]["tflops"] / peak
+    backward["roofline"] = {"bound": "tensor", "achieved": backward["full"]["tflops"], "peak": peak,
+                            "unit": "TFLOP/s", "frac": backward["full"]["tflops"] / peak,
+                            "traffic": measured_traffic("attn_bwd_d128_bf16_full_c3"),
+                            "kernel": "attn_bwd_prep + attn_bwd_dkdv + attn_bwd_dq <128,bf16,full>",
+                            "peak_source": "measured bf16 burst (MEASURED_PEAKS.json bf16_tflops)"
+                            if peak_src == "measured" else "fallback 1.9 PFLOP/s"}
     backward["workload"] = f"{WORKLOAD}: B={B} H={H} S_q=S_k={S_q} d={d} bf16, dO~N(0,1)"
     line["backward"] = backward
     if not args.no_cpu_baseline and world == 1:

@@ -72,3 +72,27 @@ def test_single_rank_needs_no_process_group():
     import bench
     assert bench.max_over_ranks(3.5, 1) == 3.5
     assert bench.replica_throughput(1e12, 10, 1, 1000.0) == pytest.approx(10.0)
+
+
+def test_measured_traffic_is_tied_to_kernel_sources(tmp_path, monkeypatch):
+    """The committed traffic record parses, and a figure counts only for unchanged sources."""
+    import json
+    import sys
+    sys.path.insert(0, ROOT)
+    import bench
+    for key in bench.KERNEL_SOURCES:
+        v = bench.measured_traffic(key)
+        assert v is None or (isinstance(v, int) and v > 0)
+    key = "attn_fwd_d128_bf16_full_c3"
+    good = bench.kernel_source_digest(bench.KERNEL_SOURCES[key])
+    (tmp_path / "profiles").mkdir()
+    rec = {key: {"bytes": 123, "sources_sha256": good},
+           "attn_fwd_d128_bf16_causal_c3": {"bytes": 456, "sources_sha256": "0" * 64},
+           "attn_bwd_d128_bf16_full_c3": 789}
+    (tmp_path / "profiles" / "traffic.json").write_text(json.dumps(rec))
+    monkeypatch.setattr(bench, "ROOT", str(tmp_path))
+    monkeypatch.setattr(bench, "kernel_source_digest", lambda names: good)
+    assert bench.measured_traffic(key) == 123
+    monkeypatch.setattr(bench, "kernel_source_digest", lambda names: "f" * 64)
+    assert bench.measured_traffic(key) is None
+    assert bench.measured_traffic("attn_bwd_d128_bf16_full_c3") is None
