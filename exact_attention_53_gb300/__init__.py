@@ -11,6 +11,7 @@ from .binding import (  # noqa: F401
     attn_bwd,
     attn_bwd_workspace_size,
     attn_fwd,
+    attn_fwd_general,
     attn_fwd_host,
     attn_fwd_plan,
     attn_fwd_splitkv,
@@ -20,6 +21,7 @@ from .binding import (  # noqa: F401
     attn_last_error,
     bwd,
     fwd,
+    fwd_general,
     fwd_splitkv,
     library_path,
     load_library,

@@ -25,7 +25,11 @@ ATTN_ERR_TIMEOUT = 4
 ATTN_DTYPE_F16 = 0
 ATTN_DTYPE_BF16 = 1
 
-EXPORTED = ("attn_fwd", "attn_fwd_host", "attn_fwd_plan", "attn_fwd_splitkv_plan",
+ATTN_MASK_NONE = 0
+ATTN_MASK_CAUSAL = 1
+ATTN_MASK_CAUSAL_BOTTOM_RIGHT = 2
+
+EXPORTED = ("attn_fwd", "attn_fwd_general", "attn_fwd_host", "attn_fwd_plan", "attn_fwd_splitkv_plan",
             "attn_fwd_splitkv", "attn_fwd_splitkv_noalloc", "attn_bwd_workspace_size", "attn_bwd",
             "attn_last_error", "attn_get_device_status", "attn_version")
 NOALLOC_SCRATCH_BYTES = 16 * 1024 * 1024    # ATTN_NOALLOC_SCRATCH_BYTES
@@ -39,6 +43,22 @@ class AttnPlan(ctypes.Structure):
                 ("units", ctypes.c_int64), ("threads", ctypes.c_int32),
                 ("smem_bytes", ctypes.c_int32), ("tmem_cols", ctypes.c_int32),
                 ("kv_stages", ctypes.c_int32)]
+
+class AttnLayout(ctypes.Structure):
+    """Mirror of attn_layout_t: element strides of batch, head and row."""
+    _fields_ = [("batch", ctypes.c_int64), ("head", ctypes.c_int64), ("row", ctypes.c_int64)]
+
+
+class AttnFwdParams(ctypes.Structure):
+    """Mirror of attn_fwd_params_t (include/attn.h)."""
+    _fields_ = [("q", ctypes.c_void_p), ("k", ctypes.c_void_p), ("v", ctypes.c_void_p),
+                ("o", ctypes.c_void_p), ("lse", ctypes.c_void_p),
+                ("B", ctypes.c_int64), ("H", ctypes.c_int64), ("H_kv", ctypes.c_int64),
+                ("S_q", ctypes.c_int64), ("S_k", ctypes.c_int64), ("d", ctypes.c_int64),
+                ("q_layout", AttnLayout), ("k_layout", AttnLayout), ("v_layout", AttnLayout),
+                ("o_layout", AttnLayout), ("mask", ctypes.c_int), ("scale", ctypes.c_float),
+                ("dtype", ctypes.c_int)]
+
 
 _DTYPE_CODE = {torch.float16: ATTN_DTYPE_F16, torch.bfloat16: ATTN_DTYPE_BF16}
 
@@ -73,6 +93,8 @@ def load_library() -> ctypes.CDLL:
         lib.attn_fwd.argtypes = [vp, vp, vp, vp, vp, i64, i64, i64, i64, i64, i32,
                                  ctypes.c_float, i32, vp]
         lib.attn_fwd.restype = i32
+        lib.attn_fwd_general.argtypes = [ctypes.POINTER(AttnFwdParams), vp]
+        lib.attn_fwd_general.restype = i32
         lib.attn_fwd_host.argtypes = [vp] * 10 + [i64, i64, i64, i64, i64, i32, ctypes.c_float,
                                                   i32, vp]
         lib.attn_fwd_host.restype = i32
@@ -125,6 +147,43 @@ def attn_fwd(q, k, v, o, lse, B, H, S_q, S_k, d, causal, scale, dtype, stream=No
     ptr = lambda t: t.data_ptr() if isinstance(t, torch.Tensor) else t  # noqa: E731
     _check(lib.attn_fwd(ptr(q), ptr(k), ptr(v), ptr(o), ptr(lse), B, H, S_q, S_k, d,
                         int(causal), float(scale), int(dtype), _stream_handle(stream)))
+
+
+def attn_fwd_general(params: AttnFwdParams, stream=None) -> None:
+    """Enqueue the general-layout forward described by ``params``."""
+    _check(load_library().attn_fwd_general(ctypes.byref(params), _stream_handle(stream)))
+
+
+def _layout(t: torch.Tensor) -> AttnLayout:
+    if t.dim() != 4 or t.stride(3) != 1:
+        raise AttnError(ATTN_ERR_INVALID_ARG, "tensors must be 4-D [B, heads, S, d] views with d contiguous")
+    return AttnLayout(t.stride(0), t.stride(1), t.stride(2))
+
+
+def fwd_general(q: torch.Tensor, k: torch.Tensor, v: torch.Tensor, mask: int = ATTN_MASK_NONE,
+                scale: float | None = None, out: torch.Tensor | None = None,
+                lse: torch.Tensor | None = None):
+    """Forward over strided views: q [B,H,S_q,d], k and v [B,H_kv,S_k,d] (any batch, head and
+    row strides, d contiguous), H_kv dividing H.  ``out`` may be any strided [B,H,S_q,d] view
+    (default: dense); ``lse`` is dense [B,H,S_q] fp32.  Returns ``(o, lse)``.
+    """
+    if q.dtype != k.dtype or q.dtype != v.dtype or q.dtype not in _DTYPE_CODE:
+        raise AttnError(ATTN_ERR_UNSUPPORTED, "q, k, v must share dtype float16 or bfloat16")
+    B, H, S_q, d = q.shape
+    H_kv, S_k = k.shape[1], k.shape[2]
+    if k.shape != (B, H_kv, S_k, d) or v.shape != k.shape:
+        raise AttnError(ATTN_ERR_INVALID_ARG, f"shape mismatch q{tuple(q.shape)} k{tuple(k.shape)} v{tuple(v.shape)}")
+    if scale is None:
+        scale = 1.0 / math.sqrt(d)
+    if out is None:
+        out = torch.empty((B, H, S_q, d), dtype=q.dtype, device=q.device)
+    if lse is None:
+        lse = torch.empty((B, H, S_q), dtype=torch.float32, device=q.device)
+    p = AttnFwdParams(q.data_ptr(), k.data_ptr(), v.data_ptr(), out.data_ptr(), lse.data_ptr(),
+                      B, H, H_kv, S_q, S_k, d, _layout(q), _layout(k), _layout(v), _layout(out),
+                      int(mask), float(scale), _DTYPE_CODE[q.dtype])
+    attn_fwd_general(p)
+    return out, lse
 
 
 def attn_fwd_host(q_host, k_host, v_host, o_host, lse_host, q_dev, k_dev, v_dev, o_dev, lse_dev,

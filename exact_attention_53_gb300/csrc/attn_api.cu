@@ -68,12 +68,26 @@ bool overlaps(const void* a, size_t na, const void* b, size_t nb) {
 
 bool aligned(const void* p, size_t n) { return (reinterpret_cast<uintptr_t>(p) % n) == 0; }
 
+// Element strides of a [B, heads, S, d] view; the d elements of a row are contiguous.
+using Layout = attn_layout_t;
+
+Layout dense_layout(int64_t heads, int64_t S, int64_t d) { return {heads * S * d, S * d, d}; }
+
+// Bytes from the first to one past the last element of a [B, heads, S, d] view.
+size_t span_bytes(const Layout& l, int64_t B, int64_t heads, int64_t S, int64_t d) {
+    return static_cast<size_t>((B - 1) * l.batch + (heads - 1) * l.head + (S - 1) * l.row + d) * 2;
+}
+
 struct Problem {
     int64_t B, H, S_q, S_k, d;
+    int64_t H_kv = 0;            // key/value heads (H for plain multi-head attention)
     bool causal;
+    int64_t causal_off = 0;      // key j visible to query i iff j <= i + causal_off
     float scale;
     attn_dtype_t dtype;
-    size_t q_bytes, kv_bytes, o_bytes, lse_bytes;
+    Layout lq, lk, lv, lo;
+    size_t q_bytes, kv_bytes, o_bytes, lse_bytes;   // spans of q, k (= v), o, lse
+    size_t v_bytes;
 };
 
 attn_status_t validate_sizes(Problem& p, int64_t B, int64_t H, int64_t S_q, int64_t S_k,
@@ -100,14 +114,83 @@ attn_status_t validate_sizes(Problem& p, int64_t B, int64_t H, int64_t S_q, int6
     if (S_q > kMaxSeq) return fail(ATTN_ERR_INVALID_ARG, "S_q=%lld exceeds 2^22", (long long)S_q);
     if (S_k > kMaxSeq) return fail(ATTN_ERR_INVALID_ARG, "S_k=%lld exceeds 2^22", (long long)S_k);
     p.B = B; p.H = H; p.S_q = S_q; p.S_k = S_k; p.d = d;
+    p.H_kv = H;
     p.causal = causal != 0;
+    p.causal_off = 0;
     p.scale = scale;
     p.dtype = dtype;
+    p.lq = p.lo = dense_layout(H, S_q, d);
+    p.lk = p.lv = dense_layout(H, S_k, d);
     const size_t bh = static_cast<size_t>(B * H);
     p.q_bytes = bh * static_cast<size_t>(S_q) * static_cast<size_t>(d) * 2;
     p.kv_bytes = bh * static_cast<size_t>(S_k) * static_cast<size_t>(d) * 2;
+    p.v_bytes = p.kv_bytes;
     p.o_bytes = p.q_bytes;
     p.lse_bytes = bh * static_cast<size_t>(S_q) * 4;
+    return ATTN_OK;
+}
+
+// A [B, heads, S, d] view whose elements are all distinct: sorted by stride,
+// each dimension must step past everything the smaller ones span.
+bool layout_injective(const Layout& l, int64_t B, int64_t heads, int64_t S, int64_t d) {
+    struct Dim { int64_t stride, extent; };
+    Dim dims[3] = {{l.row, S}, {l.head, heads}, {l.batch, B}};
+    std::sort(dims, dims + 3, [](const Dim& a, const Dim& b) { return a.stride < b.stride; });
+    int64_t reach = d;                    // elements spanned by the smaller dimensions
+    for (const Dim& x : dims) {
+        if (x.extent <= 1) continue;
+        if (x.stride < reach) return false;
+        reach = x.stride * (x.extent - 1) + reach;
+    }
+    return true;
+}
+
+attn_status_t check_layout(const Layout& l, const char* name, int64_t d) {
+    const int64_t s[3] = {l.batch, l.head, l.row};
+    const char* nm[3] = {"batch", "head", "row"};
+    for (int i = 0; i < 3; ++i) {
+        if (s[i] < 1 || s[i] % 8 != 0 || s[i] > (int64_t(1) << 39))
+            return fail(ATTN_ERR_INVALID_ARG,
+                        "%s %s stride %lld must be a positive multiple of 8 elements (16 bytes) below 2^39",
+                        name, nm[i], (long long)s[i]);
+    }
+    if (l.row < d)
+        return fail(ATTN_ERR_INVALID_ARG, "%s row stride %lld is below d=%lld", name, (long long)l.row,
+                    (long long)d);
+    return ATTN_OK;
+}
+
+attn_status_t validate_general(Problem& p, const attn_fwd_params_t* a) {
+    if (!a) return fail(ATTN_ERR_INVALID_ARG, "params is null");
+    if (a->mask < 0 || a->mask > 2)
+        return fail(ATTN_ERR_INVALID_ARG, "mask must be 0, 1 or 2, got %d", a->mask);
+    attn_status_t s = validate_sizes(p, a->B, a->H, a->S_q, a->S_k, a->d, a->mask != 0 ? 1 : 0,
+                                     a->scale, a->dtype);
+    if (s != ATTN_OK) return s;
+    if (a->H_kv < 1 || a->H_kv > a->H || a->H % a->H_kv != 0)
+        return fail(ATTN_ERR_INVALID_ARG, "H_kv=%lld must divide H=%lld", (long long)a->H_kv,
+                    (long long)a->H);
+    if (a->mask == 2 && a->S_q > a->S_k)
+        return fail(ATTN_ERR_UNSUPPORTED,
+                    "bottom-right causal mask needs S_q <= S_k (got S_q=%lld, S_k=%lld): earlier "
+                    "queries would see no key",
+                    (long long)a->S_q, (long long)a->S_k);
+    if ((s = check_layout(a->q_layout, "q", a->d)) != ATTN_OK) return s;
+    if ((s = check_layout(a->k_layout, "k", a->d)) != ATTN_OK) return s;
+    if ((s = check_layout(a->v_layout, "v", a->d)) != ATTN_OK) return s;
+    if ((s = check_layout(a->o_layout, "o", a->d)) != ATTN_OK) return s;
+    p.H_kv = a->H_kv;
+    p.causal_off = a->mask == 2 ? a->S_k - a->S_q : 0;
+    p.lq = {a->q_layout.batch, a->q_layout.head, a->q_layout.row};
+    p.lk = {a->k_layout.batch, a->k_layout.head, a->k_layout.row};
+    p.lv = {a->v_layout.batch, a->v_layout.head, a->v_layout.row};
+    p.lo = {a->o_layout.batch, a->o_layout.head, a->o_layout.row};
+    if (!layout_injective(p.lo, p.B, p.H, p.S_q, p.d))
+        return fail(ATTN_ERR_INVALID_ARG, "o layout maps two elements to one address");
+    p.q_bytes = span_bytes(p.lq, p.B, p.H, p.S_q, p.d);
+    p.kv_bytes = span_bytes(p.lk, p.B, p.H_kv, p.S_k, p.d);
+    p.v_bytes = span_bytes(p.lv, p.B, p.H_kv, p.S_k, p.d);
+    p.o_bytes = span_bytes(p.lo, p.B, p.H, p.S_q, p.d);
     return ATTN_OK;
 }
 
@@ -125,10 +208,10 @@ attn_status_t validate_device_ptrs(const Problem& p, const void* q, const void* 
     if (!aligned(lse, 4)) return fail(ATTN_ERR_INVALID_ARG, "lse is not 4-byte aligned");
     if (overlaps(o, p.o_bytes, q, p.q_bytes)) return fail(ATTN_ERR_INVALID_ARG, "o overlaps q");
     if (overlaps(o, p.o_bytes, k, p.kv_bytes)) return fail(ATTN_ERR_INVALID_ARG, "o overlaps k");
-    if (overlaps(o, p.o_bytes, v, p.kv_bytes)) return fail(ATTN_ERR_INVALID_ARG, "o overlaps v");
+    if (overlaps(o, p.o_bytes, v, p.v_bytes)) return fail(ATTN_ERR_INVALID_ARG, "o overlaps v");
     if (overlaps(lse, p.lse_bytes, q, p.q_bytes)) return fail(ATTN_ERR_INVALID_ARG, "lse overlaps q");
     if (overlaps(lse, p.lse_bytes, k, p.kv_bytes)) return fail(ATTN_ERR_INVALID_ARG, "lse overlaps k");
-    if (overlaps(lse, p.lse_bytes, v, p.kv_bytes)) return fail(ATTN_ERR_INVALID_ARG, "lse overlaps v");
+    if (overlaps(lse, p.lse_bytes, v, p.v_bytes)) return fail(ATTN_ERR_INVALID_ARG, "lse overlaps v");
     if (overlaps(lse, p.lse_bytes, o, p.o_bytes)) return fail(ATTN_ERR_INVALID_ARG, "lse overlaps o");
     return ATTN_OK;
 }
@@ -181,6 +264,28 @@ attn_status_t encode_rows(CUtensorMap* map, const void* base, const Problem& p, 
                     p.dtype == ATTN_DTYPE_BF16 ? CU_TENSOR_MAP_DATA_TYPE_BFLOAT16
                                                : CU_TENSOR_MAP_DATA_TYPE_FLOAT16,
                     3, const_cast<void*>(base), dims, strides, box, estr,
+                    CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B,
+                    CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
+    if (r != CUDA_SUCCESS) return fail(ATTN_ERR_CUDA, "cuTensorMapEncodeTiled(%s) failed with %d", name, (int)r);
+    return ATTN_OK;
+}
+
+// A [B, heads, S, d] view as a 4-D map (d, S, heads, B) with its own strides;
+// box 64 columns × box_rows rows of one head.
+attn_status_t encode_4d(CUtensorMap* map, const void* base, const Problem& p, int64_t S,
+                        int64_t heads, const Layout& l, uint32_t box_rows, const char* name) {
+    auto fn = encode_fn();
+    if (!fn) return fail(ATTN_ERR_CUDA, "cuTensorMapEncodeTiled is unavailable from the driver");
+    cuuint64_t dims[4] = {static_cast<cuuint64_t>(p.d), static_cast<cuuint64_t>(S),
+                          static_cast<cuuint64_t>(heads), static_cast<cuuint64_t>(p.B)};
+    cuuint64_t strides[3] = {static_cast<cuuint64_t>(l.row * 2), static_cast<cuuint64_t>(l.head * 2),
+                             static_cast<cuuint64_t>(l.batch * 2)};
+    cuuint32_t box[4] = {64, box_rows, 1, 1};
+    cuuint32_t estr[4] = {1, 1, 1, 1};
+    CUresult r = fn(map,
+                    p.dtype == ATTN_DTYPE_BF16 ? CU_TENSOR_MAP_DATA_TYPE_BFLOAT16
+                                               : CU_TENSOR_MAP_DATA_TYPE_FLOAT16,
+                    4, const_cast<void*>(base), dims, strides, box, estr,
                     CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B,
                     CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
     if (r != CUDA_SUCCESS) return fail(ATTN_ERR_CUDA, "cuTensorMapEncodeTiled(%s) failed with %d", name, (int)r);
@@ -260,15 +365,19 @@ LaunchFn pick_split(int64_t d, bool bf16) {
 attn_status_t fill_args(attn::FwdArgs& a, const Problem& p, int dev, const void* q, const void* k,
                         const void* v, void* o, float* lse) {
     attn_status_t s;
-    if ((s = encode_rows(&a.tm_q, q, p, p.S_q, "q")) != ATTN_OK) return s;
-    if ((s = encode_rows(&a.tm_k, k, p, p.S_k, "k")) != ATTN_OK) return s;
-    if ((s = encode_rows(&a.tm_v, v, p, p.S_k, "v")) != ATTN_OK) return s;
-    if ((s = encode_rows(&a.tm_o, o, p, p.S_q, "o")) != ATTN_OK) return s;
+    const uint32_t rows = attn::kBlockM;
+    if ((s = encode_4d(&a.tm_q, q, p, p.S_q, p.H, p.lq, rows, "q")) != ATTN_OK) return s;
+    if ((s = encode_4d(&a.tm_k, k, p, p.S_k, p.H_kv, p.lk, rows, "k")) != ATTN_OK) return s;
+    if ((s = encode_4d(&a.tm_v, v, p, p.S_k, p.H_kv, p.lv, rows, "v")) != ATTN_OK) return s;
+    if ((s = encode_4d(&a.tm_o, o, p, p.S_q, p.H, p.lo, rows, "o")) != ATTN_OK) return s;
     a.o = o;
     a.lse = lse;
     a.S_q = static_cast<int32_t>(p.S_q);
     a.S_k = static_cast<int32_t>(p.S_k);
     a.BH = static_cast<int32_t>(p.B * p.H);
+    a.H = static_cast<int32_t>(p.H);
+    a.kv_group = static_cast<int32_t>(p.H / p.H_kv);
+    a.causal_off = static_cast<int32_t>(p.causal_off);
     a.scale_log2 = static_cast<float>(static_cast<double>(p.scale) * 1.4426950408889634);
     a.status = g_status_ptr[dev].load();
     a.num_sms = g_num_sms[dev].load();
@@ -397,6 +506,15 @@ attn_status_t attn_fwd(const void* q, const void* k, const void* v, void* o, flo
     if (s != ATTN_OK) return s;
     if ((s = validate_device_ptrs(p, q, k, v, o, lse)) != ATTN_OK) return s;
     return launch_checked(p, q, k, v, o, lse, stream);
+}
+
+attn_status_t attn_fwd_general(const attn_fwd_params_t* params, struct CUstream_st* stream) {
+    Problem p;
+    attn_status_t s = validate_general(p, params);
+    if (s != ATTN_OK) return s;
+    if ((s = validate_device_ptrs(p, params->q, params->k, params->v, params->o, params->lse)) != ATTN_OK)
+        return s;
+    return launch_checked(p, params->q, params->k, params->v, params->o, params->lse, stream);
 }
 
 attn_status_t attn_fwd_host(const void* q_host, const void* k_host, const void* v_host,

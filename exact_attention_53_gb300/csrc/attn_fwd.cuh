@@ -52,12 +52,12 @@ constexpr float kLn2 = 0.693147180559945309f;
 
 // Number of key tiles query tile t of a block starting at row q0 visits.
 template <bool CAUSAL>
-__device__ __forceinline__ int kv_tiles_for(int row_begin, int S_q, int S_k) {
+__device__ __forceinline__ int kv_tiles_for(int row_begin, int S_q, int S_k, int causal_off) {
     if (row_begin >= S_q) return 0;
     int n = (S_k + kBlockN - 1) / kBlockN;
     if (CAUSAL) {
-        const int last_row = min(row_begin + kBlockM, S_q) - 1;
-        n = min(n, last_row / kBlockN + 1);
+        const int last_key = min(row_begin + kBlockM, S_q) - 1 + causal_off;
+        n = min(n, last_key / kBlockN + 1);
     }
     return n;
 }
@@ -162,7 +162,7 @@ __global__ void __launch_bounds__(KernelTile<D, SPLIT>::THREADS, 1)
                     float* __restrict__ lse_ptr, int S_q, int S_k, int BH, int n_qblk,
                     int head_group, float scale_log2, unsigned int* __restrict__ status,
                     int n_split, int kv_per_split, float* __restrict__ o_part,
-                    float* __restrict__ lse_part) {
+                    float* __restrict__ lse_part, int H, int kv_group, int causal_off) {
     using T = KernelTile<D, SPLIT>;
     using namespace sm100;
     constexpr int ROWS = T::BM * T::TILES;                 // query rows per unit
@@ -197,14 +197,21 @@ __global__ void __launch_bounds__(KernelTile<D, SPLIT>::THREADS, 1)
     auto unit_info = [&](int L, int& bh, int& q0, int& n0, int& n1, int& kb, int& sp) {
         sp = SPLIT ? L % n_split : 0;
         unit_coords<CAUSAL, ROWS>(SPLIT ? L / n_split : L, BH, n_qblk, head_group, bh, q0);
-        n0 = kv_tiles_for<CAUSAL>(q0, S_q, S_k);
-        n1 = T::TILES == 2 ? kv_tiles_for<CAUSAL>(q0 + T::BM, S_q, S_k) : 0;
+        n0 = kv_tiles_for<CAUSAL>(q0, S_q, S_k, causal_off);
+        n1 = T::TILES == 2 ? kv_tiles_for<CAUSAL>(q0 + T::BM, S_q, S_k, causal_off) : 0;
         kb = 0;
         if (SPLIT) {
             kb = sp * kv_per_split;
             n0 = max(0, min(n0, kb + kv_per_split) - kb);
             n1 = max(0, min(n1, kb + kv_per_split) - kb);
         }
+    };
+    // (b·H + h) -> batch, query head and the key/value head it reads (heads
+    // are grouped kv_group to one key/value head).
+    auto heads_of = [&](int bh, int& b, int& h, int& hk) {
+        b = bh / H;
+        h = bh - b * H;
+        hk = h / kv_group;
     };
     // Units are handed out in rounds of gridDim.x, in serpentine order (CTA c
     // takes position c of even rounds and gridDim.x-1-c of odd ones), so a CTA
@@ -272,7 +279,7 @@ __global__ void __launch_bounds__(KernelTile<D, SPLIT>::THREADS, 1)
         int uq = 0;                           // units started by this CTA
         int q_loads = 0;                      // Q loads issued
         bool ok = true;
-        auto issue = [&](const CUtensorMap* map, int j, int bh) {
+        auto issue = [&](const CUtensorMap* map, int j, int hk, int b) {
             if (!ok) return;
             const int slot = idx % T::NS;
             ok = mbar_wait(&kv_empty[slot], ((idx / T::NS) & 1) ^ 1, abort_flag, status,
@@ -284,8 +291,8 @@ __global__ void __launch_bounds__(KernelTile<D, SPLIT>::THREADS, 1)
                 uint8_t* dst = sKV + slot * T::KV_TILE_BYTES;
 #pragma unroll
                 for (int c = 0; c < T::CHUNKS; ++c)
-                    tma_load_3d(dst + c * T::KV_CHUNK_BYTES, map, &kv_full[slot], c * 64,
-                                j * T::BN, bh);
+                    tma_load_4d(dst + c * T::KV_CHUNK_BYTES, map, &kv_full[slot], c * 64,
+                                j * T::BN, hk, b);
             }
             __syncwarp();
             ++idx;
@@ -293,8 +300,9 @@ __global__ void __launch_bounds__(KernelTile<D, SPLIT>::THREADS, 1)
         for (int r = 0; r * static_cast<int>(gridDim.x) < n_units && ok; ++r) {
             const int L = unit_of_round(r);
             if (L >= n_units) continue;
-            int bh, q0, n0, n1, kb, sp;
+            int bh, q0, n0, n1, kb, sp, b, h, hk;
             unit_info(L, bh, q0, n0, n1, kb, sp);
+            heads_of(bh, b, h, hk);
             const int n_max = max(n0, n1);
             const int uq_now = uq++;
             // Q of this unit once the previous unit's last Q·Kᵀ is done.
@@ -305,23 +313,23 @@ __global__ void __launch_bounds__(KernelTile<D, SPLIT>::THREADS, 1)
                 mbar_arrive_expect_tx(q_full, T::TILES * T::Q_TILE_BYTES);
                 for (int t = 0; t < T::TILES; ++t)
                     for (int c = 0; c < T::CHUNKS; ++c)
-                        tma_load_3d(sQ + (t * T::CHUNKS + c) * T::Q_CHUNK_BYTES, &tm_q, q_full,
-                                    c * 64, q0 + t * T::BM, bh);
+                        tma_load_4d(sQ + (t * T::CHUNKS + c) * T::Q_CHUNK_BYTES, &tm_q, q_full,
+                                    c * 64, q0 + t * T::BM, h, b);
             }
             __syncwarp();
             ++q_loads;
             // K/V in the MMA warp's consumption order.
             if (T::TILES == 2) {
                 for (int j = 0; j < n_max; ++j) {
-                    issue(&tm_k, kb + j, bh);
-                    issue(&tm_v, kb + j, bh);
+                    issue(&tm_k, kb + j, hk, b);
+                    issue(&tm_v, kb + j, hk, b);
                 }
             } else {
-                issue(&tm_k, kb, bh);
-                if (n_max > 1) issue(&tm_k, kb + 1, bh);
+                issue(&tm_k, kb, hk, b);
+                if (n_max > 1) issue(&tm_k, kb + 1, hk, b);
                 for (int j = 0; j < n_max; ++j) {
-                    issue(&tm_v, kb + j, bh);
-                    if (j + 2 < n_max) issue(&tm_k, kb + j + 2, bh);
+                    issue(&tm_v, kb + j, hk, b);
+                    if (j + 2 < n_max) issue(&tm_k, kb + j + 2, hk, b);
                 }
             }
         }
@@ -552,9 +560,11 @@ __global__ void __launch_bounds__(KernelTile<D, SPLIT>::THREADS, 1)
                 }
 
                 const int kv0 = (kb + j) * T::BN;
-                const bool masked = (CAUSAL && kv0 + T::BN - 1 > row_begin) || (kv0 + T::BN > S_k);
+                const bool masked =
+                    (CAUSAL && kv0 + T::BN - 1 > row_begin + causal_off) || (kv0 + T::BN > S_k);
                 // keys kv0 + c with c < lim are visible to this row
-                const int lim = masked ? max(0, min(S_k, CAUSAL ? q_idx + 1 : S_k) - kv0) : T::BN;
+                const int lim =
+                    masked ? max(0, min(S_k, CAUSAL ? q_idx + 1 + causal_off : S_k) - kv0) : T::BN;
 
                 uint32_t pk[64];
                 bool rescale = false;
@@ -715,8 +725,9 @@ __global__ void __launch_bounds__(KernelTile<D, SPLIT>::THREADS, 1)
                         staged = __all_sync(0xffffffffu, staged);
                         if (staged && elect_one()) {
                             for (int c = 0; c < T::STAGE_CHUNKS; ++c)
-                                tma_store_3d(&tm_o, sO + c * T::Q_CHUNK_BYTES,
-                                             (rr * T::STAGE_CHUNKS + c) * 64, row_begin, bh);
+                                tma_store_4d(&tm_o, sO + c * T::Q_CHUNK_BYTES,
+                                             (rr * T::STAGE_CHUNKS + c) * 64, row_begin, bh % H,
+                                             bh / H);
                             bulk_commit_group();
                             bulk_wait_read_all();
                             mbar_arrive(stage_free);
@@ -771,7 +782,8 @@ cudaError_t launch_attn_fwd(const FwdArgs& a, cudaStream_t stream) {
     kernel<<<grid, T::THREADS, T::SMEM_BYTES, stream>>>(a.tm_q, a.tm_k, a.tm_v, a.tm_o, a.lse, a.S_q,
                                                          a.S_k, a.BH, n_qblk, head_group,
                                                          a.scale_log2, a.status, n_split,
-                                                         a.kv_per_split, a.o_part, a.lse_part);
+                                                         a.kv_per_split, a.o_part, a.lse_part, a.H,
+                                                         a.kv_group, a.causal_off);
     return cudaGetLastError();
 }
 

@@ -9,15 +9,20 @@
 namespace attn {
 
 struct FwdArgs {
-    CUtensorMap tm_q;       // [B·H, S_q, d] rows of Q, box 64 × 128
-    CUtensorMap tm_k;       // [B·H, S_k, d] rows of K, box 64 × 128
-    CUtensorMap tm_v;       // [B·H, S_k, d] rows of V, box 64 × 128
-    CUtensorMap tm_o;       // [B·H, S_q, d] rows of O, box 64 × 128 (stores)
+    // 4-D maps (d, S, heads, B) with the tensors' own row, head and batch
+    // strides; box 64 columns × 128 rows × 1 × 1.
+    CUtensorMap tm_q;       // Q: (d, S_q, H, B)
+    CUtensorMap tm_k;       // K: (d, S_k, H_kv, B)
+    CUtensorMap tm_v;       // V: (d, S_k, H_kv, B)
+    CUtensorMap tm_o;       // O: (d, S_q, H, B), stores
     void* o;                // [B, H, S_q, d], same dtype as Q
     float* lse;             // [B, H, S_q] fp32, natural log
     int32_t S_q;
     int32_t S_k;
     int32_t BH;             // B·H
+    int32_t H;              // query heads
+    int32_t kv_group;       // query heads per key/value head (H / H_kv)
+    int32_t causal_off;     // causal: key j is visible to query i iff j <= i + causal_off
     float scale_log2;       // scale · log2(e), >= 0
     int32_t num_sms;        // SMs of the device: the persistent grid size
     // split-KV only (launch_attn_fwd<..., SPLIT = true>)

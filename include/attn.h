@@ -104,6 +104,57 @@ attn_status_t attn_fwd(const void* q, const void* k, const void* v, void* o, flo
                        float scale, attn_dtype_t dtype, struct CUstream_st* stream);
 
 /*
+ * General layouts (the page's kernel takes per-tensor batch and head strides:
+ * stride_qb, stride_qh, stride_kb, ...).  An attn_layout_t gives, in
+ * elements, the distance between consecutive batch entries, heads and
+ * sequence positions of one tensor; the d elements of a position are
+ * contiguous.  The dense [B, H, S, d] layout is {H·S·d, S·d, d}; a
+ * [B, S, H, d] tensor is {S·H·d, d, H·d}; q, k and v may be views into one
+ * packed [B, S, 3, H, d] allocation.
+ */
+typedef struct {
+    int64_t batch, head, row;
+} attn_layout_t;
+
+typedef enum {
+    ATTN_MASK_NONE = 0,
+    ATTN_MASK_CAUSAL = 1,              /* key j visible to query i iff j <= i (top-left) */
+    ATTN_MASK_CAUSAL_BOTTOM_RIGHT = 2  /* iff j <= i + S_k - S_q; needs S_q <= S_k */
+} attn_mask_t;
+
+typedef struct {
+    const void* q;            /* [B, H, S_q, d] in q_layout */
+    const void* k;            /* [B, H_kv, S_k, d] in k_layout */
+    const void* v;            /* [B, H_kv, S_k, d] in v_layout */
+    void* o;                  /* [B, H, S_q, d] in o_layout; written */
+    float* lse;               /* [B, H, S_q] fp32, dense; written */
+    int64_t B, H, H_kv, S_q, S_k, d;
+    attn_layout_t q_layout, k_layout, v_layout, o_layout;
+    int mask;                 /* attn_mask_t */
+    float scale;
+    attn_dtype_t dtype;
+} attn_fwd_params_t;
+
+/*
+ * attn_fwd_general — attn_fwd over general layouts, grouped key/value heads
+ * and a choice of causal alignment.
+ *
+ *   H_kv      key/value heads, dividing H: query head h reads key/value head
+ *             h / (H / H_kv) (H_kv = H is plain multi-head attention).  The
+ *             page has only H = H_kv; this generalisation changes which K/V
+ *             a head reads, not the arithmetic.
+ *   layouts   every stride a positive multiple of 8 elements (16 bytes, the
+ *             tensor-map rule), row stride >= d; o's layout must not map two
+ *             elements to one address.  Pointers 16-byte aligned (lse 4).
+ *   mask      ATTN_MASK_NONE / _CAUSAL / _CAUSAL_BOTTOM_RIGHT (S_q <= S_k,
+ *             else ATTN_ERR_UNSUPPORTED).
+ *
+ * o and lse must not overlap each other or the byte ranges q, k and v span
+ * (inputs may overlap each other).  Errors as attn_fwd.
+ */
+attn_status_t attn_fwd_general(const attn_fwd_params_t* params, struct CUstream_st* stream);
+
+/*
  * attn_fwd_host — the same forward, for inputs and outputs in HOST memory.
  *
  * Enqueues on `stream`: copies of q_host, k_host, v_host into the caller's

@@ -26,6 +26,8 @@ Readings taken where the page is silent (each is listed in the design doc):
   * "zero out future token positions" is read as the masked logit being −∞
     (its probability is zero), not the score being set to 0.
   * causal alignment is top-left: key j is visible to query i iff j ≤ i.
+    ``bottom_right=True`` (an option the page does not have, for S_q ≤ S_k)
+    aligns the last query with the last key instead: j ≤ i + (S_k − S_q).
   * the log-sum-exp is the natural log and includes the scale:
     LSE_i = ln Σ_j exp(scale · q_i · k_j).
   * inputs are the fp16/bf16 values exactly as stored, widened to fp64; the
@@ -51,12 +53,15 @@ def _as_f64(x) -> np.ndarray:
 
 
 def _head(q: np.ndarray, k: np.ndarray, v: np.ndarray, rows: np.ndarray,
-          causal: bool, scale: float):
-    """Attention for the query rows ``rows`` of one (b, h): returns (o, lse)."""
+          causal: bool, scale: float, offset: int = 0):
+    """Attention for the query rows ``rows`` of one (b, h): returns (o, lse).
+
+    Under ``causal`` key j is visible to query i iff j <= i + offset.
+    """
     s = scale * (q[rows] @ k.T)                       # [R, S_k]
     if causal:
         keys = np.arange(k.shape[0])
-        s = np.where(keys[None, :] > rows[:, None], -np.inf, s)
+        s = np.where(keys[None, :] > rows[:, None] + offset, -np.inf, s)
     m = s.max(axis=1, keepdims=True)                  # row maximum
     p = np.exp(s - m)
     l = p.sum(axis=1, keepdims=True)                  # row sum
@@ -66,11 +71,12 @@ def _head(q: np.ndarray, k: np.ndarray, v: np.ndarray, rows: np.ndarray,
 
 
 def attention_forward(q, k, v, causal: bool = False, scale: float | None = None,
-                      row_block: int = 512):
+                      row_block: int = 512, bottom_right: bool = False):
     """O and LSE for ``q [B,H,S_q,d]``, ``k [B,H,S_k,d]``, ``v [B,H,S_k,d_v]``.
 
     Returns ``(o, lse)`` as float64 arrays of shapes ``[B,H,S_q,d_v]`` and
-    ``[B,H,S_q]``.  ``scale`` defaults to ``1/sqrt(d)``.
+    ``[B,H,S_q]``.  ``scale`` defaults to ``1/sqrt(d)``.  ``bottom_right``
+    (with ``causal``, S_q <= S_k) shifts the mask by S_k − S_q.
     """
     q, k, v = _as_f64(q), _as_f64(k), _as_f64(v)
     B, H, S_q, d = q.shape
@@ -78,6 +84,11 @@ def attention_forward(q, k, v, causal: bool = False, scale: float | None = None,
         raise ValueError(f"shape mismatch q{q.shape} k{k.shape} v{v.shape}")
     if scale is None:
         scale = 1.0 / np.sqrt(d)
+    offset = 0
+    if causal and bottom_right:
+        if S_q > k.shape[2]:
+            raise ValueError("bottom-right alignment needs S_q <= S_k")
+        offset = k.shape[2] - S_q
     o = np.empty((B, H, S_q, v.shape[3]), dtype=np.float64)
     lse = np.empty((B, H, S_q), dtype=np.float64)
     for b in range(B):
@@ -85,12 +96,12 @@ def attention_forward(q, k, v, causal: bool = False, scale: float | None = None,
             for r0 in range(0, S_q, row_block):
                 rows = np.arange(r0, min(r0 + row_block, S_q))
                 o[b, h, rows], lse[b, h, rows] = _head(q[b, h], k[b, h], v[b, h],
-                                                        rows, causal, scale)
+                                                        rows, causal, scale, offset)
     return o, lse
 
 
 def attention_rows(q_bh, k_bh, v_bh, rows, causal: bool = False,
-                   scale: float | None = None):
+                   scale: float | None = None, bottom_right: bool = False):
     """O and LSE for selected query ``rows`` of a single head.
 
     ``q_bh [S_q,d]``, ``k_bh, v_bh [S_k,d]``; returns ``(o [R,d], lse [R])``.
@@ -100,7 +111,8 @@ def attention_rows(q_bh, k_bh, v_bh, rows, causal: bool = False,
     if scale is None:
         scale = 1.0 / np.sqrt(q.shape[1])
     rows = np.asarray(rows, dtype=np.int64)
-    return _head(q, k, v, rows, causal, scale)
+    offset = k.shape[0] - q.shape[0] if (causal and bottom_right) else 0
+    return _head(q, k, v, rows, causal, scale, offset)
 
 
 def attention_probs(q_bh, k_bh, causal: bool = False, scale: float | None = None):

@@ -36,7 +36,7 @@ def _declared_functions():
 
 def test_header_declares_the_boundary():
     names = _declared_functions()
-    assert names == sorted(["attn_fwd", "attn_fwd_host", "attn_fwd_plan", "attn_fwd_splitkv_plan",
+    assert names == sorted(["attn_fwd", "attn_fwd_general", "attn_fwd_host", "attn_fwd_plan", "attn_fwd_splitkv_plan",
                             "attn_fwd_splitkv", "attn_fwd_splitkv_noalloc", "attn_bwd_workspace_size",
                             "attn_bwd", "attn_last_error", "attn_get_device_status",
                             "attn_version"])
@@ -297,3 +297,54 @@ BWD_CASES = [
 def test_bwd_validation_rejects_before_device_work(lib, kw, status, msg):
     assert _bwd(lib, **kw) == status
     assert msg in lib.attn_last_error().decode()
+
+
+# ------------------------------------------------------------------ general layouts
+
+
+def _gen(lib, **kw):
+    G = 1 << 28
+    B, H, H_kv, S_q, S_k, d = kw.pop("B", 2), kw.pop("H", 4), kw.pop("H_kv", 2), kw.pop("S_q", 64), \
+        kw.pop("S_k", 96), kw.pop("d", 64)
+    dense = lambda heads, S: binding.AttnLayout(heads * S * d, S * d, d)  # noqa: E731
+    p = binding.AttnFwdParams(A, A + G, A + 2 * G, A + 3 * G, A + 4 * G, B, H, H_kv, S_q, S_k, d,
+                              dense(H, S_q), dense(H_kv, S_k), dense(H_kv, S_k), dense(H, S_q),
+                              1, 0.125, 1)
+    for key, val in kw.items():
+        setattr(p, key, val)
+    return lib.attn_fwd_general(ctypes.byref(p), None)
+
+
+GEN_CASES = [
+    (dict(H_kv=3), binding.ATTN_ERR_INVALID_ARG, "H_kv=3 must divide H=4"),
+    (dict(H_kv=0), binding.ATTN_ERR_INVALID_ARG, "H_kv=0"),
+    (dict(mask=5), binding.ATTN_ERR_INVALID_ARG, "mask must be"),
+    (dict(mask=2, S_q=200, S_k=100), binding.ATTN_ERR_UNSUPPORTED, "S_q <= S_k"),
+    (dict(q_layout=binding.AttnLayout(8 * 64 * 64, 64 * 64, 60)), binding.ATTN_ERR_INVALID_ARG,
+     "q row stride 60"),
+    (dict(k_layout=binding.AttnLayout(0, 96 * 64, 64)), binding.ATTN_ERR_INVALID_ARG, "k batch stride"),
+    (dict(o_layout=binding.AttnLayout(64 * 64, 64, 64)), binding.ATTN_ERR_INVALID_ARG,
+     "o layout maps two elements"),
+    (dict(o=A + (1 << 28) + 4096), binding.ATTN_ERR_INVALID_ARG, "o overlaps k"),
+    (dict(d=128, q_layout=binding.AttnLayout(4 * 64 * 128, 64 * 128, 64)), binding.ATTN_ERR_INVALID_ARG,
+     "below d=128"),
+]
+
+
+@pytest.mark.parametrize("kw,status,msg", GEN_CASES, ids=[c[2] for c in GEN_CASES])
+def test_general_validation(lib, kw, status, msg):
+    assert _gen(lib, **kw) == status
+    assert msg in lib.attn_last_error().decode()
+
+
+def test_general_accepts_packed_and_head_major_views(lib):
+    """BSHD views of one packed [B, S, 3, H, d] buffer pass validation (then fail only for lack of a GPU)."""
+    import torch
+    if torch.cuda.is_available():
+        pytest.skip("a GPU is present")
+    B, H, S, d = 2, 4, 64, 64
+    packed = binding.AttnLayout(S * 3 * H * d, d, 3 * H * d)
+    st = _gen(lib, B=B, H=H, H_kv=H, S_q=S, S_k=S, d=d, q_layout=packed, k_layout=packed,
+              v_layout=packed, k=A + H * d * 2, v=A + 2 * H * d * 2,
+              o_layout=binding.AttnLayout(S * H * d, d, H * d))
+    assert st in (binding.ATTN_ERR_CUDA, binding.ATTN_ERR_UNSUPPORTED)

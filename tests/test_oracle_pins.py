@@ -24,14 +24,14 @@ def _fwd(q, k, v, causal, scale, row_block=512):
     return oracle.attention_forward(q, k, v, causal=causal, scale=scale, row_block=row_block)
 
 
-def _loops(q, k, v, causal, scale):
+def _loops(q, k, v, causal, scale, offset=0):
     """Attention by explicit Python loops over one head: q [S_q][d] lists."""
     S_q, S_k, d = len(q), len(k), len(q[0])
     o, lse = [], []
     for i in range(S_q):
         logits = []
         for j in range(S_k):
-            if causal and j > i:
+            if causal and j > i + offset:
                 continue
             dot = 0.0
             for c in range(d):
@@ -204,9 +204,42 @@ def pin_rows_and_blocks_agree():
         np.testing.assert_allclose(rl, lse[0, 1, rows], rtol=0, atol=1e-14)
 
 
+def pin_bottom_right_square_is_top_left():
+    """With S_q = S_k the two causal alignments coincide."""
+    q, k, v = RNG.standard_normal((3, 1, 2, 23, 8))
+    a = _fwd(q, k, v, True, 0.3)
+    b = oracle.attention_forward(q, k, v, causal=True, scale=0.3, bottom_right=True)
+    np.testing.assert_array_equal(a[0], b[0])
+    np.testing.assert_array_equal(a[1], b[1])
+
+
+def pin_bottom_right_is_tail_of_square():
+    """S_q < S_k, bottom-right: the last S_q rows of a top-left causal S_k × S_k problem."""
+    S_q, S_k, d = 9, 30, 8
+    k, v = RNG.standard_normal((2, 1, 1, S_k, d))
+    q_tail = RNG.standard_normal((1, 1, S_q, d))
+    q_full = np.concatenate([RNG.standard_normal((1, 1, S_k - S_q, d)), q_tail], axis=2)
+    full_o, full_l = _fwd(q_full, k, v, True, 0.4)
+    o, l = oracle.attention_forward(q_tail, k, v, causal=True, scale=0.4, bottom_right=True)
+    np.testing.assert_allclose(o, full_o[:, :, S_k - S_q:], rtol=0, atol=1e-13)
+    np.testing.assert_allclose(l, full_l[:, :, S_k - S_q:], rtol=0, atol=1e-13)
+
+
+def pin_bottom_right_loops():
+    """Brute force with the shifted mask, S_q = 5 against S_k = 8."""
+    q, k, v = RNG.standard_normal((5, 3)), RNG.standard_normal((8, 3)), RNG.standard_normal((8, 2))
+    lo, ll = _loops(q.tolist(), k.tolist(), v.tolist(), True, 0.8, offset=3)
+    o, l = oracle.attention_forward(q[None, None], k[None, None], v[None, None], causal=True,
+                                    scale=0.8, bottom_right=True)
+    np.testing.assert_allclose(o[0, 0], np.array(lo), rtol=0, atol=1e-13)
+    np.testing.assert_allclose(l[0, 0], np.array(ll), rtol=0, atol=1e-13)
+
+
 PINS = [pin_worked_example, pin_brute_force, pin_constant_v, pin_scale_zero,
         pin_causal_first_row, pin_one_hot_selection, pin_key_permutation, pin_key_shift,
-        pin_log_domain_form, pin_library_sdpa, pin_rows_and_blocks_agree]
+        pin_log_domain_form, pin_library_sdpa, pin_rows_and_blocks_agree,
+        pin_bottom_right_square_is_top_left, pin_bottom_right_is_tail_of_square,
+        pin_bottom_right_loops]
 
 
 @pytest.mark.parametrize("pin", PINS, ids=lambda p: p.__name__)
@@ -244,7 +277,11 @@ def test_half_inputs_are_widened_exactly():
 
 # ------------------------------------------------------- planted mistakes
 def _mutant(kind):
-    def head(q, k, v, rows, causal, scale):
+    def head(q, k, v, rows, causal, scale, offset=0):
+        if kind == "offset_ignored":
+            offset = 0
+        if kind == "offset_sign":
+            offset = -offset
         s = scale * (q[rows] @ k.T)
         if kind == "no_scale":
             s = q[rows] @ k.T
@@ -254,14 +291,15 @@ def _mutant(kind):
             s = scale * (k @ q.T)[: len(rows)][:, : k.shape[0]] if k.shape[0] == q.shape[0] else s.T
         if causal:
             keys = np.arange(k.shape[0])
+            r = rows[:, None] + offset
             if kind == "mask_off_by_one":
-                s = np.where(keys[None, :] >= rows[:, None], -np.inf, s)
+                s = np.where(keys[None, :] >= r, -np.inf, s)
             elif kind == "mask_flipped":
-                s = np.where(keys[None, :] < rows[:, None], -np.inf, s)
+                s = np.where(keys[None, :] < r, -np.inf, s)
             elif kind == "mask_zero_score":
-                s = np.where(keys[None, :] > rows[:, None], 0.0, s)
+                s = np.where(keys[None, :] > r, 0.0, s)
             else:
-                s = np.where(keys[None, :] > rows[:, None], -np.inf, s)
+                s = np.where(keys[None, :] > r, -np.inf, s)
         m = s.max(axis=1, keepdims=True)
         p = np.exp(s - m)
         l = p.sum(axis=1, keepdims=True)
@@ -280,7 +318,8 @@ def _mutant(kind):
 
 
 MUTANTS = ["no_scale", "inverse_scale", "transposed", "mask_off_by_one", "mask_flipped",
-           "mask_zero_score", "no_normalise", "lse_log2", "lse_no_max", "lse_unscaled"]
+           "mask_zero_score", "no_normalise", "lse_log2", "lse_no_max", "lse_unscaled",
+           "offset_ignored", "offset_sign"]
 
 
 @pytest.mark.parametrize("kind", MUTANTS)
