@@ -9,6 +9,7 @@ and a missing library raises instead of falling back to anything else.
 from .binding import (  # noqa: F401
     AttnError,
     attn_bwd,
+    attn_bwd_general,
     attn_bwd_workspace_size,
     attn_fwd,
     attn_fwd_general,
@@ -20,6 +21,7 @@ from .binding import (  # noqa: F401
     attn_get_device_status,
     attn_last_error,
     bwd,
+    bwd_general,
     fwd,
     fwd_general,
     fwd_splitkv,

@@ -31,6 +31,7 @@ ATTN_MASK_CAUSAL_BOTTOM_RIGHT = 2
 
 EXPORTED = ("attn_fwd", "attn_fwd_general", "attn_fwd_host", "attn_fwd_plan", "attn_fwd_splitkv_plan",
             "attn_fwd_splitkv", "attn_fwd_splitkv_noalloc", "attn_bwd_workspace_size", "attn_bwd",
+            "attn_bwd_general",
             "attn_last_error", "attn_get_device_status", "attn_version")
 NOALLOC_SCRATCH_BYTES = 16 * 1024 * 1024    # ATTN_NOALLOC_SCRATCH_BYTES
 
@@ -58,6 +59,20 @@ class AttnFwdParams(ctypes.Structure):
                 ("q_layout", AttnLayout), ("k_layout", AttnLayout), ("v_layout", AttnLayout),
                 ("o_layout", AttnLayout), ("mask", ctypes.c_int), ("scale", ctypes.c_float),
                 ("dtype", ctypes.c_int)]
+
+
+class AttnBwdParams(ctypes.Structure):
+    """Mirror of attn_bwd_params_t (include/attn.h)."""
+    _fields_ = [("q", ctypes.c_void_p), ("k", ctypes.c_void_p), ("v", ctypes.c_void_p),
+                ("o", ctypes.c_void_p), ("lse", ctypes.c_void_p), ("dout", ctypes.c_void_p),
+                ("dq", ctypes.c_void_p), ("dk", ctypes.c_void_p), ("dv", ctypes.c_void_p),
+                ("B", ctypes.c_int64), ("H", ctypes.c_int64), ("H_kv", ctypes.c_int64),
+                ("S_q", ctypes.c_int64), ("S_k", ctypes.c_int64), ("d", ctypes.c_int64),
+                ("q_layout", AttnLayout), ("k_layout", AttnLayout), ("v_layout", AttnLayout),
+                ("o_layout", AttnLayout), ("do_layout", AttnLayout), ("dq_layout", AttnLayout),
+                ("dk_layout", AttnLayout), ("dv_layout", AttnLayout), ("mask", ctypes.c_int),
+                ("scale", ctypes.c_float), ("dtype", ctypes.c_int), ("workspace", ctypes.c_void_p),
+                ("workspace_bytes", ctypes.c_int64)]
 
 
 _DTYPE_CODE = {torch.float16: ATTN_DTYPE_F16, torch.bfloat16: ATTN_DTYPE_BF16}
@@ -95,6 +110,8 @@ def load_library() -> ctypes.CDLL:
         lib.attn_fwd.restype = i32
         lib.attn_fwd_general.argtypes = [ctypes.POINTER(AttnFwdParams), vp]
         lib.attn_fwd_general.restype = i32
+        lib.attn_bwd_general.argtypes = [ctypes.POINTER(AttnBwdParams), vp]
+        lib.attn_bwd_general.restype = i32
         lib.attn_fwd_host.argtypes = [vp] * 10 + [i64, i64, i64, i64, i64, i32, ctypes.c_float,
                                                   i32, vp]
         lib.attn_fwd_host.restype = i32
@@ -336,4 +353,34 @@ def bwd(q: torch.Tensor, k: torch.Tensor, v: torch.Tensor, o: torch.Tensor, lse:
     dq, dk, dv = torch.empty_like(q), torch.empty_like(k), torch.empty_like(v)
     attn_bwd(q, k, v, o, lse, dout, dq, dk, dv, B, H, S_q, S_k, d, causal, scale, dtype,
              workspace, workspace.numel() * workspace.element_size())
+    return dq, dk, dv
+
+
+def attn_bwd_general(params: AttnBwdParams, stream=None) -> None:
+    """Enqueue the general-layout backward described by ``params``."""
+    _check(load_library().attn_bwd_general(ctypes.byref(params), _stream_handle(stream)))
+
+
+def bwd_general(q, k, v, o, lse, dout, mask: int = ATTN_MASK_NONE, scale: float | None = None,
+                dq=None, dk=None, dv=None, workspace=None):
+    """Backward over strided views (shapes as :func:`fwd_general`).  Gradients are written into
+    the given views (default: dense tensors).  Returns ``(dq, dk, dv)``.
+    """
+    B, H, S_q, d = q.shape
+    H_kv, S_k = k.shape[1], k.shape[2]
+    dtype = _DTYPE_CODE[q.dtype]
+    if scale is None:
+        scale = 1.0 / math.sqrt(d)
+    dq = torch.empty((B, H, S_q, d), dtype=q.dtype, device=q.device) if dq is None else dq
+    dk = torch.empty((B, H_kv, S_k, d), dtype=q.dtype, device=q.device) if dk is None else dk
+    dv = torch.empty((B, H_kv, S_k, d), dtype=q.dtype, device=q.device) if dv is None else dv
+    ws = attn_bwd_workspace_size(B, H, S_q, S_k, d, dtype)
+    if workspace is None:
+        workspace = torch.empty(ws, dtype=torch.uint8, device=q.device)
+    p = AttnBwdParams(q.data_ptr(), k.data_ptr(), v.data_ptr(), o.data_ptr(), lse.data_ptr(),
+                      dout.data_ptr(), dq.data_ptr(), dk.data_ptr(), dv.data_ptr(),
+                      B, H, H_kv, S_q, S_k, d, _layout(q), _layout(k), _layout(v), _layout(o),
+                      _layout(dout), _layout(dq), _layout(dk), _layout(dv), int(mask), float(scale),
+                      dtype, workspace.data_ptr(), workspace.numel() * workspace.element_size())
+    attn_bwd_general(p)
     return dq, dk, dv

@@ -160,37 +160,49 @@ attn_status_t check_layout(const Layout& l, const char* name, int64_t d) {
     return ATTN_OK;
 }
 
-attn_status_t validate_general(Problem& p, const attn_fwd_params_t* a) {
-    if (!a) return fail(ATTN_ERR_INVALID_ARG, "params is null");
-    if (a->mask < 0 || a->mask > 2)
-        return fail(ATTN_ERR_INVALID_ARG, "mask must be 0, 1 or 2, got %d", a->mask);
-    attn_status_t s = validate_sizes(p, a->B, a->H, a->S_q, a->S_k, a->d, a->mask != 0 ? 1 : 0,
-                                     a->scale, a->dtype);
+// Sizes, heads, mask and the q, k, v, o layouts shared by the general forward
+// and backward entry points.
+attn_status_t validate_common(Problem& p, int64_t B, int64_t H, int64_t H_kv, int64_t S_q,
+                              int64_t S_k, int64_t d, int mask, float scale, attn_dtype_t dtype,
+                              const Layout& lq, const Layout& lk, const Layout& lv,
+                              const Layout& lo) {
+    if (mask < 0 || mask > 2)
+        return fail(ATTN_ERR_INVALID_ARG, "mask must be 0, 1 or 2, got %d", mask);
+    attn_status_t s = validate_sizes(p, B, H, S_q, S_k, d, mask != 0 ? 1 : 0, scale, dtype);
     if (s != ATTN_OK) return s;
-    if (a->H_kv < 1 || a->H_kv > a->H || a->H % a->H_kv != 0)
-        return fail(ATTN_ERR_INVALID_ARG, "H_kv=%lld must divide H=%lld", (long long)a->H_kv,
-                    (long long)a->H);
-    if (a->mask == 2 && a->S_q > a->S_k)
+    if (H_kv < 1 || H_kv > H || H % H_kv != 0)
+        return fail(ATTN_ERR_INVALID_ARG, "H_kv=%lld must divide H=%lld", (long long)H_kv,
+                    (long long)H);
+    if (mask == 2 && S_q > S_k)
         return fail(ATTN_ERR_UNSUPPORTED,
                     "bottom-right causal mask needs S_q <= S_k (got S_q=%lld, S_k=%lld): earlier "
                     "queries would see no key",
-                    (long long)a->S_q, (long long)a->S_k);
-    if ((s = check_layout(a->q_layout, "q", a->d)) != ATTN_OK) return s;
-    if ((s = check_layout(a->k_layout, "k", a->d)) != ATTN_OK) return s;
-    if ((s = check_layout(a->v_layout, "v", a->d)) != ATTN_OK) return s;
-    if ((s = check_layout(a->o_layout, "o", a->d)) != ATTN_OK) return s;
-    p.H_kv = a->H_kv;
-    p.causal_off = a->mask == 2 ? a->S_k - a->S_q : 0;
-    p.lq = {a->q_layout.batch, a->q_layout.head, a->q_layout.row};
-    p.lk = {a->k_layout.batch, a->k_layout.head, a->k_layout.row};
-    p.lv = {a->v_layout.batch, a->v_layout.head, a->v_layout.row};
-    p.lo = {a->o_layout.batch, a->o_layout.head, a->o_layout.row};
-    if (!layout_injective(p.lo, p.B, p.H, p.S_q, p.d))
-        return fail(ATTN_ERR_INVALID_ARG, "o layout maps two elements to one address");
+                    (long long)S_q, (long long)S_k);
+    if ((s = check_layout(lq, "q", d)) != ATTN_OK) return s;
+    if ((s = check_layout(lk, "k", d)) != ATTN_OK) return s;
+    if ((s = check_layout(lv, "v", d)) != ATTN_OK) return s;
+    if ((s = check_layout(lo, "o", d)) != ATTN_OK) return s;
+    p.H_kv = H_kv;
+    p.causal_off = mask == 2 ? S_k - S_q : 0;
+    p.lq = lq;
+    p.lk = lk;
+    p.lv = lv;
+    p.lo = lo;
     p.q_bytes = span_bytes(p.lq, p.B, p.H, p.S_q, p.d);
     p.kv_bytes = span_bytes(p.lk, p.B, p.H_kv, p.S_k, p.d);
     p.v_bytes = span_bytes(p.lv, p.B, p.H_kv, p.S_k, p.d);
     p.o_bytes = span_bytes(p.lo, p.B, p.H, p.S_q, p.d);
+    return ATTN_OK;
+}
+
+attn_status_t validate_general(Problem& p, const attn_fwd_params_t* a) {
+    if (!a) return fail(ATTN_ERR_INVALID_ARG, "params is null");
+    attn_status_t s = validate_common(p, a->B, a->H, a->H_kv, a->S_q, a->S_k, a->d, a->mask,
+                                      a->scale, a->dtype, a->q_layout, a->k_layout, a->v_layout,
+                                      a->o_layout);
+    if (s != ATTN_OK) return s;
+    if (!layout_injective(p.lo, p.B, p.H, p.S_q, p.d))
+        return fail(ATTN_ERR_INVALID_ARG, "o layout maps two elements to one address");
     return ATTN_OK;
 }
 
@@ -670,15 +682,24 @@ attn_status_t attn_bwd_workspace_size(int64_t B, int64_t H, int64_t S_q, int64_t
     return ok();
 }
 
-attn_status_t attn_bwd(const void* q, const void* k, const void* v, const void* o,
-                       const float* lse, const void* dout, void* dq, void* dk, void* dv,
-                       int64_t B, int64_t H, int64_t S_q, int64_t S_k, int64_t d, int causal,
-                       float scale, attn_dtype_t dtype, void* workspace, int64_t workspace_bytes,
-                       struct CUstream_st* stream) {
+attn_status_t attn_bwd_general(const attn_bwd_params_t* a, struct CUstream_st* stream) {
+    if (!a) return fail(ATTN_ERR_INVALID_ARG, "params is null");
     Problem p;
-    attn_status_t s = validate_sizes(p, B, H, S_q, S_k, d, causal, scale, dtype);
+    attn_status_t s = validate_common(p, a->B, a->H, a->H_kv, a->S_q, a->S_k, a->d, a->mask,
+                                      a->scale, a->dtype, a->q_layout, a->k_layout, a->v_layout,
+                                      a->o_layout);
     if (s != ATTN_OK) return s;
     if ((s = validate_bwd_head_dim(p)) != ATTN_OK) return s;
+    if ((s = check_layout(a->do_layout, "dout", p.d)) != ATTN_OK) return s;
+    if ((s = check_layout(a->dq_layout, "dq", p.d)) != ATTN_OK) return s;
+    if ((s = check_layout(a->dk_layout, "dk", p.d)) != ATTN_OK) return s;
+    if ((s = check_layout(a->dv_layout, "dv", p.d)) != ATTN_OK) return s;
+    if (!layout_injective(a->dq_layout, p.B, p.H, p.S_q, p.d))
+        return fail(ATTN_ERR_INVALID_ARG, "dq layout maps two elements to one address");
+    if (!layout_injective(a->dk_layout, p.B, p.H_kv, p.S_k, p.d))
+        return fail(ATTN_ERR_INVALID_ARG, "dk layout maps two elements to one address");
+    if (!layout_injective(a->dv_layout, p.B, p.H_kv, p.S_k, p.d))
+        return fail(ATTN_ERR_INVALID_ARG, "dv layout maps two elements to one address");
     struct Buf {
         const void* ptr;
         size_t bytes;
@@ -688,20 +709,25 @@ attn_status_t attn_bwd(const void* q, const void* k, const void* v, const void* 
     };
     const size_t wb = static_cast<size_t>(bwd_workspace_bytes(p));
     const Buf bufs[] = {
-        {q, p.q_bytes, 16, "q", false},          {k, p.kv_bytes, 16, "k", false},
-        {v, p.kv_bytes, 16, "v", false},         {o, p.o_bytes, 16, "o", false},
-        {lse, p.lse_bytes, 4, "lse", false},     {dout, p.o_bytes, 16, "dout", false},
-        {dq, p.q_bytes, 16, "dq", true},         {dk, p.kv_bytes, 16, "dk", true},
-        {dv, p.kv_bytes, 16, "dv", true},        {workspace, wb, 16, "workspace", true},
+        {a->q, p.q_bytes, 16, "q", false},
+        {a->k, p.kv_bytes, 16, "k", false},
+        {a->v, p.v_bytes, 16, "v", false},
+        {a->o, p.o_bytes, 16, "o", false},
+        {a->lse, p.lse_bytes, 4, "lse", false},
+        {a->dout, span_bytes(a->do_layout, p.B, p.H, p.S_q, p.d), 16, "dout", false},
+        {a->dq, span_bytes(a->dq_layout, p.B, p.H, p.S_q, p.d), 16, "dq", true},
+        {a->dk, span_bytes(a->dk_layout, p.B, p.H_kv, p.S_k, p.d), 16, "dk", true},
+        {a->dv, span_bytes(a->dv_layout, p.B, p.H_kv, p.S_k, p.d), 16, "dv", true},
+        {a->workspace, wb, 16, "workspace", true},
     };
     for (const Buf& b : bufs) {
         if (!b.ptr) return fail(ATTN_ERR_INVALID_ARG, "%s is null", b.name);
         if (!aligned(b.ptr, b.align))
             return fail(ATTN_ERR_INVALID_ARG, "%s is not %zu-byte aligned", b.name, b.align);
     }
-    if (workspace_bytes < static_cast<int64_t>(wb))
+    if (a->workspace_bytes < static_cast<int64_t>(wb))
         return fail(ATTN_ERR_INVALID_ARG, "workspace_bytes=%lld is below the %lld bytes needed",
-                    (long long)workspace_bytes, (long long)wb);
+                    (long long)a->workspace_bytes, (long long)wb);
     // Every written buffer must be disjoint from every other buffer.
     for (const Buf& w : bufs) {
         if (!w.written) continue;
@@ -713,35 +739,68 @@ attn_status_t attn_bwd(const void* q, const void* k, const void* v, const void* 
     }
     int dev = 0;
     if ((s = check_device(&dev)) != ATTN_OK) return s;
-    attn::BwdArgs a;
-    if ((s = encode_rows_box(&a.tm_k_fixed, k, p, p.S_k, 128, "k")) != ATTN_OK) return s;
-    if ((s = encode_rows_box(&a.tm_v_fixed, v, p, p.S_k, 128, "v")) != ATTN_OK) return s;
-    if ((s = encode_rows_box(&a.tm_q_step, q, p, p.S_q, 64, "q")) != ATTN_OK) return s;
-    if ((s = encode_rows_box(&a.tm_do_step, dout, p, p.S_q, 64, "dout")) != ATTN_OK) return s;
-    if ((s = encode_rows_box(&a.tm_q_fixed, q, p, p.S_q, 128, "q")) != ATTN_OK) return s;
-    if ((s = encode_rows_box(&a.tm_do_fixed, dout, p, p.S_q, 128, "dout")) != ATTN_OK) return s;
+    attn::BwdArgs g;
+    if ((s = encode_4d(&g.tm_k_fixed, a->k, p, p.S_k, p.H_kv, p.lk, 128, "k")) != ATTN_OK) return s;
+    if ((s = encode_4d(&g.tm_v_fixed, a->v, p, p.S_k, p.H_kv, p.lv, 128, "v")) != ATTN_OK) return s;
+    if ((s = encode_4d(&g.tm_q_step, a->q, p, p.S_q, p.H, p.lq, 64, "q")) != ATTN_OK) return s;
+    if ((s = encode_4d(&g.tm_do_step, a->dout, p, p.S_q, p.H, a->do_layout, 64, "dout")) != ATTN_OK)
+        return s;
+    if ((s = encode_4d(&g.tm_q_fixed, a->q, p, p.S_q, p.H, p.lq, 128, "q")) != ATTN_OK) return s;
+    if ((s = encode_4d(&g.tm_do_fixed, a->dout, p, p.S_q, p.H, a->do_layout, 128, "dout")) != ATTN_OK)
+        return s;
+    auto rl = [](const attn_layout_t& l) { return attn::RowLayout{l.batch, l.head, l.row}; };
     const int64_t s_pad = bwd_s_pad(p);
-    a.o = o;
-    a.dout = dout;
-    a.lse = lse;
-    a.lse2 = static_cast<float*>(workspace);
-    a.delta = a.lse2 + p.B * p.H * s_pad;
-    a.dq = dq;
-    a.dk = dk;
-    a.dv = dv;
-    a.S_q = static_cast<int32_t>(p.S_q);
-    a.S_k = static_cast<int32_t>(p.S_k);
-    a.BH = static_cast<int32_t>(p.B * p.H);
-    a.S_pad = static_cast<int32_t>(s_pad);
-    a.scale = p.scale;
-    a.scale_log2 = static_cast<float>(static_cast<double>(p.scale) * 1.4426950408889634);
-    a.num_sms = g_num_sms[dev].load();
-    a.status = g_status_ptr[dev].load();
+    g.o = a->o;
+    g.dout = a->dout;
+    g.lse = a->lse;
+    g.lse2 = static_cast<float*>(a->workspace);
+    g.delta = g.lse2 + p.B * p.H * s_pad;
+    g.dq = a->dq;
+    g.dk = a->dk;
+    g.dv = a->dv;
+    g.o_lay = rl(p.lo);
+    g.do_lay = rl(a->do_layout);
+    g.dq_lay = rl(a->dq_layout);
+    g.dk_lay = rl(a->dk_layout);
+    g.dv_lay = rl(a->dv_layout);
+    g.S_q = static_cast<int32_t>(p.S_q);
+    g.S_k = static_cast<int32_t>(p.S_k);
+    g.BH = static_cast<int32_t>(p.B * p.H);
+    g.S_pad = static_cast<int32_t>(s_pad);
+    g.H = static_cast<int32_t>(p.H);
+    g.kv_group = static_cast<int32_t>(p.H / p.H_kv);
+    g.causal_off = static_cast<int32_t>(p.causal_off);
+    g.scale = p.scale;
+    g.scale_log2 = static_cast<float>(static_cast<double>(p.scale) * 1.4426950408889634);
+    g.num_sms = g_num_sms[dev].load();
+    g.status = g_status_ptr[dev].load();
     BwdLaunchFn fn = pick_bwd(p.d, p.dtype == ATTN_DTYPE_BF16, p.causal);
     if (!fn) return fail(ATTN_ERR_UNSUPPORTED, "no backward kernel for d=%lld", (long long)p.d);
-    cudaError_t e = fn(a, stream);
+    cudaError_t e = fn(g, stream);
     if (e != cudaSuccess) return fail(ATTN_ERR_CUDA, "backward launch: %s", cudaGetErrorString(e));
     return ok();
+}
+
+attn_status_t attn_bwd(const void* q, const void* k, const void* v, const void* o,
+                       const float* lse, const void* dout, void* dq, void* dk, void* dv,
+                       int64_t B, int64_t H, int64_t S_q, int64_t S_k, int64_t d, int causal,
+                       float scale, attn_dtype_t dtype, void* workspace, int64_t workspace_bytes,
+                       struct CUstream_st* stream) {
+    if (causal != 0 && causal != 1)
+        return fail(ATTN_ERR_INVALID_ARG, "causal must be 0 or 1, got %d", causal);
+    const attn_layout_t lq = dense_layout(H, S_q, d), lk = dense_layout(H, S_k, d);
+    attn_bwd_params_t a;
+    a.q = q; a.k = k; a.v = v; a.o = o; a.lse = lse; a.dout = dout;
+    a.dq = dq; a.dk = dk; a.dv = dv;
+    a.B = B; a.H = H; a.H_kv = H; a.S_q = S_q; a.S_k = S_k; a.d = d;
+    a.q_layout = lq; a.k_layout = lk; a.v_layout = lk; a.o_layout = lq;
+    a.do_layout = lq; a.dq_layout = lq; a.dk_layout = lk; a.dv_layout = lk;
+    a.mask = causal;
+    a.scale = scale;
+    a.dtype = dtype;
+    a.workspace = workspace;
+    a.workspace_bytes = workspace_bytes;
+    return attn_bwd_general(&a, stream);
 }
 
 const char* attn_last_error(void) { return g_msg; }

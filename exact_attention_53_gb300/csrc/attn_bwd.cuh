@@ -163,62 +163,84 @@ __device__ __forceinline__ void store_row_from_tmem(uint32_t taddr, float mul, v
 }
 
 // ============================================================== prep
-// delta[bh, i] = Σ_c dO[bh,i,c]·O[bh,i,c]; lse2[bh, i] = LSE[bh,i]·log2(e);
-// for i in [S_q, S_pad): delta = 0, lse2 = +inf.  One warp per padded row.
+// delta[bh, i] = Σ_c dO[b,h,i,c]·O[b,h,i,c]; lse2[bh, i] = LSE[bh,i]·log2(e);
+// for i in [S_q, S_pad): delta = 0, lse2 = +inf.  Each lane loads 16 bytes of
+// a row of O and of dO; a warp covers PREP_ROWS rows with all its loads
+// issued before the first is used, then reduces each row across its lanes.
+constexpr int kPrepIters = 4;
+
+template <int D>
+constexpr int prep_rows_per_warp() { return (32 / (D / 8)) * kPrepIters; }
+
+__device__ __forceinline__ float dot8(uint4 a, uint4 b, bool bf16, float acc) {
+    const uint32_t aw[4] = {a.x, a.y, a.z, a.w}, bw[4] = {b.x, b.y, b.z, b.w};
+#pragma unroll
+    for (int w = 0; w < 4; ++w) {
+        float a0, a1, b0, b1;
+        if (bf16) {
+            a0 = __uint_as_float(aw[w] << 16); a1 = __uint_as_float(aw[w] & 0xffff0000u);
+            b0 = __uint_as_float(bw[w] << 16); b1 = __uint_as_float(bw[w] & 0xffff0000u);
+        } else {
+            const float2 af = __half22float2(*reinterpret_cast<const __half2*>(&aw[w]));
+            const float2 bf = __half22float2(*reinterpret_cast<const __half2*>(&bw[w]));
+            a0 = af.x; a1 = af.y; b0 = bf.x; b1 = bf.y;
+        }
+        acc = fmaf(a0, b0, acc);
+        acc = fmaf(a1, b1, acc);
+    }
+    return acc;
+}
+
 template <int D, bool BF16>
 __global__ void __launch_bounds__(256) attn_bwd_prep_kernel(const uint16_t* __restrict__ o,
                                                             const uint16_t* __restrict__ dout,
                                                             const float* __restrict__ lse,
                                                             float* __restrict__ lse2,
                                                             float* __restrict__ delta, int S_q,
-                                                            int S_pad, long long rows_pad) {
-    constexpr int PER_LANE = D / 32;                  // 2 or 4 elements
-    const long long r = static_cast<long long>(blockIdx.x) * 8 + (threadIdx.x >> 5);
+                                                            int S_pad, long long rows_pad, int H,
+                                                            RowLayout o_lay, RowLayout do_lay) {
+    constexpr int LPR = D / 8;                        // lanes per row, 8 elements each
+    constexpr int RPI = 32 / LPR;                     // rows per load instruction
+    const long long warp_id = static_cast<long long>(blockIdx.x) * 8 + (threadIdx.x >> 5);
     const int lane = threadIdx.x & 31;
-    if (r >= rows_pad) return;
-    const long long bh = r / S_pad;
-    const int i = static_cast<int>(r - bh * S_pad);
-    if (i >= S_q) {
-        if (lane == 0) {
-            delta[r] = 0.f;
-            lse2[r] = __int_as_float(0x7f800000);
+    const int sub = lane / LPR;
+    const int col = (lane % LPR) * 8;
+    uint4 ov[kPrepIters], dv[kPrepIters];
+    long long rr[kPrepIters];
+    int ii[kPrepIters];
+    long long bb[kPrepIters];
+#pragma unroll
+    for (int it = 0; it < kPrepIters; ++it) {
+        const long long r = warp_id * (RPI * kPrepIters) + it * RPI + sub;
+        rr[it] = r;
+        ov[it] = make_uint4(0, 0, 0, 0);
+        dv[it] = make_uint4(0, 0, 0, 0);
+        const long long bh = r / S_pad;
+        const int i = static_cast<int>(r - bh * S_pad);
+        ii[it] = i;
+        bb[it] = bh;
+        if (r < rows_pad && i < S_q) {
+            const long long b_ = bh / H, h_ = bh - b_ * H;
+            ov[it] = *reinterpret_cast<const uint4*>(
+                o + (b_ * o_lay.batch + h_ * o_lay.head + i * o_lay.row + col));
+            dv[it] = *reinterpret_cast<const uint4*>(
+                dout + (b_ * do_lay.batch + h_ * do_lay.head + i * do_lay.row + col));
         }
-        return;
-    }
-    const size_t off = (static_cast<size_t>(bh) * S_q + i) * D + lane * PER_LANE;
-    float acc = 0.f;
-    uint32_t ow[PER_LANE / 2], dw[PER_LANE / 2];
-    if constexpr (PER_LANE == 2) {
-        ow[0] = *reinterpret_cast<const uint32_t*>(o + off);
-        dw[0] = *reinterpret_cast<const uint32_t*>(dout + off);
-    } else {
-        const uint2 a = *reinterpret_cast<const uint2*>(o + off);
-        const uint2 b = *reinterpret_cast<const uint2*>(dout + off);
-        ow[0] = a.x;
-        ow[1] = a.y;
-        dw[0] = b.x;
-        dw[1] = b.y;
     }
 #pragma unroll
-    for (int w = 0; w < PER_LANE / 2; ++w) {
-        float o0, o1, d0, d1;
-        if (BF16) {
-            o0 = __uint_as_float(ow[w] << 16); o1 = __uint_as_float(ow[w] & 0xffff0000u);
-            d0 = __uint_as_float(dw[w] << 16); d1 = __uint_as_float(dw[w] & 0xffff0000u);
-        } else {
-            const __half2 oh = *reinterpret_cast<const __half2*>(&ow[w]);
-            const __half2 dh = *reinterpret_cast<const __half2*>(&dw[w]);
-            const float2 of = __half22float2(oh), df = __half22float2(dh);
-            o0 = of.x; o1 = of.y; d0 = df.x; d1 = df.y;
-        }
-        acc = fmaf(o0, d0, acc);
-        acc = fmaf(o1, d1, acc);
-    }
+    for (int it = 0; it < kPrepIters; ++it) {
+        float acc = dot8(ov[it], dv[it], BF16, 0.f);
 #pragma unroll
-    for (int sh = 16; sh > 0; sh >>= 1) acc += __shfl_xor_sync(0xffffffffu, acc, sh);
-    if (lane == 0) {
-        delta[r] = acc;
-        lse2[r] = lse[static_cast<size_t>(bh) * S_q + i] * 1.4426950408889634f;
+        for (int sh = LPR / 2; sh > 0; sh >>= 1) acc += __shfl_xor_sync(0xffffffffu, acc, sh);
+        if (lane % LPR == 0 && rr[it] < rows_pad) {
+            if (ii[it] < S_q) {
+                delta[rr[it]] = acc;
+                lse2[rr[it]] = lse[static_cast<size_t>(bb[it]) * S_q + ii[it]] * 1.4426950408889634f;
+            } else {
+                delta[rr[it]] = 0.f;
+                lse2[rr[it]] = __int_as_float(0x7f800000);
+            }
+        }
     }
 }
 
@@ -230,9 +252,10 @@ __global__ void __launch_bounds__(BwdTile<D>::THREADS, 1)
                          const __grid_constant__ CUtensorMap tm_q,    // box 64 × 64
                          const __grid_constant__ CUtensorMap tm_do,   // box 64 × 64
                          const float* __restrict__ lse2, const float* __restrict__ delta,
-                         uint16_t* __restrict__ dk, uint16_t* __restrict__ dv, int S_q, int S_k,
-                         int BH, int S_pad, int head_group, float scale, float scale_log2,
-                         unsigned int* __restrict__ status) {
+                         uint16_t* __restrict__ dk, uint16_t* __restrict__ dv, RowLayout dk_lay,
+                         RowLayout dv_lay, int S_q, int S_k, int BHkv, int H, int kv_group,
+                         int S_pad, int head_group, int causal_off, float scale,
+                         float scale_log2, unsigned int* __restrict__ status) {
     using T = BwdTile<D>;
     using namespace sm100;
 
@@ -259,12 +282,26 @@ __global__ void __launch_bounds__(BwdTile<D>::THREADS, 1)
     const int lane = threadIdx.x & 31;
     const int n_kt = (S_k + T::BU - 1) / T::BU;
     const int n_qs = (S_q + T::BS - 1) / T::BS;
-    const int n_units = BH * n_kt;
-    // Query steps of key tile kt: causal skips query rows that see none of its keys.
-    auto unit_info = [&](int L, int& bh, int& kt, int& q_begin, int& n) {
-        bwd_unit_coords<CAUSAL, true>(L, BH, n_kt, head_group, bh, kt);
-        q_begin = CAUSAL ? min(n_qs, kt * (T::BU / T::BS)) : 0;
-        n = n_qs - q_begin;
+    const int n_units = BHkv * n_kt;
+    const int H_kv = H / kv_group;
+    // A unit is (batch, key/value head, key tile); its steps run over the
+    // kv_group query heads that read this head, each over its query tiles.
+    // Causal: query rows that see none of the tile's keys are skipped.
+    auto unit_info = [&](int L, int& b, int& hk, int& kt, int& q_begin, int& n) {
+        int bhk;
+        bwd_unit_coords<CAUSAL, true>(L, BHkv, n_kt, head_group, bhk, kt);
+        b = bhk / H_kv;
+        hk = bhk - b * H_kv;
+        q_begin = CAUSAL ? min(n_qs, max(0, kt * T::BU - causal_off) / T::BS) : 0;
+        n = (n_qs - q_begin) * kv_group;
+    };
+    // Steps of a unit visit query tiles q_begin .. n_qs-1 of each query head of
+    // the group in turn; advance (h, qi) to the next step.
+    auto next_step = [&](int q_begin, int& h, int& qi) {
+        if (++qi == n_qs) {
+            qi = q_begin;
+            ++h;
+        }
     };
     auto unit_of_round = [&](int r) {
         const int G = static_cast<int>(gridDim.x);
@@ -314,8 +351,8 @@ __global__ void __launch_bounds__(BwdTile<D>::THREADS, 1)
         for (int r = 0; r * static_cast<int>(gridDim.x) < n_units && ok; ++r) {
             const int L = unit_of_round(r);
             if (L >= n_units) continue;
-            int bh, kt, q_begin, n;
-            unit_info(L, bh, kt, q_begin, n);
+            int b, hk, kt, q_begin, n;
+            unit_info(L, b, hk, kt, q_begin, n);
             if (n == 0) continue;
             ok = mbar_wait(kv_empty, (uk & 1) ^ 1, abort_flag, status, kStatusBwdProducer);
             ok = __all_sync(0xffffffffu, ok);
@@ -325,29 +362,30 @@ __global__ void __launch_bounds__(BwdTile<D>::THREADS, 1)
                 mbar_arrive_expect_tx(kv_full, 2 * T::BIG_TILE);
 #pragma unroll
                 for (int c = 0; c < T::CHUNKS; ++c) {
-                    tma_load_3d(sK + c * T::BIG_CHUNK, &tm_k, kv_full, c * 64, kt * T::BU, bh);
-                    tma_load_3d(sV + c * T::BIG_CHUNK, &tm_v, kv_full, c * 64, kt * T::BU, bh);
+                    tma_load_4d(sK + c * T::BIG_CHUNK, &tm_k, kv_full, c * 64, kt * T::BU, hk, b);
+                    tma_load_4d(sV + c * T::BIG_CHUNK, &tm_v, kv_full, c * 64, kt * T::BU, hk, b);
                 }
             }
             __syncwarp();
-            for (int t = 0; t < n && ok; ++t) {
+            int h = hk * kv_group, qi = q_begin;
+            for (int t = 0; t < n && ok; ++t, next_step(q_begin, h, qi)) {
                 const int slot = idx % T::NS;
                 ok = mbar_wait(&slot_empty[slot], ((idx / T::NS) & 1) ^ 1, abort_flag, status,
                                kStatusBwdProducer);
                 ok = __all_sync(0xffffffffu, ok);
                 if (!ok) break;
                 if (leader) {
-                    const int q0 = (q_begin + t) * T::BS;
+                    const int q0 = qi * T::BS;
                     uint8_t* dst = sRing + slot * T::SLOT_BYTES;
                     float* st = sStat + slot * T::STAT_FLOATS;
-                    const size_t soff = static_cast<size_t>(bh) * S_pad + q0;
+                    const size_t soff = (static_cast<size_t>(b) * H + h) * S_pad + q0;
                     mbar_arrive_expect_tx(&slot_full[slot], T::SLOT_BYTES + T::STAT_FLOATS * 4);
 #pragma unroll
                     for (int c = 0; c < T::CHUNKS; ++c) {
-                        tma_load_3d(dst + c * T::SMALL_CHUNK, &tm_q, &slot_full[slot], c * 64, q0,
-                                    bh);
-                        tma_load_3d(dst + T::SMALL_TILE + c * T::SMALL_CHUNK, &tm_do,
-                                    &slot_full[slot], c * 64, q0, bh);
+                        tma_load_4d(dst + c * T::SMALL_CHUNK, &tm_q, &slot_full[slot], c * 64, q0,
+                                    h, b);
+                        tma_load_4d(dst + T::SMALL_TILE + c * T::SMALL_CHUNK, &tm_do,
+                                    &slot_full[slot], c * 64, q0, h, b);
                     }
                     bulk_load(st, lse2 + soff, T::BS * 4, &slot_full[slot]);
                     bulk_load(st + T::BS, delta + soff, T::BS * 4, &slot_full[slot]);
@@ -434,8 +472,8 @@ __global__ void __launch_bounds__(BwdTile<D>::THREADS, 1)
         for (int r = 0; r * static_cast<int>(gridDim.x) < n_units && ok; ++r) {
             const int L = unit_of_round(r);
             if (L >= n_units) continue;
-            int bh, kt, q_begin, n;
-            unit_info(L, bh, kt, q_begin, n);
+            int b, hk, kt, q_begin, n;
+            unit_info(L, b, hk, kt, q_begin, n);
             if (n == 0) continue;
             ok = mbar_wait(kv_full, uk & 1, abort_flag, status, kStatusBwdMma);
             ok = __all_sync(0xffffffffu, ok);
@@ -503,42 +541,47 @@ __global__ void __launch_bounds__(BwdTile<D>::THREADS, 1)
         for (int r = 0; r * static_cast<int>(gridDim.x) < n_units && ok; ++r) {
             const int L = unit_of_round(r);
             if (L >= n_units) continue;
-            int bh, kt, q_begin, n;
-            unit_info(L, bh, kt, q_begin, n);
+            int b, hk, kt, q_begin, n;
+            unit_info(L, b, hk, kt, q_begin, n);
             const int key = kt * T::BU + row;
-            const size_t out_off = (static_cast<size_t>(bh) * S_k + key) * D;
+            uint16_t* dk_row = dk + static_cast<size_t>(b * dk_lay.batch + hk * dk_lay.head +
+                                                        static_cast<long long>(key) * dk_lay.row);
+            uint16_t* dv_row = dv + static_cast<size_t>(b * dv_lay.batch + hk * dv_lay.head +
+                                                        static_cast<long long>(key) * dv_lay.row);
             if (n == 0) {
                 // No query sees these keys: their gradients are zero.
                 if (key < S_k) {
-                    uint4* a = reinterpret_cast<uint4*>(dk + out_off);
-                    uint4* b = reinterpret_cast<uint4*>(dv + out_off);
+                    uint4* pa = reinterpret_cast<uint4*>(dk_row);
+                    uint4* pb = reinterpret_cast<uint4*>(dv_row);
                     for (int i = 0; i < D / 8; ++i) {
-                        a[i] = make_uint4(0, 0, 0, 0);
-                        b[i] = make_uint4(0, 0, 0, 0);
+                        pa[i] = make_uint4(0, 0, 0, 0);
+                        pb[i] = make_uint4(0, 0, 0, 0);
                     }
                 }
                 continue;
             }
-            for (int t = 0; t < n; ++t) {
+            int h = hk * kv_group, qi = q_begin;
+            for (int t = 0; t < n; ++t, next_step(q_begin, h, qi)) {
                 const uint32_t s = gs + static_cast<uint32_t>(t);
-                const int b = static_cast<int>(s & 1);
+                const int buf = static_cast<int>(s & 1);
                 const int slot = static_cast<int>(s % T::NS);
-                ok = mbar_wait(&s_full[b], (s >> 1) & 1, abort_flag, status, kStatusBwdSoftmax);
+                ok = mbar_wait(&s_full[buf], (s >> 1) & 1, abort_flag, status, kStatusBwdSoftmax);
                 if (ok) ok = mbar_wait(&slot_full[slot], (s / T::NS) & 1, abort_flag, status,
                                        kStatusBwdSoftmax);
                 ok = __all_sync(0xffffffffu, ok);
                 if (!ok) break;
                 tc_fence_after();
                 uint32_t sv[64], dpv[64];
-                tmem_ld64(lane_base + T::S_COL + b * 64, sv);
-                tmem_ld64(lane_base + T::DP_COL + b * 64, dpv);
+                tmem_ld64(lane_base + T::S_COL + buf * 64, sv);
+                tmem_ld64(lane_base + T::DP_COL + buf * 64, dpv);
                 const float* st = sStat + slot * T::STAT_FLOATS;
-                const int q0 = (q_begin + t) * T::BS;
-                // key > query is masked; only steps that reach below the diagonal need it
-                const bool masked = CAUSAL && q0 < kt * T::BU + T::BU - 1;
+                const int q0 = qi * T::BS;
+                // key > query + causal_off is masked; only steps that reach below the
+                // diagonal need it
+                const bool masked = CAUSAL && q0 + causal_off < kt * T::BU + T::BU - 1;
                 uint32_t pk_p[32], pk_ds[32];
                 if (masked) {
-                    const int lim = key - q0;                  // visible iff c >= lim
+                    const int lim = key - q0 - causal_off;     // visible iff c >= lim
                     grad_pack64<true, BF16, true, true>(sv, dpv, st, st + T::BS, 0.f, 0.f,
                                                         scale_log2,
                                                         [&](int c) { return c >= lim; }, pk_p, pk_ds);
@@ -547,12 +590,12 @@ __global__ void __launch_bounds__(BwdTile<D>::THREADS, 1)
                                                          scale_log2, [](int) { return true; },
                                                          pk_p, pk_ds);
                 }
-                tmem_st32(lane_base + T::S_COL + b * 64 + T::PK_OFF, pk_p);
-                tmem_st32(lane_base + T::DP_COL + b * 64 + T::PK_OFF, pk_ds);
+                tmem_st32(lane_base + T::S_COL + buf * 64 + T::PK_OFF, pk_p);
+                tmem_st32(lane_base + T::DP_COL + buf * 64 + T::PK_OFF, pk_ds);
                 tmem_st_wait();
                 tc_fence_before();
                 __syncwarp();
-                if (lane == 0) mbar_arrive(&p_full[b]);
+                if (lane == 0) mbar_arrive(&p_full[buf]);
             }
             if (!ok) break;
             gs += static_cast<uint32_t>(n);
@@ -562,8 +605,8 @@ __global__ void __launch_bounds__(BwdTile<D>::THREADS, 1)
             if (!ok) break;
             tc_fence_after();
             const bool store = key < S_k;
-            store_row_from_tmem<D, BF16>(lane_base + T::ACC_COL, 1.f, dv + out_off, store);
-            store_row_from_tmem<D, BF16>(lane_base + T::ACC_COL + D, scale, dk + out_off, store);
+            store_row_from_tmem<D, BF16>(lane_base + T::ACC_COL, 1.f, dv_row, store);
+            store_row_from_tmem<D, BF16>(lane_base + T::ACC_COL + D, scale, dk_row, store);
         }
     }
     tc_fence_before();
@@ -613,9 +656,9 @@ __global__ void __launch_bounds__(DqTile<D>::THREADS, 1)
                        const __grid_constant__ CUtensorMap tm_k,    // box 64 × 128
                        const __grid_constant__ CUtensorMap tm_v,    // box 64 × 128
                        const float* __restrict__ lse2, const float* __restrict__ delta,
-                       uint16_t* __restrict__ dq, int S_q, int S_k, int BH, int S_pad,
-                       int head_group, float scale, float scale_log2,
-                       unsigned int* __restrict__ status) {
+                       uint16_t* __restrict__ dq, RowLayout dq_lay, int S_q, int S_k, int BH,
+                       int H, int kv_group, int S_pad, int head_group, int causal_off,
+                       float scale, float scale_log2, unsigned int* __restrict__ status) {
     using T = DqTile<D>;
     using namespace sm100;
 
@@ -650,8 +693,8 @@ __global__ void __launch_bounds__(DqTile<D>::THREADS, 1)
         bwd_unit_coords<CAUSAL, false>(L, BH, n_qt, head_group, bh, qt);
         n = n_ks;
         if (CAUSAL) {
-            const int last_row = min(qt * T::BU + T::BU, S_q) - 1;
-            n = min(n_ks, last_row / T::BS + 1);
+            const int last_key = min(qt * T::BU + T::BU, S_q) - 1 + causal_off;
+            n = min(n_ks, last_key / T::BS + 1);
         }
     };
     auto unit_of_round = [&](int r) {
@@ -705,7 +748,7 @@ __global__ void __launch_bounds__(DqTile<D>::THREADS, 1)
         int uq = 0;
         // One tile into ring slot idx % SLOTS once its previous use is released.
         auto load = [&](const CUtensorMap* map, uint8_t* ring, uint64_t* full, uint64_t* empty,
-                        int slots, int& idx, int row, int bh) {
+                        int slots, int& idx, int row, int hk, int b) {
             if (!ok) return;
             const int slot = idx % slots;
             ok = mbar_wait(&empty[slot], ((idx / slots) & 1) ^ 1, abort_flag, status,
@@ -716,8 +759,8 @@ __global__ void __launch_bounds__(DqTile<D>::THREADS, 1)
                 mbar_arrive_expect_tx(&full[slot], T::TILE);
 #pragma unroll
                 for (int c = 0; c < T::CHUNKS; ++c)
-                    tma_load_3d(ring + slot * T::TILE + c * T::CHUNK, map, &full[slot], c * 64,
-                                row, bh);
+                    tma_load_4d(ring + slot * T::TILE + c * T::CHUNK, map, &full[slot], c * 64,
+                                row, hk, b);
             }
             __syncwarp();
             ++idx;
@@ -727,6 +770,7 @@ __global__ void __launch_bounds__(DqTile<D>::THREADS, 1)
             if (L >= n_units) continue;
             int bh, qt, n;
             unit_info(L, bh, qt, n);
+            const int b = bh / H, h = bh - b * H, hk = h / kv_group;
             ok = mbar_wait(q_empty, (uq & 1) ^ 1, abort_flag, status, kStatusBwdProducer);
             ok = __all_sync(0xffffffffu, ok);
             if (!ok) break;
@@ -735,14 +779,14 @@ __global__ void __launch_bounds__(DqTile<D>::THREADS, 1)
                 mbar_arrive_expect_tx(q_full, 2 * T::TILE);
 #pragma unroll
                 for (int c = 0; c < T::CHUNKS; ++c) {
-                    tma_load_3d(sQ + c * T::CHUNK, &tm_q, q_full, c * 64, qt * T::BU, bh);
-                    tma_load_3d(sdO + c * T::CHUNK, &tm_do, q_full, c * 64, qt * T::BU, bh);
+                    tma_load_4d(sQ + c * T::CHUNK, &tm_q, q_full, c * 64, qt * T::BU, h, b);
+                    tma_load_4d(sdO + c * T::CHUNK, &tm_do, q_full, c * 64, qt * T::BU, h, b);
                 }
             }
             __syncwarp();
             for (int t = 0; t < n && ok; ++t) {
-                load(&tm_k, sKr, k_full, k_empty, T::KS, kidx, t * T::BS, bh);
-                load(&tm_v, sVr, v_full, v_empty, T::VS, vidx, t * T::BS, bh);
+                load(&tm_k, sKr, k_full, k_empty, T::KS, kidx, t * T::BS, hk, b);
+                load(&tm_v, sVr, v_full, v_empty, T::VS, vidx, t * T::BS, hk, b);
             }
         }
         if (*abort_flag && leader) {
@@ -933,8 +977,9 @@ __global__ void __launch_bounds__(DqTile<D>::THREADS, 1)
                 tc_fence_after();
                 const int kv0 = t * T::BS;
                 const bool masked =
-                    (CAUSAL && kv0 + T::BS - 1 > row_begin) || (kv0 + T::BS > S_k);
-                const int lim = masked ? min(S_k, CAUSAL ? q_idx + 1 : S_k) - kv0 : T::BS;
+                    (CAUSAL && kv0 + T::BS - 1 > row_begin + causal_off) || (kv0 + T::BS > S_k);
+                const int lim =
+                    masked ? min(S_k, CAUSAL ? q_idx + 1 + causal_off : S_k) - kv0 : T::BS;
                 const uint32_t sb = lane_base + T::S_COL + b * 128;
                 // Two halves of 64 keys; dS of half h goes to columns 32h..32h+31
                 // of S_b, which have been read by then.
@@ -975,9 +1020,12 @@ __global__ void __launch_bounds__(DqTile<D>::THREADS, 1)
             ++uq;
             if (!ok) break;
             tc_fence_after();
-            store_row_from_tmem<D, BF16>(lane_base + T::ACC_COL, scale,
-                                         dq + (static_cast<size_t>(bh) * S_q + q_idx) * D,
-                                         q_idx < S_q);
+            const int b = bh / H, h = bh - b * H;
+            store_row_from_tmem<D, BF16>(
+                lane_base + T::ACC_COL, scale,
+                dq + static_cast<size_t>(b * dq_lay.batch + h * dq_lay.head +
+                                         static_cast<long long>(q_idx) * dq_lay.row),
+                q_idx < S_q);
         }
     }
     tc_fence_before();
@@ -994,11 +1042,12 @@ cudaError_t launch_attn_bwd(const BwdArgs& a, cudaStream_t stream) {
     using T = BwdTile<D>;
     // D and LSE·log2e into the padded workspace.
     const long long rows_pad = static_cast<long long>(a.BH) * a.S_pad;
-    const long long pblocks = (rows_pad + 7) / 8;
+    const long long rows_per_block = 8LL * prep_rows_per_warp<D>();
+    const long long pblocks = (rows_pad + rows_per_block - 1) / rows_per_block;
     if (pblocks > 0x7fffffffLL) return cudaErrorInvalidConfiguration;
     attn_bwd_prep_kernel<D, BF16><<<static_cast<unsigned>(pblocks), 256, 0, stream>>>(
         static_cast<const uint16_t*>(a.o), static_cast<const uint16_t*>(a.dout), a.lse, a.lse2,
-        a.delta, a.S_q, a.S_pad, rows_pad);
+        a.delta, a.S_q, a.S_pad, rows_pad, a.H, a.o_lay, a.do_lay);
     cudaError_t err = cudaGetLastError();
     if (err != cudaSuccess) return err;
 
@@ -1009,13 +1058,16 @@ cudaError_t launch_attn_bwd(const BwdArgs& a, cudaStream_t stream) {
     err = cudaFuncSetAttribute(kdkdv, cudaFuncAttributeMaxDynamicSharedMemorySize, T::SMEM_BYTES);
     if (err != cudaSuccess) return err;
     const int n_kt = (a.S_k + T::BU - 1) / T::BU;
-    const long long units_kv = static_cast<long long>(a.BH) * n_kt;
+    const int bh_kv = a.BH / a.kv_group;
+    const long long units_kv = static_cast<long long>(bh_kv) * n_kt;
     if (units_kv > 0x7fffffffLL) return cudaErrorInvalidConfiguration;
-    const int hg_kv = static_cast<int>(std::max<long long>(1, group_bytes / (op_bytes * a.S_q)));
+    const int hg_kv = static_cast<int>(
+        std::max<long long>(1, group_bytes / (op_bytes * a.S_q * a.kv_group)));
     kdkdv<<<static_cast<int>(std::min<long long>(units_kv, a.num_sms)), T::THREADS, T::SMEM_BYTES,
             stream>>>(a.tm_k_fixed, a.tm_v_fixed, a.tm_q_step, a.tm_do_step, a.lse2, a.delta,
-                      static_cast<uint16_t*>(a.dk), static_cast<uint16_t*>(a.dv), a.S_q, a.S_k,
-                      a.BH, a.S_pad, hg_kv, a.scale, a.scale_log2, a.status);
+                      static_cast<uint16_t*>(a.dk), static_cast<uint16_t*>(a.dv), a.dk_lay,
+                      a.dv_lay, a.S_q, a.S_k, bh_kv, a.H, a.kv_group, a.S_pad, hg_kv,
+                      a.causal_off, a.scale, a.scale_log2, a.status);
     err = cudaGetLastError();
     if (err != cudaSuccess) return err;
 
@@ -1029,8 +1081,8 @@ cudaError_t launch_attn_bwd(const BwdArgs& a, cudaStream_t stream) {
     const int hg_q = static_cast<int>(std::max<long long>(1, group_bytes / (op_bytes * a.S_k)));
     kdq<<<static_cast<int>(std::min<long long>(units_q, a.num_sms)), TQ::THREADS, TQ::SMEM_BYTES,
           stream>>>(a.tm_q_fixed, a.tm_do_fixed, a.tm_k_fixed, a.tm_v_fixed, a.lse2, a.delta,
-                    static_cast<uint16_t*>(a.dq), a.S_q, a.S_k, a.BH, a.S_pad, hg_q, a.scale,
-                    a.scale_log2, a.status);
+                    static_cast<uint16_t*>(a.dq), a.dq_lay, a.S_q, a.S_k, a.BH, a.H, a.kv_group,
+                    a.S_pad, hg_q, a.causal_off, a.scale, a.scale_log2, a.status);
     return cudaGetLastError();
 }
 

@@ -101,13 +101,19 @@ cudaError_t launch_attn_combine(const float* o_part, const float* lse_part, void
                                 int n_split, long long rows, int d, bool bf16,
                                 cudaStream_t stream);
 
+// Element strides of a [B, heads, S, d] tensor (d contiguous).
+struct RowLayout {
+    long long batch, head, row;
+};
+
 // Backward launch contract (attn_bwd.cuh).  The dK/dV kernel keeps 128-row K
 // and V tiles and streams 64-row Q and dO steps; the dQ kernel keeps 128-row
 // Q and dO tiles and streams 128-row K and V steps.
 struct BwdArgs {
-    CUtensorMap tm_k_fixed, tm_v_fixed;   // [B·H, S_k, d], box 64 × 128
-    CUtensorMap tm_q_step, tm_do_step;    // [B·H, S_q, d], box 64 × 64
-    CUtensorMap tm_q_fixed, tm_do_fixed;  // [B·H, S_q, d], box 64 × 128
+    // 4-D maps (d, S, heads, B) in each tensor's own layout
+    CUtensorMap tm_k_fixed, tm_v_fixed;   // K, V: (d, S_k, H_kv, B), box 64 × 128
+    CUtensorMap tm_q_step, tm_do_step;    // Q, dO: (d, S_q, H, B), box 64 × 64
+    CUtensorMap tm_q_fixed, tm_do_fixed;  // Q, dO: (d, S_q, H, B), box 64 × 128
     const void* o;                        // forward output [B, H, S_q, d]
     const void* dout;                     // dO [B, H, S_q, d]
     const float* lse;                     // forward LSE [B, H, S_q], natural log
@@ -116,7 +122,11 @@ struct BwdArgs {
     void* dq;
     void* dk;
     void* dv;
+    RowLayout o_lay, do_lay, dq_lay, dk_lay, dv_lay;
     int32_t S_q, S_k, BH, S_pad;          // S_pad = S_q rounded up to 128
+    int32_t H;                            // query heads
+    int32_t kv_group;                     // query heads per key/value head
+    int32_t causal_off;                   // key j visible to query i iff j <= i + causal_off
     float scale, scale_log2;
     int32_t num_sms;
     unsigned int* status;

@@ -269,6 +269,37 @@ attn_status_t attn_bwd(const void* q, const void* k, const void* v, const void* 
                        struct CUstream_st* stream);
 
 /*
+ * attn_bwd_general — attn_bwd over general layouts, grouped key/value heads
+ * and a choice of causal alignment (the same rules as attn_fwd_general).  dk
+ * and dv are the gradients of the H_kv key/value heads: each sums the
+ * contributions of the H / H_kv query heads that read it.  Every output
+ * layout must map distinct elements to distinct addresses; outputs and the
+ * workspace must not overlap anything.  The workspace size is the one
+ * attn_bwd_workspace_size reports for (B, H, S_q, S_k, d).
+ */
+typedef struct {
+    const void* q;
+    const void* k;
+    const void* v;
+    const void* o;            /* the forward's output for these inputs */
+    const float* lse;         /* the forward's LSE, dense [B, H, S_q] */
+    const void* dout;         /* dO, [B, H, S_q, d] in do_layout */
+    void* dq;                 /* [B, H, S_q, d] in dq_layout; written */
+    void* dk;                 /* [B, H_kv, S_k, d] in dk_layout; written */
+    void* dv;                 /* [B, H_kv, S_k, d] in dv_layout; written */
+    int64_t B, H, H_kv, S_q, S_k, d;
+    attn_layout_t q_layout, k_layout, v_layout, o_layout, do_layout, dq_layout, dk_layout,
+        dv_layout;
+    int mask;                 /* attn_mask_t */
+    float scale;
+    attn_dtype_t dtype;
+    void* workspace;
+    int64_t workspace_bytes;
+} attn_bwd_params_t;
+
+attn_status_t attn_bwd_general(const attn_bwd_params_t* params, struct CUstream_st* stream);
+
+/*
  * attn_fwd_splitkv_noalloc — attn_fwd_splitkv without a caller workspace and
  * without allocating anything.
  *

@@ -26,7 +26,8 @@ P, O and D formed exactly in fp64 (not read back from a rounded forward):
     dQ = scale·dS·K      dK = scale·dSᵀ·Q
 
 Readings (listed in the design doc): masking and its top-left alignment as in the
-forward oracle; D computed as rowsum(dO ∘ O); the scale applied to dQ and dK.
+forward oracle (``bottom_right`` shifts it by S_k − S_q, as there); D computed
+as rowsum(dO ∘ O); the scale applied to dQ and dK.
 """
 
 from __future__ import annotations
@@ -38,7 +39,8 @@ from .attention import _as_f64
 __all__ = ["attention_backward", "backward_terms"]
 
 
-def backward_terms(q_bh, k_bh, v_bh, do_bh, causal: bool = False, scale: float | None = None):
+def backward_terms(q_bh, k_bh, v_bh, do_bh, causal: bool = False, scale: float | None = None,
+                   bottom_right: bool = False):
     """Every intermediate of one head's backward: P, O, D, dP, dS, dQ, dK, dV (fp64).
 
     ``q_bh [S_q,d]``, ``k_bh [S_k,d]``, ``v_bh [S_k,d_v]``, ``do_bh [S_q,d_v]``.
@@ -48,9 +50,10 @@ def backward_terms(q_bh, k_bh, v_bh, do_bh, causal: bool = False, scale: float |
         scale = 1.0 / np.sqrt(q.shape[1])
     s = scale * (q @ k.T)
     if causal:
+        offset = k.shape[0] - q.shape[0] if bottom_right else 0
         i = np.arange(q.shape[0])[:, None]
         j = np.arange(k.shape[0])[None, :]
-        s = np.where(j > i, -np.inf, s)
+        s = np.where(j > i + offset, -np.inf, s)
     m = s.max(axis=1, keepdims=True)
     e = np.exp(s - m)
     p = e / e.sum(axis=1, keepdims=True)        # masked entries are exactly 0
@@ -64,7 +67,8 @@ def backward_terms(q_bh, k_bh, v_bh, do_bh, causal: bool = False, scale: float |
     return {"P": p, "O": o, "D": dd, "dP": dp, "dS": ds, "dQ": dq, "dK": dk, "dV": dv}
 
 
-def attention_backward(q, k, v, do, causal: bool = False, scale: float | None = None):
+def attention_backward(q, k, v, do, causal: bool = False, scale: float | None = None,
+                       bottom_right: bool = False):
     """dQ, dK, dV (fp64) of Σ O∘dO for ``q [B,H,S_q,d]``, ``k, v [B,H,S_k,d]``, ``do [B,H,S_q,d]``."""
     q, k, v, do = _as_f64(q), _as_f64(k), _as_f64(v), _as_f64(do)
     B, H, S_q, d = q.shape
@@ -73,6 +77,6 @@ def attention_backward(q, k, v, do, causal: bool = False, scale: float | None = 
     dq, dk, dv = np.empty_like(q), np.empty_like(k), np.empty_like(v)
     for b in range(B):
         for h in range(H):
-            t = backward_terms(q[b, h], k[b, h], v[b, h], do[b, h], causal, scale)
+            t = backward_terms(q[b, h], k[b, h], v[b, h], do[b, h], causal, scale, bottom_right)
             dq[b, h], dk[b, h], dv[b, h] = t["dQ"], t["dK"], t["dV"]
     return dq, dk, dv

@@ -38,7 +38,7 @@ def test_header_declares_the_boundary():
     names = _declared_functions()
     assert names == sorted(["attn_fwd", "attn_fwd_general", "attn_fwd_host", "attn_fwd_plan", "attn_fwd_splitkv_plan",
                             "attn_fwd_splitkv", "attn_fwd_splitkv_noalloc", "attn_bwd_workspace_size",
-                            "attn_bwd", "attn_last_error", "attn_get_device_status",
+                            "attn_bwd", "attn_bwd_general", "attn_last_error", "attn_get_device_status",
                             "attn_version"])
 
 

@@ -27,8 +27,8 @@ def _rand(*shape):
     return RNG.standard_normal(shape)
 
 
-def _loss(q, k, v, do, causal, scale):
-    o, _ = oracle.attention_forward(q, k, v, causal=causal, scale=scale)
+def _loss(q, k, v, do, causal, scale, bottom_right=False):
+    o, _ = oracle.attention_forward(q, k, v, causal=causal, scale=scale, bottom_right=bottom_right)
     return float((o * do).sum())
 
 
@@ -51,6 +51,24 @@ def pin_finite_differences():
                 x[idx] = x0
                 num[idx] = (lp - lm) / (2 * h)
             np.testing.assert_allclose(g, num, rtol=0, atol=2e-7)
+
+
+def pin_finite_differences_bottom_right():
+    """The shifted mask (S_q = 3 against S_k = 5) against differences of the forward oracle."""
+    h = 1e-6
+    q, k, v, do = _rand(1, 1, 3, 3), _rand(1, 1, 5, 3), _rand(1, 1, 5, 2), _rand(1, 1, 3, 2)
+    dq, dk, dv = oab.attention_backward(q, k, v, do, causal=True, scale=0.6, bottom_right=True)
+    for x, g in ((q, dq), (k, dk), (v, dv)):
+        num = np.zeros_like(x)
+        for idx in np.ndindex(x.shape):
+            x0 = x[idx]
+            x[idx] = x0 + h
+            lp = _loss(q, k, v, do, True, 0.6, True)
+            x[idx] = x0 - h
+            lm = _loss(q, k, v, do, True, 0.6, True)
+            x[idx] = x0
+            num[idx] = (lp - lm) / (2 * h)
+        np.testing.assert_allclose(g, num, rtol=0, atol=2e-7)
 
 
 def pin_torch_autograd():
@@ -101,7 +119,8 @@ def pin_two_forms_of_d():
         np.testing.assert_allclose(t["O"], o, atol=1e-13)
 
 
-PINS = [pin_finite_differences, pin_torch_autograd, pin_invariants, pin_two_forms_of_d]
+PINS = [pin_finite_differences, pin_finite_differences_bottom_right, pin_torch_autograd,
+        pin_invariants, pin_two_forms_of_d]
 
 
 @pytest.mark.parametrize("pin", PINS, ids=lambda f: f.__name__)
@@ -121,8 +140,10 @@ def test_default_scale_is_inverse_sqrt_d():
 def _mutant(kind):
     real = oab.backward_terms
 
-    def terms(q_bh, k_bh, v_bh, do_bh, causal=False, scale=None):
-        t = real(q_bh, k_bh, v_bh, do_bh, causal, scale)
+    def terms(q_bh, k_bh, v_bh, do_bh, causal=False, scale=None, bottom_right=False):
+        if kind == "offset_ignored":
+            bottom_right = False
+        t = real(q_bh, k_bh, v_bh, do_bh, causal, scale, bottom_right)
         sc = 1.0 / np.sqrt(np.shape(q_bh)[1]) if scale is None else scale
         q, k = oab._as_f64(q_bh), oab._as_f64(k_bh)
         if kind == "no_D":
@@ -144,14 +165,14 @@ def _mutant(kind):
             t["dQ"], t["dK"] = sc * ds @ k, sc * ds.T @ q
         elif kind == "mask_ignored":
             if causal:
-                u = real(q_bh, k_bh, v_bh, do_bh, False, scale)
+                u = real(q_bh, k_bh, v_bh, do_bh, False, scale, bottom_right)
                 t["dQ"], t["dK"], t["dV"] = u["dQ"], u["dK"], u["dV"]
         return t
     return terms
 
 
 MUTANTS = ["no_D", "D_sign", "no_scale_dk", "no_scale_dq", "dq_with_q", "dv_unnormalised",
-           "D_from_dO_only", "mask_ignored"]
+           "D_from_dO_only", "mask_ignored", "offset_ignored"]
 
 
 @pytest.mark.parametrize("kind", MUTANTS)
