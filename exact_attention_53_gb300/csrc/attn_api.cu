@@ -506,6 +506,38 @@ attn_status_t validate_bwd_head_dim(const Problem& p) {
     return ATTN_OK;
 }
 
+// Helper streams and events of the host-buffer entry point, created on a
+// device's first attn_fwd_host call and kept for the life of the process.
+struct HostPipe {
+    static constexpr int kChunks = 4;
+    std::mutex mu;
+    bool ready = false;
+    cudaStream_t in = nullptr, out = nullptr;
+    cudaEvent_t start = nullptr, out_done = nullptr;
+    cudaEvent_t in_done[kChunks] = {}, comp_done[kChunks] = {};
+};
+HostPipe g_pipes[kMaxDevices];
+
+attn_status_t host_pipe(int dev, HostPipe** out) {
+    HostPipe& pp = g_pipes[dev];
+    std::lock_guard<std::mutex> lock(pp.mu);
+    if (!pp.ready) {
+        cudaError_t e = cudaStreamCreateWithFlags(&pp.in, cudaStreamNonBlocking);
+        if (e == cudaSuccess) e = cudaStreamCreateWithFlags(&pp.out, cudaStreamNonBlocking);
+        if (e == cudaSuccess) e = cudaEventCreateWithFlags(&pp.start, cudaEventDisableTiming);
+        if (e == cudaSuccess) e = cudaEventCreateWithFlags(&pp.out_done, cudaEventDisableTiming);
+        for (int i = 0; i < HostPipe::kChunks && e == cudaSuccess; ++i) {
+            e = cudaEventCreateWithFlags(&pp.in_done[i], cudaEventDisableTiming);
+            if (e == cudaSuccess) e = cudaEventCreateWithFlags(&pp.comp_done[i], cudaEventDisableTiming);
+        }
+        if (e != cudaSuccess)
+            return fail(ATTN_ERR_CUDA, "creating the copy streams: %s", cudaGetErrorString(e));
+        pp.ready = true;
+    }
+    *out = &pp;
+    return ATTN_OK;
+}
+
 }  // namespace
 
 extern "C" {
@@ -548,15 +580,70 @@ attn_status_t attn_fwd_host(const void* q_host, const void* k_host, const void* 
         return fail(ATTN_ERR_INVALID_ARG, "q_dev, k_dev and v_dev must not overlap (they are copy targets)");
     int dev = 0;
     if ((s = check_device(&dev)) != ATTN_OK) return s;
+    HostPipe* pipe = nullptr;
+    if ((s = host_pipe(dev, &pipe)) != ATTN_OK) return s;
+    std::lock_guard<std::mutex> lock(pipe->mu);
+
+    // Heads are independent problems, so the call is cut into chunks of
+    // consecutive (b, h): chunk c's upload (helper stream `in`), its forward
+    // (the caller's stream) and its download (helper stream `out`) overlap
+    // with those of its neighbours.  Dense layouts keep each chunk contiguous.
+    const int64_t BH = B * H;
+    const size_t total = p.q_bytes + 2 * p.kv_bytes + p.o_bytes;
+    const int64_t chunks = total < (size_t(32) << 20) ? 1 : std::min<int64_t>(HostPipe::kChunks, BH);
+    const size_t q_head = static_cast<size_t>(S_q * d * 2), kv_head = static_cast<size_t>(S_k * d * 2);
+    const size_t l_head = static_cast<size_t>(S_q * 4);
     cudaError_t e;
-    if ((e = cudaMemcpyAsync(q_dev, q_host, p.q_bytes, cudaMemcpyHostToDevice, stream)) != cudaSuccess ||
-        (e = cudaMemcpyAsync(k_dev, k_host, p.kv_bytes, cudaMemcpyHostToDevice, stream)) != cudaSuccess ||
-        (e = cudaMemcpyAsync(v_dev, v_host, p.kv_bytes, cudaMemcpyHostToDevice, stream)) != cudaSuccess)
-        return fail(ATTN_ERR_CUDA, "host-to-device copy: %s", cudaGetErrorString(e));
-    if ((s = launch_checked(p, q_dev, k_dev, v_dev, o_dev, lse_dev, stream)) != ATTN_OK) return s;
-    if ((e = cudaMemcpyAsync(o_host, o_dev, p.o_bytes, cudaMemcpyDeviceToHost, stream)) != cudaSuccess ||
-        (e = cudaMemcpyAsync(lse_host, lse_dev, p.lse_bytes, cudaMemcpyDeviceToHost, stream)) != cudaSuccess)
-        return fail(ATTN_ERR_CUDA, "device-to-host copy: %s", cudaGetErrorString(e));
+    auto cuda_fail = [&](const char* what) {
+        return fail(ATTN_ERR_CUDA, "%s: %s", what, cudaGetErrorString(e));
+    };
+    // The helper streams start after everything already queued on `stream`.
+    if ((e = cudaEventRecord(pipe->start, stream)) != cudaSuccess ||
+        (e = cudaStreamWaitEvent(pipe->in, pipe->start, 0)) != cudaSuccess ||
+        (e = cudaStreamWaitEvent(pipe->out, pipe->start, 0)) != cudaSuccess)
+        return cuda_fail("ordering the copy streams");
+    for (int64_t c = 0; c < chunks; ++c) {
+        const int64_t h0 = BH * c / chunks, h1 = BH * (c + 1) / chunks;
+        const size_t n = static_cast<size_t>(h1 - h0);
+        auto at = [&](const void* base, size_t per_head) {
+            return static_cast<const char*>(base) + static_cast<size_t>(h0) * per_head;
+        };
+        if ((e = cudaMemcpyAsync(const_cast<char*>(at(q_dev, q_head)), at(q_host, q_head), n * q_head,
+                                 cudaMemcpyHostToDevice, pipe->in)) != cudaSuccess ||
+            (e = cudaMemcpyAsync(const_cast<char*>(at(k_dev, kv_head)), at(k_host, kv_head), n * kv_head,
+                                 cudaMemcpyHostToDevice, pipe->in)) != cudaSuccess ||
+            (e = cudaMemcpyAsync(const_cast<char*>(at(v_dev, kv_head)), at(v_host, kv_head), n * kv_head,
+                                 cudaMemcpyHostToDevice, pipe->in)) != cudaSuccess ||
+            (e = cudaEventRecord(pipe->in_done[c], pipe->in)) != cudaSuccess)
+            return cuda_fail("host-to-device copy");
+    }
+    for (int64_t c = 0; c < chunks; ++c) {
+        const int64_t h0 = BH * c / chunks, h1 = BH * (c + 1) / chunks;
+        const size_t n = static_cast<size_t>(h1 - h0);
+        auto at = [&](const void* base, size_t per_head) {
+            return const_cast<char*>(static_cast<const char*>(base) + static_cast<size_t>(h0) * per_head);
+        };
+        Problem pc;
+        if ((s = validate_sizes(pc, 1, h1 - h0, S_q, S_k, d, causal, scale, dtype)) != ATTN_OK) return s;
+        if ((e = cudaStreamWaitEvent(stream, pipe->in_done[c], 0)) != cudaSuccess)
+            return cuda_fail("ordering the forward");
+        if ((s = launch_checked(pc, at(q_dev, q_head), at(k_dev, kv_head), at(v_dev, kv_head),
+                                at(o_dev, q_head), reinterpret_cast<float*>(at(lse_dev, l_head)),
+                                stream)) != ATTN_OK)
+            return s;
+        if ((e = cudaEventRecord(pipe->comp_done[c], stream)) != cudaSuccess ||
+            (e = cudaStreamWaitEvent(pipe->out, pipe->comp_done[c], 0)) != cudaSuccess)
+            return cuda_fail("ordering the download");
+        if ((e = cudaMemcpyAsync(at(o_host, q_head), at(o_dev, q_head), n * q_head,
+                                 cudaMemcpyDeviceToHost, pipe->out)) != cudaSuccess ||
+            (e = cudaMemcpyAsync(at(lse_host, l_head), at(lse_dev, l_head), n * l_head,
+                                 cudaMemcpyDeviceToHost, pipe->out)) != cudaSuccess)
+            return cuda_fail("device-to-host copy");
+    }
+    // `stream` reaches this point only once every download has finished.
+    if ((e = cudaEventRecord(pipe->out_done, pipe->out)) != cudaSuccess ||
+        (e = cudaStreamWaitEvent(stream, pipe->out_done, 0)) != cudaSuccess)
+        return cuda_fail("joining the copy streams");
     return ok();
 }
 

@@ -18,10 +18,12 @@
  * all dense row-major (d contiguous) in the element type `dtype`.  LSE is
  * [B, H, S_q] fp32.  d ∈ {64, 128, 256} (SUPPORTED_HEAD_DIMS on the page).
  *
- * Ownership.  The caller owns every buffer.  The library allocates no memory,
- * keeps no pointer after a call returns, and enqueues all device work on
- * `stream` (NULL = the legacy default stream); calls return before the work
- * completes.
+ * Ownership.  The caller owns every buffer.  The library allocates no device
+ * memory (split-KV partials go to a caller workspace or to a static array
+ * built into the library), keeps no pointer after a call returns, and
+ * enqueues all device work on `stream` (NULL = the legacy default stream;
+ * attn_fwd_host also uses two helper streams of its own); calls return before
+ * the work completes.
  *
  * Errors.  Argument checks happen on the host before anything is enqueued and
  * return a status; attn_last_error() then describes the offending argument
@@ -157,13 +159,19 @@ attn_status_t attn_fwd_general(const attn_fwd_params_t* params, struct CUstream_
 /*
  * attn_fwd_host — the same forward, for inputs and outputs in HOST memory.
  *
- * Enqueues on `stream`: copies of q_host, k_host, v_host into the caller's
- * device buffers q_dev, k_dev, v_dev; attn_fwd on them into o_dev, lse_dev;
- * copies of o_dev, lse_dev back into o_host, lse_host.  Host buffers should be
- * page-locked for the copies to be asynchronous.  Shapes, alignment and
- * argument rules are those of attn_fwd (device buffers as there; host buffers
- * non-null).  The results are in o_host / lse_host once the stream has
- * reached this point (e.g. after cudaStreamSynchronize).
+ * Copies q_host, k_host, v_host into the caller's device buffers q_dev,
+ * k_dev, v_dev, runs attn_fwd on them into o_dev, lse_dev, and copies o_dev,
+ * lse_dev back into o_host, lse_host.  Heads are independent, so problems
+ * above 32 MB are cut into up to four chunks of consecutive (b, h) whose
+ * uploads, forwards and downloads overlap: the copies run on two helper
+ * streams that the library creates on a device's first call (with a few
+ * events; no memory is allocated) and orders after the work already on
+ * `stream`; the forwards run on `stream`, which reaches the end of this call
+ * only when every download has finished.  Host buffers should be page-locked
+ * for the copies to be asynchronous.  Shapes, alignment and argument rules
+ * are those of attn_fwd (device buffers as there; host buffers non-null).
+ * Calls on one device are enqueued one at a time (a host lock); the results
+ * are in o_host / lse_host once `stream` has reached this point.
  */
 attn_status_t attn_fwd_host(const void* q_host, const void* k_host, const void* v_host,
                             void* o_host, float* lse_host, void* q_dev, void* k_dev, void* v_dev,

@@ -206,6 +206,26 @@ def test_host_buffers_entry_point():
     assert torch.equal(o2.cpu(), oh) and torch.equal(l2.cpu(), lh)
 
 
+@pytest.mark.parametrize("causal", [False, True], ids=["full", "causal"])
+def test_host_entry_point_pipelined_chunks(causal):
+    """Above 32 MB the host entry point overlaps chunks of heads; results match the device path."""
+    B, H, S, d = 2, 16, 2048, 128
+    q, k, v = make_qkv(B, H, S, S, d, "bf16", seed=18)
+    qh, kh, vh = q.pin_memory(), k.pin_memory(), v.pin_memory()
+    oh = torch.full_like(qh, 3.0).pin_memory()
+    lh = torch.full((B, H, S), 3.0, dtype=torch.float32).pin_memory()
+    dev = [torch.empty_like(t, device=DEV) for t in (q, k, v, q)]
+    ld = torch.empty((B, H, S), dtype=torch.float32, device=DEV)
+    side = torch.cuda.Stream()
+    with torch.cuda.stream(side):
+        attn_fwd_host(qh, kh, vh, oh, lh, *dev, ld, B, H, S, S, d, int(causal), 1 / math.sqrt(d),
+                      ATTN_DTYPE_BF16)
+    side.synchronize()
+    o2, l2 = fwd(q.to(DEV), k.to(DEV), v.to(DEV), causal=causal)
+    torch.cuda.synchronize()
+    assert torch.equal(o2.cpu(), oh) and torch.equal(l2.cpu(), lh)
+
+
 def test_invalid_arguments_raise_on_gpu():
     q, k, v = make_qkv(1, 1, 64, 64, 96, "bf16", seed=17)
     with pytest.raises(AttnError) as e:
