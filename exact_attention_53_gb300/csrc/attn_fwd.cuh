@@ -550,8 +550,7 @@ __global__ void __launch_bounds__(KernelTile<D, SPLIT>::THREADS, 1)
                 ++sc;
 
                 uint32_t sa[64], sb[64];
-                tmem_ld64(lane_base + b * T::S_STRIDE, sa);
-                tmem_ld64(lane_base + b * T::S_STRIDE + 64, sb);
+                tmem_ld64x2(lane_base + b * T::S_STRIDE, lane_base + b * T::S_STRIDE + 64, sa, sb);
                 float s[128];
 #pragma unroll
                 for (int c = 0; c < 64; ++c) {
@@ -588,8 +587,8 @@ __global__ void __launch_bounds__(KernelTile<D, SPLIT>::THREADS, 1)
                         : exp_pack128<false, BF16, true>(s, lim, scale_log2, -m, pk, &xmax);
                     if (__any_sync(0xffffffffu, xmax > kRescaleLog2)) {
                         uint32_t ra[64], rb[64];
-                        tmem_ld64(lane_base + b * T::S_STRIDE, ra);
-                        tmem_ld64(lane_base + b * T::S_STRIDE + 64, rb);
+                        tmem_ld64x2(lane_base + b * T::S_STRIDE, lane_base + b * T::S_STRIDE + 64,
+                                    ra, rb);
                         if (xmax > kRescaleLog2) {
 #pragma unroll
                             for (int c = 0; c < 64; ++c) {

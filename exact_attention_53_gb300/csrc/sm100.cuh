@@ -358,6 +358,31 @@ __device__ __forceinline__ void tmem_ld64(uint32_t taddr, uint32_t (&r)[64]) {
         : "memory");
 }
 
+// Two 64-column loads in flight together, one wait for both.
+#define ATTN_Q8(i) "=r"(q[i]), "=r"(q[i + 1]), "=r"(q[i + 2]), "=r"(q[i + 3]), \
+    "=r"(q[i + 4]), "=r"(q[i + 5]), "=r"(q[i + 6]), "=r"(q[i + 7])
+__device__ __forceinline__ void tmem_ld64x2(uint32_t taddr_a, uint32_t taddr_b, uint32_t (&r)[64],
+                                            uint32_t (&q)[64]) {
+    asm volatile(
+        "tcgen05.ld.sync.aligned.32x32b.x64.b32 "
+        "{%0,%1,%2,%3,%4,%5,%6,%7,%8,%9,%10,%11,%12,%13,%14,%15,"
+        "%16,%17,%18,%19,%20,%21,%22,%23,%24,%25,%26,%27,%28,%29,%30,%31,"
+        "%32,%33,%34,%35,%36,%37,%38,%39,%40,%41,%42,%43,%44,%45,%46,%47,"
+        "%48,%49,%50,%51,%52,%53,%54,%55,%56,%57,%58,%59,%60,%61,%62,%63}, [%128];\n\t"
+        "tcgen05.ld.sync.aligned.32x32b.x64.b32 "
+        "{%64,%65,%66,%67,%68,%69,%70,%71,%72,%73,%74,%75,%76,%77,%78,%79,"
+        "%80,%81,%82,%83,%84,%85,%86,%87,%88,%89,%90,%91,%92,%93,%94,%95,"
+        "%96,%97,%98,%99,%100,%101,%102,%103,%104,%105,%106,%107,%108,%109,%110,%111,"
+        "%112,%113,%114,%115,%116,%117,%118,%119,%120,%121,%122,%123,%124,%125,%126,%127}, [%129];\n\t"
+        "tcgen05.wait::ld.sync.aligned;"
+        : ATTN_R8(0), ATTN_R8(8), ATTN_R8(16), ATTN_R8(24), ATTN_R8(32), ATTN_R8(40),
+          ATTN_R8(48), ATTN_R8(56), ATTN_Q8(0), ATTN_Q8(8), ATTN_Q8(16), ATTN_Q8(24), ATTN_Q8(32),
+          ATTN_Q8(40), ATTN_Q8(48), ATTN_Q8(56)
+        : "r"(taddr_a), "r"(taddr_b)
+        : "memory");
+}
+#undef ATTN_Q8
+
 __device__ __forceinline__ void tmem_st32(uint32_t taddr, const uint32_t* r) {
     asm volatile(
         "tcgen05.st.sync.aligned.32x32b.x32.b32 [%0], "
