@@ -24,6 +24,7 @@ from .binding import (  # noqa: F401
     bwd_general,
     fwd,
     fwd_general,
+    fwd_splitkv_general,
     fwd_splitkv,
     library_path,
     load_library,

@@ -31,7 +31,7 @@ ATTN_MASK_CAUSAL_BOTTOM_RIGHT = 2
 
 EXPORTED = ("attn_fwd", "attn_fwd_general", "attn_fwd_host", "attn_fwd_plan", "attn_fwd_splitkv_plan",
             "attn_fwd_splitkv", "attn_fwd_splitkv_noalloc", "attn_bwd_workspace_size", "attn_bwd",
-            "attn_bwd_general",
+            "attn_bwd_general", "attn_fwd_splitkv_general_plan", "attn_fwd_splitkv_general",
             "attn_last_error", "attn_get_device_status", "attn_version")
 NOALLOC_SCRATCH_BYTES = 16 * 1024 * 1024    # ATTN_NOALLOC_SCRATCH_BYTES
 
@@ -110,6 +110,11 @@ def load_library() -> ctypes.CDLL:
         lib.attn_fwd.restype = i32
         lib.attn_fwd_general.argtypes = [ctypes.POINTER(AttnFwdParams), vp]
         lib.attn_fwd_general.restype = i32
+        lib.attn_fwd_splitkv_general_plan.argtypes = [ctypes.POINTER(AttnFwdParams), i64,
+                                                      ctypes.POINTER(i64), ctypes.POINTER(i64)]
+        lib.attn_fwd_splitkv_general_plan.restype = i32
+        lib.attn_fwd_splitkv_general.argtypes = [ctypes.POINTER(AttnFwdParams), i64, vp, i64, vp]
+        lib.attn_fwd_splitkv_general.restype = i32
         lib.attn_bwd_general.argtypes = [ctypes.POINTER(AttnBwdParams), vp]
         lib.attn_bwd_general.restype = i32
         lib.attn_fwd_host.argtypes = [vp] * 10 + [i64, i64, i64, i64, i64, i32, ctypes.c_float,
@@ -200,6 +205,47 @@ def fwd_general(q: torch.Tensor, k: torch.Tensor, v: torch.Tensor, mask: int = A
                       B, H, H_kv, S_q, S_k, d, _layout(q), _layout(k), _layout(v), _layout(out),
                       int(mask), float(scale), _DTYPE_CODE[q.dtype])
     attn_fwd_general(p)
+    return out, lse
+
+
+def _fwd_params(q, k, v, out, lse, mask, scale):
+    if q.dtype != k.dtype or q.dtype != v.dtype or q.dtype not in _DTYPE_CODE:
+        raise AttnError(ATTN_ERR_UNSUPPORTED, "q, k, v must share dtype float16 or bfloat16")
+    B, H, S_q, d = q.shape
+    H_kv, S_k = k.shape[1], k.shape[2]
+    if k.shape != (B, H_kv, S_k, d) or v.shape != k.shape:
+        raise AttnError(ATTN_ERR_INVALID_ARG, f"shape mismatch q{tuple(q.shape)} k{tuple(k.shape)} v{tuple(v.shape)}")
+    if scale is None:
+        scale = 1.0 / math.sqrt(d)
+    if out is None:
+        out = torch.empty((B, H, S_q, d), dtype=q.dtype, device=q.device)
+    if lse is None:
+        lse = torch.empty((B, H, S_q), dtype=torch.float32, device=q.device)
+    p = AttnFwdParams(q.data_ptr(), k.data_ptr(), v.data_ptr(), out.data_ptr(), lse.data_ptr(),
+                      B, H, H_kv, S_q, S_k, d, _layout(q), _layout(k), _layout(v), _layout(out),
+                      int(mask), float(scale), _DTYPE_CODE[q.dtype])
+    return p, out, lse
+
+
+def attn_fwd_splitkv_general_plan(params: AttnFwdParams, n_split: int = 0) -> tuple[int, int]:
+    """(ranges used, workspace bytes) of the general split-KV forward."""
+    n_used, ws = ctypes.c_int64(), ctypes.c_int64()
+    _check(load_library().attn_fwd_splitkv_general_plan(ctypes.byref(params), int(n_split),
+                                                        ctypes.byref(n_used), ctypes.byref(ws)))
+    return n_used.value, ws.value
+
+
+def fwd_splitkv_general(q, k, v, n_split: int = 0, mask: int = ATTN_MASK_NONE,
+                        scale: float | None = None, workspace=None, out=None, lse=None):
+    """Split-KV forward over strided views with grouped key/value heads (see
+    :func:`fwd_general`); returns ``(o, lse)``."""
+    p, out, lse = _fwd_params(q, k, v, out, lse, mask, scale)
+    _, ws = attn_fwd_splitkv_general_plan(p, n_split)
+    if workspace is None:
+        workspace = torch.empty(max(ws, 16), dtype=torch.uint8, device=q.device)
+    _check(load_library().attn_fwd_splitkv_general(
+        ctypes.byref(p), int(n_split), workspace.data_ptr(),
+        workspace.numel() * workspace.element_size(), _stream_handle(None)))
     return out, lse
 
 

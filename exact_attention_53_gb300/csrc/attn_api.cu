@@ -83,6 +83,7 @@ struct Problem {
     int64_t H_kv = 0;            // key/value heads (H for plain multi-head attention)
     bool causal;
     int64_t causal_off = 0;      // key j visible to query i iff j <= i + causal_off
+    int64_t pack = 1;            // split-KV: query heads sharing one query tile
     float scale;
     attn_dtype_t dtype;
     Layout lq, lk, lv, lo;
@@ -285,14 +286,15 @@ attn_status_t encode_rows(CUtensorMap* map, const void* base, const Problem& p, 
 // A [B, heads, S, d] view as a 4-D map (d, S, heads, B) with its own strides;
 // box 64 columns × box_rows rows of one head.
 attn_status_t encode_4d(CUtensorMap* map, const void* base, const Problem& p, int64_t S,
-                        int64_t heads, const Layout& l, uint32_t box_rows, const char* name) {
+                        int64_t heads, const Layout& l, uint32_t box_rows, const char* name,
+                        uint32_t box_heads = 1) {
     auto fn = encode_fn();
     if (!fn) return fail(ATTN_ERR_CUDA, "cuTensorMapEncodeTiled is unavailable from the driver");
     cuuint64_t dims[4] = {static_cast<cuuint64_t>(p.d), static_cast<cuuint64_t>(S),
                           static_cast<cuuint64_t>(heads), static_cast<cuuint64_t>(p.B)};
     cuuint64_t strides[3] = {static_cast<cuuint64_t>(l.row * 2), static_cast<cuuint64_t>(l.head * 2),
                              static_cast<cuuint64_t>(l.batch * 2)};
-    cuuint32_t box[4] = {64, box_rows, 1, 1};
+    cuuint32_t box[4] = {64, box_rows, box_heads, 1};
     cuuint32_t estr[4] = {1, 1, 1, 1};
     CUresult r = fn(map,
                     p.dtype == ATTN_DTYPE_BF16 ? CU_TENSOR_MAP_DATA_TYPE_BFLOAT16
@@ -397,6 +399,7 @@ attn_status_t fill_args(attn::FwdArgs& a, const Problem& p, int dev, const void*
     a.kv_per_split = 0;
     a.o_part = nullptr;
     a.lse_part = nullptr;
+    a.pack = 1;
     return ATTN_OK;
 }
 
@@ -430,7 +433,7 @@ int64_t split_query_blocks(const Problem& p) { return (p.S_q + attn::kBlockM - 1
 // to fewer ranges, which also keeps the merge pass small.
 attn_status_t split_plan(const Problem& p, int64_t n_req, int num_sms, SplitPlan* out) {
     const int64_t n_kv = (p.S_k + attn::kBlockN - 1) / attn::kBlockN;
-    const int64_t base = p.B * p.H * split_query_blocks(p);
+    const int64_t base = p.pack > 1 ? p.B * p.H_kv : p.B * p.H * split_query_blocks(p);
     int64_t n = 1;
     if (n_req > 0) {
         n = std::min(n_req, n_kv);
@@ -458,8 +461,11 @@ attn_status_t split_plan(const Problem& p, int64_t n_req, int num_sms, SplitPlan
                     (long long)n);
     out->n_split = n;
     out->kv_per_split = per;
-    out->workspace_bytes =
-        n > 1 ? n * p.B * p.H * p.S_q * (p.d + 1) * int64_t(sizeof(float)) : 0;
+    // One range runs the one-pass kernel without a workspace, except for
+    // packed head groups, which only the split kernel computes.
+    out->workspace_bytes = (n > 1 || p.pack > 1)
+                               ? n * p.B * p.H * p.S_q * (p.d + 1) * int64_t(sizeof(float))
+                               : 0;
     return ATTN_OK;
 }
 
@@ -475,6 +481,23 @@ attn_status_t resolve_split(const Problem& p, int64_t n_split, SplitPlan* sp) {
         sms = g_num_sms[dev].load();
     }
     return split_plan(p, n_split, sms, sp);
+}
+
+// Split-KV over general layouts: full attention (a bottom-right mask with one
+// query row is the same thing); grouped heads pack into one query tile when
+// their S_q rows fit in 128.
+attn_status_t validate_split_general(Problem& p, const attn_fwd_params_t* a) {
+    attn_status_t s = validate_general(p, a);
+    if (s != ATTN_OK) return s;
+    const bool full = a->mask == 0 || (a->mask == 2 && a->S_q == 1);
+    if (!full)
+        return fail(ATTN_ERR_UNSUPPORTED,
+                    "split-KV computes full attention (mask 0, or the bottom-right mask with S_q = 1)");
+    p.causal = false;
+    p.causal_off = 0;
+    const int64_t group = p.H / p.H_kv;
+    p.pack = (group > 1 && p.S_q * group <= attn::kBlockM) ? group : 1;
+    return ATTN_OK;
 }
 
 // ---------------------------------------------------------------- backward
@@ -708,7 +731,75 @@ attn_status_t attn_fwd_splitkv(const void* q, const void* k, const void* v, void
     cudaError_t e = fn(a, stream);
     if (e != cudaSuccess) return fail(ATTN_ERR_CUDA, "kernel launch: %s", cudaGetErrorString(e));
     e = attn::launch_attn_combine(a.o_part, a.lse_part, o, lse, a.n_split, rows,
-                                  static_cast<int>(p.d), p.dtype == ATTN_DTYPE_BF16, stream);
+                                  static_cast<int>(p.d), p.dtype == ATTN_DTYPE_BF16,
+                                  static_cast<int>(p.H), static_cast<int>(p.S_q),
+                                  attn::RowLayout{p.lo.batch, p.lo.head, p.lo.row}, stream);
+    if (e != cudaSuccess) return fail(ATTN_ERR_CUDA, "combine launch: %s", cudaGetErrorString(e));
+    return ok();
+}
+
+attn_status_t attn_fwd_splitkv_general_plan(const attn_fwd_params_t* params, int64_t n_split,
+                                            int64_t* n_split_used, int64_t* workspace_bytes) {
+    if (!n_split_used) return fail(ATTN_ERR_INVALID_ARG, "n_split_used is null");
+    if (!workspace_bytes) return fail(ATTN_ERR_INVALID_ARG, "workspace_bytes is null");
+    Problem p;
+    attn_status_t s = validate_split_general(p, params);
+    if (s != ATTN_OK) return s;
+    SplitPlan sp;
+    if ((s = resolve_split(p, n_split, &sp)) != ATTN_OK) return s;
+    *n_split_used = sp.n_split;
+    *workspace_bytes = sp.workspace_bytes;
+    return ok();
+}
+
+attn_status_t attn_fwd_splitkv_general(const attn_fwd_params_t* params, int64_t n_split,
+                                       void* workspace, int64_t workspace_bytes,
+                                       struct CUstream_st* stream) {
+    Problem p;
+    attn_status_t s = validate_split_general(p, params);
+    if (s != ATTN_OK) return s;
+    const void *q = params->q, *k = params->k, *v = params->v;
+    void* o = params->o;
+    float* lse = params->lse;
+    if ((s = validate_device_ptrs(p, q, k, v, o, lse)) != ATTN_OK) return s;
+    SplitPlan sp;
+    if ((s = resolve_split(p, n_split, &sp)) != ATTN_OK) return s;
+    if (sp.workspace_bytes == 0) return launch_checked(p, q, k, v, o, lse, stream);
+    if (!workspace) return fail(ATTN_ERR_INVALID_ARG, "workspace is null");
+    if (!aligned(workspace, 16)) return fail(ATTN_ERR_INVALID_ARG, "workspace is not 16-byte aligned");
+    if (workspace_bytes < sp.workspace_bytes)
+        return fail(ATTN_ERR_INVALID_ARG, "workspace_bytes=%lld is below the %lld bytes %lld ranges need",
+                    (long long)workspace_bytes, (long long)sp.workspace_bytes, (long long)sp.n_split);
+    const size_t wb = static_cast<size_t>(sp.workspace_bytes);
+    if (overlaps(workspace, wb, q, p.q_bytes)) return fail(ATTN_ERR_INVALID_ARG, "workspace overlaps q");
+    if (overlaps(workspace, wb, k, p.kv_bytes)) return fail(ATTN_ERR_INVALID_ARG, "workspace overlaps k");
+    if (overlaps(workspace, wb, v, p.v_bytes)) return fail(ATTN_ERR_INVALID_ARG, "workspace overlaps v");
+    if (overlaps(workspace, wb, o, p.o_bytes)) return fail(ATTN_ERR_INVALID_ARG, "workspace overlaps o");
+    if (overlaps(workspace, wb, lse, p.lse_bytes)) return fail(ATTN_ERR_INVALID_ARG, "workspace overlaps lse");
+    int dev = 0;
+    if ((s = check_device(&dev)) != ATTN_OK) return s;
+    attn::FwdArgs a;
+    if ((s = fill_args(a, p, dev, q, k, v, o, lse)) != ATTN_OK) return s;
+    if (p.pack > 1) {
+        // one box = the S_q rows of the pack query heads of a key/value head
+        if ((s = encode_4d(&a.tm_q, q, p, p.S_q, p.H, p.lq, static_cast<uint32_t>(p.S_q), "q",
+                           static_cast<uint32_t>(p.pack))) != ATTN_OK)
+            return s;
+        a.pack = static_cast<int32_t>(p.pack);
+    }
+    const int64_t rows = p.B * p.H * p.S_q;
+    a.n_split = static_cast<int32_t>(sp.n_split);
+    a.kv_per_split = static_cast<int32_t>(sp.kv_per_split);
+    a.o_part = static_cast<float*>(workspace);
+    a.lse_part = a.o_part + sp.n_split * rows * p.d;
+    LaunchFn fn = pick_split(p.d, p.dtype == ATTN_DTYPE_BF16);
+    if (!fn) return fail(ATTN_ERR_UNSUPPORTED, "no kernel for d=%lld", (long long)p.d);
+    cudaError_t e = fn(a, stream);
+    if (e != cudaSuccess) return fail(ATTN_ERR_CUDA, "kernel launch: %s", cudaGetErrorString(e));
+    e = attn::launch_attn_combine(a.o_part, a.lse_part, o, lse, a.n_split, rows,
+                                  static_cast<int>(p.d), p.dtype == ATTN_DTYPE_BF16,
+                                  static_cast<int>(p.H), static_cast<int>(p.S_q),
+                                  attn::RowLayout{p.lo.batch, p.lo.head, p.lo.row}, stream);
     if (e != cudaSuccess) return fail(ATTN_ERR_CUDA, "combine launch: %s", cudaGetErrorString(e));
     return ok();
 }
@@ -753,7 +844,9 @@ attn_status_t attn_fwd_splitkv_noalloc(const void* q, const void* k, const void*
     cudaError_t e = fn(a, stream);
     if (e != cudaSuccess) return fail(ATTN_ERR_CUDA, "kernel launch: %s", cudaGetErrorString(e));
     e = attn::launch_attn_combine(a.o_part, a.lse_part, o, lse, a.n_split, rows,
-                                  static_cast<int>(p.d), p.dtype == ATTN_DTYPE_BF16, stream);
+                                  static_cast<int>(p.d), p.dtype == ATTN_DTYPE_BF16,
+                                  static_cast<int>(p.H), static_cast<int>(p.S_q),
+                                  attn::RowLayout{p.lo.batch, p.lo.head, p.lo.row}, stream);
     if (e != cudaSuccess) return fail(ATTN_ERR_CUDA, "combine launch: %s", cudaGetErrorString(e));
     return ok();
 }

@@ -12,7 +12,8 @@
 //     O_i   = Σ_s exp(LSE_s,i − LSE_i) · O_s,i
 //
 // One warp per query row; lane l owns d/32 consecutive columns, so every load
-// and store of a warp covers one contiguous row segment.  The pass is bound by
+// and store of a warp covers one contiguous row segment.  O is written in the
+// caller's layout (batch, head and row strides), LSE densely.  The pass is bound by
 // reading the partials once (n_split · (d + 1) · 4 bytes per row).
 #include <cuda_bf16.h>
 #include <cuda_fp16.h>
@@ -27,7 +28,8 @@ __global__ void __launch_bounds__(256) attn_combine_kernel(const float* __restri
                                                            const float* __restrict__ lse_part,
                                                            void* __restrict__ o,
                                                            float* __restrict__ lse, int n_split,
-                                                           long long rows) {
+                                                           long long rows, int H, int S_q,
+                                                           RowLayout o_lay) {
     constexpr int PER_LANE = D / 32;          // 2, 4 or 8 columns
     const long long row = static_cast<long long>(blockIdx.x) * 8 + (threadIdx.x >> 5);
     const int lane = threadIdx.x & 31;
@@ -77,7 +79,10 @@ __global__ void __launch_bounds__(256) attn_combine_kernel(const float* __restri
             packed[i] = *reinterpret_cast<const uint32_t*>(&h);
         }
     }
-    uint16_t* dst = static_cast<uint16_t*>(o) + static_cast<size_t>(row) * D + col;
+    const long long bh = row / S_q, q = row - bh * S_q;
+    const long long b = bh / H, h = bh - b * H;
+    uint16_t* dst = static_cast<uint16_t*>(o) +
+                    static_cast<size_t>(b * o_lay.batch + h * o_lay.head + q * o_lay.row) + col;
     if constexpr (PER_LANE == 2) {
         *reinterpret_cast<uint32_t*>(dst) = packed[0];
     } else if constexpr (PER_LANE == 4) {
@@ -90,28 +95,32 @@ __global__ void __launch_bounds__(256) attn_combine_kernel(const float* __restri
 
 template <int D>
 cudaError_t launch_d(const float* o_part, const float* lse_part, void* o, float* lse, int n_split,
-                     long long rows, bool bf16, cudaStream_t stream) {
+                     long long rows, bool bf16, int H, int S_q, const RowLayout& o_lay,
+                     cudaStream_t stream) {
     const long long blocks = (rows + 7) / 8;
     if (blocks > 0x7fffffffLL) return cudaErrorInvalidConfiguration;
     if (bf16)
         attn_combine_kernel<D, true><<<static_cast<unsigned>(blocks), 256, 0, stream>>>(
-            o_part, lse_part, o, lse, n_split, rows);
+            o_part, lse_part, o, lse, n_split, rows, H, S_q, o_lay);
     else
         attn_combine_kernel<D, false><<<static_cast<unsigned>(blocks), 256, 0, stream>>>(
-            o_part, lse_part, o, lse, n_split, rows);
+            o_part, lse_part, o, lse, n_split, rows, H, S_q, o_lay);
     return cudaGetLastError();
 }
 
 }  // namespace
 
 cudaError_t launch_attn_combine(const float* o_part, const float* lse_part, void* o, float* lse,
-                                int n_split, long long rows, int d, bool bf16,
-                                cudaStream_t stream) {
+                                int n_split, long long rows, int d, bool bf16, int H, int S_q,
+                                const RowLayout& o_lay, cudaStream_t stream) {
     if (rows <= 0) return cudaSuccess;
     switch (d) {
-        case 64: return launch_d<64>(o_part, lse_part, o, lse, n_split, rows, bf16, stream);
-        case 128: return launch_d<128>(o_part, lse_part, o, lse, n_split, rows, bf16, stream);
-        case 256: return launch_d<256>(o_part, lse_part, o, lse, n_split, rows, bf16, stream);
+        case 64:
+            return launch_d<64>(o_part, lse_part, o, lse, n_split, rows, bf16, H, S_q, o_lay, stream);
+        case 128:
+            return launch_d<128>(o_part, lse_part, o, lse, n_split, rows, bf16, H, S_q, o_lay, stream);
+        case 256:
+            return launch_d<256>(o_part, lse_part, o, lse, n_split, rows, bf16, H, S_q, o_lay, stream);
         default: return cudaErrorInvalidValue;
     }
 }

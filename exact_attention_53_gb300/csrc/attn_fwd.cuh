@@ -162,7 +162,8 @@ __global__ void __launch_bounds__(KernelTile<D, SPLIT>::THREADS, 1)
                     float* __restrict__ lse_ptr, int S_q, int S_k, int BH, int n_qblk,
                     int head_group, float scale_log2, unsigned int* __restrict__ status,
                     int n_split, int kv_per_split, float* __restrict__ o_part,
-                    float* __restrict__ lse_part, int H, int kv_group, int causal_off) {
+                    float* __restrict__ lse_part, int H, int kv_group, int causal_off,
+                    int pack) {
     using T = KernelTile<D, SPLIT>;
     using namespace sm100;
     constexpr int ROWS = T::BM * T::TILES;                 // query rows per unit
@@ -191,12 +192,18 @@ __global__ void __launch_bounds__(KernelTile<D, SPLIT>::THREADS, 1)
     const int lane = threadIdx.x & 31;
     // SPLIT: every (head, query block) is cut into n_split work units along the
     // keys (kv_per_split key tiles each); each writes O/l in fp32 and its own
-    // log-sum-exp to o_part / lse_part for attn_combine to merge.
-    const int n_units = BH * n_qblk * (SPLIT ? n_split : 1);
-    // Unit L -> head, first query row, key tiles of each query tile, first key tile, split.
+    // log-sum-exp to o_part / lse_part for attn_combine to merge.  With
+    // pack > 1 (split only) a unit's query tile holds the S_q rows of all
+    // `pack` query heads that share one key/value head (pack·S_q <= 128 rows),
+    // so each K/V tile is read and multiplied once for the whole group.
+    const bool packed = SPLIT && pack > 1;
+    const int units_bh = packed ? BH / pack : BH;
+    const int n_units = units_bh * n_qblk * (SPLIT ? n_split : 1);
+    // Unit L -> unit head (query head, or key/value head when packed), first
+    // query row, key tiles of each query tile, first key tile, split.
     auto unit_info = [&](int L, int& bh, int& q0, int& n0, int& n1, int& kb, int& sp) {
         sp = SPLIT ? L % n_split : 0;
-        unit_coords<CAUSAL, ROWS>(SPLIT ? L / n_split : L, BH, n_qblk, head_group, bh, q0);
+        unit_coords<CAUSAL, ROWS>(SPLIT ? L / n_split : L, units_bh, n_qblk, head_group, bh, q0);
         n0 = kv_tiles_for<CAUSAL>(q0, S_q, S_k, causal_off);
         n1 = T::TILES == 2 ? kv_tiles_for<CAUSAL>(q0 + T::BM, S_q, S_k, causal_off) : 0;
         kb = 0;
@@ -209,9 +216,16 @@ __global__ void __launch_bounds__(KernelTile<D, SPLIT>::THREADS, 1)
     // (b·H + h) -> batch, query head and the key/value head it reads (heads
     // are grouped kv_group to one key/value head).
     auto heads_of = [&](int bh, int& b, int& h, int& hk) {
-        b = bh / H;
-        h = bh - b * H;
-        hk = h / kv_group;
+        if (packed) {                        // bh counts key/value heads; h = first query head
+            const int H_kv = H / kv_group;
+            b = bh / H_kv;
+            hk = bh - b * H_kv;
+            h = hk * kv_group;
+        } else {
+            b = bh / H;
+            h = bh - b * H;
+            hk = h / kv_group;
+        }
     };
     // Units are handed out in rounds of gridDim.x, in serpentine order (CTA c
     // takes position c of even rounds and gridDim.x-1-c of odd ones), so a CTA
@@ -222,6 +236,14 @@ __global__ void __launch_bounds__(KernelTile<D, SPLIT>::THREADS, 1)
         return r * G + ((r & 1) ? (G - 1 - c) : c);
     };
 
+    if (packed) {
+        // Rows past pack·S_q of the query tile are never loaded; keep them zero
+        // so their (unstored) scores stay finite.
+        uint4* zq = reinterpret_cast<uint4*>(sQ);
+        for (int i = threadIdx.x; i < T::TILES * T::Q_TILE_BYTES / 16; i += blockDim.x)
+            zq[i] = make_uint4(0, 0, 0, 0);
+        fence_proxy_async_smem();
+    }
     if (threadIdx.x == 0) {
         mbar_init(q_full, 1);
         mbar_init(q_empty, 1);
@@ -310,11 +332,18 @@ __global__ void __launch_bounds__(KernelTile<D, SPLIT>::THREADS, 1)
             ok = __all_sync(0xffffffffu, ok);
             if (!ok) break;
             if (leader) {
-                mbar_arrive_expect_tx(q_full, T::TILES * T::Q_TILE_BYTES);
-                for (int t = 0; t < T::TILES; ++t)
+                if (packed) {
+                    // one box of S_q rows × pack heads per 64-column chunk
+                    mbar_arrive_expect_tx(q_full, T::CHUNKS * S_q * pack * 128);
                     for (int c = 0; c < T::CHUNKS; ++c)
-                        tma_load_4d(sQ + (t * T::CHUNKS + c) * T::Q_CHUNK_BYTES, &tm_q, q_full,
-                                    c * 64, q0 + t * T::BM, h, b);
+                        tma_load_4d(sQ + c * T::Q_CHUNK_BYTES, &tm_q, q_full, c * 64, 0, h, b);
+                } else {
+                    mbar_arrive_expect_tx(q_full, T::TILES * T::Q_TILE_BYTES);
+                    for (int t = 0; t < T::TILES; ++t)
+                        for (int c = 0; c < T::CHUNKS; ++c)
+                            tma_load_4d(sQ + (t * T::CHUNKS + c) * T::Q_CHUNK_BYTES, &tm_q,
+                                        q_full, c * 64, q0 + t * T::BM, h, b);
+                }
             }
             __syncwarp();
             ++q_loads;
@@ -650,8 +679,17 @@ __global__ void __launch_bounds__(KernelTile<D, SPLIT>::THREADS, 1)
                     ++oc;
                     tc_fence_after();
                     const float inv_l = 1.f / l;
-                    const bool store = q_idx < S_q;
-                    const size_t prow = (static_cast<size_t>(sp) * BH + bh) * S_q + q_idx;
+                    bool store = q_idx < S_q;
+                    size_t prow = (static_cast<size_t>(sp) * BH + bh) * S_q + q_idx;
+                    if (packed) {
+                        // row = (query head within the group) · S_q + query
+                        int b_, h_, hk_;
+                        heads_of(bh, b_, h_, hk_);
+                        const int hl = row / S_q;
+                        store = row < S_q * pack;
+                        prow = (static_cast<size_t>(sp) * BH + static_cast<size_t>(b_) * H + h_ + hl) *
+                                   S_q + (row - hl * S_q);
+                    }
                     float4* dst = reinterpret_cast<float4*>(o_part + prow * D);
                     const uint32_t o_base = lane_base + T::O_COL + t * D;
 #pragma unroll 1
@@ -774,7 +812,8 @@ cudaError_t launch_attn_fwd(const FwdArgs& a, cudaStream_t stream) {
     const int rows_per_cta = T::BM * T::TILES;
     const int n_qblk = (a.S_q + rows_per_cta - 1) / rows_per_cta;
     const int n_split = SPLIT ? a.n_split : 1;
-    const long long units = static_cast<long long>(a.BH) * n_qblk * n_split;
+    const int pack = SPLIT ? a.pack : 1;
+    const long long units = static_cast<long long>(a.BH / pack) * n_qblk * n_split;
     if (units > 0x7fffffffLL) return cudaErrorInvalidConfiguration;
     // One CTA per SM (each takes the whole of tensor memory), looping over units.
     const int grid = static_cast<int>(std::min<long long>(units, a.num_sms));
@@ -782,7 +821,7 @@ cudaError_t launch_attn_fwd(const FwdArgs& a, cudaStream_t stream) {
                                                          a.S_k, a.BH, n_qblk, head_group,
                                                          a.scale_log2, a.status, n_split,
                                                          a.kv_per_split, a.o_part, a.lse_part, a.H,
-                                                         a.kv_group, a.causal_off);
+                                                         a.kv_group, a.causal_off, pack);
     return cudaGetLastError();
 }
 

@@ -30,7 +30,13 @@ struct FwdArgs {
     int32_t kv_per_split;   // key tiles per range
     float* o_part;          // [n_split, B·H, S_q, d] fp32: O/l of each range
     float* lse_part;        // [n_split, B·H, S_q] fp32: LSE of each range
+    int32_t pack;           // query heads per unit's query tile (1, or H / H_kv when packed)
     unsigned int* status;   // device status word (bit set on a wait that ran out)
+};
+
+// Element strides of a [B, heads, S, d] tensor (d contiguous).
+struct RowLayout {
+    long long batch, head, row;
 };
 
 // Rows per query tile and keys per key/value tile, fixed for every head_dim.
@@ -96,15 +102,11 @@ template <int D, bool BF16, bool CAUSAL, bool SPLIT>
 cudaError_t launch_attn_fwd(const FwdArgs& args, cudaStream_t stream);
 
 // Merge n_split partial results: LSE = ln Σ_s exp(LSE_s), O = Σ_s exp(LSE_s − LSE)·O_s,
-// written as the output dtype into o and as fp32 into lse.  rows = B·H·S_q.
+// written as the output dtype into o (element strides o_lay over [B, H, S_q, d])
+// and as fp32 into the dense lse.  rows = B·H·S_q.
 cudaError_t launch_attn_combine(const float* o_part, const float* lse_part, void* o, float* lse,
-                                int n_split, long long rows, int d, bool bf16,
-                                cudaStream_t stream);
-
-// Element strides of a [B, heads, S, d] tensor (d contiguous).
-struct RowLayout {
-    long long batch, head, row;
-};
+                                int n_split, long long rows, int d, bool bf16, int H, int S_q,
+                                const RowLayout& o_lay, cudaStream_t stream);
 
 // Backward launch contract (attn_bwd.cuh).  The dK/dV kernel keeps 128-row K
 // and V tiles and streams 64-row Q and dO steps; the dQ kernel keeps 128-row

@@ -3,6 +3,7 @@
     python -m exact_attention_53_gb300.run --workload c3 --causal 0 --iters 2
     python -m exact_attention_53_gb300.run --workload decode --split 0 --iters 2
     python -m exact_attention_53_gb300.run --split-sweep
+    python -m exact_attention_53_gb300.run --gqa-sweep
     python -m exact_attention_53_gb300.run --workload c3 --causal 1 --bwd --iters 3
 
 Inputs are the seeded synthetic ones of ``workloads``; the forward is
@@ -22,7 +23,8 @@ import argparse
 
 import torch
 
-from . import attn_fwd_splitkv_plan, attn_get_device_status, bwd, fwd, fwd_splitkv
+from . import (attn_fwd_splitkv_plan, attn_get_device_status, bwd, fwd, fwd_general, fwd_splitkv,
+               fwd_splitkv_general)
 from .workloads import WORKLOADS, make_qkv, workload_qkv
 
 
@@ -63,6 +65,30 @@ def split_sweep():
         print(f"| {B}, {H}, {S_q}, {S_k}, {d} | " + " | ".join(cells) + " |", flush=True)
 
 
+GQA_SHAPES = [(8, 32, 8, 1, 8192, 128), (2, 64, 8, 1, 32768, 128), (4, 32, 4, 4, 16384, 128),
+              (16, 32, 8, 1, 4096, 128), (2, 32, 8, 1, 65536, 64)]
+
+
+def gqa_sweep():
+    """Decoding with grouped key/value heads: one-pass vs split-KV with packed heads."""
+    dev = torch.device("cuda")
+    print("| shape (B, H, H_kv, S_q, S_k, d) | one-pass µs | split-KV µs (auto) | split GB/s |")
+    print("|---|---|---|---|")
+    for B, H, H_kv, S_q, S_k, d in GQA_SHAPES:
+        q = make_qkv(B, H, S_q, 1, d, "bf16", seed=2)[0].to(dev)
+        _, k, v = (t.to(dev) for t in make_qkv(B, H_kv, 1, S_k, d, "bf16", seed=3))
+        o = torch.empty_like(q)
+        lse = torch.empty((B, H, S_q), dtype=torch.float32, device=dev)
+        work = torch.empty(64 << 20, dtype=torch.uint8, device=dev)
+        t1 = 1e3 * _mean_ms(lambda: fwd_general(q, k, v, out=o, lse=lse))
+        t2 = 1e3 * _mean_ms(lambda: fwd_splitkv_general(q, k, v, n_split=0, workspace=work,
+                                                         out=o, lse=lse))
+        by = 2 * (2 * B * H * S_q * d + 2 * B * H_kv * S_k * d) + 4 * B * H * S_q
+        attn_get_device_status()
+        print(f"| {B}, {H}, {H_kv}, {S_q}, {S_k}, {d} | {t1:.1f} | {t2:.1f} | {by / t2 / 1e3:.0f} |",
+              flush=True)
+
+
 def main(argv=None):
     ap = argparse.ArgumentParser(description=__doc__.split("\n")[0])
     ap.add_argument("--workload", default="c3", choices=sorted(WORKLOADS))
@@ -74,9 +100,14 @@ def main(argv=None):
     ap.add_argument("--split-sweep", action="store_true",
                     help="time split-KV over short-query shapes and range counts")
     ap.add_argument("--bwd", action="store_true", help="time the backward instead of the forward")
+    ap.add_argument("--gqa-sweep", action="store_true",
+                    help="time decoding with grouped key/value heads, one-pass vs split-KV")
     args = ap.parse_args(argv)
     if args.split_sweep:
         split_sweep()
+        return 0
+    if args.gqa_sweep:
+        gqa_sweep()
         return 0
     w = WORKLOADS[args.workload]
     causal = bool(w.causal[0] if args.causal is None else args.causal)

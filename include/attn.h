@@ -157,6 +157,24 @@ typedef struct {
 attn_status_t attn_fwd_general(const attn_fwd_params_t* params, struct CUstream_st* stream);
 
 /*
+ * attn_fwd_splitkv_general_plan / attn_fwd_splitkv_general — the split-KV
+ * forward (attn_fwd_splitkv) over general layouts and grouped key/value
+ * heads.  `params` as attn_fwd_general with mask ATTN_MASK_NONE (or
+ * ATTN_MASK_CAUSAL_BOTTOM_RIGHT with S_q = 1, which is the same); n_split,
+ * workspace and its rules as attn_fwd_splitkv (the workspace size is the
+ * same for the same B, H, S_q, d).  When H_kv < H and S_q·(H / H_kv) <= 128
+ * the query rows of all heads that share a key/value head are computed in
+ * one tile, so each key/value tile is read and multiplied once per group
+ * (decoding with grouped-query attention); such packed groups always take
+ * the split path, so their workspace is needed even for one range.
+ */
+attn_status_t attn_fwd_splitkv_general_plan(const attn_fwd_params_t* params, int64_t n_split,
+                                            int64_t* n_split_used, int64_t* workspace_bytes);
+attn_status_t attn_fwd_splitkv_general(const attn_fwd_params_t* params, int64_t n_split,
+                                       void* workspace, int64_t workspace_bytes,
+                                       struct CUstream_st* stream);
+
+/*
  * attn_fwd_host — the same forward, for inputs and outputs in HOST memory.
  *
  * Copies q_host, k_host, v_host into the caller's device buffers q_dev,

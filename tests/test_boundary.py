@@ -38,7 +38,8 @@ def test_header_declares_the_boundary():
     names = _declared_functions()
     assert names == sorted(["attn_fwd", "attn_fwd_general", "attn_fwd_host", "attn_fwd_plan", "attn_fwd_splitkv_plan",
                             "attn_fwd_splitkv", "attn_fwd_splitkv_noalloc", "attn_bwd_workspace_size",
-                            "attn_bwd", "attn_bwd_general", "attn_last_error", "attn_get_device_status",
+                            "attn_bwd", "attn_bwd_general", "attn_fwd_splitkv_general_plan",
+                            "attn_fwd_splitkv_general", "attn_last_error", "attn_get_device_status",
                             "attn_version"])
 
 
@@ -348,3 +349,18 @@ def test_general_accepts_packed_and_head_major_views(lib):
               v_layout=packed, k=A + H * d * 2, v=A + 2 * H * d * 2,
               o_layout=binding.AttnLayout(S * H * d, d, H * d))
     assert st in (binding.ATTN_ERR_CUDA, binding.ATTN_ERR_UNSUPPORTED)
+
+
+def test_splitkv_general_plan_and_mask_rules(lib):
+    G = 1 << 28
+    d = 128
+    dense = lambda heads, S: binding.AttnLayout(heads * S * d, S * d, d)  # noqa: E731
+    p = binding.AttnFwdParams(A, A + G, A + 2 * G, A + 3 * G, A + 4 * G, 2, 32, 8, 1, 9000, d,
+                              dense(32, 1), dense(8, 9000), dense(8, 9000), dense(32, 1), 0, 0.1, 1)
+    n, ws = binding.attn_fwd_splitkv_general_plan(p, 6)
+    assert n == 6 and ws == 6 * 2 * 32 * 1 * (d + 1) * 4
+    p.mask = binding.ATTN_MASK_CAUSAL_BOTTOM_RIGHT          # one query row: same as full
+    assert binding.attn_fwd_splitkv_general_plan(p, 6)[0] == 6
+    p.mask = binding.ATTN_MASK_CAUSAL
+    with pytest.raises(binding.AttnError, match="full attention"):
+        binding.attn_fwd_splitkv_general_plan(p, 6)

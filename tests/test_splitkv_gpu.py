@@ -133,3 +133,53 @@ def test_decode_workload_full_size():
     assert np.isfinite(o.float().cpu().numpy()).all()
     ro, rl = oracle.attention_forward(q, k, v, causal=False, scale=w.scale)
     assert_parity(o, lse, ro, rl, w.dtype, "decode workload")
+
+
+# ------------------------------------------------- grouped heads, general layouts
+from exact_attention_53_gb300 import fwd_splitkv_general  # noqa: E402
+
+
+def _gqa_inputs(B, H, H_kv, S_q, S_k, d, dtype, seed):
+    q = make_qkv(B, H, S_q, 1, d, dtype, seed=seed)[0]
+    _, k, v = make_qkv(B, H_kv, 1, S_k, d, dtype, seed=seed + 1)
+    return q, k, v
+
+
+def _bshd(t):
+    return t.transpose(1, 2).contiguous().transpose(1, 2)
+
+
+# (B, H, H_kv, S_q, S_k): decode with groups of 4 and 8 (packed), 16·8 = 128
+# rows exactly, MQA, and 40·4 = 160 rows (too many to pack: one head per tile)
+GQA_SHAPES = [(2, 32, 8, 1, 5000), (1, 16, 2, 1, 9000), (1, 16, 2, 16, 3000), (2, 16, 1, 1, 4100),
+              (1, 8, 2, 40, 2000), (16, 32, 8, 1, 4096)]
+
+
+@pytest.mark.parametrize("n_split", [1, 3, 0], ids=lambda n: f"split{n}")
+@pytest.mark.parametrize("shape", GQA_SHAPES, ids=lambda s: "x".join(map(str, s)))
+@pytest.mark.parametrize("dtype", ["f16", "bf16"])
+@pytest.mark.parametrize("d", [64, 128, 256])
+def test_splitkv_grouped_heads_match_oracle(d, dtype, shape, n_split):
+    B, H, H_kv, S_q, S_k = shape
+    q, k, v = _gqa_inputs(B, H, H_kv, S_q, S_k, d, dtype, seed=S_k + H * 3 + d)
+    scale = 1 / math.sqrt(d)
+    o = _bshd(torch.empty((B, H, S_q, d), dtype=q.dtype, device=DEV))
+    o, lse = fwd_splitkv_general(_bshd(q.to(DEV)), _bshd(k.to(DEV)), _bshd(v.to(DEV)),
+                                 n_split=n_split, scale=scale, out=o)
+    torch.cuda.synchronize()
+    g = H // H_kv
+    ro, rl = oracle.attention_forward(q, k.repeat_interleave(g, dim=1),
+                                      v.repeat_interleave(g, dim=1), causal=False, scale=scale)
+    assert_parity(o, lse, ro, rl, dtype, f"grouped split-KV d={d} {dtype} {shape} n={n_split}")
+
+
+def test_packed_groups_match_repeated_heads_bitwise():
+    """Packing a group's heads into one tile changes no row's arithmetic."""
+    B, H, H_kv, S_q, S_k, d = 2, 32, 8, 1, 8192, 128
+    q, k, v = _gqa_inputs(B, H, H_kv, S_q, S_k, d, "bf16", seed=71)
+    qd, kd, vd = q.to(DEV), k.to(DEV), v.to(DEV)
+    o1, l1 = fwd_splitkv_general(qd, kd, vd, n_split=5)
+    o2, l2 = fwd_splitkv(qd, kd.repeat_interleave(4, dim=1).contiguous(),
+                         vd.repeat_interleave(4, dim=1).contiguous(), n_split=5)
+    torch.cuda.synchronize()
+    assert torch.equal(o1, o2) and torch.equal(l1, l2)
