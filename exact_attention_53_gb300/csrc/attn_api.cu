@@ -532,7 +532,7 @@ attn_status_t validate_bwd_head_dim(const Problem& p) {
 // Helper streams and events of the host-buffer entry point, created on a
 // device's first attn_fwd_host call and kept for the life of the process.
 struct HostPipe {
-    static constexpr int kChunks = 4;
+    static constexpr int kChunks = 8;
     std::mutex mu;
     bool ready = false;
     cudaStream_t in = nullptr, out = nullptr;

@@ -180,7 +180,7 @@ attn_status_t attn_fwd_splitkv_general(const attn_fwd_params_t* params, int64_t 
  * Copies q_host, k_host, v_host into the caller's device buffers q_dev,
  * k_dev, v_dev, runs attn_fwd on them into o_dev, lse_dev, and copies o_dev,
  * lse_dev back into o_host, lse_host.  Heads are independent, so problems
- * above 32 MB are cut into up to four chunks of consecutive (b, h) whose
+ * above 32 MB are cut into up to eight chunks of consecutive (b, h) whose
  * uploads, forwards and downloads overlap: the copies run on two helper
  * streams that the library creates on a device's first call (with a few
  * events; no memory is allocated) and orders after the work already on
