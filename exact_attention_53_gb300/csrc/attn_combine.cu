@@ -31,11 +31,15 @@ __global__ void __launch_bounds__(256) attn_combine_kernel(const float* __restri
                                                            long long rows, int H, int S_q,
                                                            RowLayout o_lay) {
     constexpr int PER_LANE = D / 32;          // 2, 4 or 8 columns
+    // Launched as a programmatic dependent of the range kernel: wait until
+    // that grid has completed and its writes are visible.
+    asm volatile("griddepcontrol.wait;" ::: "memory");
     const long long row = static_cast<long long>(blockIdx.x) * 8 + (threadIdx.x >> 5);
     const int lane = threadIdx.x & 31;
     if (row >= rows) return;
 
-    // Largest partial LSE first, so every weight exp(LSE_s − m) is at most 1.
+    // Weights, lane-parallel over ranges (32 per pass): the largest partial LSE
+    // first, so every weight exp(LSE_s − m) is at most 1.
     float m = -INFINITY;
     for (int s = lane; s < n_split; s += 32) m = fmaxf(m, lse_part[s * rows + row]);
 #pragma unroll
@@ -46,25 +50,35 @@ __global__ void __launch_bounds__(256) attn_combine_kernel(const float* __restri
     for (int i = 0; i < PER_LANE; ++i) acc[i] = 0.f;
     float wsum = 0.f;
     const size_t col = static_cast<size_t>(lane) * PER_LANE;
-    for (int s = 0; s < n_split; ++s) {
-        const float w = expf(lse_part[s * rows + row] - m);
-        wsum += w;
-        const float* src = o_part + (static_cast<size_t>(s) * rows + row) * D + col;
-        if constexpr (PER_LANE == 2) {
-            const float2 x = *reinterpret_cast<const float2*>(src);
-            acc[0] = fmaf(w, x.x, acc[0]);
-            acc[1] = fmaf(w, x.y, acc[1]);
-        } else {
+    for (int s0 = 0; s0 < n_split; s0 += 32) {
+        const int s_lane = s0 + lane;
+        const float w_lane = s_lane < n_split ? expf(lse_part[s_lane * rows + row] - m) : 0.f;
+        wsum += w_lane;
+        const int cnt = min(32, n_split - s0);
+        // The ranges' partial rows are independent loads: unrolled so several are
+        // in flight at once.
+#pragma unroll 4
+        for (int j = 0; j < cnt; ++j) {
+            const float w = __shfl_sync(0xffffffffu, w_lane, j);
+            const float* src = o_part + (static_cast<size_t>(s0 + j) * rows + row) * D + col;
+            if constexpr (PER_LANE == 2) {
+                const float2 x = *reinterpret_cast<const float2*>(src);
+                acc[0] = fmaf(w, x.x, acc[0]);
+                acc[1] = fmaf(w, x.y, acc[1]);
+            } else {
 #pragma unroll
-            for (int i = 0; i < PER_LANE; i += 4) {
-                const float4 x = *reinterpret_cast<const float4*>(src + i);
-                acc[i] = fmaf(w, x.x, acc[i]);
-                acc[i + 1] = fmaf(w, x.y, acc[i + 1]);
-                acc[i + 2] = fmaf(w, x.z, acc[i + 2]);
-                acc[i + 3] = fmaf(w, x.w, acc[i + 3]);
+                for (int i = 0; i < PER_LANE; i += 4) {
+                    const float4 x = *reinterpret_cast<const float4*>(src + i);
+                    acc[i] = fmaf(w, x.x, acc[i]);
+                    acc[i + 1] = fmaf(w, x.y, acc[i + 1]);
+                    acc[i + 2] = fmaf(w, x.z, acc[i + 2]);
+                    acc[i + 3] = fmaf(w, x.w, acc[i + 3]);
+                }
             }
         }
     }
+#pragma unroll
+    for (int off = 16; off > 0; off >>= 1) wsum += __shfl_xor_sync(0xffffffffu, wsum, off);
     // wsum >= 1 (the largest range contributes exp(0)).
     const float inv = 1.f / wsum;
     uint32_t packed[PER_LANE / 2];
@@ -99,13 +113,23 @@ cudaError_t launch_d(const float* o_part, const float* lse_part, void* o, float*
                      cudaStream_t stream) {
     const long long blocks = (rows + 7) / 8;
     if (blocks > 0x7fffffffLL) return cudaErrorInvalidConfiguration;
+    // Programmatic stream serialisation: the launch is set up while the range
+    // kernel is still running; the kernel's griddepcontrol.wait orders the reads.
+    cudaLaunchConfig_t cfg = {};
+    cfg.gridDim = dim3(static_cast<unsigned>(blocks));
+    cfg.blockDim = dim3(256);
+    cfg.dynamicSmemBytes = 0;
+    cfg.stream = stream;
+    cudaLaunchAttribute attr[1];
+    attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+    attr[0].val.programmaticStreamSerializationAllowed = 1;
+    cfg.attrs = attr;
+    cfg.numAttrs = 1;
     if (bf16)
-        attn_combine_kernel<D, true><<<static_cast<unsigned>(blocks), 256, 0, stream>>>(
-            o_part, lse_part, o, lse, n_split, rows, H, S_q, o_lay);
-    else
-        attn_combine_kernel<D, false><<<static_cast<unsigned>(blocks), 256, 0, stream>>>(
-            o_part, lse_part, o, lse, n_split, rows, H, S_q, o_lay);
-    return cudaGetLastError();
+        return cudaLaunchKernelEx(&cfg, attn_combine_kernel<D, true>, o_part, lse_part, o, lse,
+                                  n_split, rows, H, S_q, o_lay);
+    return cudaLaunchKernelEx(&cfg, attn_combine_kernel<D, false>, o_part, lse_part, o, lse,
+                              n_split, rows, H, S_q, o_lay);
 }
 
 }  // namespace
