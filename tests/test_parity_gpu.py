@@ -235,3 +235,33 @@ def test_invalid_arguments_raise_on_gpu():
 
 def test_device_status_clean():
     attn_get_device_status()
+
+
+def test_concurrent_host_threads_on_separate_streams():
+    """Calls from two host threads on two streams give the single-threaded results."""
+    import threading
+    cases = [make_qkv(2, 4, 700, 700, 128, "bf16", seed=19 + i) for i in range(2)]
+    dev = [tuple(t.to(DEV) for t in c) for c in cases]
+    ref = [fwd(*qkv, causal=bool(i)) for i, qkv in enumerate(dev)]
+    torch.cuda.synchronize()
+    out = [None, None]
+    errors = []
+
+    def worker(i):
+        try:
+            s = torch.cuda.Stream()
+            with torch.cuda.stream(s):
+                res = [fwd(*dev[i], causal=bool(i)) for _ in range(20)]
+            s.synchronize()
+            out[i] = res[-1]
+        except Exception as e:  # noqa: BLE001 - reported below
+            errors.append(e)
+
+    threads = [threading.Thread(target=worker, args=(i,)) for i in range(2)]
+    for t in threads:
+        t.start()
+    for t in threads:
+        t.join()
+    assert not errors, errors
+    for i in range(2):
+        assert torch.equal(out[i][0], ref[i][0]) and torch.equal(out[i][1], ref[i][1])
