@@ -18,10 +18,12 @@
 //     tensor memory.  Softmax reads S with tcgen05.ld, writes P (fp16/bf16)
 //     back over the upper half of the S columns with tcgen05.st, and the PV
 //     MMA takes P straight from tensor memory.
-//   * The running maximum used for exponentiation is only raised when a row's
-//     maximum grows by more than 2^8 (kRescaleLog2); O and l then share the
-//     same stale maximum, so O / l is unchanged.  This skips almost all O
-//     rescales without approximating anything.
+//   * The running maximum used for exponentiation is only raised when a
+//     tile's row sum of exponentials exceeds 2^20 (kRescaleSum), i.e. when the
+//     scores have outgrown the maximum by enough to matter for the fp32 range;
+//     O and l always share the same (possibly stale) maximum, so O / l and the
+//     log-sum-exp are unchanged.  This skips almost all O rescales and the
+//     per-element maximum tracking, without approximating anything.
 //   * Causal: key tiles entirely above the diagonal are never loaded or
 //     computed; only tiles that straddle it (or the ragged end of the keys)
 //     take the masked path.  Query blocks are issued heaviest first.
@@ -46,7 +48,7 @@ enum : unsigned int {
     kStatusDrain = 16u,
 };
 
-constexpr float kRescaleLog2 = 8.0f;
+constexpr float kRescaleSum = 1048576.0f;   // 2^20
 constexpr float kLn2 = 0.693147180559945309f;
 
 
@@ -85,18 +87,15 @@ __device__ __forceinline__ float row_max128(float (&s)[128], int lim) {
 
 // p = 2^(s·scale_log2 − m) for one row, packed to 16-bit pairs in `pk`;
 // returns Σ p (fp32).  Two lanes at a time on the packed fp32 pipe.
-// MASKED: p = 0 for c >= lim.  TRACK: also returns in *xmax the largest
-// exponent s·scale_log2 − m over the visible keys (a maximum taken alongside
-// the exponentials, on another pipe).
-template <bool MASKED, bool BF16, bool TRACK>
+// MASKED: p = 0 for c >= lim.
+template <bool MASKED, bool BF16>
 __device__ __forceinline__ float exp_pack128(const float (&s)[128], int lim, float scale_log2,
-                                             float neg_m, uint32_t (&pk)[64], float* xmax) {
+                                             float neg_m, uint32_t (&pk)[64]) {
     using namespace sm100;
     const float2 sl2 = make_float2(scale_log2, scale_log2);
     const float2 nm = make_float2(neg_m, neg_m);
     float2 acc[4] = {make_float2(0.f, 0.f), make_float2(0.f, 0.f), make_float2(0.f, 0.f),
                      make_float2(0.f, 0.f)};
-    float mx[4] = {-INFINITY, -INFINITY, -INFINITY, -INFINITY};
 #pragma unroll
     for (int c = 0; c < 128; c += 2) {
         const float2 x = __ffma2_rn(make_float2(s[c], s[c + 1]), sl2, nm);
@@ -106,18 +105,9 @@ __device__ __forceinline__ float exp_pack128(const float (&s)[128], int lim, flo
             p0 = c < lim ? p0 : 0.f;
             p1 = c + 1 < lim ? p1 : 0.f;
         }
-        if (TRACK) {
-            if (MASKED) {
-                mx[(c >> 1) & 3] = fmax3(mx[(c >> 1) & 3], c < lim ? x.x : -INFINITY,
-                                         c + 1 < lim ? x.y : -INFINITY);
-            } else {
-                mx[(c >> 1) & 3] = fmax3(mx[(c >> 1) & 3], x.x, x.y);
-            }
-        }
         acc[(c >> 1) & 3] = __fadd2_rn(acc[(c >> 1) & 3], make_float2(p0, p1));
         pk[c >> 1] = BF16 ? pack_bf16(p0, p1) : pack_f16(p0, p1);
     }
-    if (TRACK) *xmax = fmaxf(fmax3(mx[0], mx[1], mx[2]), mx[3]);
     const float2 a01 = __fadd2_rn(acc[0], acc[1]);
     const float2 a23 = __fadd2_rn(acc[2], acc[3]);
     const float2 t = __fadd2_rn(a01, a23);
@@ -602,37 +592,37 @@ __global__ void __launch_bounds__(KernelTile<D, SPLIT>::THREADS, 1)
                     const float mx = masked ? row_max128<true>(s, lim) : row_max128<false>(s, lim);
                     m = (mx == -INFINITY) ? -INFINITY : mx * scale_log2;
                     const float neg_m = (m == -INFINITY) ? 0.f : -m;
-                    l = masked ? exp_pack128<true, BF16, false>(s, lim, scale_log2, neg_m, pk, nullptr)
-                               : exp_pack128<false, BF16, false>(s, lim, scale_log2, neg_m, pk, nullptr);
+                    l = masked ? exp_pack128<true, BF16>(s, lim, scale_log2, neg_m, pk)
+                               : exp_pack128<false, BF16>(s, lim, scale_log2, neg_m, pk);
                 } else {
-                    // Exponentiate against the running maximum and take this tile's
-                    // maximum exponent alongside.  A row whose maximum grew by more
-                    // than 2^kRescaleLog2 (rare) re-reads its scores from TMEM (P has
-                    // not been written over them yet) and is redone against the new
-                    // maximum, so the result equals the max-first order exactly.
-                    float xmax;
+                    // Exponentiate against the running maximum.  A row whose sum of
+                    // exponentials exceeds kRescaleSum (its scores outgrew the
+                    // maximum; rare) re-reads its scores from TMEM (P has not been
+                    // written over them yet) and is redone against its new maximum.
+                    // Either way O and l share one maximum, so the result is exact.
                     float lsum = masked
-                        ? exp_pack128<true, BF16, true>(s, lim, scale_log2, -m, pk, &xmax)
-                        : exp_pack128<false, BF16, true>(s, lim, scale_log2, -m, pk, &xmax);
-                    if (__any_sync(0xffffffffu, xmax > kRescaleLog2)) {
+                        ? exp_pack128<true, BF16>(s, lim, scale_log2, -m, pk)
+                        : exp_pack128<false, BF16>(s, lim, scale_log2, -m, pk);
+                    const bool grow = !(lsum <= kRescaleSum);      // also catches inf and NaN
+                    if (__any_sync(0xffffffffu, grow)) {
                         uint32_t ra[64], rb[64];
                         tmem_ld64x2(lane_base + b * T::S_STRIDE, lane_base + b * T::S_STRIDE + 64,
                                     ra, rb);
-                        if (xmax > kRescaleLog2) {
+                        if (grow) {
 #pragma unroll
                             for (int c = 0; c < 64; ++c) {
                                 s[c] = __uint_as_float(ra[c]);
                                 s[64 + c] = __uint_as_float(rb[c]);
                             }
                             const float mx = masked ? row_max128<true>(s, lim) : row_max128<false>(s, lim);
-                            const float m_new = mx * scale_log2;
+                            const float m_new = fmaxf(m, mx * scale_log2);
                             alpha = ex2_approx(m - m_new);
                             m = m_new;
                             l *= alpha;
                             rescale = true;
                             lsum = masked
-                                ? exp_pack128<true, BF16, false>(s, lim, scale_log2, -m, pk, nullptr)
-                                : exp_pack128<false, BF16, false>(s, lim, scale_log2, -m, pk, nullptr);
+                                ? exp_pack128<true, BF16>(s, lim, scale_log2, -m, pk)
+                                : exp_pack128<false, BF16>(s, lim, scale_log2, -m, pk);
                         }
                     }
                     l += lsum;
