@@ -97,41 +97,47 @@ __device__ __forceinline__ void bwd_unit_coords(int L, int BH, int n_tiles, int 
 // where masked), dS = P·(dP − Dv); packs dS (and P when WANT_P) as 16-bit
 // pairs.  Per column c: lse2[c], dd[c] (COLUMN_STATS: one value per column,
 // read from shared memory; else the row's own, broadcast).  keep(c) tells
-// whether column c is visible.
+// whether column c is visible.  Two columns at a time on the packed fp32 pipe.
 template <bool MASKED, bool BF16, bool WANT_P, bool COLUMN_STATS, typename Keep>
 __device__ __forceinline__ void grad_pack64(const uint32_t (&s)[64], const uint32_t (&dp)[64],
                                             const float* lse2, const float* dd, float row_lse2,
                                             float row_dd, float scale_log2, Keep keep,
                                             uint32_t (&pk_p)[32], uint32_t (&pk_ds)[32]) {
     using namespace sm100;
+    const float2 sl2 = make_float2(scale_log2, scale_log2);
+    const float2 row_nl = make_float2(-row_lse2, -row_lse2);
+    const float2 row_nd = make_float2(-row_dd, -row_dd);
 #pragma unroll
     for (int c = 0; c < 64; c += 4) {
-        float l[4], dv[4];
+        float2 nl[2], nd[2];
         if (COLUMN_STATS) {
             const float4 l4 = *reinterpret_cast<const float4*>(lse2 + c);
             const float4 d4 = *reinterpret_cast<const float4*>(dd + c);
-            l[0] = l4.x; l[1] = l4.y; l[2] = l4.z; l[3] = l4.w;
-            dv[0] = d4.x; dv[1] = d4.y; dv[2] = d4.z; dv[3] = d4.w;
+            nl[0] = make_float2(-l4.x, -l4.y);
+            nl[1] = make_float2(-l4.z, -l4.w);
+            nd[0] = make_float2(-d4.x, -d4.y);
+            nd[1] = make_float2(-d4.z, -d4.w);
         } else {
+            nl[0] = nl[1] = row_nl;
+            nd[0] = nd[1] = row_nd;
+        }
 #pragma unroll
-            for (int i = 0; i < 4; ++i) {
-                l[i] = row_lse2;
-                dv[i] = row_dd;
+        for (int i = 0; i < 2; ++i) {
+            const int cc = c + 2 * i;
+            const float2 x = __ffma2_rn(make_float2(__uint_as_float(s[cc]), __uint_as_float(s[cc + 1])),
+                                        sl2, nl[i]);
+            float p0 = ex2_approx(x.x);
+            float p1 = ex2_approx(x.y);
+            if (MASKED) {
+                p0 = keep(cc) ? p0 : 0.f;
+                p1 = keep(cc + 1) ? p1 : 0.f;
             }
+            const float2 t = __fadd2_rn(make_float2(__uint_as_float(dp[cc]), __uint_as_float(dp[cc + 1])),
+                                        nd[i]);
+            const float2 g = __fmul2_rn(make_float2(p0, p1), t);
+            if (WANT_P) pk_p[cc / 2] = BF16 ? pack_bf16(p0, p1) : pack_f16(p0, p1);
+            pk_ds[cc / 2] = BF16 ? pack_bf16(g.x, g.y) : pack_f16(g.x, g.y);
         }
-        float p[4], g[4];
-#pragma unroll
-        for (int i = 0; i < 4; ++i) {
-            p[i] = ex2_approx(fmaf(__uint_as_float(s[c + i]), scale_log2, -l[i]));
-            if (MASKED) p[i] = keep(c + i) ? p[i] : 0.f;
-            g[i] = p[i] * (__uint_as_float(dp[c + i]) - dv[i]);
-        }
-        if (WANT_P) {
-            pk_p[c / 2] = BF16 ? pack_bf16(p[0], p[1]) : pack_f16(p[0], p[1]);
-            pk_p[c / 2 + 1] = BF16 ? pack_bf16(p[2], p[3]) : pack_f16(p[2], p[3]);
-        }
-        pk_ds[c / 2] = BF16 ? pack_bf16(g[0], g[1]) : pack_f16(g[0], g[1]);
-        pk_ds[c / 2 + 1] = BF16 ? pack_bf16(g[2], g[3]) : pack_f16(g[2], g[3]);
     }
 }
 
