@@ -279,6 +279,62 @@ def measure_splitkv(dev, stream, iters: int = 50):
             "gpu_launches_per_call": 2 if n_split > 1 else 1, "calls_timed": iters}
 
 
+def percentiles(ms):
+    """median, p10 and p90 of a list of launch times (ms)."""
+    xs = sorted(ms)
+    pick = lambda f: xs[min(len(xs) - 1, int(round(f * (len(xs) - 1))))]  # noqa: E731
+    return {"median_ms": pick(0.5), "p10_ms": pick(0.1), "p90_ms": pick(0.9)}
+
+
+def measure_short(dev, stream, launches: int = 50):
+    """The short-sequence workloads: c1 (one 128×128 tile; launch/latency-bound, so µs and
+    GB/s of its 66 KB are reported, with a 256 MB L2 flush before every launch) and c2
+    (S = 1024, d = 64, causal): median of `launches` CUDA-event-timed launches."""
+    import torch
+
+    from exact_attention_53_gb300 import attn_fwd
+    from exact_attention_53_gb300.binding import ATTN_DTYPE_BF16, ATTN_DTYPE_F16
+    from exact_attention_53_gb300.workloads import WORKLOADS, workload_qkv
+
+    flush = torch.empty(256 << 20, dtype=torch.uint8, device=dev)
+    out = {}
+    for name in ("c1", "c2"):
+        w = WORKLOADS[name]
+        q, k, v = (t.to(dev) for t in workload_qkv(w))
+        o = torch.empty_like(q)
+        lse = torch.empty((w.B, w.H, w.S_q), dtype=torch.float32, device=dev)
+        causal = w.causal[0]
+        code = ATTN_DTYPE_BF16 if w.dtype == "bf16" else ATTN_DTYPE_F16
+
+        def launch():
+            attn_fwd(q, k, v, o, lse, w.B, w.H, w.S_q, w.S_k, w.d, int(causal), w.scale, code,
+                     stream)
+
+        for _ in range(10):
+            launch()
+        torch.cuda.synchronize(dev)
+        ms = []
+        for _ in range(launches):
+            if name == "c1":
+                flush.fill_(1)
+            a, b = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+            a.record(stream)
+            launch()
+            b.record(stream)
+            torch.cuda.synchronize(dev)
+            ms.append(a.elapsed_time(b))
+        pc = percentiles(ms)
+        t = pc["median_ms"] * 1e-3
+        out[name] = {"workload": f"{name}: B={w.B} H={w.H} S={w.S_q} d={w.d} {w.dtype} "
+                                 f"{'causal' if causal else 'full'}",
+                     "us": pc["median_ms"] * 1e3, "p10_us": pc["p10_ms"] * 1e3,
+                     "p90_us": pc["p90_ms"] * 1e3, "bytes": w.io_bytes(),
+                     "gbs": w.io_bytes() / t / 1e9, "tflops": w.flops(causal) / t / 1e12,
+                     "l2": "256 MB flush before each launch" if name == "c1" else "no flush"}
+    out["c1"]["note"] = "latency-bound (66 KB, one tile): the roofline fraction is not meaningful"
+    return out
+
+
 def measure_bwd(dev, stream, w, q, k, v, iters: int = 10):
     """Backward (dQ, dK, dV) on the benchmark workload, both masking modes.
 
@@ -428,6 +484,9 @@ def run_gpu(args, rank, world):
     out_bytes = o.numel() * 2 + lse.numel() * 4
     splitkv = measure_splitkv(dev, stream)
     backward = measure_bwd(dev, stream, w, q, k, v)
+    short = measure_short(dev, stream)
+    from exact_attention_53_gb300.binding import probe_ex2_rate
+    ex2_peak = probe_ex2_rate()
     attn_get_device_status(stream)
     sampler.stop()
 
@@ -452,9 +511,10 @@ def run_gpu(args, rank, world):
                    "global_batch": B * world, "seq_len": S_q,
                    "parallelism": f"replicas x{world}" if world > 1 else "single GPU",
                    "l2": "inputs larger than L2 (Q+K+V = 201 MB > 129 MB), no flush"},
-        "modes": {"full": {"ms": full_avg, "tflops": achieved, "frac_of_peak": achieved / peak},
+        "modes": {"full": {"ms": full_avg, "tflops": achieved, "frac_of_peak": achieved / peak,
+                           **percentiles(full_ms)},
                   "causal": {"ms": causal_avg, "tflops": achieved_c,
-                             "frac_of_peak": achieved_c / peak}},
+                             "frac_of_peak": achieved_c / peak, **percentiles(causal_ms)}},
         "roofline": {"bound": "tensor", "achieved": achieved, "peak": peak, "unit": "TFLOP/s",
                      "frac": achieved / peak, "traffic": traffic,
                      "kernel": "attn_fwd_kernel<128,bf16,full>",
@@ -482,6 +542,16 @@ def run_gpu(args, rank, world):
                             if peak_src == "measured" else "fallback 1.9 PFLOP/s"}
     backward["workload"] = f"{WORKLOAD}: B={B} H={H} S_q=S_k={S_q} d={d} bf16, dO~N(0,1)"
     line["backward"] = backward
+    line["short"] = short
+    # Secondary ceiling: exponentials (S_q·S_k per head, halved causal) per second against the
+    # ex2.approx throughput of the MUFU pipe measured by attn_probe_ex2 in this run.
+    exps = {False: B * H * S_q * S_k, True: B * H * S_q * S_k / 2}
+    line["exp_rate"] = {
+        "probe_ex2_per_s": ex2_peak,
+        "full": {"ex2_per_s": exps[False] / (full_avg * 1e-3),
+                 "frac": exps[False] / (full_avg * 1e-3) / ex2_peak},
+        "causal": {"ex2_per_s": exps[True] / (causal_avg * 1e-3),
+                   "frac": exps[True] / (causal_avg * 1e-3) / ex2_peak}}
     if not args.no_cpu_baseline and world == 1:
         line["cpu_baseline"] = cpu_baseline()
     print(json.dumps(line), flush=True)

@@ -136,6 +136,8 @@ def load_library() -> ctypes.CDLL:
         lib.attn_bwd.argtypes = [vp] * 9 + [i64, i64, i64, i64, i64, i32, ctypes.c_float, i32, vp,
                                             i64, vp]
         lib.attn_bwd.restype = i32
+        lib.attn_probe_ex2.argtypes = [vp, i32, i32, vp]
+        lib.attn_probe_ex2.restype = i32
         lib.attn_last_error.argtypes = []
         lib.attn_last_error.restype = ctypes.c_char_p
         lib.attn_get_device_status.argtypes = [vp]
@@ -311,6 +313,27 @@ def attn_bwd(q, k, v, o, lse, dout, dq, dk, dv, B, H, S_q, S_k, d, causal, scale
     _check(lib.attn_bwd(ptr(q), ptr(k), ptr(v), ptr(o), ptr(lse), ptr(dout), ptr(dq), ptr(dk),
                         ptr(dv), B, H, S_q, S_k, d, int(causal), float(scale), int(dtype),
                         ptr(workspace), int(workspace_bytes), _stream_handle(stream)))
+
+
+PROBES = ("attn_probe_ex2",)     # declared in include/attn_probe.h
+
+
+def probe_ex2_rate(blocks: int = 0, iters: int = 4096) -> float:
+    """ex2.approx evaluations per second on the current device (MUFU throughput)."""
+    lib = load_library()
+    if blocks <= 0:
+        blocks = 8 * torch.cuda.get_device_properties(torch.cuda.current_device()).multi_processor_count
+    out = torch.empty(blocks * 256, dtype=torch.float32, device="cuda")
+    st = _stream_handle(None)
+    for _ in range(2):
+        if lib.attn_probe_ex2(out.data_ptr(), blocks, iters, st) != 0:
+            raise AttnError(ATTN_ERR_CUDA, "attn_probe_ex2 failed")
+    a, b = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    a.record()
+    lib.attn_probe_ex2(out.data_ptr(), blocks, iters, st)
+    b.record()
+    torch.cuda.synchronize()
+    return blocks * 256 * 8 * iters / (a.elapsed_time(b) * 1e-3)
 
 
 def attn_get_device_status(stream=None) -> None:

@@ -42,7 +42,7 @@ def _nvcc() -> str:
 
 def _deps() -> list[str]:
     return [os.path.join(CSRC, f) for f in os.listdir(CSRC)
-            if f.endswith((".cu", ".cuh", ".h"))] + [os.path.join(INCLUDE, "attn.h")]
+            if f.endswith((".cu", ".cuh", ".h"))] + [os.path.join(INCLUDE, f) for f in os.listdir(INCLUDE)]
 
 
 def _stale(target: str, deps: list[str]) -> bool:
@@ -63,7 +63,7 @@ def build(verbose: bool = False, jobs: int | None = None) -> str:
     nvcc = _nvcc()
     os.makedirs(BUILD, exist_ok=True)
     deps = _deps()
-    jobs = jobs or max(1, min(len(INSTANCES) + len(BWD_INSTANCES) + 3, os.cpu_count() or 4))
+    jobs = jobs or max(1, min(len(INSTANCES) + len(BWD_INSTANCES) + 4, os.cpu_count() or 4))
     steps = []
     objs = []
     for d, bf16, causal, split in INSTANCES:
@@ -81,7 +81,7 @@ def build(verbose: bool = False, jobs: int | None = None) -> str:
             steps.append([nvcc, *ARCH, *FLAGS, f"-DATTN_D={d}", f"-DATTN_BF16={bf16}",
                           f"-DATTN_CAUSAL={causal}", "-c", os.path.join(CSRC, "attn_bwd_inst.cu"),
                           "-o", obj])
-    for name in ("attn_api", "attn_combine", "attn_noalloc"):
+    for name in ("attn_api", "attn_combine", "attn_noalloc", "attn_probe"):
         obj = os.path.join(BUILD, f"{name}.o")
         objs.append(obj)
         if _stale(obj, deps):

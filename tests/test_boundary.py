@@ -46,6 +46,9 @@ def test_header_declares_the_boundary():
 def test_library_exports_every_declared_symbol(lib):
     for name in _declared_functions():
         assert hasattr(lib, name), name
+    probe = open(os.path.join(ROOT, "include", "attn_probe.h")).read()
+    for name in binding.PROBES:
+        assert re.search(rf"\b{name}\s*\(", probe) and hasattr(lib, name), name
     assert set(binding.EXPORTED) == set(_declared_functions())
     assert lib.attn_version() == 10000
 
