@@ -100,5 +100,94 @@ def build(verbose: bool = False, jobs: int | None = None) -> str:
     return LIB
 
 
+def _strip_params(name: str) -> str:
+    """A demangled signature without its parameter list and leading return type."""
+    depth = 0
+    for i, ch in enumerate(name):
+        if ch == "<":
+            depth += 1
+        elif ch == ">":
+            depth -= 1
+        elif ch == "(" and depth == 0 and i > 0 and name[i - 1] in ">_abcdefghijklmnopqrstuvwxyz0123456789":
+            name = name[:i]
+            break
+    return name[5:] if name.startswith("void ") else name
+
+
+def resources(jobs: int | None = None) -> str:
+    """Compile every kernel instantiation with ``-Xptxas -v`` (into a scratch folder) and
+    return a markdown table of what ptxas reports per entry function: registers per thread at
+    launch, named barriers, stack frame and spill bytes."""
+    import re
+    import tempfile
+
+    nvcc = _nvcc()
+    jobs = jobs or max(1, min(len(INSTANCES) + len(BWD_INSTANCES), os.cpu_count() or 4))
+    with tempfile.TemporaryDirectory() as tmp:
+        cmds = []
+        for d, bf16, causal, split in INSTANCES:
+            cmds.append([nvcc, *ARCH, *FLAGS, "-Xptxas", "-v", f"-DATTN_D={d}",
+                         f"-DATTN_BF16={bf16}", f"-DATTN_CAUSAL={causal}", f"-DATTN_SPLIT={split}",
+                         "-c", os.path.join(CSRC, "attn_inst.cu"),
+                         "-o", os.path.join(tmp, f"f{len(cmds)}.o")])
+        for d, bf16, causal in BWD_INSTANCES:
+            cmds.append([nvcc, *ARCH, *FLAGS, "-Xptxas", "-v", f"-DATTN_D={d}",
+                         f"-DATTN_BF16={bf16}", f"-DATTN_CAUSAL={causal}", "-c",
+                         os.path.join(CSRC, "attn_bwd_inst.cu"),
+                         "-o", os.path.join(tmp, f"b{len(cmds)}.o")])
+        for name in ("attn_combine", "attn_probe"):
+            cmds.append([nvcc, *ARCH, *FLAGS, "-Xptxas", "-v", "-c",
+                         os.path.join(CSRC, f"{name}.cu"), "-o", os.path.join(tmp, f"{name}.o")])
+
+        def one(cmd):
+            r = subprocess.run(cmd, stdout=subprocess.PIPE, stderr=subprocess.STDOUT, text=True)
+            if r.returncode != 0:
+                raise RuntimeError("build step failed:\n" + " ".join(cmd) + "\n" + r.stdout)
+            return r.stdout
+
+        with ThreadPoolExecutor(jobs) as ex:
+            logs = list(ex.map(one, cmds))
+    rows = {}
+    for log in logs:
+        entry = None
+        for line in log.splitlines():
+            m = re.search(r"Compiling entry function '([^']+)'", line)
+            if m:
+                entry = m.group(1)
+                rows.setdefault(entry, {})
+                continue
+            if entry is None:
+                continue
+            m = re.search(r"(\d+) bytes stack frame, (\d+) bytes spill stores, (\d+) bytes spill loads",
+                          line)
+            if m:
+                rows[entry].update(stack=m.group(1), spill_st=m.group(2), spill_ld=m.group(3))
+            m = re.search(r"Used (\d+) registers(?:, used (\d+) barriers)?", line)
+            if m:
+                rows[entry].update(regs=m.group(1), barriers=m.group(2) or "0")
+    names = list(rows)
+    filt = shutil.which("cu++filt") or shutil.which("c++filt")
+    if filt:
+        out = subprocess.run([filt], input="\n".join(names), stdout=subprocess.PIPE, text=True)
+        pretty = out.stdout.splitlines()
+        if len(pretty) == len(names):
+            names_map = dict(zip(names, pretty))
+        else:
+            names_map = {n: n for n in names}
+    else:
+        names_map = {n: n for n in names}
+    lines = ["| kernel | registers/thread at launch | barriers | stack B | spill stores B | "
+             "spill loads B |", "|---|---|---|---|---|---|"]
+    for n in sorted(rows, key=lambda x: names_map[x]):
+        r = rows[n]
+        sig = _strip_params(names_map[n])
+        lines.append(f"| `{sig}` | {r.get('regs', '?')} | {r.get('barriers', '?')} | "
+                     f"{r.get('stack', '?')} | {r.get('spill_st', '?')} | {r.get('spill_ld', '?')} |")
+    return "\n".join(lines)
+
+
 if __name__ == "__main__":
-    build(verbose=True)
+    if "--resources" in sys.argv[1:]:
+        print(resources())
+    else:
+        build(verbose=True)

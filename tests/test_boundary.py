@@ -367,3 +367,10 @@ def test_splitkv_general_plan_and_mask_rules(lib):
     p.mask = binding.ATTN_MASK_CAUSAL
     with pytest.raises(binding.AttnError, match="full attention"):
         binding.attn_fwd_splitkv_general_plan(p, 6)
+
+
+def test_resource_report_strips_parameter_lists():
+    from exact_attention_53_gb300.build import _strip_params
+    assert (_strip_params("void attn::attn_fwd_kernel<(int)128, (bool)1>(CUtensorMap_st, int)")
+            == "attn::attn_fwd_kernel<(int)128, (bool)1>")
+    assert _strip_params("<unnamed>::ex2_rate_kernel(float*, int)") == "<unnamed>::ex2_rate_kernel"
