@@ -139,10 +139,14 @@ __device__ __forceinline__ void unit_coords(int L, int BH, int n_qblk, int head_
     q0 = qblk * ROWS_PER_UNIT;
 }
 
-// Persistent kernel: CTA c processes units c, c + gridDim.x, ...  Every
-// mbarrier phase and the K/V ring position carry over from one unit to the
-// next, so the next unit's Q load and first Q·Kᵀ overlap the current unit's
-// last P·V and epilogue.
+// Persistent kernel over a hardware work queue.  The grid has one CTA per
+// work unit, but only about one per SM ever starts: a running CTA does its own
+// unit (blockIdx.x), then claims further units by cancelling CTAs that have
+// not started yet (cluster launch control) and doing their work, until none
+// is left.  Units are numbered heaviest first, so this is longest-first list
+// scheduling with no counter in global memory.  Every mbarrier phase and the
+// K/V ring position carry over from one unit to the next, so the next unit's
+// Q load and first Q·Kᵀ overlap the current unit's last P·V and epilogue.
 template <int D, bool BF16, bool CAUSAL, bool SPLIT>
 __global__ void __launch_bounds__(KernelTile<D, SPLIT>::THREADS, 1)
     attn_fwd_kernel(const __grid_constant__ CUtensorMap tm_q,
@@ -164,7 +168,8 @@ __global__ void __launch_bounds__(KernelTile<D, SPLIT>::THREADS, 1)
     uint8_t* sQ = smem;
     uint8_t* sKV = sQ + T::TILES * T::Q_TILE_BYTES;
     uint8_t* sO = sKV + T::NS * T::KV_TILE_BYTES;           // O staging for TMA stores
-    uint64_t* bars = reinterpret_cast<uint64_t*>(smem + T::TILE_BYTES);
+    uint8_t* clc_resp = smem + T::TILE_BYTES;               // [CLC_SLOTS] 16-byte answers
+    uint64_t* bars = reinterpret_cast<uint64_t*>(clc_resp + T::CLC_SLOTS * 16);
     uint64_t* q_full = bars;                 // Q of the current unit landed
     uint64_t* q_empty = q_full + 1;          // last Q·Kᵀ of the unit finished
     uint64_t* kv_full = q_empty + 1;
@@ -175,7 +180,9 @@ __global__ void __launch_bounds__(KernelTile<D, SPLIT>::THREADS, 1)
     uint64_t* drain = o_done + 2;            // every MMA of the CTA finished
     uint64_t* epi_bar = drain + 1;           // [2] O rows of tile t staged, per warp
     uint64_t* stage_free = epi_bar + 2;      // staging buffer read by its TMA store
-    uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(stage_free + 1);
+    uint64_t* clc_full = stage_free + 1;     // [CLC_SLOTS] work-queue answer landed
+    uint64_t* clc_empty = clc_full + T::CLC_SLOTS;  // [CLC_SLOTS] answer read by every consumer
+    uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(clc_empty + T::CLC_SLOTS);
     volatile int* abort_flag = reinterpret_cast<volatile int*>(tmem_slot + 1);
 
     const int warp = threadIdx.x >> 5;
@@ -188,7 +195,6 @@ __global__ void __launch_bounds__(KernelTile<D, SPLIT>::THREADS, 1)
     // so each K/V tile is read and multiplied once for the whole group.
     const bool packed = SPLIT && pack > 1;
     const int units_bh = packed ? BH / pack : BH;
-    const int n_units = units_bh * n_qblk * (SPLIT ? n_split : 1);
     // Unit L -> unit head (query head, or key/value head when packed), first
     // query row, key tiles of each query tile, first key tile, split.
     auto unit_info = [&](int L, int& bh, int& q0, int& n0, int& n1, int& kb, int& sp) {
@@ -217,13 +223,30 @@ __global__ void __launch_bounds__(KernelTile<D, SPLIT>::THREADS, 1)
             hk = h / kv_group;
         }
     };
-    // Units are handed out in rounds of gridDim.x, in serpentine order (CTA c
-    // takes position c of even rounds and gridDim.x-1-c of odd ones), so a CTA
-    // that got a heavy unit in one round gets a light one in the next.
-    auto unit_of_round = [&](int r) {
-        const int G = static_cast<int>(gridDim.x);
-        const int c = static_cast<int>(blockIdx.x);
-        return r * G + ((r & 1) ? (G - 1 - c) : c);
+    // The r-th unit of this CTA: its own for r = 0, else the answer to the
+    // work-queue request the producer warp made for it (answer r-1, in slot
+    // (r-1) % CLC_SLOTS).  Returns 1 with the unit in L, 0 when the queue is
+    // empty, -1 when the wait gave up.  Warp-uniform; consumers (every warp
+    // but the producer) free the slot once read.
+    constexpr int CLC_CONSUMERS = T::SOFTMAX_WARPS + 1;
+    auto unit_at = [&](int r, int& L, unsigned int bit, bool consumer) -> int {
+        if (r == 0) {
+            L = static_cast<int>(blockIdx.x);
+            return 1;
+        }
+        const int i = r - 1;
+        const int slot = i % T::CLC_SLOTS;
+        bool got = mbar_wait(&clc_full[slot], (i / T::CLC_SLOTS) & 1, abort_flag, status, bit);
+        got = __all_sync(0xffffffffu, got);
+        if (!got) return -1;
+        int x = 0;
+        const bool won = clc_query(smem_u32(clc_resp + slot * 16), x);
+        if (consumer) {
+            __syncwarp();
+            if (lane == 0) mbar_arrive(&clc_empty[slot]);
+        }
+        L = x;
+        return won ? 1 : 0;
     };
 
     if (packed) {
@@ -249,6 +272,10 @@ __global__ void __launch_bounds__(KernelTile<D, SPLIT>::THREADS, 1)
         }
         mbar_init(drain, 1);
         mbar_init(stage_free, 1);
+        for (int s = 0; s < T::CLC_SLOTS; ++s) {
+            mbar_init(&clc_full[s], 1);
+            mbar_init(&clc_empty[s], CLC_CONSUMERS);
+        }
         *abort_flag = 0;
         fence_mbar_init();
         fence_proxy_async_smem();
@@ -309,9 +336,12 @@ __global__ void __launch_bounds__(KernelTile<D, SPLIT>::THREADS, 1)
             __syncwarp();
             ++idx;
         };
-        for (int r = 0; r * static_cast<int>(gridDim.x) < n_units && ok; ++r) {
-            const int L = unit_of_round(r);
-            if (L >= n_units) continue;
+        int claims = 0;                       // work-queue requests issued
+        for (int r = 0; ok; ++r) {
+            int L = 0;
+            const int got = unit_at(r, L, kStatusProducer, false);
+            if (got < 0) ok = false;
+            if (got <= 0) break;
             int bh, q0, n0, n1, kb, sp, b, h, hk;
             unit_info(L, bh, q0, n0, n1, kb, sp);
             heads_of(bh, b, h, hk);
@@ -351,6 +381,24 @@ __global__ void __launch_bounds__(KernelTile<D, SPLIT>::THREADS, 1)
                     if (j + 2 < n_max) issue(&tm_k, kb + j + 2, hk, b);
                 }
             }
+            if (!ok) break;
+            // Claim the next unit only now, with this unit's last loads in the
+            // ring: a unit claimed earlier would wait behind this whole unit
+            // while idle CTAs find the queue empty.
+            {
+                const int slot = claims % T::CLC_SLOTS;
+                ok = mbar_wait(&clc_empty[slot], ((claims / T::CLC_SLOTS) & 1) ^ 1, abort_flag,
+                               status, kStatusProducer);
+                ok = __all_sync(0xffffffffu, ok);
+                if (!ok) break;
+                if (leader) {
+                    fence_proxy_async_smem();     // earlier reads of the slot come first
+                    mbar_arrive_expect_tx(&clc_full[slot], 16);
+                    clc_try_cancel(smem_u32(clc_resp + slot * 16), &clc_full[slot]);
+                }
+                __syncwarp();
+                ++claims;
+            }
         }
         if (*abort_flag && leader) {
             // Let every copy this CTA started land before it exits.
@@ -368,6 +416,17 @@ __global__ void __launch_bounds__(KernelTile<D, SPLIT>::THREADS, 1)
                 const uint32_t a = smem_u32(q_full);
                 const uint32_t last = static_cast<uint32_t>(q_loads - 1) & 1u;
                 while (!mbar_try_wait(a, last)) {
+                    if (global_timer_ns() - t0 > kWaitLimitNs) {
+                        atomicOr(status, kStatusDrain);
+                        break;
+                    }
+                }
+            }
+            if (claims > 0) {
+                // and the last work-queue answer
+                const int i = claims - 1;
+                const uint32_t a = smem_u32(&clc_full[i % T::CLC_SLOTS]);
+                while (!mbar_try_wait(a, (i / T::CLC_SLOTS) & 1)) {
                     if (global_timer_ns() - t0 > kWaitLimitNs) {
                         atomicOr(status, kStatusDrain);
                         break;
@@ -437,9 +496,11 @@ __global__ void __launch_bounds__(KernelTile<D, SPLIT>::THREADS, 1)
             }
         };
         int gs = 0;                           // TILES == 1: S/PV steps across units
-        for (int r = 0; r * static_cast<int>(gridDim.x) < n_units && ok; ++r) {
-            const int L = unit_of_round(r);
-            if (L >= n_units) continue;
+        for (int r = 0; ok; ++r) {
+            int L = 0;
+            const int got = unit_at(r, L, kStatusMma, true);
+            if (got < 0) ok = false;
+            if (got <= 0) break;
             int bh, q0, n0, n1, kb, sp;
             unit_info(L, bh, q0, n0, n1, kb, sp);
             const int n_max = max(n0, n1);
@@ -546,9 +607,11 @@ __global__ void __launch_bounds__(KernelTile<D, SPLIT>::THREADS, 1)
         uint32_t my_rounds = 0;                       // staging rounds of this warpgroup
         bool stored = false;                          // this thread issued TMA stores
 
-        for (int r = 0; r * static_cast<int>(gridDim.x) < n_units && ok; ++r) {
-            const int L = unit_of_round(r);
-            if (L >= n_units) continue;
+        for (int r = 0; ok; ++r) {
+            int L = 0;
+            const int got = unit_at(r, L, kStatusSoftmax, true);
+            if (got < 0) ok = false;
+            if (got <= 0) break;
             int bh, q0, n0, n1, kb, sp;
             unit_info(L, bh, q0, n0, n1, kb, sp);
             const int n = t == 0 ? n0 : n1;
@@ -805,8 +868,9 @@ cudaError_t launch_attn_fwd(const FwdArgs& a, cudaStream_t stream) {
     const int pack = SPLIT ? a.pack : 1;
     const long long units = static_cast<long long>(a.BH / pack) * n_qblk * n_split;
     if (units > 0x7fffffffLL) return cudaErrorInvalidConfiguration;
-    // One CTA per SM (each takes the whole of tensor memory), looping over units.
-    const int grid = static_cast<int>(std::min<long long>(units, a.num_sms));
+    // One CTA per unit; each takes the whole of tensor memory and most of shared
+    // memory, so one runs per SM and the running ones cancel and take over the rest.
+    const int grid = static_cast<int>(units);
     kernel<<<grid, T::THREADS, T::SMEM_BYTES, stream>>>(a.tm_q, a.tm_k, a.tm_v, a.tm_o, a.lse, a.S_q,
                                                          a.S_k, a.BH, n_qblk, head_group,
                                                          a.scale_log2, a.status, n_split,

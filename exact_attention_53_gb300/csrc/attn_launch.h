@@ -71,8 +71,11 @@ struct FwdTile {
     static constexpr int STAGE_ROUNDS = CHUNKS / STAGE_CHUNKS;
     static constexpr int STAGE_BYTES = STAGE_CHUNKS * Q_CHUNK_BYTES;
     static constexpr int TILE_BYTES = TILES * Q_TILE_BYTES + NS * KV_TILE_BYTES + STAGE_BYTES;
-    static constexpr int NUM_BARS = 2 + 2 * NS + 2 + 2 + 2 + 1 + 2 + 1;
-    static constexpr int SMEM_BYTES = 1024 + TILE_BYTES + NUM_BARS * 8 + 16;
+    // Work-queue answers (cluster launch control) in flight: unit ids this CTA
+    // has claimed ahead of the ones it is working on.
+    static constexpr int CLC_SLOTS = 4;
+    static constexpr int NUM_BARS = 2 + 2 * NS + 2 + 2 + 2 + 1 + 2 + 1 + 2 * CLC_SLOTS;
+    static constexpr int SMEM_BYTES = 1024 + TILE_BYTES + CLC_SLOTS * 16 + NUM_BARS * 8 + 16;
     static constexpr int SOFTMAX_WARPS = 4 * TILES;
     static constexpr int PRODUCER_WARP = SOFTMAX_WARPS;       // first warp of the aux warpgroup
     static constexpr int MMA_WARP = SOFTMAX_WARPS + 1;

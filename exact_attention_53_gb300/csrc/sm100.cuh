@@ -161,6 +161,38 @@ __device__ __forceinline__ void fence_proxy_async_smem() {
     asm volatile("fence.proxy.async.shared::cta;" ::: "memory");
 }
 
+// ---------------------------------------------------------------- cluster launch control
+// Ask the hardware to cancel one CTA of this grid that has not started yet.
+// The 16-byte answer lands at `resp` (16-byte aligned shared memory) and
+// completes 16 transaction bytes on `bar`, which the caller has armed with
+// mbar_arrive_expect_tx(bar, 16).  A CTA that wins a cancellation does that
+// CTA's work itself: a hardware work queue for persistent kernels.
+__device__ __forceinline__ void clc_try_cancel(uint32_t resp, uint64_t* bar) {
+    asm volatile(
+        "clusterlaunchcontrol.try_cancel.async.shared::cta.mbarrier::complete_tx::bytes.b128 "
+        "[%0], [%1];" ::"r"(resp),
+        "r"(smem_u32(bar))
+        : "memory");
+}
+
+// Decode an answer: true and the cancelled CTA's blockIdx.x if the request
+// won a CTA; false once no CTA was left to cancel.
+__device__ __forceinline__ bool clc_query(uint32_t resp, int& ctaid_x) {
+    uint32_t won;
+    uint32_t x = 0;
+    asm volatile(
+        "{\n\t.reg .b128 r;\n\t.reg .pred p;\n\t"
+        "ld.shared.b128 r, [%2];\n\t"
+        "clusterlaunchcontrol.query_cancel.is_canceled.pred.b128 p, r;\n\t"
+        "selp.u32 %0, 1, 0, p;\n\t"
+        "@p clusterlaunchcontrol.query_cancel.get_first_ctaid::x.b32.b128 %1, r;\n\t}"
+        : "=r"(won), "+r"(x)
+        : "r"(resp)
+        : "memory");
+    ctaid_x = static_cast<int>(x);
+    return won != 0;
+}
+
 // Barrier over `count` threads (a multiple of 32) on hardware barrier `id`.
 __device__ __forceinline__ void named_bar_sync(uint32_t id, uint32_t count) {
     asm volatile("bar.sync %0, %1;" ::"r"(id), "r"(count) : "memory");
