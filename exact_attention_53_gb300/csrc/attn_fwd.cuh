@@ -11,7 +11,8 @@
 //   * One CTA owns one (batch·head, query block).  A query block is two
 //     128-row query tiles for d = 64/128, one tile for d = 256.
 //   * Warp roles: 4 softmax warps per query tile (one row per thread, the
-//     warp's TMEM lane quarter), one TMA producer warp, one MMA-issuing warp.
+//     warp's TMEM lane quarter), one TMA producer warp, one MMA-issuing warp
+//     and one warp that issues the TMA stores of O.
 //   * K and V tiles (128 keys × d, 128-byte swizzled) stream through an
 //     NS-slot shared-memory ring, handed over with full/empty mbarriers.
 //   * S = Q·Kᵀ and O += P·V are tcgen05.mma (M = 128, fp32 accumulate) into
@@ -226,9 +227,10 @@ __global__ void __launch_bounds__(KernelTile<D, SPLIT>::THREADS, 1)
     // The r-th unit of this CTA: its own for r = 0, else the answer to the
     // work-queue request the producer warp made for it (answer r-1, in slot
     // (r-1) % CLC_SLOTS).  Returns 1 with the unit in L, 0 when the queue is
-    // empty, -1 when the wait gave up.  Warp-uniform; consumers (every warp
-    // but the producer) free the slot once read.
-    constexpr int CLC_CONSUMERS = T::SOFTMAX_WARPS + 1;
+    // empty, -1 when the wait gave up.  Warp-uniform; consumers (the softmax,
+    // MMA and, without SPLIT, store warps) free the slot once read.
+    constexpr int CLC_CONSUMERS = T::SOFTMAX_WARPS + (SPLIT ? 1 : 2);
+    constexpr int STORE_WARP = T::SOFTMAX_WARPS + 2;
     auto unit_at = [&](int r, int& L, unsigned int bit, bool consumer) -> int {
         if (r == 0) {
             L = static_cast<int>(blockIdx.x);
@@ -591,6 +593,43 @@ __global__ void __launch_bounds__(KernelTile<D, SPLIT>::THREADS, 1)
             }
         }
         __syncwarp();
+      } else if (warp == STORE_WARP && !SPLIT) {
+        // ------------------------------------------------------------ O stores
+        // Stores each staged round of O with TMA and frees the staging buffer
+        // once the copy has read it, so the softmax warps never wait on a store.
+        bool ok = true;
+        uint32_t ph[2] = {0, 0};
+        bool stored = false;
+        for (int r = 0; ok; ++r) {
+            int L = 0;
+            const int got = unit_at(r, L, kStatusEpilogue, true);
+            if (got < 0) ok = false;
+            if (got <= 0) break;
+            int bh, q0, n0, n1, kb, sp;
+            unit_info(L, bh, q0, n0, n1, kb, sp);
+            for (int t = 0; t < T::TILES && ok; ++t) {
+                if ((t == 0 ? n0 : n1) <= 0) continue;
+                for (int rr = 0; rr < T::STAGE_ROUNDS; ++rr) {
+                    ok = mbar_wait(&epi_bar[t], ph[t] & 1, abort_flag, status, kStatusEpilogue);
+                    ok = __all_sync(0xffffffffu, ok);
+                    ++ph[t];
+                    if (!ok) break;
+                    if (elect_one()) {
+                        for (int c = 0; c < T::STAGE_CHUNKS; ++c)
+                            tma_store_4d(&tm_o, sO + c * T::Q_CHUNK_BYTES,
+                                         (rr * T::STAGE_CHUNKS + c) * 64, q0 + t * T::BM, bh % H,
+                                         bh / H);
+                        bulk_commit_group();
+                        bulk_wait_read_all();
+                        mbar_arrive(stage_free);
+                        stored = true;
+                    }
+                    __syncwarp();
+                }
+            }
+        }
+        if (stored) bulk_wait_all();
+        __syncwarp();
       }
       teardown();
     } else {
@@ -604,8 +643,6 @@ __global__ void __launch_bounds__(KernelTile<D, SPLIT>::THREADS, 1)
         uint32_t sc = 0;                              // S tiles consumed by this warpgroup
         uint32_t oc = 0;                              // o_done phases consumed
         uint32_t round = 0;                           // staging rounds of the whole CTA
-        uint32_t my_rounds = 0;                       // staging rounds of this warpgroup
-        bool stored = false;                          // this thread issued TMA stores
 
         for (int r = 0; ok; ++r) {
             int L = 0;
@@ -804,29 +841,11 @@ __global__ void __launch_bounds__(KernelTile<D, SPLIT>::THREADS, 1)
                                 make_uint4(w[4 * i], w[4 * i + 1], w[4 * i + 2], w[4 * i + 3]);
                         }
                     }
-                    // Every warp publishes its rows; the first warp's leader stores the
-                    // round once all four have (a bounded wait, like every other).
+                    // Every warp publishes its rows; the store warp issues the round's
+                    // TMA store once all four have.
                     fence_proxy_async_smem();
                     __syncwarp();
                     if (lane == 0) mbar_arrive(&epi_bar[t]);
-                    if (wq == 0) {
-                        bool staged = mbar_wait(&epi_bar[t], my_rounds & 1, abort_flag, status,
-                                                kStatusEpilogue);
-                        staged = __all_sync(0xffffffffu, staged);
-                        if (staged && elect_one()) {
-                            for (int c = 0; c < T::STAGE_CHUNKS; ++c)
-                                tma_store_4d(&tm_o, sO + c * T::Q_CHUNK_BYTES,
-                                             (rr * T::STAGE_CHUNKS + c) * 64, row_begin, bh % H,
-                                             bh / H);
-                            bulk_commit_group();
-                            bulk_wait_read_all();
-                            mbar_arrive(stage_free);
-                            stored = true;
-                        }
-                        __syncwarp();
-                        ok = staged;
-                    }
-                    ++my_rounds;
                     if (!ok) break;
                 }
                 if (!ok) break;
@@ -835,7 +854,6 @@ __global__ void __launch_bounds__(KernelTile<D, SPLIT>::THREADS, 1)
             }
             round += rounds_t0 + rounds_t1;
         }
-        if (stored) bulk_wait_all();                  // O writes complete before exit
         teardown();
     }
 }
