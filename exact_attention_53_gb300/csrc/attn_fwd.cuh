@@ -224,31 +224,14 @@ __global__ void __launch_bounds__(KernelTile<D, SPLIT>::THREADS, 1)
             hk = h / kv_group;
         }
     };
-    // The r-th unit of this CTA: its own for r = 0, else the answer to the
-    // work-queue request the producer warp made for it (answer r-1, in slot
-    // (r-1) % CLC_SLOTS).  Returns 1 with the unit in L, 0 when the queue is
-    // empty, -1 when the wait gave up.  Warp-uniform; consumers (the softmax,
-    // MMA and, without SPLIT, store warps) free the slot once read.
+    // Units of this CTA: its own, then those the producer warp claims from
+    // the hardware work queue.  Consumers (the softmax, MMA and, without
+    // SPLIT, store warps) free each answer's slot once read.
     constexpr int CLC_CONSUMERS = T::SOFTMAX_WARPS + (SPLIT ? 1 : 2);
     constexpr int STORE_WARP = T::SOFTMAX_WARPS + 2;
+    const WorkQueue<T::CLC_SLOTS> queue{clc_resp, clc_full, clc_empty};
     auto unit_at = [&](int r, int& L, unsigned int bit, bool consumer) -> int {
-        if (r == 0) {
-            L = static_cast<int>(blockIdx.x);
-            return 1;
-        }
-        const int i = r - 1;
-        const int slot = i % T::CLC_SLOTS;
-        bool got = mbar_wait(&clc_full[slot], (i / T::CLC_SLOTS) & 1, abort_flag, status, bit);
-        got = __all_sync(0xffffffffu, got);
-        if (!got) return -1;
-        int x = 0;
-        const bool won = clc_query(smem_u32(clc_resp + slot * 16), x);
-        if (consumer) {
-            __syncwarp();
-            if (lane == 0) mbar_arrive(&clc_empty[slot]);
-        }
-        L = x;
-        return won ? 1 : 0;
+        return queue.unit(r, L, consumer, abort_flag, status, bit);
     };
 
     if (packed) {
@@ -387,20 +370,7 @@ __global__ void __launch_bounds__(KernelTile<D, SPLIT>::THREADS, 1)
             // Claim the next unit only now, with this unit's last loads in the
             // ring: a unit claimed earlier would wait behind this whole unit
             // while idle CTAs find the queue empty.
-            {
-                const int slot = claims % T::CLC_SLOTS;
-                ok = mbar_wait(&clc_empty[slot], ((claims / T::CLC_SLOTS) & 1) ^ 1, abort_flag,
-                               status, kStatusProducer);
-                ok = __all_sync(0xffffffffu, ok);
-                if (!ok) break;
-                if (leader) {
-                    fence_proxy_async_smem();     // earlier reads of the slot come first
-                    mbar_arrive_expect_tx(&clc_full[slot], 16);
-                    clc_try_cancel(smem_u32(clc_resp + slot * 16), &clc_full[slot]);
-                }
-                __syncwarp();
-                ++claims;
-            }
+            ok = queue.claim(claims, leader, abort_flag, status, kStatusProducer);
         }
         if (*abort_flag && leader) {
             // Let every copy this CTA started land before it exits.
@@ -424,17 +394,7 @@ __global__ void __launch_bounds__(KernelTile<D, SPLIT>::THREADS, 1)
                     }
                 }
             }
-            if (claims > 0) {
-                // and the last work-queue answer
-                const int i = claims - 1;
-                const uint32_t a = smem_u32(&clc_full[i % T::CLC_SLOTS]);
-                while (!mbar_try_wait(a, (i / T::CLC_SLOTS) & 1)) {
-                    if (global_timer_ns() - t0 > kWaitLimitNs) {
-                        atomicOr(status, kStatusDrain);
-                        break;
-                    }
-                }
-            }
+            queue.drain(claims, status, kStatusDrain);   // and the last work-queue answer
         }
         __syncwarp();
       } else if (warp == T::MMA_WARP) {

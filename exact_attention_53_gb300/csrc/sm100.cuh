@@ -193,6 +193,75 @@ __device__ __forceinline__ bool clc_query(uint32_t resp, int& ctaid_x) {
     return won != 0;
 }
 
+// A CTA's sequence of work units over a grid with one CTA per unit.  Unit 0
+// is the CTA's own (blockIdx.x); unit r >= 1 is the answer to claim r-1,
+// which lands in slot (r-1) % SLOTS of `resp` (16 bytes a slot) and completes
+// full[slot].  Every consumer warp arrives once on empty[slot] after reading
+// it; the claiming warp reuses a slot only after that.  At most one claim is
+// in flight, and none is made once one has come back empty.
+template <int SLOTS>
+struct WorkQueue {
+    uint8_t* resp;
+    uint64_t* full;
+    uint64_t* empty;
+
+    // Unit r: 1 with the unit in L, 0 when the queue is empty, -1 when the
+    // wait gave up.  Warp-uniform.
+    __device__ __forceinline__ int unit(int r, int& L, bool consumer, volatile int* abort_flag,
+                                        unsigned int* status, unsigned int code) const {
+        if (r == 0) {
+            L = static_cast<int>(blockIdx.x);
+            return 1;
+        }
+        const int i = r - 1;
+        const int slot = i % SLOTS;
+        bool got = mbar_wait(&full[slot], (i / SLOTS) & 1, abort_flag, status, code);
+        got = __all_sync(0xffffffffu, got);
+        if (!got) return -1;
+        int x = 0;
+        const bool won = clc_query(smem_u32(resp + slot * 16), x);
+        if (consumer) {
+            __syncwarp();
+            if ((threadIdx.x & 31) == 0) mbar_arrive(&empty[slot]);
+        }
+        L = x;
+        return won ? 1 : 0;
+    }
+
+    // Claim the next unit (claim number `claims`, then incremented); the
+    // calling warp's `leader` lane issues it.  False when the wait gave up.
+    __device__ __forceinline__ bool claim(int& claims, bool leader, volatile int* abort_flag,
+                                          unsigned int* status, unsigned int code) const {
+        const int slot = claims % SLOTS;
+        bool ok = mbar_wait(&empty[slot], ((claims / SLOTS) & 1) ^ 1, abort_flag, status, code);
+        ok = __all_sync(0xffffffffu, ok);
+        if (!ok) return false;
+        if (leader) {
+            fence_proxy_async_smem();           // earlier reads of the slot come first
+            mbar_arrive_expect_tx(&full[slot], 16);
+            clc_try_cancel(smem_u32(resp + slot * 16), &full[slot]);
+        }
+        __syncwarp();
+        ++claims;
+        return true;
+    }
+
+    // After an abort: wait (bounded) for the last claim's answer to land.
+    __device__ __forceinline__ void drain(int claims, unsigned int* status,
+                                          unsigned int code) const {
+        if (claims == 0) return;
+        const int i = claims - 1;
+        const uint32_t a = smem_u32(&full[i % SLOTS]);
+        const uint64_t t0 = global_timer_ns();
+        while (!mbar_try_wait(a, (i / SLOTS) & 1)) {
+            if (global_timer_ns() - t0 > kWaitLimitNs) {
+                atomicOr(status, code);
+                break;
+            }
+        }
+    }
+};
+
 // Barrier over `count` threads (a multiple of 32) on hardware barrier `id`.
 __device__ __forceinline__ void named_bar_sync(uint32_t id, uint32_t count) {
     asm volatile("bar.sync %0, %1;" ::"r"(id), "r"(count) : "memory");
