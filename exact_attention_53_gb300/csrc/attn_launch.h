@@ -24,7 +24,7 @@ struct FwdArgs {
     int32_t kv_group;       // query heads per key/value head (H / H_kv)
     int32_t causal_off;     // causal: key j is visible to query i iff j <= i + causal_off
     float scale_log2;       // scale · log2(e), >= 0
-    int32_t num_sms;        // SMs of the device: the persistent grid size
+    int32_t num_sms;        // SMs of the device (split-KV range planning)
     // split-KV only (launch_attn_fwd<..., SPLIT = true>)
     int32_t n_split;        // key ranges per (head, query block)
     int32_t kv_per_split;   // key tiles per range
