@@ -189,6 +189,77 @@ def cpu_baseline(budget_s: float = 12.0):
                       f"alternating full/causal, fp64 numpy, {dt:.1f} s"}
 
 
+def cpu_per_config():
+    """The fp64 oracle timed on a bounded sample of every workload (wall clock, host cores):
+    c1 and c2 whole heads; c4 and c5 a block of 512 query rows from the middle of one head
+    (FLOPs counted exactly: a causal row i sees i + 1 keys)."""
+    import numpy as np
+
+    import oracle
+    from exact_attention_53_gb300.workloads import WORKLOADS, workload_qkv
+
+    out = {}
+    for name in ("c1", "c2", "c4", "c5"):
+        w = WORKLOADS[name]
+        causal = w.causal[0]
+        q, k, v = workload_qkv(w)
+        if name in ("c1", "c2"):
+            rows = np.arange(w.S_q)
+            what = "one whole (b,h) head"
+        else:
+            rows = np.arange(w.S_q // 2 - 256, w.S_q // 2 + 256)
+            what = f"rows {rows[0]}..{rows[-1]} of one (b,h) head"
+        keys = (rows + 1) if causal else np.full(rows.shape, w.S_k)
+        flops = float(4 * w.d * keys.sum())
+        t0 = time.perf_counter()
+        oracle.attention_rows(q[0, 0], k[0, 0], v[0, 0], rows, causal=causal, scale=w.scale)
+        dt = time.perf_counter() - t0
+        out[name] = {"tflops": flops / dt / 1e12, "seconds": dt, "sample": what}
+    return out
+
+
+def measure_long(dev, stream, launches: int = 30):
+    """The long-sequence workloads c4 (S = 16384, causal) and c5 (d = 256): median, p10 and p90
+    of `launches` CUDA-event-timed launches after 10 warm-ups; inputs (≥ 201 MB) exceed L2."""
+    import torch
+
+    from exact_attention_53_gb300 import attn_fwd
+    from exact_attention_53_gb300.binding import ATTN_DTYPE_BF16
+    from exact_attention_53_gb300.workloads import WORKLOADS, workload_qkv
+
+    peak = load_peaks()[0].get("bf16_tflops")
+    out = {}
+    for name in ("c4", "c5"):
+        w = WORKLOADS[name]
+        causal = w.causal[0]
+        q, k, v = (t.to(dev) for t in workload_qkv(w))
+        o = torch.empty_like(q)
+        lse = torch.empty((w.B, w.H, w.S_q), dtype=torch.float32, device=dev)
+
+        def launch():
+            attn_fwd(q, k, v, o, lse, w.B, w.H, w.S_q, w.S_k, w.d, int(causal), w.scale,
+                     ATTN_DTYPE_BF16, stream)
+
+        for _ in range(10):
+            launch()
+        torch.cuda.synchronize(dev)
+        ms = []
+        for _ in range(launches):
+            a, b = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+            a.record(stream)
+            launch()
+            b.record(stream)
+            torch.cuda.synchronize(dev)
+            ms.append(a.elapsed_time(b))
+        pc = percentiles(ms)
+        tf = w.flops(causal) / (pc["median_ms"] * 1e-3) / 1e12
+        out[name] = {"workload": f"{name}: B={w.B} H={w.H} S={w.S_q} d={w.d} {w.dtype} "
+                                 f"{'causal' if causal else 'full'}",
+                     **pc, "tflops": tf, "frac_of_peak": tf / peak if peak else None}
+        del q, k, v, o, lse
+    return out
+
+
 def run_reference(args, rank, world):
     """The fp64 oracle on the host cores, K timed steps of one head pair each."""
     if rank != 0:
@@ -485,6 +556,7 @@ def run_gpu(args, rank, world):
     splitkv = measure_splitkv(dev, stream)
     backward = measure_bwd(dev, stream, w, q, k, v)
     short = measure_short(dev, stream)
+    long_ = measure_long(dev, stream)
     from exact_attention_53_gb300.binding import probe_ex2_rate
     ex2_peak = probe_ex2_rate()
     attn_get_device_status(stream)
@@ -543,6 +615,7 @@ def run_gpu(args, rank, world):
     backward["workload"] = f"{WORKLOAD}: B={B} H={H} S_q=S_k={S_q} d={d} bf16, dO~N(0,1)"
     line["backward"] = backward
     line["short"] = short
+    line["long"] = long_
     # Secondary ceiling: exponentials (S_q·S_k per head, halved causal) per second against the
     # ex2.approx throughput of the MUFU pipe measured by attn_probe_ex2 in this run.
     exps = {False: B * H * S_q * S_k, True: B * H * S_q * S_k / 2}
@@ -554,6 +627,7 @@ def run_gpu(args, rank, world):
                    "frac": exps[True] / (causal_avg * 1e-3) / ex2_peak}}
     if not args.no_cpu_baseline and world == 1:
         line["cpu_baseline"] = cpu_baseline()
+        line["cpu_baseline"]["per_config"] = cpu_per_config()
     print(json.dumps(line), flush=True)
 
 
