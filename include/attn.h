@@ -23,7 +23,10 @@
  * built into the library), keeps no pointer after a call returns, and
  * enqueues all device work on `stream` (NULL = the legacy default stream;
  * attn_fwd_host also uses two helper streams of its own); calls return before
- * the work completes.
+ * the work completes.  Forward kernels hand out their work units through the
+ * GPU's own work queue (one CTA per unit; running CTAs cancel and take over
+ * CTAs that have not started), so they keep no counter in device memory and
+ * calls on different streams may run concurrently without coordination.
  *
  * Errors.  Argument checks happen on the host before anything is enqueued and
  * return a status; attn_last_error() then describes the offending argument
