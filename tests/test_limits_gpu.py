@@ -72,3 +72,28 @@ def test_many_more_units_than_sms(causal):
                                           scale=1 / math.sqrt(d))
         assert_parity(o[b:b + 1, h:h + 1], lse[b:b + 1, h:h + 1], ro, rl, "f16",
                       f"head ({b},{h}) causal={causal}")
+
+
+def test_grid_beyond_65535_units():
+    """66560 one-block units: a grid far past 65535 CTAs, all but about one per SM taken over
+    through the work queue.  Every output row must be written (O starts as NaN), and sampled
+    heads, the first and the last among them, match the oracle.  Heads of different batches
+    get different V (a per-batch offset), so a unit written to the wrong place shows up."""
+    B, H, S, d = 512, 130, 128, 64
+    q1, k1, v1 = (t.to(DEV) for t in make_qkv(1, H, S, S, d, "bf16", seed=64))
+    shift = (torch.arange(B, device=DEV, dtype=torch.float32) / B).view(B, 1, 1, 1)
+    q = q1.expand(B, -1, -1, -1).contiguous()
+    k = k1.expand(B, -1, -1, -1).contiguous()
+    v = (v1.float() + shift).to(torch.bfloat16)
+    o = torch.full_like(q, float("nan"))
+    lse = torch.full((B, H, S), float("nan"), dtype=torch.float32, device=DEV)
+    o, lse = fwd(q, k, v, causal=True, out=o, lse=lse)
+    torch.cuda.synchronize()
+    assert torch.isfinite(o).all().item() and torch.isfinite(lse).all().item()
+    rng = np.random.default_rng(65)
+    picks = {(0, 0), (B - 1, H - 1), *((int(x), int(y)) for x, y in rng.integers(0, (B, H), (6, 2)))}
+    for b, h in picks:
+        qc, kc, vc = (t[b:b + 1, h:h + 1].cpu() for t in (q, k, v))
+        ro, rl = oracle.attention_forward(qc, kc, vc, causal=True, scale=1 / math.sqrt(d))
+        assert_parity(o[b:b + 1, h:h + 1], lse[b:b + 1, h:h + 1], ro, rl, "bf16",
+                      f"head ({b},{h}) of {B * H}")
