@@ -8,8 +8,9 @@
 // SM.
 //
 // How it maps onto Blackwell:
-//   * One CTA owns one (batch·head, query block).  A query block is two
-//     128-row query tiles for d = 64/128, one tile for d = 256.
+//   * A work unit is one (batch·head, query block); a query block is two
+//     128-row query tiles for d = 64/128, one tile for d = 256.  One CTA runs
+//     per SM and takes units from the hardware work queue (below).
 //   * Warp roles: 4 softmax warps per query tile (one row per thread, the
 //     warp's TMEM lane quarter), one TMA producer warp, one MMA-issuing warp
 //     and one warp that issues the TMA stores of O.
