@@ -561,6 +561,31 @@ attn_status_t host_pipe(int dev, HostPipe** out) {
     return ATTN_OK;
 }
 
+// One helper stream per device for the backward's dQ kernel (see BwdArgs).
+struct BwdFork {
+    std::mutex mu;
+    bool ready = false;
+    cudaStream_t aux = nullptr;
+    cudaEvent_t fork = nullptr, join = nullptr;
+};
+BwdFork g_bwd_fork[kMaxDevices];
+
+attn_status_t bwd_fork(int dev, BwdFork** out) {
+    BwdFork& f = g_bwd_fork[dev];
+    std::lock_guard<std::mutex> lock(f.mu);
+    if (!f.ready) {
+        cudaError_t e = cudaStreamCreateWithFlags(&f.aux, cudaStreamNonBlocking);
+        if (e == cudaSuccess) e = cudaEventCreateWithFlags(&f.fork, cudaEventDisableTiming);
+        if (e == cudaSuccess) e = cudaEventCreateWithFlags(&f.join, cudaEventDisableTiming);
+        if (e != cudaSuccess)
+            return fail(ATTN_ERR_CUDA, "creating the backward helper stream: %s",
+                        cudaGetErrorString(e));
+        f.ready = true;
+    }
+    *out = &f;
+    return ATTN_OK;
+}
+
 }  // namespace
 
 extern "C" {
@@ -956,7 +981,16 @@ attn_status_t attn_bwd_general(const attn_bwd_params_t* a, struct CUstream_st* s
     g.status = g_status_ptr[dev].load();
     BwdLaunchFn fn = pick_bwd(p.d, p.dtype == ATTN_DTYPE_BF16, p.causal);
     if (!fn) return fail(ATTN_ERR_UNSUPPORTED, "no backward kernel for d=%lld", (long long)p.d);
-    cudaError_t e = fn(g, stream);
+    BwdFork* fork = nullptr;
+    if ((s = bwd_fork(dev, &fork)) != ATTN_OK) return s;
+    g.aux_stream = fork->aux;
+    g.ev_fork = fork->fork;
+    g.ev_join = fork->join;
+    cudaError_t e;
+    {
+        std::lock_guard<std::mutex> lock(fork->mu);
+        e = fn(g, stream);
+    }
     if (e != cudaSuccess) return fail(ATTN_ERR_CUDA, "backward launch: %s", cudaGetErrorString(e));
     return ok();
 }

@@ -56,9 +56,10 @@ struct BwdTile {
     static constexpr int NS = D == 64 ? 8 : 4;        // ring slots, two 64-row tiles each
     static constexpr int SLOT_BYTES = 2 * SMALL_TILE;
     static constexpr int STAT_FLOATS = 2 * BS;        // per slot: LSE·log2e and D of 64 rows
-    static constexpr int NUM_BARS = 2 + 2 * NS + 2 + 2 + 1 + 1;
+    static constexpr int CLC_SLOTS = 4;               // work-queue answers in flight
+    static constexpr int NUM_BARS = 2 + 2 * NS + 2 + 2 + 1 + 1 + 2 * CLC_SLOTS;
     static constexpr int TILE_BYTES = 2 * BIG_TILE + NS * SLOT_BYTES + NS * STAT_FLOATS * 4;
-    static constexpr int SMEM_BYTES = 1024 + TILE_BYTES + NUM_BARS * 8 + 16;
+    static constexpr int SMEM_BYTES = 1024 + TILE_BYTES + CLC_SLOTS * 16 + NUM_BARS * 8 + 16;
     static constexpr int THREADS = 192;               // 4 softmax warps, producer, MMA
     static constexpr int PRODUCER_WARP = 4;
     static constexpr int MMA_WARP = 5;
@@ -272,7 +273,8 @@ __global__ void __launch_bounds__(BwdTile<D>::THREADS, 1)
     uint8_t* sV = sK + T::BIG_TILE;
     uint8_t* sRing = sV + T::BIG_TILE;                // slot s: Q at s·SLOT, dO at +SMALL_TILE
     float* sStat = reinterpret_cast<float*>(sRing + T::NS * T::SLOT_BYTES);
-    uint64_t* bars = reinterpret_cast<uint64_t*>(smem + T::TILE_BYTES);
+    uint8_t* clc_resp = smem + T::TILE_BYTES;         // [CLC_SLOTS] 16-byte answers
+    uint64_t* bars = reinterpret_cast<uint64_t*>(clc_resp + T::CLC_SLOTS * 16);
     uint64_t* kv_full = bars;
     uint64_t* kv_empty = kv_full + 1;
     uint64_t* slot_full = kv_empty + 1;
@@ -281,7 +283,9 @@ __global__ void __launch_bounds__(BwdTile<D>::THREADS, 1)
     uint64_t* p_full = s_full + 2;            // [2] Pᵀ and dSᵀ of buffer b written (per warp)
     uint64_t* acc_done = p_full + 2;          // dV and dK of the unit complete
     uint64_t* drain = acc_done + 1;
-    uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(drain + 1);
+    uint64_t* clc_full = drain + 1;           // [CLC_SLOTS] work-queue answer landed
+    uint64_t* clc_empty = clc_full + T::CLC_SLOTS;
+    uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(clc_empty + T::CLC_SLOTS);
     volatile int* abort_flag = reinterpret_cast<volatile int*>(tmem_slot + 1);
 
     const int warp = threadIdx.x >> 5;
@@ -309,10 +313,22 @@ __global__ void __launch_bounds__(BwdTile<D>::THREADS, 1)
             ++h;
         }
     };
-    auto unit_of_round = [&](int r) {
+    // Full attention: units come from the hardware work queue (one CTA per
+    // unit in the grid; see WorkQueue), the producer claiming the next one
+    // after each unit's loads.  Causal: a persistent grid takes the units in
+    // rounds of gridDim.x, in serpentine order (CTA c takes position c of even
+    // rounds and gridDim.x-1-c of odd ones).  unit_at returns 1 with the unit
+    // in L, 2 when this CTA has no unit in round r, 0 when it is done, -1 when
+    // a wait gave up.  The four softmax warps and the MMA warp consume queue
+    // answers.
+    const WorkQueue<T::CLC_SLOTS> queue{clc_resp, clc_full, clc_empty};
+    auto unit_at = [&](int r, int& L, bool consumer, unsigned int code) -> int {
+        if (!CAUSAL) return queue.unit(r, L, consumer, abort_flag, status, code);
         const int G = static_cast<int>(gridDim.x);
         const int c = static_cast<int>(blockIdx.x);
-        return r * G + ((r & 1) ? (G - 1 - c) : c);
+        if (static_cast<long long>(r) * G >= n_units) return 0;
+        L = r * G + ((r & 1) ? (G - 1 - c) : c);
+        return L < n_units ? 1 : 2;
     };
 
     if (threadIdx.x == 0) {
@@ -328,6 +344,10 @@ __global__ void __launch_bounds__(BwdTile<D>::THREADS, 1)
         }
         mbar_init(acc_done, 1);
         mbar_init(drain, 1);
+        for (int s = 0; s < T::CLC_SLOTS; ++s) {
+            mbar_init(&clc_full[s], 1);
+            mbar_init(&clc_empty[s], 5);         // softmax warps 0-3 and the MMA warp
+        }
         *abort_flag = 0;
         fence_mbar_init();
         fence_proxy_async_smem();
@@ -354,12 +374,22 @@ __global__ void __launch_bounds__(BwdTile<D>::THREADS, 1)
         bool ok = true;
         int idx = 0;      // ring position, across units
         int uk = 0;       // units with work started by this CTA
-        for (int r = 0; r * static_cast<int>(gridDim.x) < n_units && ok; ++r) {
-            const int L = unit_of_round(r);
-            if (L >= n_units) continue;
+        int claims = 0;   // work-queue requests issued (full attention)
+        auto claim_next = [&]() {
+            if (!CAUSAL) ok = queue.claim(claims, leader, abort_flag, status, kStatusBwdProducer);
+        };
+        for (int r = 0; ok; ++r) {
+            int L = 0;
+            const int got = unit_at(r, L, false, kStatusBwdProducer);
+            if (got < 0) ok = false;
+            if (got <= 0) break;
+            if (got == 2) continue;
             int b, hk, kt, q_begin, n;
             unit_info(L, b, hk, kt, q_begin, n);
-            if (n == 0) continue;
+            if (n == 0) {
+                claim_next();
+                continue;
+            }
             ok = mbar_wait(kv_empty, (uk & 1) ^ 1, abort_flag, status, kStatusBwdProducer);
             ok = __all_sync(0xffffffffu, ok);
             if (!ok) break;
@@ -399,6 +429,8 @@ __global__ void __launch_bounds__(BwdTile<D>::THREADS, 1)
                 __syncwarp();
                 ++idx;
             }
+            if (!ok) break;
+            claim_next();    // the next unit, once this one's loads are all issued
         }
         if (*abort_flag && leader) {
             // Let every copy this CTA started land before it exits.
@@ -421,6 +453,7 @@ __global__ void __launch_bounds__(BwdTile<D>::THREADS, 1)
                     }
                 }
             }
+            queue.drain(claims, status, kStatusBwdDrain);
         }
         __syncwarp();
     } else if (warp == T::MMA_WARP) {
@@ -475,9 +508,12 @@ __global__ void __launch_bounds__(BwdTile<D>::THREADS, 1)
             }
         };
         uint32_t pc0 = 0, pc1 = 0;
-        for (int r = 0; r * static_cast<int>(gridDim.x) < n_units && ok; ++r) {
-            const int L = unit_of_round(r);
-            if (L >= n_units) continue;
+        for (int r = 0; ok; ++r) {
+            int L = 0;
+            const int got = unit_at(r, L, true, kStatusBwdMma);
+            if (got < 0) ok = false;
+            if (got <= 0) break;
+            if (got == 2) continue;
             int b, hk, kt, q_begin, n;
             unit_info(L, b, hk, kt, q_begin, n);
             if (n == 0) continue;
@@ -544,9 +580,12 @@ __global__ void __launch_bounds__(BwdTile<D>::THREADS, 1)
         bool ok = true;
         uint32_t gs = 0;
         int uk = 0;
-        for (int r = 0; r * static_cast<int>(gridDim.x) < n_units && ok; ++r) {
-            const int L = unit_of_round(r);
-            if (L >= n_units) continue;
+        for (int r = 0; ok; ++r) {
+            int L = 0;
+            const int got = unit_at(r, L, true, kStatusBwdSoftmax);
+            if (got < 0) ok = false;
+            if (got <= 0) break;
+            if (got == 2) continue;
             int b, hk, kt, q_begin, n;
             unit_info(L, b, hk, kt, q_begin, n);
             const int key = kt * T::BU + row;
@@ -641,9 +680,10 @@ struct DqTile {
     // dP MMA is done, K only after the step's dQ MMA.
     static constexpr int KS = D == 64 ? 5 : 3;        // K ring slots
     static constexpr int VS = D == 64 ? 4 : 2;        // V ring slots
-    static constexpr int NUM_BARS = 2 + 2 * KS + 2 * VS + 2 + 1 + 2 + 1 + 1;
+    static constexpr int CLC_SLOTS = 4;               // work-queue answers in flight
+    static constexpr int NUM_BARS = 2 + 2 * KS + 2 * VS + 2 + 1 + 2 + 1 + 1 + 2 * CLC_SLOTS;
     static constexpr int TILE_BYTES = 2 * TILE + (KS + VS) * TILE;
-    static constexpr int SMEM_BYTES = 1024 + TILE_BYTES + NUM_BARS * 8 + 16;
+    static constexpr int SMEM_BYTES = 1024 + TILE_BYTES + CLC_SLOTS * 16 + NUM_BARS * 8 + 16;
     static constexpr int THREADS = 192;
     static constexpr int PRODUCER_WARP = 4;
     static constexpr int MMA_WARP = 5;
@@ -675,7 +715,8 @@ __global__ void __launch_bounds__(DqTile<D>::THREADS, 1)
     uint8_t* sdO = sQ + T::TILE;
     uint8_t* sKr = sdO + T::TILE;                      // K ring
     uint8_t* sVr = sKr + T::KS * T::TILE;              // V ring
-    uint64_t* bars = reinterpret_cast<uint64_t*>(smem + T::TILE_BYTES);
+    uint8_t* clc_resp = smem + T::TILE_BYTES;          // [CLC_SLOTS] 16-byte answers
+    uint64_t* bars = reinterpret_cast<uint64_t*>(clc_resp + T::CLC_SLOTS * 16);
     uint64_t* q_full = bars;
     uint64_t* q_empty = q_full + 1;
     uint64_t* k_full = q_empty + 1;
@@ -687,7 +728,9 @@ __global__ void __launch_bounds__(DqTile<D>::THREADS, 1)
     uint64_t* p_full = dp_free + 1;          // [2] dS written over S_b (per warp)
     uint64_t* acc_done = p_full + 2;
     uint64_t* drain = acc_done + 1;
-    uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(drain + 1);
+    uint64_t* clc_full = drain + 1;          // [CLC_SLOTS] work-queue answer landed
+    uint64_t* clc_empty = clc_full + T::CLC_SLOTS;
+    uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(clc_empty + T::CLC_SLOTS);
     volatile int* abort_flag = reinterpret_cast<volatile int*>(tmem_slot + 1);
 
     const int warp = threadIdx.x >> 5;
@@ -703,10 +746,22 @@ __global__ void __launch_bounds__(DqTile<D>::THREADS, 1)
             n = min(n_ks, last_key / T::BS + 1);
         }
     };
-    auto unit_of_round = [&](int r) {
+    // Full attention: units come from the hardware work queue (one CTA per
+    // unit in the grid; see WorkQueue), the producer claiming the next one
+    // after each unit's loads.  Causal: a persistent grid takes the units in
+    // rounds of gridDim.x, in serpentine order (CTA c takes position c of even
+    // rounds and gridDim.x-1-c of odd ones).  unit_at returns 1 with the unit
+    // in L, 2 when this CTA has no unit in round r, 0 when it is done, -1 when
+    // a wait gave up.  The four softmax warps and the MMA warp consume queue
+    // answers.
+    const WorkQueue<T::CLC_SLOTS> queue{clc_resp, clc_full, clc_empty};
+    auto unit_at = [&](int r, int& L, bool consumer, unsigned int code) -> int {
+        if (!CAUSAL) return queue.unit(r, L, consumer, abort_flag, status, code);
         const int G = static_cast<int>(gridDim.x);
         const int c = static_cast<int>(blockIdx.x);
-        return r * G + ((r & 1) ? (G - 1 - c) : c);
+        if (static_cast<long long>(r) * G >= n_units) return 0;
+        L = r * G + ((r & 1) ? (G - 1 - c) : c);
+        return L < n_units ? 1 : 2;
     };
 
     if (threadIdx.x == 0) {
@@ -727,6 +782,10 @@ __global__ void __launch_bounds__(DqTile<D>::THREADS, 1)
         mbar_init(dp_free, 4);
         mbar_init(acc_done, 1);
         mbar_init(drain, 1);
+        for (int s = 0; s < T::CLC_SLOTS; ++s) {
+            mbar_init(&clc_full[s], 1);
+            mbar_init(&clc_empty[s], 5);         // softmax warps 0-3 and the MMA warp
+        }
         *abort_flag = 0;
         fence_mbar_init();
         fence_proxy_async_smem();
@@ -771,9 +830,13 @@ __global__ void __launch_bounds__(DqTile<D>::THREADS, 1)
             __syncwarp();
             ++idx;
         };
-        for (int r = 0; r * static_cast<int>(gridDim.x) < n_units && ok; ++r) {
-            const int L = unit_of_round(r);
-            if (L >= n_units) continue;
+        int claims = 0;   // work-queue requests issued (full attention)
+        for (int r = 0; ok; ++r) {
+            int L = 0;
+            const int got = unit_at(r, L, false, kStatusBwdProducer);
+            if (got < 0) ok = false;
+            if (got <= 0) break;
+            if (got == 2) continue;
             int bh, qt, n;
             unit_info(L, bh, qt, n);
             const int b = bh / H, h = bh - b * H, hk = h / kv_group;
@@ -794,6 +857,9 @@ __global__ void __launch_bounds__(DqTile<D>::THREADS, 1)
                 load(&tm_k, sKr, k_full, k_empty, T::KS, kidx, t * T::BS, hk, b);
                 load(&tm_v, sVr, v_full, v_empty, T::VS, vidx, t * T::BS, hk, b);
             }
+            if (!ok) break;
+            // the next unit, once this one's loads are all issued
+            if (!CAUSAL) ok = queue.claim(claims, leader, abort_flag, status, kStatusBwdProducer);
         }
         if (*abort_flag && leader) {
             const uint64_t t0 = global_timer_ns();
@@ -819,6 +885,7 @@ __global__ void __launch_bounds__(DqTile<D>::THREADS, 1)
                     }
                 }
             }
+            queue.drain(claims, status, kStatusBwdDrain);
         }
         __syncwarp();
     } else if (warp == T::MMA_WARP) {
@@ -887,9 +954,12 @@ __global__ void __launch_bounds__(DqTile<D>::THREADS, 1)
         };
         // The dP buffer is free for the first step of a unit once the previous
         // unit's last step has released it (dpf counts releases; gs counts steps).
-        for (int r = 0; r * static_cast<int>(gridDim.x) < n_units && ok; ++r) {
-            const int L = unit_of_round(r);
-            if (L >= n_units) continue;
+        for (int r = 0; ok; ++r) {
+            int L = 0;
+            const int got = unit_at(r, L, true, kStatusBwdMma);
+            if (got < 0) ok = false;
+            if (got <= 0) break;
+            if (got == 2) continue;
             int bh, qt, n;
             unit_info(L, bh, qt, n);
             ok = mbar_wait(q_full, uq & 1, abort_flag, status, kStatusBwdMma);
@@ -965,9 +1035,12 @@ __global__ void __launch_bounds__(DqTile<D>::THREADS, 1)
         bool ok = true;
         uint32_t gs = 0;
         int uq = 0;
-        for (int r = 0; r * static_cast<int>(gridDim.x) < n_units && ok; ++r) {
-            const int L = unit_of_round(r);
-            if (L >= n_units) continue;
+        for (int r = 0; ok; ++r) {
+            int L = 0;
+            const int got = unit_at(r, L, true, kStatusBwdSoftmax);
+            if (got < 0) ok = false;
+            if (got <= 0) break;
+            if (got == 2) continue;
             int bh, qt, n;
             unit_info(L, bh, qt, n);
             const int q_idx = qt * T::BU + row;
@@ -1057,6 +1130,16 @@ cudaError_t launch_attn_bwd(const BwdArgs& a, cudaStream_t stream) {
     cudaError_t err = cudaGetLastError();
     if (err != cudaSuccess) return err;
 
+    // dQ and dK/dV only read what prep wrote: with a helper stream, the dQ
+    // kernel forks off here and its CTAs take the SMs that the dK/dV kernel's
+    // last units leave idle.
+    cudaStream_t dq_stream = stream;
+    if (a.aux_stream) {
+        err = cudaEventRecord(a.ev_fork, stream);
+        if (err == cudaSuccess) err = cudaStreamWaitEvent(a.aux_stream, a.ev_fork, 0);
+        if (err != cudaSuccess) return err;
+        dq_stream = a.aux_stream;
+    }
     const long long op_bytes = 2LL * D * 2;   // per row of one head: two operands
     const long long group_bytes = 48LL << 20;
 
@@ -1069,7 +1152,10 @@ cudaError_t launch_attn_bwd(const BwdArgs& a, cudaStream_t stream) {
     if (units_kv > 0x7fffffffLL) return cudaErrorInvalidConfiguration;
     const int hg_kv = static_cast<int>(
         std::max<long long>(1, group_bytes / (op_bytes * a.S_q * a.kv_group)));
-    kdkdv<<<static_cast<int>(std::min<long long>(units_kv, a.num_sms)), T::THREADS, T::SMEM_BYTES,
+    // Full attention: one CTA per unit (the work queue hands the units out);
+    // causal: one persistent CTA per SM.
+    kdkdv<<<static_cast<int>(CAUSAL ? std::min<long long>(units_kv, a.num_sms) : units_kv), T::THREADS,
+            T::SMEM_BYTES,
             stream>>>(a.tm_k_fixed, a.tm_v_fixed, a.tm_q_step, a.tm_do_step, a.lse2, a.delta,
                       static_cast<uint16_t*>(a.dk), static_cast<uint16_t*>(a.dv), a.dk_lay,
                       a.dv_lay, a.S_q, a.S_k, bh_kv, a.H, a.kv_group, a.S_pad, hg_kv,
@@ -1085,11 +1171,16 @@ cudaError_t launch_attn_bwd(const BwdArgs& a, cudaStream_t stream) {
     const long long units_q = static_cast<long long>(a.BH) * n_qt;
     if (units_q > 0x7fffffffLL) return cudaErrorInvalidConfiguration;
     const int hg_q = static_cast<int>(std::max<long long>(1, group_bytes / (op_bytes * a.S_k)));
-    kdq<<<static_cast<int>(std::min<long long>(units_q, a.num_sms)), TQ::THREADS, TQ::SMEM_BYTES,
-          stream>>>(a.tm_q_fixed, a.tm_do_fixed, a.tm_k_fixed, a.tm_v_fixed, a.lse2, a.delta,
+    kdq<<<static_cast<int>(CAUSAL ? std::min<long long>(units_q, a.num_sms) : units_q), TQ::THREADS,
+          TQ::SMEM_BYTES,
+          dq_stream>>>(a.tm_q_fixed, a.tm_do_fixed, a.tm_k_fixed, a.tm_v_fixed, a.lse2, a.delta,
                     static_cast<uint16_t*>(a.dq), a.dq_lay, a.S_q, a.S_k, a.BH, a.H, a.kv_group,
                     a.S_pad, hg_q, a.causal_off, a.scale, a.scale_log2, a.status);
-    return cudaGetLastError();
+    err = cudaGetLastError();
+    if (err != cudaSuccess || !a.aux_stream) return err;
+    err = cudaEventRecord(a.ev_join, a.aux_stream);
+    if (err != cudaSuccess) return err;
+    return cudaStreamWaitEvent(stream, a.ev_join, 0);
 }
 
 }  // namespace attn

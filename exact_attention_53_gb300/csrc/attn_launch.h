@@ -135,6 +135,13 @@ struct BwdArgs {
     float scale, scale_log2;
     int32_t num_sms;
     unsigned int* status;
+    // When set, the dQ kernel runs on aux_stream, concurrently with the dK/dV
+    // kernel on the caller's stream (they read the same inputs and write
+    // disjoint outputs): ev_fork orders it after the prep kernel, ev_join
+    // brings the caller's stream back after it.  The caller holds a lock that
+    // serialises use of these three.
+    cudaStream_t aux_stream;
+    cudaEvent_t ev_fork, ev_join;
 };
 
 template <int D, bool BF16, bool CAUSAL>

@@ -22,7 +22,8 @@
  * memory (split-KV partials go to a caller workspace or to a static array
  * built into the library), keeps no pointer after a call returns, and
  * enqueues all device work on `stream` (NULL = the legacy default stream;
- * attn_fwd_host also uses two helper streams of its own); calls return before
+ * attn_fwd_host also uses two helper streams of its own, attn_bwd one, each
+ * forked from and joined back to `stream`); calls return before
  * the work completes.  Forward kernels hand out their work units through the
  * GPU's own work queue (one CTA per unit; running CTAs cancel and take over
  * CTAs that have not started), so they keep no counter in device memory and
@@ -71,7 +72,8 @@ typedef struct {
     int64_t q_tiles_per_cta;  /* 2 for d <= 128 (ping-pong), 1 for d = 256 */
     int64_t bh;               /* B·H */
     int64_t units;            /* work units, bh · ceil(q_tiles / q_tiles_per_cta); the launch
-                                 runs min(units, SM count) persistent CTAs over them */
+                                 has one CTA per unit, of which about one per SM runs and
+                                 takes the rest over through the GPU's work queue */
     int32_t threads;          /* threads per CTA */
     int32_t smem_bytes;       /* dynamic shared memory per CTA */
     int32_t tmem_cols;        /* tensor-memory columns allocated per CTA */
@@ -275,7 +277,13 @@ attn_status_t attn_bwd_workspace_size(int64_t B, int64_t H, int64_t S_q, int64_t
                                       attn_dtype_t dtype, int64_t* workspace_bytes);
 
 /*
- * attn_bwd — enqueue the backward on `stream` (three kernels, in order).
+ * attn_bwd — enqueue the backward on `stream`: a prep kernel, then the dK/dV
+ * kernel on `stream` and the dQ kernel, at the same time, on a helper stream
+ * that the library creates for the device on its first backward call (forked
+ * from `stream` after the prep kernel and joined back before the call's end,
+ * so `stream` sees one ordered operation).  A stream capture of `stream`
+ * takes the helper stream in with it; keep other captures of attn_bwd on the
+ * same device from overlapping it in time.
  *
  *   q, k, v    the forward's inputs (layouts as attn_fwd), device, 16-byte aligned
  *   o, lse     the forward's outputs for the same q, k, v, causal and scale
