@@ -154,3 +154,68 @@ def test_bwd_key_gradients_sum_to_zero():
         s = dk.float().sum(dim=2)
         scale = dk.float().abs().sum(dim=2)
         assert (s.abs() <= 0.02 * scale + 1e-3).all()
+
+
+def _bwd_into(q, k, v, o, lse, do, dq, dk, dv, ws, causal, scale):
+    from exact_attention_53_gb300 import attn_bwd
+    B, H, S_q, d = q.shape
+    attn_bwd(q, k, v, o, lse, do, dq, dk, dv, B, H, S_q, k.shape[2], d, int(causal), scale, 1, ws,
+             ws.numel())
+
+
+@pytest.mark.parametrize("causal", [False, True], ids=["full", "causal"])
+def test_bwd_result_ordered_on_callers_stream(causal):
+    """dQ is computed on a helper stream; work queued on the caller's stream after the call
+    must see all three gradients complete (the call joins the helper stream back)."""
+    from exact_attention_53_gb300 import attn_bwd_workspace_size
+    q, k, v = (t.to(DEV) for t in make_qkv(2, 8, 1024, 1024, 128, "bf16", seed=37))
+    do = make_qkv(2, 8, 1024, 1, 128, "bf16", seed=38)[0].to(DEV)
+    scale = 1 / math.sqrt(128)
+    o, lse = fwd(q, k, v, causal=causal, scale=scale)
+    ws = torch.empty(attn_bwd_workspace_size(2, 8, 1024, 1024, 128, 1), dtype=torch.uint8,
+                     device=DEV)
+    ref = bwd(q, k, v, o, lse, do, causal=causal, scale=scale)
+    torch.cuda.synchronize()
+    s = torch.cuda.Stream()
+    with torch.cuda.stream(s):
+        for _ in range(5):
+            dq, dk, dv = (torch.zeros_like(t) for t in (q, k, v))
+            _bwd_into(q, k, v, o, lse, do, dq, dk, dv, ws, causal, scale)
+            copies = [t.clone() for t in (dq, dk, dv)]     # queued right behind the call
+            s.synchronize()
+            for x, y in zip(copies, ref):
+                assert torch.equal(x, y)
+
+
+def test_bwd_captures_into_a_cuda_graph():
+    """A stream capture of the call takes the helper stream in with it; replays give the
+    eager result bit for bit."""
+    from exact_attention_53_gb300 import attn_bwd_workspace_size
+    q, k, v = (t.to(DEV) for t in make_qkv(1, 4, 700, 900, 64, "f16", seed=39))
+    do = make_qkv(1, 4, 700, 1, 64, "f16", seed=40)[0].to(DEV)
+    o, lse = fwd(q, k, v, scale=0.125)
+    ws = torch.empty(attn_bwd_workspace_size(1, 4, 700, 900, 64, 0), dtype=torch.uint8,
+                     device=DEV)
+    dq, dk, dv = (torch.empty_like(t) for t in (q, k, v))
+    from exact_attention_53_gb300 import attn_bwd
+
+    def call():
+        attn_bwd(q, k, v, o, lse, do, dq, dk, dv, 1, 4, 700, 900, 64, 0, 0.125, 0, ws, ws.numel())
+
+    call()                                              # eager (creates the helper stream)
+    torch.cuda.synchronize()
+    ref = [t.clone() for t in (dq, dk, dv)]
+    g = torch.cuda.CUDAGraph()
+    s = torch.cuda.Stream()
+    with torch.cuda.stream(s):
+        call()
+    s.synchronize()
+    with torch.cuda.graph(g, stream=s):
+        call()
+    for _ in range(3):
+        for t in (dq, dk, dv):
+            t.zero_()
+        g.replay()
+        torch.cuda.synchronize()
+        for x, y in zip((dq, dk, dv), ref):
+            assert torch.equal(x, y)
