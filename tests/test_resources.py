@@ -1,0 +1,47 @@
+"""Build-time resource checks (CPU only; needs nvcc).
+
+Every kernel instantiation is compiled with ``-Xptxas -v`` (the build's own flags) and must not
+spill, and the two-tile forward kernels must launch with exactly the 168 registers per thread
+that their warpgroup register split assumes (the host refuses to launch them otherwise, so a
+drift here would only show up on a GPU).
+"""
+
+import re
+
+import pytest
+
+
+@pytest.fixture(scope="module")
+def table():
+    from exact_attention_53_gb300 import build as b
+    try:
+        b._nvcc()
+    except RuntimeError:
+        pytest.skip("nvcc not available")
+    rows = {}
+    for line in b.resources().splitlines()[2:]:
+        cells = [c.strip() for c in line.strip("|").split("|")]
+        rows[cells[0].strip("`")] = tuple(int(x) for x in cells[1:])
+    return rows
+
+
+def test_every_kernel_reported(table):
+    from exact_attention_53_gb300.build import BWD_INSTANCES, INSTANCES
+    fwd = [k for k in table if "attn_fwd_kernel" in k]
+    bwd = [k for k in table if re.search(r"attn_bwd_(dkdv|dq|prep)_kernel", k)]
+    assert len(fwd) == len(INSTANCES)
+    # dK/dV and dQ per instance, prep per (d, dtype)
+    assert len(bwd) == 2 * len(BWD_INSTANCES) + len(BWD_INSTANCES) // 2
+
+
+def test_no_kernel_spills(table):
+    spilling = {k: v for k, v in table.items() if v[3] or v[4]}
+    assert not spilling, f"register spills: {spilling}"
+
+
+def test_two_tile_forward_launch_registers(table):
+    # (head dim, split): head dims 64 and 128 without split-KV run two query tiles per CTA
+    for name, (regs, *_rest) in table.items():
+        m = re.match(r"attn::attn_fwd_kernel<\(int\)(\d+), \(bool\)\d, \(bool\)\d, \(bool\)(\d)>", name)
+        if m and int(m.group(1)) in (64, 128) and m.group(2) == "0":
+            assert regs == 168, f"{name}: {regs} registers at launch, the split expects 168"
