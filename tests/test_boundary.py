@@ -374,3 +374,25 @@ def test_resource_report_strips_parameter_lists():
     assert (_strip_params("void attn::attn_fwd_kernel<(int)128, (bool)1>(CUtensorMap_st, int)")
             == "attn::attn_fwd_kernel<(int)128, (bool)1>")
     assert _strip_params("<unnamed>::ex2_rate_kernel(float*, int)") == "<unnamed>::ex2_rate_kernel"
+
+
+@pytest.mark.parametrize("lang", ["c99", "c++17"])
+def test_public_headers_compile_as_plain_c_and_cpp(tmp_path, lang):
+    """include/*.h is a C ABI: it must compile on its own as strict C99 and as C++, with no
+    CUDA or torch headers on the include path."""
+    import shutil
+    import subprocess
+    cc = shutil.which("gcc" if lang == "c99" else "g++")
+    if cc is None:
+        pytest.skip("no host compiler")
+    inc = os.path.join(os.path.dirname(os.path.dirname(os.path.abspath(__file__))), "include")
+    headers = sorted(f for f in os.listdir(inc) if f.endswith(".h"))
+    src = tmp_path / "use_headers.c"
+    src.write_text("".join(f'#include "{h}"\n' for h in headers) + "int main(void) { return 0; }\n")
+    cmd = [cc, f"-std={lang}", "-Wall", "-Wextra", "-Werror", "-fsyntax-only", "-I", inc]
+    if lang == "c99":
+        cmd.append("-pedantic")
+    else:
+        cmd += ["-x", "c++"]
+    r = subprocess.run(cmd + [str(src)], capture_output=True, text=True)
+    assert r.returncode == 0, r.stderr
