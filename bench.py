@@ -629,6 +629,81 @@ def run_gpu(args, rank, world):
         line["cpu_baseline"]["per_config"] = cpu_per_config()
     print(json.dumps(line), flush=True)
 
+# ------------------------------------------------------------------ sweeps
+# Range-count and grouped-head sweeps of the split-KV forward (``--sweep``):
+# µs per call, printed as markdown tables, outside the benchmark's timed steps.
+SWEEP_SHAPES = [(2, 16, 1, 32768, 128), (1, 8, 1, 131072, 128), (8, 32, 1, 8192, 128),
+                (2, 16, 1, 32768, 64), (2, 8, 1, 32768, 256), (2, 16, 128, 32768, 128)]
+SWEEP_SPLITS = (0, 2, 4, 8, 16, 32)
+GQA_SHAPES = [(8, 32, 8, 1, 8192, 128), (2, 64, 8, 1, 32768, 128), (4, 32, 4, 4, 16384, 128),
+              (16, 32, 8, 1, 4096, 128), (2, 32, 8, 1, 65536, 64)]
+
+
+def _mean_ms(fn, iters=20):
+    import torch
+
+    for _ in range(3):
+        fn()
+    torch.cuda.synchronize()
+    a, b = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    a.record()
+    for _ in range(iters):
+        fn()
+    b.record()
+    torch.cuda.synchronize()
+    return a.elapsed_time(b) / iters
+
+
+def split_sweep():
+    """µs per call of the one-pass and split-KV forwards (bf16, full attention)."""
+    import torch
+
+    from exact_attention_53_gb300 import (attn_fwd_splitkv_plan, attn_get_device_status, fwd,
+                                          fwd_splitkv)
+    from exact_attention_53_gb300.workloads import make_qkv
+
+    dev = torch.device("cuda")
+    print("| shape (B, H, S_q, S_k, d) | one-pass | " +
+          " | ".join("auto (ranges)" if n == 0 else str(n) for n in SWEEP_SPLITS) + " |")
+    for B, H, S_q, S_k, d in SWEEP_SHAPES:
+        q, k, v = (t.to(dev) for t in make_qkv(B, H, S_q, S_k, d, "bf16", seed=1))
+        o = torch.empty_like(q)
+        lse = torch.empty((B, H, S_q), dtype=torch.float32, device=dev)
+        cells = [f"{1e3 * _mean_ms(lambda: fwd(q, k, v, out=o, lse=lse)):.1f}"]
+        for n in SWEEP_SPLITS:
+            used, ws = attn_fwd_splitkv_plan(B, H, S_q, S_k, d, 1, n)
+            work = torch.empty(max(ws, 16), dtype=torch.uint8, device=dev)
+            t = 1e3 * _mean_ms(lambda: fwd_splitkv(q, k, v, n_split=n, workspace=work, out=o,
+                                                   lse=lse))
+            cells.append(f"{t:.1f} ({used})" if n == 0 else f"{t:.1f}")
+        attn_get_device_status()
+        print(f"| {B}, {H}, {S_q}, {S_k}, {d} | " + " | ".join(cells) + " |", flush=True)
+
+
+def gqa_sweep():
+    """Decoding with grouped key/value heads: one-pass vs split-KV with packed heads."""
+    import torch
+
+    from exact_attention_53_gb300 import attn_get_device_status, fwd_general, fwd_splitkv_general
+    from exact_attention_53_gb300.workloads import make_qkv
+
+    dev = torch.device("cuda")
+    print("| shape (B, H, H_kv, S_q, S_k, d) | one-pass µs | split-KV µs (auto) | split GB/s |")
+    print("|---|---|---|---|")
+    for B, H, H_kv, S_q, S_k, d in GQA_SHAPES:
+        q = make_qkv(B, H, S_q, 1, d, "bf16", seed=2)[0].to(dev)
+        _, k, v = (t.to(dev) for t in make_qkv(B, H_kv, 1, S_k, d, "bf16", seed=3))
+        o = torch.empty_like(q)
+        lse = torch.empty((B, H, S_q), dtype=torch.float32, device=dev)
+        work = torch.empty(64 << 20, dtype=torch.uint8, device=dev)
+        t1 = 1e3 * _mean_ms(lambda: fwd_general(q, k, v, out=o, lse=lse))
+        t2 = 1e3 * _mean_ms(lambda: fwd_splitkv_general(q, k, v, n_split=0, workspace=work,
+                                                         out=o, lse=lse))
+        by = 2 * (2 * B * H * S_q * d + 2 * B * H_kv * S_k * d) + 4 * B * H * S_q
+        attn_get_device_status()
+        print(f"| {B}, {H}, {H_kv}, {S_q}, {S_k}, {d} | {t1:.1f} | {t2:.1f} | {by / t2 / 1e3:.0f} |",
+              flush=True)
+
 
 def main():
     ap = argparse.ArgumentParser(description=__doc__.split("\n")[0])
@@ -638,7 +713,12 @@ def main():
     ap.add_argument("--impl", choices=["ours", "reference"], default="ours")
     ap.add_argument("--no-cpu-baseline", action="store_true",
                     help="skip the ~12 s oracle timing on the host cores")
+    ap.add_argument("--sweep", choices=["split", "gqa"], default=None,
+                    help="print a split-KV range-count or grouped-head table instead")
     args = ap.parse_args()
+    if args.sweep:
+        (split_sweep if args.sweep == "split" else gqa_sweep)()
+        return
     args.warmup = max(3, args.warmup)   # at least three untimed warm-up steps
     world = _env_int("WORLD_SIZE", 1)
     rank = _env_int("RANK", 0)

@@ -148,6 +148,32 @@ def load_library() -> ctypes.CDLL:
         return lib
 
 
+DEBUG_EXPORTS = ("attn_debug_fwd", "attn_debug_status")   # declared in include/attn_debug.h
+_debug_lib = None
+
+
+def load_debug_library() -> ctypes.CDLL:
+    """Open libattn_debug.so (once): the forward kernel built with 1 ms waits and a hook
+    that makes one work unit's waits run out (include/attn_debug.h).  Tests only."""
+    global _debug_lib
+    with _lock:
+        if _debug_lib is not None:
+            return _debug_lib
+        path = os.path.join(_PKG, "libattn_debug.so")
+        if not os.path.exists(path):
+            raise AttnError(ATTN_ERR_UNSUPPORTED,
+                            f"{path} is missing; build it with exact_attention_53_gb300.build.build()")
+        lib = ctypes.CDLL(path)
+        i64, vp = ctypes.c_int64, ctypes.c_void_p
+        lib.attn_debug_fwd.argtypes = [vp, vp, vp, vp, vp, i64, i64, i64, ctypes.c_float,
+                                       ctypes.c_int, vp]
+        lib.attn_debug_fwd.restype = ctypes.c_int
+        lib.attn_debug_status.argtypes = [ctypes.POINTER(ctypes.c_uint), vp]
+        lib.attn_debug_status.restype = ctypes.c_int
+        _debug_lib = lib
+        return lib
+
+
 def attn_last_error() -> str:
     return load_library().attn_last_error().decode()
 

@@ -1,9 +1,12 @@
-"""Build libattn.so in-tree with nvcc for sm_103a.
+"""Build libattn.so (and its debug twin libattn_debug.so) in-tree with nvcc for sm_103a.
 
 Each (head_dim, dtype, causal / split-KV) instantiation of the kernel is
 compiled as its own object in parallel, then linked with the merge kernel and
 the C-ABI layer into
-``exact_attention_53_gb300/libattn.so``.  Objects go to ``_build/`` beside this
+``exact_attention_53_gb300/libattn.so``.  ``libattn_debug.so`` holds one forward
+instantiation compiled with ``ATTN_DEBUG_FAULTS`` (1 ms waits and a hook that
+makes one work unit's waits run out) for the failure-detection tests; the
+release library never contains it.  Objects go to ``_build/`` beside this
 file; an object is rebuilt only when a source or header is newer than it.
 """
 
@@ -21,6 +24,7 @@ CSRC = os.path.join(PKG, "csrc")
 INCLUDE = os.path.join(ROOT, "include")
 BUILD = os.path.join(PKG, "_build")
 LIB = os.path.join(PKG, "libattn.so")
+DEBUG_LIB = os.path.join(PKG, "libattn_debug.so")
 
 ARCH = ["-gencode", "arch=compute_103a,code=sm_103a"]
 FLAGS = ["-O3", "-std=c++17", "-lineinfo", "-Xcompiler", "-fPIC", "-I" + INCLUDE, "-I" + CSRC]
@@ -86,17 +90,22 @@ def build(verbose: bool = False, jobs: int | None = None) -> str:
         objs.append(obj)
         if _stale(obj, deps):
             steps.append([nvcc, *ARCH, *FLAGS, "-c", os.path.join(CSRC, f"{name}.cu"), "-o", obj])
+    debug_obj = os.path.join(BUILD, "attn_debug.o")
+    if _stale(debug_obj, deps):
+        steps.append([nvcc, *ARCH, *FLAGS, "-c", os.path.join(CSRC, "attn_debug.cu"), "-o",
+                      debug_obj])
     if steps:
         if verbose:
             print(f"[build] compiling {len(steps)} objects with {jobs} jobs", file=sys.stderr)
         with ThreadPoolExecutor(jobs) as ex:
             list(ex.map(_run, steps))
-    if steps or _stale(LIB, objs):
-        tmp = LIB + ".tmp"
-        _run([nvcc, *ARCH, "-shared", "-Xcompiler", "-fPIC", *objs, "-o", tmp])
-        os.replace(tmp, LIB)
-        if verbose:
-            print(f"[build] linked {LIB}", file=sys.stderr)
+    for lib, lib_objs in ((LIB, objs), (DEBUG_LIB, [debug_obj])):
+        if _stale(lib, lib_objs):
+            tmp = lib + ".tmp"
+            _run([nvcc, *ARCH, "-shared", "-Xcompiler", "-fPIC", *lib_objs, "-o", tmp])
+            os.replace(tmp, lib)
+            if verbose:
+                print(f"[build] linked {lib}", file=sys.stderr)
     return LIB
 
 

@@ -17,6 +17,7 @@
 
 #include "attn.h"
 #include "attn_launch.h"
+#include "sm100.cuh"
 
 namespace {
 
@@ -39,11 +40,13 @@ attn_status_t ok() {
     return ATTN_OK;
 }
 
-// Set (bit per role) by a kernel whose bounded wait ran out.
-__device__ unsigned int g_attn_status;
+// Status bits (bit per role) set by a kernel whose bounded wait ran out, and
+// the number of the last launch that gave up.
+__device__ attn::DeviceWords g_attn_words;
 
 std::atomic<int> g_device_checked[kMaxDevices];          // 0 unknown, 1 ok, 2 unsupported
-std::atomic<unsigned int*> g_status_ptr[kMaxDevices];
+std::atomic<attn::DeviceWords*> g_words_ptr[kMaxDevices];
+std::atomic<unsigned long long> g_launches[kMaxDevices];  // kernel launches numbered per device
 std::atomic<int> g_num_sms[kMaxDevices];
 std::atomic<void*> g_noalloc_scratch[kMaxDevices];       // attn_fwd_splitkv_noalloc's scratch
 
@@ -108,8 +111,6 @@ attn_status_t validate_sizes(Problem& p, int64_t B, int64_t H, int64_t S_q, int6
         return fail(ATTN_ERR_INVALID_ARG, "causal must be 0 or 1, got %d", causal);
     if (!std::isfinite(scale))
         return fail(ATTN_ERR_INVALID_ARG, "scale must be finite");
-    if (scale < 0.f)
-        return fail(ATTN_ERR_UNSUPPORTED, "scale must be >= 0, got %g", (double)scale);
     if (B * H > INT32_MAX || B > INT32_MAX || H > INT32_MAX)
         return fail(ATTN_ERR_INVALID_ARG, "B*H = %lld exceeds 2^31-1", (long long)(B * H));
     if (S_q > kMaxSeq) return fail(ATTN_ERR_INVALID_ARG, "S_q=%lld exceeds 2^22", (long long)S_q);
@@ -249,18 +250,30 @@ attn_status_t check_device(int* dev_out) {
         g_device_checked[dev].store(state, std::memory_order_release);
         if (state == 1) {
             void* sp = nullptr;
-            e = cudaGetSymbolAddress(&sp, g_attn_status);
+            e = cudaGetSymbolAddress(&sp, g_attn_words);
             if (e != cudaSuccess) {
                 g_device_checked[dev].store(0);
                 return fail(ATTN_ERR_CUDA, "cudaGetSymbolAddress(status): %s", cudaGetErrorString(e));
             }
-            g_status_ptr[dev].store(static_cast<unsigned int*>(sp));
+            g_words_ptr[dev].store(static_cast<attn::DeviceWords*>(sp));
         }
     }
     if (state != 1)
         return fail(ATTN_ERR_UNSUPPORTED, "device %d is not an sm_103 GPU; this library is built for sm_103a only", dev);
     *dev_out = dev;
     return ATTN_OK;
+}
+
+// A fresh launch number on device dev (never 0, which the abort word holds
+// when no launch has given up).
+unsigned long long next_launch(int dev) { return g_launches[dev].fetch_add(1) + 1; }
+
+// Time budget of each CTA of a launch doing `flops` of work: 5 s plus the
+// time the work would take at 10 TFLOP/s, two orders of magnitude below what
+// the kernels sustain, so only a CTA that has stopped making progress meets it.
+unsigned long long budget_ns(double flops) {
+    const double ns = 5e9 + flops / 1e4;
+    return ns > 1e18 ? 1000000000000000000ull : static_cast<unsigned long long>(ns);
 }
 
 attn_status_t encode_rows(CUtensorMap* map, const void* base, const Problem& p, int64_t S,
@@ -393,7 +406,10 @@ attn_status_t fill_args(attn::FwdArgs& a, const Problem& p, int dev, const void*
     a.kv_group = static_cast<int32_t>(p.H / p.H_kv);
     a.causal_off = static_cast<int32_t>(p.causal_off);
     a.scale_log2 = static_cast<float>(static_cast<double>(p.scale) * 1.4426950408889634);
-    a.status = g_status_ptr[dev].load();
+    a.words = g_words_ptr[dev].load();
+    a.launch = next_launch(dev);
+    a.budget_ns = budget_ns(4.0 * double(p.B) * double(p.H) * double(p.S_q) * double(p.S_k) *
+                            double(p.d));
     a.num_sms = g_num_sms[dev].load();
     a.n_split = 1;
     a.kv_per_split = 0;
@@ -978,7 +994,12 @@ attn_status_t attn_bwd_general(const attn_bwd_params_t* a, struct CUstream_st* s
     g.scale = p.scale;
     g.scale_log2 = static_cast<float>(static_cast<double>(p.scale) * 1.4426950408889634);
     g.num_sms = g_num_sms[dev].load();
-    g.status = g_status_ptr[dev].load();
+    g.words = g_words_ptr[dev].load();
+    g.launch_dkdv = next_launch(dev);
+    g.launch_dq = next_launch(dev);
+    // seven S_q×S_k×d products of 2 flops per element between the two kernels
+    g.budget_ns = budget_ns(14.0 * double(p.B) * double(p.H) * double(p.S_q) * double(p.S_k) *
+                            double(p.d));
     BwdLaunchFn fn = pick_bwd(p.d, p.dtype == ATTN_DTYPE_BF16, p.causal);
     if (!fn) return fail(ATTN_ERR_UNSUPPORTED, "no backward kernel for d=%lld", (long long)p.d);
     BwdFork* fork = nullptr;
@@ -1025,18 +1046,20 @@ attn_status_t attn_get_device_status(struct CUstream_st* stream) {
     int dev = 0;
     attn_status_t s = check_device(&dev);
     if (s != ATTN_OK) return s;
-    unsigned int v = 0;
-    e = cudaMemcpyFromSymbol(&v, g_attn_status, sizeof(v));
+    attn::DeviceWords w{};
+    e = cudaMemcpyFromSymbol(&w, g_attn_words, sizeof(w));
     if (e != cudaSuccess) return fail(ATTN_ERR_CUDA, "reading status: %s", cudaGetErrorString(e));
-    if (v == 0) return ok();
-    const unsigned int zero = 0;
-    e = cudaMemcpyToSymbol(g_attn_status, &zero, sizeof(zero));
+    const unsigned int v = w.status;
+    if (v == 0 && w.abort_launch == 0) return ok();
+    const attn::DeviceWords zero{};
+    e = cudaMemcpyToSymbol(g_attn_words, &zero, sizeof(zero));
     if (e != cudaSuccess) return fail(ATTN_ERR_CUDA, "clearing status: %s", cudaGetErrorString(e));
-    return fail(ATTN_ERR_TIMEOUT, "a bounded wait ran out in:%s%s%s%s%s%s%s%s%s",
+    return fail(ATTN_ERR_TIMEOUT, "a bounded wait ran out in:%s%s%s%s%s%s%s%s%s%s",
                 (v & 1u) ? " producer" : "", (v & 2u) ? " mma" : "", (v & 4u) ? " softmax" : "",
                 (v & 8u) ? " epilogue" : "", (v & 16u) ? " drain" : "",
                 (v & 32u) ? " bwd-producer" : "", (v & 64u) ? " bwd-mma" : "",
-                (v & 128u) ? " bwd-softmax" : "", (v & 256u) ? " bwd-drain" : "");
+                (v & 128u) ? " bwd-softmax" : "", (v & 256u) ? " bwd-drain" : "",
+                (v & attn::sm100::kStatusDeadline) ? " (launch deadline passed)" : "");
 }
 
 int attn_version(void) { return kVersion; }

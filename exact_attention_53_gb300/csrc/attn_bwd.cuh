@@ -262,7 +262,8 @@ __global__ void __launch_bounds__(BwdTile<D>::THREADS, 1)
                          uint16_t* __restrict__ dk, uint16_t* __restrict__ dv, RowLayout dk_lay,
                          RowLayout dv_lay, int S_q, int S_k, int BHkv, int H, int kv_group,
                          int S_pad, int head_group, int causal_off, float scale,
-                         float scale_log2, unsigned int* __restrict__ status) {
+                         float scale_log2, DeviceWords* __restrict__ words,
+                         unsigned long long launch, unsigned long long budget_ns) {
     using T = BwdTile<D>;
     using namespace sm100;
 
@@ -287,6 +288,7 @@ __global__ void __launch_bounds__(BwdTile<D>::THREADS, 1)
     uint64_t* clc_empty = clc_full + T::CLC_SLOTS;
     uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(clc_empty + T::CLC_SLOTS);
     volatile int* abort_flag = reinterpret_cast<volatile int*>(tmem_slot + 1);
+    unsigned int* status = &words->status;
 
     const int warp = threadIdx.x >> 5;
     const int lane = threadIdx.x & 31;
@@ -371,6 +373,7 @@ __global__ void __launch_bounds__(BwdTile<D>::THREADS, 1)
             tma_prefetch_desc(&tm_do);
         }
         __syncwarp();
+        LaunchWatch watch(words, launch, budget_ns);
         bool ok = true;
         int idx = 0;      // ring position, across units
         int uk = 0;       // units with work started by this CTA
@@ -379,6 +382,7 @@ __global__ void __launch_bounds__(BwdTile<D>::THREADS, 1)
             if (!CAUSAL) ok = queue.claim(claims, leader, abort_flag, status, kStatusBwdProducer);
         };
         for (int r = 0; ok; ++r) {
+            if (watch.stop(abort_flag, status)) break;
             int L = 0;
             const int got = unit_at(r, L, false, kStatusBwdProducer);
             if (got < 0) ok = false;
@@ -405,6 +409,10 @@ __global__ void __launch_bounds__(BwdTile<D>::THREADS, 1)
             __syncwarp();
             int h = hk * kv_group, qi = q_begin;
             for (int t = 0; t < n && ok; ++t, next_step(q_begin, h, qi)) {
+                if ((idx & 7) == 0 && watch.stop(abort_flag, status)) {
+                    ok = false;
+                    break;
+                }
                 const int slot = idx % T::NS;
                 ok = mbar_wait(&slot_empty[slot], ((idx / T::NS) & 1) ^ 1, abort_flag, status,
                                kStatusBwdProducer);
@@ -566,8 +574,8 @@ __global__ void __launch_bounds__(BwdTile<D>::THREADS, 1)
         while (!mbar_try_wait(a, 0)) {
             if (global_timer_ns() - t0 > kWaitLimitNs) {
                 if (elect_one()) {
-                    atomicOr(status, kStatusBwdDrain);
                     *abort_flag = 1;
+                    atomicOr(status, kStatusBwdDrain);
                 }
                 break;
             }
@@ -659,6 +667,7 @@ __global__ void __launch_bounds__(BwdTile<D>::THREADS, 1)
     if (warp == 0) {
         tc_fence_after();
         tmem_dealloc(tmem, T::TMEM_COLS);
+        if (lane == 0) publish_abort(abort_flag, words, launch);
     }
 }
 
@@ -684,7 +693,7 @@ struct DqTile {
     static constexpr int NUM_BARS = 2 + 2 * KS + 2 * VS + 2 + 1 + 2 + 1 + 1 + 2 * CLC_SLOTS;
     static constexpr int TILE_BYTES = 2 * TILE + (KS + VS) * TILE;
     static constexpr int SMEM_BYTES = 1024 + TILE_BYTES + CLC_SLOTS * 16 + NUM_BARS * 8 + 16;
-    static constexpr int THREADS = 192;
+    static constexpr int THREADS = 192;               // 4 softmax warps, producer, MMA
     static constexpr int PRODUCER_WARP = 4;
     static constexpr int MMA_WARP = 5;
     static constexpr uint32_t TMEM_COLS = 512;
@@ -704,7 +713,8 @@ __global__ void __launch_bounds__(DqTile<D>::THREADS, 1)
                        const float* __restrict__ lse2, const float* __restrict__ delta,
                        uint16_t* __restrict__ dq, RowLayout dq_lay, int S_q, int S_k, int BH,
                        int H, int kv_group, int S_pad, int head_group, int causal_off,
-                       float scale, float scale_log2, unsigned int* __restrict__ status) {
+                       float scale, float scale_log2, DeviceWords* __restrict__ words,
+                       unsigned long long launch, unsigned long long budget_ns) {
     using T = DqTile<D>;
     using namespace sm100;
 
@@ -732,6 +742,7 @@ __global__ void __launch_bounds__(DqTile<D>::THREADS, 1)
     uint64_t* clc_empty = clc_full + T::CLC_SLOTS;
     uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(clc_empty + T::CLC_SLOTS);
     volatile int* abort_flag = reinterpret_cast<volatile int*>(tmem_slot + 1);
+    unsigned int* status = &words->status;
 
     const int warp = threadIdx.x >> 5;
     const int lane = threadIdx.x & 31;
@@ -808,6 +819,7 @@ __global__ void __launch_bounds__(DqTile<D>::THREADS, 1)
             tma_prefetch_desc(&tm_v);
         }
         __syncwarp();
+        LaunchWatch watch(words, launch, budget_ns);
         bool ok = true;
         int kidx = 0, vidx = 0;
         int uq = 0;
@@ -815,6 +827,10 @@ __global__ void __launch_bounds__(DqTile<D>::THREADS, 1)
         auto load = [&](const CUtensorMap* map, uint8_t* ring, uint64_t* full, uint64_t* empty,
                         int slots, int& idx, int row, int hk, int b) {
             if (!ok) return;
+            if ((idx & 7) == 0 && watch.stop(abort_flag, status)) {
+                ok = false;
+                return;
+            }
             const int slot = idx % slots;
             ok = mbar_wait(&empty[slot], ((idx / slots) & 1) ^ 1, abort_flag, status,
                            kStatusBwdProducer);
@@ -832,6 +848,7 @@ __global__ void __launch_bounds__(DqTile<D>::THREADS, 1)
         };
         int claims = 0;   // work-queue requests issued (full attention)
         for (int r = 0; ok; ++r) {
+            if (watch.stop(abort_flag, status)) break;
             int L = 0;
             const int got = unit_at(r, L, false, kStatusBwdProducer);
             if (got < 0) ok = false;
@@ -1022,8 +1039,8 @@ __global__ void __launch_bounds__(DqTile<D>::THREADS, 1)
         while (!mbar_try_wait(a, 0)) {
             if (global_timer_ns() - t0 > kWaitLimitNs) {
                 if (elect_one()) {
-                    atomicOr(status, kStatusBwdDrain);
                     *abort_flag = 1;
+                    atomicOr(status, kStatusBwdDrain);
                 }
                 break;
             }
@@ -1112,6 +1129,7 @@ __global__ void __launch_bounds__(DqTile<D>::THREADS, 1)
     if (warp == 0) {
         tc_fence_after();
         tmem_dealloc(tmem, T::TMEM_COLS);
+        if (lane == 0) publish_abort(abort_flag, words, launch);
     }
 }
 
@@ -1159,7 +1177,8 @@ cudaError_t launch_attn_bwd(const BwdArgs& a, cudaStream_t stream) {
             stream>>>(a.tm_k_fixed, a.tm_v_fixed, a.tm_q_step, a.tm_do_step, a.lse2, a.delta,
                       static_cast<uint16_t*>(a.dk), static_cast<uint16_t*>(a.dv), a.dk_lay,
                       a.dv_lay, a.S_q, a.S_k, bh_kv, a.H, a.kv_group, a.S_pad, hg_kv,
-                      a.causal_off, a.scale, a.scale_log2, a.status);
+                      a.causal_off, a.scale, a.scale_log2, a.words, a.launch_dkdv,
+                      a.budget_ns);
     err = cudaGetLastError();
     if (err != cudaSuccess) return err;
 
@@ -1175,7 +1194,8 @@ cudaError_t launch_attn_bwd(const BwdArgs& a, cudaStream_t stream) {
           TQ::SMEM_BYTES,
           dq_stream>>>(a.tm_q_fixed, a.tm_do_fixed, a.tm_k_fixed, a.tm_v_fixed, a.lse2, a.delta,
                     static_cast<uint16_t*>(a.dq), a.dq_lay, a.S_q, a.S_k, a.BH, a.H, a.kv_group,
-                    a.S_pad, hg_q, a.causal_off, a.scale, a.scale_log2, a.status);
+                    a.S_pad, hg_q, a.causal_off, a.scale, a.scale_log2, a.words, a.launch_dq,
+                    a.budget_ns);
     err = cudaGetLastError();
     if (err != cudaSuccess || !a.aux_stream) return err;
     err = cudaEventRecord(a.ev_join, a.aux_stream);

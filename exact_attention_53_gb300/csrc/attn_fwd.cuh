@@ -21,9 +21,10 @@
 //     back over the upper half of the S columns with tcgen05.st, and the PV
 //     MMA takes P straight from tensor memory.
 //   * The running maximum used for exponentiation is only raised when a
-//     tile's row sum of exponentials exceeds 2^20 (kRescaleSum), i.e. when the
-//     scores have outgrown the maximum by enough to matter for the fp32 range;
-//     O and l always share the same (possibly stale) maximum, so O / l and the
+//     tile's row sum of exponentials exceeds rescale_sum<BF16>() (2^20 for
+//     bf16, 2^15 for fp16), i.e. when the scores have outgrown the maximum by
+//     enough to matter for the range of the 16-bit P or of fp32; O and l
+//     always share the same (possibly stale) maximum, so O / l and the
 //     log-sum-exp are unchanged.  This skips almost all O rescales and the
 //     per-element maximum tracking, without approximating anything.
 //   * Causal: key tiles entirely above the diagonal are never loaded or
@@ -50,8 +51,23 @@ enum : unsigned int {
     kStatusDrain = 16u,
 };
 
-constexpr float kRescaleSum = 1048576.0f;   // 2^20
+// Largest row sum of one tile's exponentials that is kept without raising the
+// running maximum.  Every p of the tile is at most that sum, and P goes to the
+// P·V product as a 16-bit value: bf16 has fp32's exponent range, so 2^20 only
+// keeps the fp32 sums well inside range; fp16 overflows above 65504, so its
+// bound is 2^15 (a larger p would round to +inf in the packed P).
+template <bool BF16>
+__host__ __device__ constexpr float rescale_sum() {
+    return BF16 ? 1048576.0f : 32768.0f;
+}
 constexpr float kLn2 = 0.693147180559945309f;
+
+#ifdef ATTN_DEBUG_FAULTS
+// Debug builds only (never the release library): the producer loads nothing
+// for this work unit and stops, so the unit's consumers wait until their limit
+// runs out.  -1: no unit is skipped.
+__device__ int g_attn_debug_skip_unit = -1;
+#endif
 
 
 // Number of key tiles query tile t of a block starting at row q0 visits.
@@ -156,7 +172,8 @@ __global__ void __launch_bounds__(KernelTile<D, SPLIT>::THREADS, 1)
                     const __grid_constant__ CUtensorMap tm_v,
                     const __grid_constant__ CUtensorMap tm_o,
                     float* __restrict__ lse_ptr, int S_q, int S_k, int BH, int n_qblk,
-                    int head_group, float scale_log2, unsigned int* __restrict__ status,
+                    int head_group, float scale_log2_signed, DeviceWords* __restrict__ words,
+                    unsigned long long launch, unsigned long long budget_ns,
                     int n_split, int kv_per_split, float* __restrict__ o_part,
                     float* __restrict__ lse_part, int H, int kv_group, int causal_off,
                     int pack) {
@@ -186,9 +203,16 @@ __global__ void __launch_bounds__(KernelTile<D, SPLIT>::THREADS, 1)
     uint64_t* clc_empty = clc_full + T::CLC_SLOTS;  // [CLC_SLOTS] answer read by every consumer
     uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(clc_empty + T::CLC_SLOTS);
     volatile int* abort_flag = reinterpret_cast<volatile int*>(tmem_slot + 1);
+    unsigned int* status = &words->status;
 
     const int warp = threadIdx.x >> 5;
     const int lane = threadIdx.x & 31;
+    // The softmax folds the scale into its exponent and its running maximum,
+    // which needs a non-negative factor.  A negative scale is applied as
+    // |scale| on S = (−Q)·Kᵀ: the Q·Kᵀ MMA negates its A operand, an exact
+    // sign flip, so max_j(scale·s_ij) is the maximum of the scores it writes.
+    const bool neg_scale = scale_log2_signed < 0.f;
+    const float scale_log2 = fabsf(scale_log2_signed);
     // SPLIT: every (head, query block) is cut into n_split work units along the
     // keys (kv_per_split key tiles each); each writes O/l in fp32 and its own
     // log-sum-exp to o_part / lse_part for attn_combine to merge.  With
@@ -229,7 +253,7 @@ __global__ void __launch_bounds__(KernelTile<D, SPLIT>::THREADS, 1)
     // the hardware work queue.  Consumers (the softmax, MMA and, without
     // SPLIT, store warps) free each answer's slot once read.
     constexpr int CLC_CONSUMERS = T::SOFTMAX_WARPS + (SPLIT ? 1 : 2);
-    constexpr int STORE_WARP = T::SOFTMAX_WARPS + 2;
+    constexpr int STORE_WARP = T::STORE_WARP;
     const WorkQueue<T::CLC_SLOTS> queue{clc_resp, clc_full, clc_empty};
     auto unit_at = [&](int r, int& L, unsigned int bit, bool consumer) -> int {
         return queue.unit(r, L, consumer, abort_flag, status, bit);
@@ -283,6 +307,7 @@ __global__ void __launch_bounds__(KernelTile<D, SPLIT>::THREADS, 1)
         if (warp == 0) {
             tc_fence_after();
             tmem_dealloc(tmem, T::TMEM_COLS);
+            if (lane == 0) publish_abort(abort_flag, words, launch);
         }
     };
 
@@ -300,15 +325,19 @@ __global__ void __launch_bounds__(KernelTile<D, SPLIT>::THREADS, 1)
             tma_prefetch_desc(&tm_o);
         }
         __syncwarp();
+        LaunchWatch watch(words, launch, budget_ns);
         int idx = 0;                          // K/V ring position, across units
         int uq = 0;                           // units started by this CTA
         int q_loads = 0;                      // Q loads issued
         bool ok = true;
         auto issue = [&](const CUtensorMap* map, int j, int hk, int b) {
             if (!ok) return;
+            if ((idx & 7) == 0 && watch.stop(abort_flag, status)) {
+                ok = false;
+                return;
+            }
             const int slot = idx % T::NS;
-            ok = mbar_wait(&kv_empty[slot], ((idx / T::NS) & 1) ^ 1, abort_flag, status,
-                           kStatusProducer);
+            ok = mbar_wait(&kv_empty[slot], ((idx / T::NS) & 1) ^ 1, abort_flag, status, kStatusProducer);
             ok = __all_sync(0xffffffffu, ok);
             if (!ok) return;
             if (leader) {
@@ -324,6 +353,7 @@ __global__ void __launch_bounds__(KernelTile<D, SPLIT>::THREADS, 1)
         };
         int claims = 0;                       // work-queue requests issued
         for (int r = 0; ok; ++r) {
+            if (watch.stop(abort_flag, status)) break;
             int L = 0;
             const int got = unit_at(r, L, kStatusProducer, false);
             if (got < 0) ok = false;
@@ -331,6 +361,11 @@ __global__ void __launch_bounds__(KernelTile<D, SPLIT>::THREADS, 1)
             int bh, q0, n0, n1, kb, sp, b, h, hk;
             unit_info(L, bh, q0, n0, n1, kb, sp);
             heads_of(bh, b, h, hk);
+#ifdef ATTN_DEBUG_FAULTS
+            // Debug builds only: load nothing for the chosen unit and stop, so
+            // its consumers' waits run out.
+            if (L == g_attn_debug_skip_unit) break;
+#endif
             const int n_max = max(n0, n1);
             const int uq_now = uq++;
             // Q of this unit once the previous unit's last Q·Kᵀ is done.
@@ -355,14 +390,14 @@ __global__ void __launch_bounds__(KernelTile<D, SPLIT>::THREADS, 1)
             ++q_loads;
             // K/V in the MMA warp's consumption order.
             if (T::TILES == 2) {
-                for (int j = 0; j < n_max; ++j) {
+                for (int j = 0; j < n_max && ok; ++j) {
                     issue(&tm_k, kb + j, hk, b);
                     issue(&tm_v, kb + j, hk, b);
                 }
             } else {
                 issue(&tm_k, kb, hk, b);
                 if (n_max > 1) issue(&tm_k, kb + 1, hk, b);
-                for (int j = 0; j < n_max; ++j) {
+                for (int j = 0; j < n_max && ok; ++j) {
                     issue(&tm_v, kb + j, hk, b);
                     if (j + 2 < n_max) issue(&tm_k, kb + j + 2, hk, b);
                 }
@@ -376,31 +411,17 @@ __global__ void __launch_bounds__(KernelTile<D, SPLIT>::THREADS, 1)
         if (*abort_flag && leader) {
             // Let every copy this CTA started land before it exits.
             const uint64_t t0 = global_timer_ns();
-            for (int i = max(0, idx - T::NS); i < idx; ++i) {
-                const uint32_t a = smem_u32(&kv_full[i % T::NS]);
-                while (!mbar_try_wait(a, (i / T::NS) & 1)) {
-                    if (global_timer_ns() - t0 > kWaitLimitNs) {
-                        atomicOr(status, kStatusDrain);
-                        break;
-                    }
-                }
-            }
-            if (q_loads > 0) {
-                const uint32_t a = smem_u32(q_full);
-                const uint32_t last = static_cast<uint32_t>(q_loads - 1) & 1u;
-                while (!mbar_try_wait(a, last)) {
-                    if (global_timer_ns() - t0 > kWaitLimitNs) {
-                        atomicOr(status, kStatusDrain);
-                        break;
-                    }
-                }
-            }
+            for (int i = max(0, idx - T::NS); i < idx; ++i)
+                drain_wait(&kv_full[i % T::NS], (i / T::NS) & 1, t0, status, kStatusDrain);
+            if (q_loads > 0)
+                drain_wait(q_full, static_cast<uint32_t>(q_loads - 1) & 1u, t0, status, kStatusDrain);
             queue.drain(claims, status, kStatusDrain);   // and the last work-queue answer
         }
         __syncwarp();
       } else if (warp == T::MMA_WARP) {
         // ------------------------------------------------------------ MMA issuer
-        constexpr uint32_t id_s = idesc_f16(128, T::BN, BF16, false, false);
+        const uint32_t id_s =
+            idesc_f16(128, T::BN, BF16, false, false) | (neg_scale ? kIdescNegateA : 0u);
         constexpr uint32_t id_o = idesc_f16(128, D, BF16, false, true);
         const uint32_t q_base = smem_u32(sQ);
         const uint32_t kv_base = smem_u32(sKV);
@@ -547,8 +568,8 @@ __global__ void __launch_bounds__(KernelTile<D, SPLIT>::THREADS, 1)
         while (!mbar_try_wait(a, 0)) {
             if (global_timer_ns() - t0 > kWaitLimitNs) {
                 if (elect_one()) {
-                    atomicOr(status, kStatusDrain);
                     *abort_flag = 1;
+                    atomicOr(status, kStatusDrain);
                 }
                 break;
             }
@@ -657,14 +678,14 @@ __global__ void __launch_bounds__(KernelTile<D, SPLIT>::THREADS, 1)
                                : exp_pack128<false, BF16>(s, lim, scale_log2, neg_m, pk);
                 } else {
                     // Exponentiate against the running maximum.  A row whose sum of
-                    // exponentials exceeds kRescaleSum (its scores outgrew the
+                    // exponentials exceeds rescale_sum (its scores outgrew the
                     // maximum; rare) re-reads its scores from TMEM (P has not been
                     // written over them yet) and is redone against its new maximum.
                     // Either way O and l share one maximum, so the result is exact.
                     float lsum = masked
                         ? exp_pack128<true, BF16>(s, lim, scale_log2, -m, pk)
                         : exp_pack128<false, BF16>(s, lim, scale_log2, -m, pk);
-                    const bool grow = !(lsum <= kRescaleSum);      // also catches inf and NaN
+                    const bool grow = !(lsum <= rescale_sum<BF16>());   // also catches inf and NaN
                     if (__any_sync(0xffffffffu, grow)) {
                         uint32_t ra[64], rb[64];
                         tmem_ld64x2(lane_base + b * T::S_STRIDE, lane_base + b * T::S_STRIDE + 64,
@@ -852,7 +873,8 @@ cudaError_t launch_attn_fwd(const FwdArgs& a, cudaStream_t stream) {
     const int grid = static_cast<int>(units);
     kernel<<<grid, T::THREADS, T::SMEM_BYTES, stream>>>(a.tm_q, a.tm_k, a.tm_v, a.tm_o, a.lse, a.S_q,
                                                          a.S_k, a.BH, n_qblk, head_group,
-                                                         a.scale_log2, a.status, n_split,
+                                                         a.scale_log2, a.words, a.launch,
+                                                         a.budget_ns, n_split,
                                                          a.kv_per_split, a.o_part, a.lse_part, a.H,
                                                          a.kv_group, a.causal_off, pack);
     return cudaGetLastError();

@@ -8,6 +8,15 @@
 
 namespace attn {
 
+namespace sm100 {
+struct DeviceWords;     // per-GPU status and abort words (sm100.cuh)
+}
+using sm100::DeviceWords;
+
+// Every kernel launch with bounded waits gets a launch number, unique per
+// device, and a time budget after which each of its CTAs gives up (sm100.cuh,
+// Guard).
+
 struct FwdArgs {
     // 4-D maps (d, S, heads, B) with the tensors' own row, head and batch
     // strides; box 64 columns × 128 rows × 1 × 1.
@@ -23,7 +32,7 @@ struct FwdArgs {
     int32_t H;              // query heads
     int32_t kv_group;       // query heads per key/value head (H / H_kv)
     int32_t causal_off;     // causal: key j is visible to query i iff j <= i + causal_off
-    float scale_log2;       // scale · log2(e), >= 0
+    float scale_log2;       // scale · log2(e), either sign
     int32_t num_sms;        // SMs of the device (split-KV range planning)
     // split-KV only (launch_attn_fwd<..., SPLIT = true>)
     int32_t n_split;        // key ranges per (head, query block)
@@ -31,7 +40,9 @@ struct FwdArgs {
     float* o_part;          // [n_split, B·H, S_q, d] fp32: O/l of each range
     float* lse_part;        // [n_split, B·H, S_q] fp32: LSE of each range
     int32_t pack;           // query heads per unit's query tile (1, or H / H_kv when packed)
-    unsigned int* status;   // device status word (bit set on a wait that ran out)
+    DeviceWords* words;     // device status word (bit set on a wait that ran out) and abort word
+    unsigned long long launch;      // launch number of the forward kernel
+    unsigned long long budget_ns;   // deadline of each CTA, from its start
 };
 
 // Element strides of a [B, heads, S, d] tensor (d contiguous).
@@ -79,6 +90,7 @@ struct FwdTile {
     static constexpr int SOFTMAX_WARPS = 4 * TILES;
     static constexpr int PRODUCER_WARP = SOFTMAX_WARPS;       // first warp of the aux warpgroup
     static constexpr int MMA_WARP = SOFTMAX_WARPS + 1;
+    static constexpr int STORE_WARP = SOFTMAX_WARPS + 2;      // O stores (not in split-KV)
     static constexpr int THREADS = 32 * (SOFTMAX_WARPS + 4);  // + one aux warpgroup
     // Register split (TILES == 2): 12 warps put 3 on each SM sub-partition, so
     // the launch gets 168 registers a thread (16384 / 3 warps / 32, rounded to
@@ -134,7 +146,9 @@ struct BwdArgs {
     int32_t causal_off;                   // key j visible to query i iff j <= i + causal_off
     float scale, scale_log2;
     int32_t num_sms;
-    unsigned int* status;
+    DeviceWords* words;
+    // Launch numbers of the dK/dV and dQ kernels, and the CTAs' time budget.
+    unsigned long long launch_dkdv, launch_dq, budget_ns;
     // When set, the dQ kernel runs on aux_stream, concurrently with the dK/dV
     // kernel on the caller's stream (they read the same inputs and write
     // disjoint outputs): ev_fork orders it after the prep kernel, ev_join

@@ -2,10 +2,10 @@
 // mbarriers with bounded waits, TMA tensor loads, tcgen05 tensor-memory
 // allocation, MMA issue, commit, and TMEM <-> register moves.
 //
-// Every wait here is bounded by a wall-clock limit read from %globaltimer.  A
-// wait that runs out records a code in the caller's device status word, raises
-// the CTA's abort flag and returns false, so the kernel can drain and return
-// instead of spinning forever.
+// Every wait here is bounded by a wall-clock limit read from %globaltimer, and
+// every launch by a deadline and a launch-wide stop (LaunchWatch).  A wait that
+// runs out records a code in the device status word, stops its CTA and returns
+// false, so the kernel can drain and return instead of spinning forever.
 #pragma once
 
 #include <cuda.h>
@@ -57,12 +57,35 @@ __device__ __forceinline__ bool mbar_try_wait(uint32_t bar, uint32_t parity) {
     return ok != 0;
 }
 
-// Upper bound on one wait.  Real waits in this library last microseconds.
+// Upper bound on one wait.  Real waits in this library last microseconds.  A
+// debug build (ATTN_DEBUG_FAULTS, never the release library) waits 1 ms so
+// that a test can make a wait run out quickly.
+#ifdef ATTN_DEBUG_FAULTS
+constexpr uint64_t kWaitLimitNs = 1000000ull;
+#else
 constexpr uint64_t kWaitLimitNs = 2000000000ull;
+#endif
+// How often a CTA's producer looks whether another CTA of its launch gave up.
+constexpr uint64_t kPeerCheckNs = 50000ull;
 
-// Wait for the phase of parity `parity` to complete.  Returns false (and
-// records `code` in *status, raises *abort_flag) when the limit runs out or
-// another role of this CTA has already aborted.
+// Status bit recorded when a CTA passes its launch's deadline.
+constexpr unsigned int kStatusDeadline = 1u << 9;
+
+// Per-GPU words in global memory, shared by every launch of the library:
+// the status bits of waits that ran out (read and cleared by the host), and
+// the number of the last launch that gave up.
+struct DeviceWords {
+    unsigned int status;
+    unsigned int reserved;
+    unsigned long long abort_launch;
+};
+
+// Wait for the phase of parity `parity` to complete.  Returns false (after
+// recording `code` in *status and raising the CTA's abort flag) when the
+// limit runs out, or at once when this CTA has been stopped.  The spin and its
+// exit path are kept to the fewest instructions: the wait is inlined at every
+// handoff of every role, and extra code here (even on the exit path) was
+// measured to slow the kernels by a few percent.
 __device__ __forceinline__ bool mbar_wait(uint64_t* bar, uint32_t parity,
                                           volatile int* abort_flag, unsigned int* status,
                                           unsigned int code) {
@@ -76,6 +99,81 @@ __device__ __forceinline__ bool mbar_wait(uint64_t* bar, uint32_t parity,
             *abort_flag = 1;
             atomicOr(status, code);
             return false;
+        }
+    }
+}
+
+// Launch-wide bounds, kept in registers by each CTA's TMA producer warp (the
+// one role that runs ahead of the others and is never on the critical path).
+// Together with the bounded waits they make every launch end in bounded time:
+//   * one wait gives up after kWaitLimitNs (mbar_wait), raising the CTA's
+//     abort flag, so every other role of the CTA leaves at its next wait;
+//   * the producer checks at every eighth load it issues and at every work
+//     unit that the CTA has not run past its deadline (its start plus a budget the host
+//     derives from the launch's work, far above its real duration), and stops
+//     the CTA if it has;
+//   * a CTA that gave up records its launch number in words->abort_launch on
+//     its way out (publish_abort); producers read it when they start and every
+//     kPeerCheckNs after that, so the launch's other CTAs stop too.
+// Every role's step loop waits on a barrier that the producer (directly or
+// through the MMA warp) completes once per step, so a role that ran past its
+// partners (a wrong trip count) blocks within a ring's depth of steps and
+// leaves there; the producer itself is bounded by the deadline.
+struct LaunchWatch {
+    const DeviceWords* words;
+    unsigned long long launch;        // this launch's number (host counter, per device)
+    uint64_t deadline;                // %globaltimer value after which the CTA gives up
+    uint64_t next_peer;               // when to read words->abort_launch next
+
+    __device__ __forceinline__ LaunchWatch(const DeviceWords* w, unsigned long long launch_no,
+                                           unsigned long long budget_ns)
+        : words(w), launch(launch_no) {
+        const uint64_t now = global_timer_ns();
+        deadline = now + budget_ns;
+        // The first read of the word comes a microsecond in, after the first
+        // unit's first loads are on their way, so it does not delay them.
+        next_peer = now + 1000;
+    }
+
+    // True once the CTA must stop: it already has, it passed its deadline
+    // (status bit kStatusDeadline), or another CTA of the launch gave up.
+    // Warp-uniform: lane 0 decides.
+    __device__ __forceinline__ bool stop(volatile int* abort_flag, unsigned int* status) {
+        int s = *abort_flag;
+        if (!s) {
+            const uint64_t now = global_timer_ns();
+            if (now > deadline) {
+                if ((threadIdx.x & 31) == 0) {
+                    *abort_flag = 1;
+                    atomicOr(status, kStatusDeadline);
+                }
+                s = 1;
+            } else if (now >= next_peer) {
+                s = *reinterpret_cast<const volatile unsigned long long*>(&words->abort_launch) ==
+                    launch;
+                if (s && (threadIdx.x & 31) == 0) *abort_flag = 1;
+                next_peer = now + kPeerCheckNs;
+            }
+        }
+        return __shfl_sync(0xffffffffu, s, 0) != 0;
+    }
+};
+
+// On a CTA's way out: if it gave up, tell the launch's other CTAs.
+__device__ __forceinline__ void publish_abort(volatile int* abort_flag, DeviceWords* words,
+                                              unsigned long long launch) {
+    if (*abort_flag) atomicMax(&words->abort_launch, launch);
+}
+
+// After this CTA gave up: wait (bounded) for the phase of parity `parity` of
+// `bar` to complete, e.g. for a copy in flight to land before the CTA exits.
+__device__ __forceinline__ void drain_wait(uint64_t* bar, uint32_t parity, uint64_t t0,
+                                           unsigned int* status, unsigned int code) {
+    const uint32_t a = smem_u32(bar);
+    while (!mbar_try_wait(a, parity)) {
+        if (global_timer_ns() - t0 > kWaitLimitNs) {
+            atomicOr(status, code);
+            break;
         }
     }
 }
@@ -251,14 +349,7 @@ struct WorkQueue {
                                           unsigned int code) const {
         if (claims == 0) return;
         const int i = claims - 1;
-        const uint32_t a = smem_u32(&full[i % SLOTS]);
-        const uint64_t t0 = global_timer_ns();
-        while (!mbar_try_wait(a, (i / SLOTS) & 1)) {
-            if (global_timer_ns() - t0 > kWaitLimitNs) {
-                atomicOr(status, code);
-                break;
-            }
-        }
+        drain_wait(&full[i % SLOTS], (i / SLOTS) & 1, global_timer_ns(), status, code);
     }
 };
 
@@ -417,13 +508,18 @@ __device__ __forceinline__ uint64_t sdesc_sw128(uint32_t saddr, uint32_t lbo_byt
 
 // Instruction descriptor for kind::f16 with an fp32 accumulator.
 //   bits 4-5 D type (1 = f32); 7-9 A type, 10-12 B type (0 = f16, 1 = bf16);
-//   15 / 16 A / B major (0 = K-major, 1 = MN-major); 17-22 N >> 3; 24-28 M >> 4.
+//   13 / 14 negate A / B; 15 / 16 A / B major (0 = K-major, 1 = MN-major);
+//   17-22 N >> 3; 24-28 M >> 4.
 __host__ __device__ constexpr uint32_t idesc_f16(int M, int N, bool bf16, bool a_mn_major,
                                                  bool b_mn_major) {
     return (1u << 4) | ((bf16 ? 1u : 0u) << 7) | ((bf16 ? 1u : 0u) << 10) |
            ((a_mn_major ? 1u : 0u) << 15) | ((b_mn_major ? 1u : 0u) << 16) |
            (static_cast<uint32_t>(N >> 3) << 17) | (static_cast<uint32_t>(M >> 4) << 24);
 }
+
+// OR-ed into an instruction descriptor: the MMA uses −A in place of A (an
+// exact sign flip of every A element).
+constexpr uint32_t kIdescNegateA = 1u << 13;
 
 // ---------------------------------------------------------------- TMEM <-> registers
 // 32x32b shape: thread i of the warp gets lane (base lane + i); .xN gives N

@@ -31,9 +31,16 @@
  *
  * Errors.  Argument checks happen on the host before anything is enqueued and
  * return a status; attn_last_error() then describes the offending argument
- * by name (as the page's validate_config does).  A kernel whose internal
- * bounded wait runs out does not hang: it returns early, and the next
- * attn_get_device_status() reports ATTN_ERR_TIMEOUT.
+ * by name (as the page's validate_config does).
+ *
+ * Bounded execution.  No kernel of this library can hang its stream.  Every
+ * wait inside a kernel gives up after 2 s; every CTA gives up once it has run
+ * longer than a budget the host derives from the launch's work (5 s plus the
+ * time the work would take at 10 TFLOP/s), checked in its waits and at the
+ * head of each of its loops; and a CTA that gives up stops the rest of its
+ * launch (CTAs that start later leave at once, running ones at their next
+ * wait that lasts over 0.1 ms).  Such a launch returns early with its outputs
+ * incomplete, and the next attn_get_device_status() reports ATTN_ERR_TIMEOUT.
  */
 #ifndef ATTN_GB300_ATTN_H_
 #define ATTN_GB300_ATTN_H_
@@ -54,7 +61,7 @@ typedef enum {
 typedef enum {
     ATTN_OK = 0,
     ATTN_ERR_INVALID_ARG = 1, /* null or misaligned pointer, size < 1, overlap, non-finite scale, size too large */
-    ATTN_ERR_UNSUPPORTED = 2, /* head_dim not in {64,128,256}, dtype not f16/bf16, negative scale, no sm_103 device */
+    ATTN_ERR_UNSUPPORTED = 2, /* head_dim not in {64,128,256}, dtype not f16/bf16, no sm_103 device */
     ATTN_ERR_CUDA = 3,        /* a CUDA runtime or driver call failed (message has the CUDA error) */
     ATTN_ERR_TIMEOUT = 4      /* a kernel's bounded internal wait ran out (reported by attn_get_device_status) */
 } attn_status_t;
@@ -100,7 +107,9 @@ attn_status_t attn_fwd_plan(int64_t B, int64_t H, int64_t S_q, int64_t S_k, int6
  *   S_q, S_k query and key lengths, 1 .. 2^22 (need not be tile multiples)
  *   d        head dimension: 64, 128 or 256
  *   causal   0 or 1; 1 masks key j for query i when j > i (top-left)
- *   scale    multiplier of Q·Kᵀ, finite and >= 0 (1/sqrt(d) is the usual)
+ *   scale    multiplier of Q·Kᵀ, any finite value (1/sqrt(d) is the usual;
+ *            0 gives uniform weights, a negative scale favours the keys least
+ *            aligned with the query)
  *   stream   CUDA stream
  *
  * o and lse must not overlap q, k, v or each other.  Returns ATTN_OK once the
@@ -385,9 +394,13 @@ const char* attn_last_error(void);
 
 /*
  * attn_get_device_status — synchronise `stream`, then read and clear the
- * current device's status word (shared by the forward and backward kernels).  ATTN_OK if every kernel since the last read
- * finished its waits; ATTN_ERR_TIMEOUT if one ran out (the message names the
- * role that gave up); ATTN_ERR_CUDA if the synchronisation itself failed.
+ * current device's status words (shared by the forward and backward kernels).
+ * ATTN_OK if every kernel since the last read finished its waits;
+ * ATTN_ERR_TIMEOUT if one gave up (the message names the roles, and says when
+ * a CTA passed its launch's deadline); ATTN_ERR_CUDA if the synchronisation
+ * itself failed.  A launch captured in a CUDA graph keeps its launch number,
+ * so after a replay that gave up, later replays of the same graph stop at
+ * once until this call clears the words.
  */
 attn_status_t attn_get_device_status(struct CUstream_st* stream);
 

@@ -1,0 +1,44 @@
+/*
+ * attn_debug.h — failure-detection hooks of libattn_debug.so, a debug build of
+ * the attention forward kernel.  Not part of the attention operation, and not
+ * exported by the release library libattn.so.
+ *
+ * libattn_debug.so compiles the release kernel source with its bounded waits
+ * shortened from 2 s to 1 ms and with one hook: the TMA producer warp can be
+ * told to issue no load for one work unit and stop.  The consumers of that
+ * unit then wait on barriers nothing completes, their waits run out, the CTA
+ * records which roles gave up, tells the launch's other CTAs to stop, frees its
+ * tensor memory and returns; the GPU context stays usable.  Tests use it to
+ * check that a wait that runs out is reported and does not hang.
+ *
+ * attn_debug_fwd — enqueue one full-attention forward on `stream` over dense
+ *   bf16 q, k, v, o [B, H, S, 64] (device, 16-byte aligned) and fp32 lse
+ *   [B, H, S], scaled by `scale`.  skip_unit: the work unit (one head and 256
+ *   query rows, numbered head-major) whose loads the producer skips, or -1 for
+ *   none (then the call computes the forward like attn_fwd).  Returns 0, or a
+ *   cudaError_t value (1 for bad arguments).
+ * attn_debug_status — synchronise `stream`, write the debug library's status
+ *   word (bit 1: producer, 2: MMA, 4: softmax, 8: epilogue, 16: drain, 512:
+ *   deadline; 0 when no wait ran out) to *status and clear it.  Returns 0 or a
+ *   cudaError_t value.
+ */
+#ifndef ATTN_GB300_ATTN_DEBUG_H_
+#define ATTN_GB300_ATTN_DEBUG_H_
+
+#include <stdint.h>
+
+#ifdef __cplusplus
+extern "C" {
+#endif
+
+struct CUstream_st;
+
+int attn_debug_fwd(const void* q, const void* k, const void* v, void* o, float* lse, int64_t B,
+                   int64_t H, int64_t S, float scale, int skip_unit, struct CUstream_st* stream);
+int attn_debug_status(unsigned int* status, struct CUstream_st* stream);
+
+#ifdef __cplusplus
+}
+#endif
+
+#endif /* ATTN_GB300_ATTN_DEBUG_H_ */

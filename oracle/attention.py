@@ -22,7 +22,7 @@ before ``exp``), so this oracle is the plain definition written out:
     P      = exp(S − m_i)          l_i = Σ_j P[i,j]
     O      = (P / l) · V           LSE_i = m_i + ln(l_i)
 
-Readings taken where the page is silent (each is listed in the design doc):
+Readings taken where the page is silent:
   * "zero out future token positions" is read as the masked logit being −∞
     (its probability is zero), not the score being set to 0.
   * causal alignment is top-left: key j is visible to query i iff j ≤ i.
@@ -30,6 +30,9 @@ Readings taken where the page is silent (each is listed in the design doc):
     aligns the last query with the last key instead: j ≤ i + (S_k − S_q).
   * the log-sum-exp is the natural log and includes the scale:
     LSE_i = ln Σ_j exp(scale · q_i · k_j).
+  * the scale is any finite number (the page's ``sm_scale`` is a plain f32):
+    zero gives uniform weights, a negative scale favours the keys least
+    aligned with the query.
   * inputs are the fp16/bf16 values exactly as stored, widened to fp64; the
     oracle does not round P or O to the input dtype.
 

@@ -25,7 +25,7 @@ P, O and D formed exactly in fp64 (not read back from a rounded forward):
     dV = Pᵀ·dO      dP = dO·Vᵀ      dS = P ∘ (dP − D)
     dQ = scale·dS·K      dK = scale·dSᵀ·Q
 
-Readings (listed in the design doc): masking and its top-left alignment as in the
+Readings where the page is silent: masking and its top-left alignment as in the
 forward oracle (``bottom_right`` shifts it by S_k − S_q, as there); D computed
 as rowsum(dO ∘ O); the scale applied to dQ and dK.
 """

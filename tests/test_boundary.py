@@ -53,6 +53,26 @@ def test_library_exports_every_declared_symbol(lib):
     assert lib.attn_version() == 10000
 
 
+def test_debug_library_exports_only_its_hooks(lib):
+    """The failure-detection hooks live in libattn_debug.so alone, as include/attn_debug.h
+    declares; the release library exports none of them."""
+    text = re.sub(r"/\*.*?\*/", "", open(os.path.join(ROOT, "include", "attn_debug.h")).read(),
+                  flags=re.S)
+    declared = sorted(set(re.findall(r"\b(attn_debug_\w+)\s*\(", text)))
+    assert declared == sorted(binding.DEBUG_EXPORTS)
+    dbg = binding.load_debug_library()
+    for name in declared:
+        assert hasattr(dbg, name), name
+        assert not hasattr(lib, name), name
+
+
+def test_debug_entry_rejects_bad_arguments_before_device_work():
+    dbg = binding.load_debug_library()
+    assert dbg.attn_debug_fwd(None, A, A, A, A, 1, 1, 128, 0.125, -1, None) == 1
+    assert dbg.attn_debug_fwd(A, A, A, A, A, 1, 1, 0, 0.125, -1, None) == 1
+    assert dbg.attn_debug_status(None, None) == 1
+
+
 def _fwd(lib, q=A, k=A + MB, v=A + 2 * MB, o=A + 3 * MB, lse=A + 4 * MB, B=1, H=2, S_q=128,
          S_k=128, d=128, causal=0, scale=0.125, dtype=1):
     return lib.attn_fwd(q, k, v, o, lse, B, H, S_q, S_k, d, causal, scale, dtype, None)
@@ -75,7 +95,6 @@ CASES = [
     (dict(causal=2), binding.ATTN_ERR_INVALID_ARG, "causal"),
     (dict(scale=float("nan")), binding.ATTN_ERR_INVALID_ARG, "scale"),
     (dict(scale=float("inf")), binding.ATTN_ERR_INVALID_ARG, "scale"),
-    (dict(scale=-0.5), binding.ATTN_ERR_UNSUPPORTED, "scale"),
     (dict(q=A + 8), binding.ATTN_ERR_INVALID_ARG, "q is not 16-byte aligned"),
     (dict(k=A + MB + 2), binding.ATTN_ERR_INVALID_ARG, "k is not 16-byte aligned"),
     (dict(o=A + 3 * MB + 4), binding.ATTN_ERR_INVALID_ARG, "o is not 16-byte aligned"),
@@ -93,6 +112,13 @@ CASES = [
 def test_validation_rejects_before_device_work(lib, kw, status, msg):
     assert _fwd(lib, **kw) == status
     assert msg in lib.attn_last_error().decode()
+
+
+def test_negative_scale_passes_validation(lib):
+    """Any finite scale is accepted (the page's sm_scale is a plain f32): a negative one gets
+    past validation to the device check, which fails here without a GPU."""
+    assert _fwd(lib, scale=-0.5) == binding.ATTN_ERR_CUDA
+    assert "scale" not in lib.attn_last_error().decode()
 
 
 def test_host_entry_point_checks_host_pointers(lib):

@@ -9,8 +9,8 @@ each element must satisfy |Δ| ≤ 2·bound + 1e-6·max|ref| where
     δD_i   = 2u · Σ_c |dO_ic| · (|P|·|V|)_ic            (O as rounded by the forward)
     δdS_ij = P_ij · δD_i + u · |dS_ij|                  (dS rounded to the dtype)
     dV:  2u · (|P|ᵀ·|dO|)_jc       + u·|dV_jc|
-    dK:  scale · (δdSᵀ·|Q|)_jc     + u·|dK_jc|
-    dQ:  scale · (δdS·|K|)_ic      + u·|dQ_ic|
+    dK:  |scale| · (δdSᵀ·|Q|)_jc   + u·|dK_jc|
+    dQ:  |scale| · (δdS·|K|)_ic    + u·|dQ_ic|
 
 all formed in fp64 from the oracle's exact P, dS, V, dO, Q, K.
 """
@@ -53,8 +53,8 @@ def _check_head(got, q, k, v, do, causal, scale, dtype, what):
     ddS = P * dD[:, None] + u * np.abs(dS)
     bounds = {
         "dV": 2 * u * (np.abs(P).T @ np.abs(dO)) + u * np.abs(t["dV"]),
-        "dK": scale * (ddS.T @ np.abs(Q)) + u * np.abs(t["dK"]),
-        "dQ": scale * (ddS @ np.abs(K)) + u * np.abs(t["dQ"]),
+        "dK": abs(scale) * (ddS.T @ np.abs(Q)) + u * np.abs(t["dK"]),
+        "dQ": abs(scale) * (ddS @ np.abs(K)) + u * np.abs(t["dQ"]),
     }
     for name, g in zip(("dQ", "dK", "dV"), got):
         ref = t[name]
@@ -97,6 +97,22 @@ def test_bwd_small_shapes(d, dtype, causal, shape):
             got = (_f64(dq[b, h]), _f64(dk[b, h]), _f64(dv[b, h]))
             _check_head(got, q[b, h], k[b, h], v[b, h], do[b, h], causal, scale, dtype,
                         f"d={d} {dtype} causal={causal} {shape} head=({b},{h})")
+
+
+@pytest.mark.parametrize("causal", [False, True], ids=["full", "causal"])
+@pytest.mark.parametrize("dtype", ["f16", "bf16"])
+@pytest.mark.parametrize("d", [64, 128])
+def test_bwd_negative_scale(d, dtype, causal):
+    """A negative scale (the page's sm_scale is any f32): forward and backward of the same
+    problem, gradients within the derived bound (with |scale| in it)."""
+    B, H, S = 1, 2, 300
+    q, k, v = make_qkv(B, H, S, S, d, dtype, seed=610 + d)
+    do = make_qkv(B, H, S, 1, d, dtype, seed=611 + d)[0]
+    dq, dk, dv = _run_bwd(q, k, v, do, causal, -0.1)
+    for h in range(H):
+        got = (_f64(dq[0, h]), _f64(dk[0, h]), _f64(dv[0, h]))
+        _check_head(got, q[0, h], k[0, h], v[0, h], do[0, h], causal, -0.1, dtype,
+                    f"scale=-0.1 d={d} {dtype} causal={causal} head={h}")
 
 
 def test_bwd_c2_full():

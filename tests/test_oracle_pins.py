@@ -235,16 +235,90 @@ def pin_bottom_right_loops():
     np.testing.assert_allclose(l[0, 0], np.array(ll), rtol=0, atol=1e-13)
 
 
+def pin_negative_scale():
+    """Any finite scale: a negative one against PyTorch's fp64 SDPA and a closed form.
+
+    With one-hot keys, q_i = e_t and scale −200, key t gets logit −200 and every
+    other key 0, so O_i is the mean of the other V rows and LSE_i = ln(S − 1 + e^−200).
+    """
+    g = torch.Generator().manual_seed(9)
+    for causal in (False, True):
+        q, k, v = (torch.randn(1, 2, 21, 8, generator=g, dtype=torch.float64) for _ in range(3))
+        if causal:
+            # (PyTorch's math SDPA returns NaN for a negative scale under is_causal, so the
+            # masked case goes through torch.softmax directly.)
+            s = (-0.4 * q @ k.transpose(-1, -2)).masked_fill(
+                torch.ones(21, 21, dtype=torch.bool).triu(1), float("-inf"))
+            ref = torch.softmax(s, dim=-1) @ v
+        else:
+            ref = torch.nn.functional.scaled_dot_product_attention(q, k, v, scale=-0.4)
+        o, _ = _fwd(q.numpy(), k.numpy(), v.numpy(), causal, -0.4)
+        np.testing.assert_allclose(o, ref.numpy(), rtol=0, atol=1e-12)
+    S, d = 6, 8
+    k = np.eye(d)[:S][None, None]
+    target = np.array([3, 0, 5, 1, 4, 2])
+    q = np.eye(d)[target][None, None]
+    v = RNG.standard_normal((1, 1, S, d))
+    o, lse = _fwd(q, k, v, False, -200.0)
+    for i, t in enumerate(target):
+        others = [j for j in range(S) if j != t]
+        np.testing.assert_allclose(o[0, 0, i], v[0, 0, others].mean(axis=0), rtol=0, atol=1e-12)
+    np.testing.assert_allclose(lse[0, 0], math.log(S - 1 + math.exp(-200.0)), rtol=0, atol=1e-13)
+
+
 PINS = [pin_worked_example, pin_brute_force, pin_constant_v, pin_scale_zero,
         pin_causal_first_row, pin_one_hot_selection, pin_key_permutation, pin_key_shift,
         pin_log_domain_form, pin_library_sdpa, pin_rows_and_blocks_agree,
         pin_bottom_right_square_is_top_left, pin_bottom_right_is_tail_of_square,
-        pin_bottom_right_loops]
+        pin_bottom_right_loops, pin_negative_scale]
 
 
 @pytest.mark.parametrize("pin", PINS, ids=lambda p: p.__name__)
 def test_oracle_pin(pin):
     pin()
+
+
+def pin_probs_worked_example(probs):
+    """attention_probs on a 2×2 case derived by hand: with q = k = I and scale = ln 3 the
+    logits are [[ln 3, 0], [0, ln 3]], so the rows are [3/4, 1/4] and [1/4, 3/4]; scale −ln 3
+    swaps them; causal row 0 is [1, 0] and row 1 stays [1/4, 3/4]."""
+    eye = np.eye(2)
+    ln3 = math.log(3.0)
+    np.testing.assert_allclose(probs(eye, eye, causal=False, scale=ln3),
+                               [[0.75, 0.25], [0.25, 0.75]], rtol=0, atol=1e-15)
+    np.testing.assert_allclose(probs(eye, eye, causal=False, scale=-ln3),
+                               [[0.25, 0.75], [0.75, 0.25]], rtol=0, atol=1e-15)
+    np.testing.assert_allclose(probs(eye, eye, causal=True, scale=ln3),
+                               [[1.0, 0.0], [0.25, 0.75]], rtol=0, atol=1e-15)
+    # an asymmetric case, so a transposed product shows: logits [[ln 3, 0], [2 ln 3, 0]]
+    q = np.array([[1.0, 0.0], [2.0, 0.0]])
+    k = np.array([[1.0, 0.0], [0.0, 1.0]])
+    np.testing.assert_allclose(probs(q, k, causal=False, scale=ln3),
+                               [[0.75, 0.25], [0.9, 0.1]], rtol=0, atol=1e-15)
+
+
+def test_probs_worked_example():
+    pin_probs_worked_example(oracle.attention_probs)
+
+
+@pytest.mark.parametrize("kind", ["no_scale", "inverse_scale", "transposed", "mask_flipped"])
+def test_probs_pin_catches_planted_mistakes(kind):
+    def probs(q, k, causal=False, scale=None):
+        s = scale * (q @ k.T)
+        if kind == "no_scale":
+            s = q @ k.T
+        elif kind == "inverse_scale":
+            s = (q @ k.T) / scale
+        elif kind == "transposed":
+            s = scale * (k @ q.T)
+        if causal:
+            i = np.arange(q.shape[0])[:, None]
+            j = np.arange(k.shape[0])[None, :]
+            s = np.where((j < i) if kind == "mask_flipped" else (j > i), -np.inf, s)
+        e = np.exp(s - s.max(axis=1, keepdims=True))
+        return e / e.sum(axis=1, keepdims=True)
+    with pytest.raises(AssertionError):
+        pin_probs_worked_example(probs)
 
 
 def test_probs_rows_sum_to_one_and_mask():
