@@ -356,10 +356,16 @@ def percentiles(ms):
     return {"median_ms": pick(0.5), "p10_ms": pick(0.1), "p90_ms": pick(0.9)}
 
 
-def measure_short(dev, stream, launches: int = 50):
+def measure_short(dev, stream, launches: int = 50, graph_launches: int = 20, replays: int = 10):
     """The short-sequence workloads: c1 (one 128×128 tile; launch/latency-bound, so µs and
     GB/s of its 66 KB are reported, with a 256 MB L2 flush before every launch) and c2
-    (S = 1024, d = 64, causal): median of `launches` CUDA-event-timed launches."""
+    (S = 1024, d = 64, causal): median of `launches` CUDA-event-timed calls, each call's host
+    work (validation, tensor maps, launch) inside its events.  Beside it, the device time
+    alone: `graph_launches` calls captured back to back in one CUDA graph, replayed
+    `replays` times, total ÷ launches (no host work and no L2 flush between them), and the
+    host time of one call (wall clock over 200 calls, Python binding included)."""
+    import time
+
     import torch
 
     from exact_attention_53_gb300 import attn_fwd
@@ -395,12 +401,40 @@ def measure_short(dev, stream, launches: int = 50):
             ms.append(a.elapsed_time(b))
         pc = percentiles(ms)
         t = pc["median_ms"] * 1e-3
+        # device time: back-to-back launches replayed from a CUDA graph
+        cap = torch.cuda.Stream(device=dev)
+        graph = torch.cuda.CUDAGraph()
+        with torch.cuda.graph(graph, stream=cap):
+            for _ in range(graph_launches):
+                attn_fwd(q, k, v, o, lse, w.B, w.H, w.S_q, w.S_k, w.d, int(causal), w.scale,
+                         code, cap)
+        for _ in range(3):
+            graph.replay()
+        torch.cuda.synchronize(dev)
+        a, b = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+        a.record()
+        for _ in range(replays):
+            graph.replay()
+        b.record()
+        torch.cuda.synchronize(dev)
+        dev_us = a.elapsed_time(b) * 1e3 / (replays * graph_launches)
+        # host time of one call (launches queue up; the GPU keeps pace or falls behind)
+        t0 = time.perf_counter()
+        for _ in range(200):
+            launch()
+        host_us = (time.perf_counter() - t0) * 1e6 / 200
+        torch.cuda.synchronize(dev)
         out[name] = {"workload": f"{name}: B={w.B} H={w.H} S={w.S_q} d={w.d} {w.dtype} "
                                  f"{'causal' if causal else 'full'}",
                      "us": pc["median_ms"] * 1e3, "p10_us": pc["p10_ms"] * 1e3,
                      "p90_us": pc["p90_ms"] * 1e3, "bytes": w.io_bytes(),
                      "gbs": w.io_bytes() / t / 1e9, "tflops": w.flops(causal) / t / 1e12,
-                     "l2": "256 MB flush before each launch" if name == "c1" else "no flush"}
+                     "l2": "256 MB flush before each launch" if name == "c1" else "no flush",
+                     "device_us": dev_us, "device_gbs": w.io_bytes() / (dev_us * 1e-6) / 1e9,
+                     "device_tflops": w.flops(causal) / (dev_us * 1e-6) / 1e12,
+                     "device_how": f"{graph_launches} launches back to back in one CUDA graph, "
+                                   f"{replays} replays, L2 not flushed",
+                     "host_us_per_call": host_us}
     out["c1"]["note"] = "latency-bound (66 KB, one tile): the roofline fraction is not meaningful"
     return out
 

@@ -27,7 +27,11 @@ LIB = os.path.join(PKG, "libattn.so")
 DEBUG_LIB = os.path.join(PKG, "libattn_debug.so")
 
 ARCH = ["-gencode", "arch=compute_103a,code=sm_103a"]
-FLAGS = ["-O3", "-std=c++17", "-lineinfo", "-Xcompiler", "-fPIC", "-I" + INCLUDE, "-I" + CSRC]
+# Host code is compiled with hidden visibility: each library exports its C ABI
+# (declared under a default-visibility pragma) and nothing else, so two of
+# them in one process never share template code or its static state.
+FLAGS = ["-O3", "-std=c++17", "-lineinfo", "-Xcompiler", "-fPIC", "-Xcompiler", "-fvisibility=hidden",
+         "-I" + INCLUDE, "-I" + CSRC]
 
 # (head_dim, bf16, causal, split): every masked/unmasked kernel, plus the
 # split-KV variant of full attention.

@@ -15,7 +15,9 @@
 #include <cstring>
 #include <mutex>
 
+#pragma GCC visibility push(default)    // the C ABI is the library's only export
 #include "attn.h"
+#pragma GCC visibility pop
 #include "attn_launch.h"
 #include "sm100.cuh"
 
@@ -296,18 +298,59 @@ attn_status_t encode_rows(CUtensorMap* map, const void* base, const Problem& p, 
     return ATTN_OK;
 }
 
+// Recently encoded tensor maps of this host thread.  A map is a function of
+// its encoding inputs alone (address, sizes, strides, box, element type), so a
+// repeated call on the same buffers reuses it instead of encoding it again.
+struct MapKey {
+    const void* base;
+    uint64_t dims[4];
+    uint64_t strides[3];
+    uint32_t box[4];
+    int32_t dtype;
+    int32_t pad;
+};
+
+struct MapCache {
+    static constexpr int kEntries = 16;
+    MapKey key[kEntries];
+    CUtensorMap map[kEntries];
+    int used = 0, next = 0;
+};
+
+thread_local MapCache t_maps;
+
 // A [B, heads, S, d] view as a 4-D map (d, S, heads, B) with its own strides;
 // box 64 columns × box_rows rows of one head.
 attn_status_t encode_4d(CUtensorMap* map, const void* base, const Problem& p, int64_t S,
                         int64_t heads, const Layout& l, uint32_t box_rows, const char* name,
                         uint32_t box_heads = 1) {
+    MapKey key;
+    std::memset(&key, 0, sizeof(key));
+    key.base = base;
+    key.dims[0] = static_cast<uint64_t>(p.d);
+    key.dims[1] = static_cast<uint64_t>(S);
+    key.dims[2] = static_cast<uint64_t>(heads);
+    key.dims[3] = static_cast<uint64_t>(p.B);
+    key.strides[0] = static_cast<uint64_t>(l.row * 2);
+    key.strides[1] = static_cast<uint64_t>(l.head * 2);
+    key.strides[2] = static_cast<uint64_t>(l.batch * 2);
+    key.box[0] = 64;
+    key.box[1] = box_rows;
+    key.box[2] = box_heads;
+    key.box[3] = 1;
+    key.dtype = static_cast<int32_t>(p.dtype);
+    MapCache& c = t_maps;
+    for (int i = 0; i < c.used; ++i) {
+        if (std::memcmp(&c.key[i], &key, sizeof(key)) == 0) {
+            *map = c.map[i];
+            return ATTN_OK;
+        }
+    }
     auto fn = encode_fn();
     if (!fn) return fail(ATTN_ERR_CUDA, "cuTensorMapEncodeTiled is unavailable from the driver");
-    cuuint64_t dims[4] = {static_cast<cuuint64_t>(p.d), static_cast<cuuint64_t>(S),
-                          static_cast<cuuint64_t>(heads), static_cast<cuuint64_t>(p.B)};
-    cuuint64_t strides[3] = {static_cast<cuuint64_t>(l.row * 2), static_cast<cuuint64_t>(l.head * 2),
-                             static_cast<cuuint64_t>(l.batch * 2)};
-    cuuint32_t box[4] = {64, box_rows, box_heads, 1};
+    cuuint64_t dims[4] = {key.dims[0], key.dims[1], key.dims[2], key.dims[3]};
+    cuuint64_t strides[3] = {key.strides[0], key.strides[1], key.strides[2]};
+    cuuint32_t box[4] = {key.box[0], key.box[1], key.box[2], key.box[3]};
     cuuint32_t estr[4] = {1, 1, 1, 1};
     CUresult r = fn(map,
                     p.dtype == ATTN_DTYPE_BF16 ? CU_TENSOR_MAP_DATA_TYPE_BFLOAT16
@@ -316,6 +359,10 @@ attn_status_t encode_4d(CUtensorMap* map, const void* base, const Problem& p, in
                     CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B,
                     CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
     if (r != CUDA_SUCCESS) return fail(ATTN_ERR_CUDA, "cuTensorMapEncodeTiled(%s) failed with %d", name, (int)r);
+    const int slot = c.used < MapCache::kEntries ? c.used++ : c.next;
+    if (slot == c.next) c.next = (c.next + 1) % MapCache::kEntries;
+    c.key[slot] = key;
+    c.map[slot] = *map;
     return ATTN_OK;
 }
 
@@ -411,6 +458,7 @@ attn_status_t fill_args(attn::FwdArgs& a, const Problem& p, int dev, const void*
     a.budget_ns = budget_ns(4.0 * double(p.B) * double(p.H) * double(p.S_q) * double(p.S_k) *
                             double(p.d));
     a.num_sms = g_num_sms[dev].load();
+    a.device = dev;
     a.n_split = 1;
     a.kv_per_split = 0;
     a.o_part = nullptr;
@@ -994,6 +1042,7 @@ attn_status_t attn_bwd_general(const attn_bwd_params_t* a, struct CUstream_st* s
     g.scale = p.scale;
     g.scale_log2 = static_cast<float>(static_cast<double>(p.scale) * 1.4426950408889634);
     g.num_sms = g_num_sms[dev].load();
+    g.device = dev;
     g.words = g_words_ptr[dev].load();
     g.launch_dkdv = next_launch(dev);
     g.launch_dq = next_launch(dev);

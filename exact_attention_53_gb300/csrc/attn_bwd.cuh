@@ -438,6 +438,7 @@ __global__ void __launch_bounds__(BwdTile<D>::THREADS, 1)
                 ++idx;
             }
             if (!ok) break;
+            if (uk == 1 && watch.launch_gave_up(abort_flag)) break;
             claim_next();    // the next unit, once this one's loads are all issued
         }
         if (*abort_flag && leader) {
@@ -875,6 +876,7 @@ __global__ void __launch_bounds__(DqTile<D>::THREADS, 1)
                 load(&tm_v, sVr, v_full, v_empty, T::VS, vidx, t * T::BS, hk, b);
             }
             if (!ok) break;
+            if (uq == 1 && watch.launch_gave_up(abort_flag)) break;
             // the next unit, once this one's loads are all issued
             if (!CAUSAL) ok = queue.claim(claims, leader, abort_flag, status, kStatusBwdProducer);
         }
@@ -1162,7 +1164,11 @@ cudaError_t launch_attn_bwd(const BwdArgs& a, cudaStream_t stream) {
     const long long group_bytes = 48LL << 20;
 
     auto kdkdv = attn_bwd_dkdv_kernel<D, BF16, CAUSAL>;
-    err = cudaFuncSetAttribute(kdkdv, cudaFuncAttributeMaxDynamicSharedMemorySize, T::SMEM_BYTES);
+    static std::atomic<uint64_t> configured_dkdv{0};
+    err = configure_once(configured_dkdv, a.device, [&]() {
+        return cudaFuncSetAttribute(kdkdv, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                    T::SMEM_BYTES);
+    });
     if (err != cudaSuccess) return err;
     const int n_kt = (a.S_k + T::BU - 1) / T::BU;
     const int bh_kv = a.BH / a.kv_group;
@@ -1184,7 +1190,11 @@ cudaError_t launch_attn_bwd(const BwdArgs& a, cudaStream_t stream) {
 
     using TQ = DqTile<D>;
     auto kdq = attn_bwd_dq_kernel<D, BF16, CAUSAL>;
-    err = cudaFuncSetAttribute(kdq, cudaFuncAttributeMaxDynamicSharedMemorySize, TQ::SMEM_BYTES);
+    static std::atomic<uint64_t> configured_dq{0};
+    err = configure_once(configured_dq, a.device, [&]() {
+        return cudaFuncSetAttribute(kdq, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                    TQ::SMEM_BYTES);
+    });
     if (err != cudaSuccess) return err;
     const int n_qt = (a.S_q + TQ::BU - 1) / TQ::BU;
     const long long units_q = static_cast<long long>(a.BH) * n_qt;

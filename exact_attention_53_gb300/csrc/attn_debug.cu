@@ -16,7 +16,13 @@
 #include <atomic>
 #include <mutex>
 
+// Built with -fvisibility=hidden: only the two entry points below are
+// exported.  Everything else (the kernel's host stub, the per-kernel set-up
+// flags of its launcher) stays private to this library, so a process that
+// also loads libattn.so never mixes the two builds' code or state.
+#pragma GCC visibility push(default)
 #include "attn_debug.h"
+#pragma GCC visibility pop
 #include "attn_fwd.cuh"
 
 namespace {
@@ -82,6 +88,11 @@ int attn_debug_fwd(const void* q, const void* k, const void* v, void* o, float* 
     a.scale_log2 = static_cast<float>(static_cast<double>(scale) * 1.4426950408889634);
     a.n_split = 1;
     a.pack = 1;
+    int dev = 0;
+    e = cudaGetDevice(&dev);
+    if (e != cudaSuccess) return static_cast<int>(e);
+    if (dev < 0 || dev >= 64) return static_cast<int>(cudaErrorInvalidDevice);
+    a.device = dev;
     a.words = static_cast<attn::DeviceWords*>(words);
     a.launch = ++g_debug_launches;
     a.budget_ns = 5000000000ull;

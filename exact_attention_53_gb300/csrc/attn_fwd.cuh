@@ -403,6 +403,7 @@ __global__ void __launch_bounds__(KernelTile<D, SPLIT>::THREADS, 1)
                 }
             }
             if (!ok) break;
+            if (r == 0 && watch.launch_gave_up(abort_flag)) break;
             // Claim the next unit only now, with this unit's last loads in the
             // ring: a unit claimed earlier would wait behind this whole unit
             // while idle CTAs find the queue empty.
@@ -845,17 +846,19 @@ cudaError_t launch_attn_fwd(const FwdArgs& a, cudaStream_t stream) {
     using T = KernelTile<D, SPLIT>;
     static_assert(!(SPLIT && CAUSAL), "split-KV is built for full attention only");
     auto kernel = attn_fwd_kernel<D, BF16, CAUSAL, SPLIT>;
-    cudaError_t err = cudaFuncSetAttribute(kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
-                                           T::SMEM_BYTES);
-    if (err != cudaSuccess) return err;
-    if (T::TILES == 2) {
+    static std::atomic<uint64_t> configured{0};
+    cudaError_t err = configure_once(configured, a.device, [&]() {
+        cudaError_t e = cudaFuncSetAttribute(kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                             T::SMEM_BYTES);
+        if (e != cudaSuccess || T::TILES != 2) return e;
         // The warpgroup register split assumes the launch grants LAUNCH_REGS a
         // thread; refuse to launch a build where it does not (it would stall).
         cudaFuncAttributes fa;
-        err = cudaFuncGetAttributes(&fa, kernel);
-        if (err != cudaSuccess) return err;
-        if (fa.numRegs != T::LAUNCH_REGS) return cudaErrorInvalidConfiguration;
-    }
+        e = cudaFuncGetAttributes(&fa, kernel);
+        if (e != cudaSuccess) return e;
+        return fa.numRegs == T::LAUNCH_REGS ? cudaSuccess : cudaErrorInvalidConfiguration;
+    });
+    if (err != cudaSuccess) return err;
     int head_group = 1;
     if (CAUSAL) {
         const long long kv_head_bytes = 2LL * a.S_k * D * 2;

@@ -4,6 +4,8 @@
 
 #include <cuda.h>
 #include <cuda_runtime.h>
+
+#include <atomic>
 #include <cstdint>
 
 namespace attn {
@@ -34,6 +36,7 @@ struct FwdArgs {
     int32_t causal_off;     // causal: key j is visible to query i iff j <= i + causal_off
     float scale_log2;       // scale · log2(e), either sign
     int32_t num_sms;        // SMs of the device (split-KV range planning)
+    int32_t device;         // CUDA device ordinal the launch runs on (< 64)
     // split-KV only (launch_attn_fwd<..., SPLIT = true>)
     int32_t n_split;        // key ranges per (head, query block)
     int32_t kv_per_split;   // key tiles per range
@@ -44,6 +47,18 @@ struct FwdArgs {
     unsigned long long launch;      // launch number of the forward kernel
     unsigned long long budget_ns;   // deadline of each CTA, from its start
 };
+
+// Run `setup` (a kernel's shared-memory opt-in and resource check) on the
+// first launch of that kernel on `device` only; `done` holds one bit per
+// device.  Returns setup's error, and keeps trying until it succeeds.
+template <typename F>
+cudaError_t configure_once(std::atomic<uint64_t>& done, int device, F&& setup) {
+    const uint64_t bit = uint64_t(1) << device;
+    if (done.load(std::memory_order_acquire) & bit) return cudaSuccess;
+    const cudaError_t e = setup();
+    if (e == cudaSuccess) done.fetch_or(bit, std::memory_order_acq_rel);
+    return e;
+}
 
 // Element strides of a [B, heads, S, d] tensor (d contiguous).
 struct RowLayout {
@@ -146,6 +161,7 @@ struct BwdArgs {
     int32_t causal_off;                   // key j visible to query i iff j <= i + causal_off
     float scale, scale_log2;
     int32_t num_sms;
+    int32_t device;                       // CUDA device ordinal (< 64)
     DeviceWords* words;
     // Launch numbers of the dK/dV and dQ kernels, and the CTAs' time budget.
     unsigned long long launch_dkdv, launch_dq, budget_ns;

@@ -4,7 +4,9 @@
 // loading (the default) its memory is reserved only in processes that call the
 // allocation-free entry point.  The host looks its address up with
 // cudaGetSymbolAddress from this file, where the symbol is visible.
+#pragma GCC visibility push(default)    // the C ABI is the library's only export
 #include "attn.h"
+#pragma GCC visibility pop
 #include "attn_launch.h"
 
 static __device__ __align__(256) unsigned char g_splitkv_scratch[ATTN_NOALLOC_SCRATCH_BYTES];

@@ -3,7 +3,9 @@
 // dependency latency, limits the rate.  Declared in include/attn_probe.h.
 #include <cuda_runtime.h>
 
+#pragma GCC visibility push(default)    // the C ABI is the library's only export
 #include "attn_probe.h"
+#pragma GCC visibility pop
 #include "sm100.cuh"
 
 namespace {

@@ -113,8 +113,9 @@ __device__ __forceinline__ bool mbar_wait(uint64_t* bar, uint32_t parity,
 //     derives from the launch's work, far above its real duration), and stops
 //     the CTA if it has;
 //   * a CTA that gave up records its launch number in words->abort_launch on
-//     its way out (publish_abort); producers read it when they start and every
-//     kPeerCheckNs after that, so the launch's other CTAs stop too.
+//     its way out (publish_abort); producers read it once their first unit's
+//     loads are issued and every kPeerCheckNs after that, so the launch's
+//     other CTAs stop too.
 // Every role's step loop waits on a barrier that the producer (directly or
 // through the MMA warp) completes once per step, so a role that ran past its
 // partners (a wrong trip count) blocks within a ring's depth of steps and
@@ -130,9 +131,18 @@ struct LaunchWatch {
         : words(w), launch(launch_no) {
         const uint64_t now = global_timer_ns();
         deadline = now + budget_ns;
-        // The first read of the word comes a microsecond in, after the first
-        // unit's first loads are on their way, so it does not delay them.
-        next_peer = now + 1000;
+        next_peer = now + kPeerCheckNs;
+    }
+
+    // Read the abort word now (the producer calls this once its first unit's
+    // loads are in flight, so the read's latency hides behind them): a CTA
+    // that starts after its launch gave up stops here.
+    __device__ __forceinline__ bool launch_gave_up(volatile int* abort_flag) {
+        int s = *reinterpret_cast<const volatile unsigned long long*>(&words->abort_launch) ==
+                launch;
+        s = __shfl_sync(0xffffffffu, s, 0);
+        if (s && (threadIdx.x & 31) == 0) *abort_flag = 1;
+        return s != 0;
     }
 
     // True once the CTA must stop: it already has, it passed its deadline

@@ -66,6 +66,28 @@ def test_debug_library_exports_only_its_hooks(lib):
         assert not hasattr(lib, name), name
 
 
+def _exported(path):
+    import shutil
+    import subprocess
+    nm = shutil.which("nm")
+    if not nm:
+        pytest.skip("nm is not installed")
+    out = subprocess.run([nm, "-D", "--defined-only", path], stdout=subprocess.PIPE, text=True,
+                         check=True).stdout
+    return {line.split()[-1] for line in out.splitlines() if line.strip()}
+
+
+def test_libraries_export_only_their_c_abi(lib):
+    """Each library exports the functions its headers declare and nothing else of its own, so
+    loading both in one process never mixes their template code or its static state."""
+    pkg = os.path.dirname(binding.library_path())
+    ours = {n for n in _exported(binding.library_path()) if n.startswith("attn")}
+    assert ours == set(_declared_functions()) | set(binding.PROBES)
+    assert not {n for n in _exported(binding.library_path()) if "attn" in n and n not in ours}
+    dbg = _exported(os.path.join(pkg, "libattn_debug.so"))
+    assert {n for n in dbg if "attn" in n} == set(binding.DEBUG_EXPORTS)
+
+
 def test_debug_entry_rejects_bad_arguments_before_device_work():
     dbg = binding.load_debug_library()
     assert dbg.attn_debug_fwd(None, A, A, A, A, 1, 1, 128, 0.125, -1, None) == 1
