@@ -38,7 +38,7 @@ FLAGS = ["-O3", "-std=c++17", "-lineinfo", "-Xcompiler", "-fPIC", "-Xcompiler", 
 INSTANCES = ([(d, bf16, causal, 0) for d in (64, 128, 256) for bf16 in (0, 1) for causal in (0, 1)]
              + [(d, bf16, 0, 1) for d in (64, 128, 256) for bf16 in (0, 1)])
 # (head_dim, bf16, causal) of the backward
-BWD_INSTANCES = [(d, bf16, causal) for d in (64, 128) for bf16 in (0, 1) for causal in (0, 1)]
+BWD_INSTANCES = [(d, bf16, causal) for d in (64, 128, 256) for bf16 in (0, 1) for causal in (0, 1)]
 
 
 def _nvcc() -> str:

@@ -577,6 +577,7 @@ BwdLaunchFn pick_bwd(int64_t d, bool bf16, bool causal) {
     }
     ATTN_PICK_BWD(64)
     ATTN_PICK_BWD(128)
+    ATTN_PICK_BWD(256)
 #undef ATTN_PICK_BWD
     return nullptr;
 }
@@ -586,9 +587,9 @@ int64_t bwd_s_pad(const Problem& p) { return (p.S_q + 127) / 128 * 128; }
 int64_t bwd_workspace_bytes(const Problem& p) { return 2 * p.B * p.H * bwd_s_pad(p) * 4; }
 
 attn_status_t validate_bwd_head_dim(const Problem& p) {
-    if (p.d != 64 && p.d != 128)
+    if (p.d != 64 && p.d != 128 && p.d != 256)
         return fail(ATTN_ERR_UNSUPPORTED,
-                    "head_dim d=%lld not supported by the backward; must be one of [64, 128]",
+                    "head_dim d=%lld not supported by the backward; must be one of [64, 128, 256]",
                     (long long)p.d);
     return ATTN_OK;
 }
@@ -1017,6 +1018,10 @@ attn_status_t attn_bwd_general(const attn_bwd_params_t* a, struct CUstream_st* s
     if ((s = encode_4d(&g.tm_q_fixed, a->q, p, p.S_q, p.H, p.lq, 128, "q")) != ATTN_OK) return s;
     if ((s = encode_4d(&g.tm_do_fixed, a->dout, p, p.S_q, p.H, a->do_layout, 128, "dout")) != ATTN_OK)
         return s;
+    if (p.d == 256) {
+        if ((s = encode_4d(&g.tm_k_step, a->k, p, p.S_k, p.H_kv, p.lk, 64, "k")) != ATTN_OK) return s;
+        if ((s = encode_4d(&g.tm_v_step, a->v, p, p.S_k, p.H_kv, p.lv, 64, "v")) != ATTN_OK) return s;
+    }
     auto rl = [](const attn_layout_t& l) { return attn::RowLayout{l.batch, l.head, l.row}; };
     const int64_t s_pad = bwd_s_pad(p);
     g.o = a->o;
@@ -1045,9 +1050,11 @@ attn_status_t attn_bwd_general(const attn_bwd_params_t* a, struct CUstream_st* s
     g.device = dev;
     g.words = g_words_ptr[dev].load();
     g.launch_dkdv = next_launch(dev);
+    g.launch_key2 = next_launch(dev);
     g.launch_dq = next_launch(dev);
-    // seven S_q×S_k×d products of 2 flops per element between the two kernels
-    g.budget_ns = budget_ns(14.0 * double(p.B) * double(p.H) * double(p.S_q) * double(p.S_k) *
+    // seven S_q×S_k×d products of 2 flops per element between the kernels
+    // (eight at d = 256)
+    g.budget_ns = budget_ns(16.0 * double(p.B) * double(p.H) * double(p.S_q) * double(p.S_k) *
                             double(p.d));
     BwdLaunchFn fn = pick_bwd(p.d, p.dtype == ATTN_DTYPE_BF16, p.causal);
     if (!fn) return fail(ATTN_ERR_UNSUPPORTED, "no backward kernel for d=%lld", (long long)p.d);

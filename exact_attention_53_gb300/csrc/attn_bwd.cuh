@@ -673,36 +673,39 @@ __global__ void __launch_bounds__(BwdTile<D>::THREADS, 1)
 }
 
 // ============================================================== dQ
-// 128-key steps, so every Q·Kᵀ / dO·Vᵀ MMA has N = 128.  Tensor memory: S in
-// two buffers (columns 0 and 128; dS overwrites the first 64 columns of its
-// own buffer as packed 16-bit pairs), one dP buffer (256) that the softmax
-// warps release as soon as they have read it, dQ at 384.  K and V arrive
-// through separate shared-memory rings.
+// 128-key steps for d <= 128, so every Q·Kᵀ / dO·Vᵀ MMA has N = 128; 64-key
+// steps for d = 256, where the fixed Q and dO tiles take 128 KB of shared
+// memory.  Tensor memory: S in two buffers (columns 0 and BS; dS overwrites
+// the first BS/2 columns of its own buffer as packed 16-bit pairs), one dP
+// buffer (2·BS) that the softmax warps release as soon as they have read it,
+// and dQ.  K and V arrive through separate shared-memory rings.
 template <int D>
 struct DqTile {
-    static_assert(D == 64 || D == 128, "the backward is built for head_dim 64 and 128");
+    static_assert(D == 64 || D == 128 || D == 256, "head_dim 64, 128 or 256");
     static constexpr int BU = 128;                    // query rows per unit
-    static constexpr int BS = 128;                    // keys per step
+    static constexpr int BS = D == 256 ? 64 : 128;    // keys per step
     static constexpr int CHUNKS = D / 64;
-    static constexpr int CHUNK = 128 * 128;           // one atom column of a 128-row tile
-    static constexpr int TILE = 128 * D * 2;
+    static constexpr int FIX_CHUNK = BU * 128;        // one atom column of the 128-row Q / dO
+    static constexpr int FIX_TILE = BU * D * 2;
+    static constexpr int KV_CHUNK = BS * 128;         // of a K / V step
+    static constexpr int KV_TILE = BS * D * 2;
     // K and V stream through rings of their own: V of a step is free once its
     // dP MMA is done, K only after the step's dQ MMA.
-    static constexpr int KS = D == 64 ? 5 : 3;        // K ring slots
-    static constexpr int VS = D == 64 ? 4 : 2;        // V ring slots
+    static constexpr int KS = D == 64 ? 5 : (D == 128 ? 3 : 2);   // K ring slots
+    static constexpr int VS = D == 64 ? 4 : (D == 128 ? 2 : 1);   // V ring slots
     static constexpr int CLC_SLOTS = 4;               // work-queue answers in flight
     static constexpr int NUM_BARS = 2 + 2 * KS + 2 * VS + 2 + 1 + 2 + 1 + 1 + 2 * CLC_SLOTS;
-    static constexpr int TILE_BYTES = 2 * TILE + (KS + VS) * TILE;
+    static constexpr int TILE_BYTES = 2 * FIX_TILE + (KS + VS) * KV_TILE;
     static constexpr int SMEM_BYTES = 1024 + TILE_BYTES + CLC_SLOTS * 16 + NUM_BARS * 8 + 16;
     static constexpr int THREADS = 192;               // 4 softmax warps, producer, MMA
     static constexpr int PRODUCER_WARP = 4;
     static constexpr int MMA_WARP = 5;
     static constexpr uint32_t TMEM_COLS = 512;
-    static constexpr uint32_t S_COL = 0;              // S buffer b at 128·b
-    static constexpr uint32_t DP_COL = 256;
-    static constexpr uint32_t ACC_COL = 384;
+    static constexpr uint32_t S_COL = 0;              // S buffer b at BS·b
+    static constexpr uint32_t DP_COL = 2 * BS;
+    static constexpr uint32_t ACC_COL = D == 256 ? 256 : 384;
     static_assert(SMEM_BYTES <= 232448, "shared memory budget");
-    static_assert(ACC_COL + D <= TMEM_COLS, "tensor memory budget");
+    static_assert(DP_COL + BS <= ACC_COL && ACC_COL + D <= TMEM_COLS, "tensor memory budget");
 };
 
 template <int D, bool BF16, bool CAUSAL>
@@ -723,9 +726,9 @@ __global__ void __launch_bounds__(DqTile<D>::THREADS, 1)
     const uint32_t raw_addr = smem_u32(smem_raw);
     uint8_t* smem = smem_raw + ((1024u - (raw_addr & 1023u)) & 1023u);
     uint8_t* sQ = smem;
-    uint8_t* sdO = sQ + T::TILE;
-    uint8_t* sKr = sdO + T::TILE;                      // K ring
-    uint8_t* sVr = sKr + T::KS * T::TILE;              // V ring
+    uint8_t* sdO = sQ + T::FIX_TILE;
+    uint8_t* sKr = sdO + T::FIX_TILE;                  // K ring
+    uint8_t* sVr = sKr + T::KS * T::KV_TILE;           // V ring
     uint8_t* clc_resp = smem + T::TILE_BYTES;          // [CLC_SLOTS] 16-byte answers
     uint64_t* bars = reinterpret_cast<uint64_t*>(clc_resp + T::CLC_SLOTS * 16);
     uint64_t* q_full = bars;
@@ -838,10 +841,10 @@ __global__ void __launch_bounds__(DqTile<D>::THREADS, 1)
             ok = __all_sync(0xffffffffu, ok);
             if (!ok) return;
             if (leader) {
-                mbar_arrive_expect_tx(&full[slot], T::TILE);
+                mbar_arrive_expect_tx(&full[slot], T::KV_TILE);
 #pragma unroll
                 for (int c = 0; c < T::CHUNKS; ++c)
-                    tma_load_4d(ring + slot * T::TILE + c * T::CHUNK, map, &full[slot], c * 64,
+                    tma_load_4d(ring + slot * T::KV_TILE + c * T::KV_CHUNK, map, &full[slot], c * 64,
                                 row, hk, b);
             }
             __syncwarp();
@@ -863,11 +866,11 @@ __global__ void __launch_bounds__(DqTile<D>::THREADS, 1)
             if (!ok) break;
             ++uq;
             if (leader) {
-                mbar_arrive_expect_tx(q_full, 2 * T::TILE);
+                mbar_arrive_expect_tx(q_full, 2 * T::FIX_TILE);
 #pragma unroll
                 for (int c = 0; c < T::CHUNKS; ++c) {
-                    tma_load_4d(sQ + c * T::CHUNK, &tm_q, q_full, c * 64, qt * T::BU, h, b);
-                    tma_load_4d(sdO + c * T::CHUNK, &tm_do, q_full, c * 64, qt * T::BU, h, b);
+                    tma_load_4d(sQ + c * T::FIX_CHUNK, &tm_q, q_full, c * 64, qt * T::BU, h, b);
+                    tma_load_4d(sdO + c * T::FIX_CHUNK, &tm_do, q_full, c * 64, qt * T::BU, h, b);
                 }
             }
             __syncwarp();
@@ -913,7 +916,7 @@ __global__ void __launch_bounds__(DqTile<D>::THREADS, 1)
         const uint64_t q_desc = sdesc_sw128(smem_u32(sQ), 16, 1024);
         const uint64_t do_desc = sdesc_sw128(smem_u32(sdO), 16, 1024);
         const uint64_t kk_desc = sdesc_sw128(smem_u32(sKr), 16, 1024);          // K as K-major B
-        const uint64_t km_desc = sdesc_sw128(smem_u32(sKr), T::CHUNK, 1024);    // K as MN-major B
+        const uint64_t km_desc = sdesc_sw128(smem_u32(sKr), T::KV_CHUNK, 1024); // K as MN-major B
         const uint64_t vk_desc = sdesc_sw128(smem_u32(sVr), 16, 1024);
         const uint32_t q_lo = static_cast<uint32_t>(q_desc), q_hi = static_cast<uint32_t>(q_desc >> 32);
         const uint32_t do_lo = static_cast<uint32_t>(do_desc), do_hi = static_cast<uint32_t>(do_desc >> 32);
@@ -936,31 +939,33 @@ __global__ void __launch_bounds__(DqTile<D>::THREADS, 1)
         };
         // S_b = Q·K_slotᵀ: M = 128 queries, N = 128 keys, K = D
         auto mma_s = [&](int slot, int b) {
-            const uint32_t koff = (slot * T::TILE) >> 4;
+            const uint32_t koff = (slot * T::KV_TILE) >> 4;
 #pragma unroll
             for (int kk = 0; kk < D / 16; ++kk) {
-                const uint32_t o = ((kk >> 2) * T::CHUNK + (kk & 3) * 32) >> 4;
-                mma_ss_warp(tmem + T::S_COL + b * 128, q_lo + o, q_hi, kk_lo + koff + o, kk_hi,
+                const uint32_t o = ((kk >> 2) * T::FIX_CHUNK + (kk & 3) * 32) >> 4;
+                const uint32_t ok_ = ((kk >> 2) * T::KV_CHUNK + (kk & 3) * 32) >> 4;
+                mma_ss_warp(tmem + T::S_COL + b * T::BS, q_lo + o, q_hi, kk_lo + koff + ok_, kk_hi,
                             id_s, kk > 0 ? 1u : 0u);
             }
         };
         // dP = dO·V_slotᵀ
         auto mma_dp = [&](int slot) {
-            const uint32_t voff = (slot * T::TILE) >> 4;
+            const uint32_t voff = (slot * T::KV_TILE) >> 4;
 #pragma unroll
             for (int kk = 0; kk < D / 16; ++kk) {
-                const uint32_t o = ((kk >> 2) * T::CHUNK + (kk & 3) * 32) >> 4;
-                mma_ss_warp(tmem + T::DP_COL, do_lo + o, do_hi, vk_lo + voff + o, vk_hi, id_s,
+                const uint32_t o = ((kk >> 2) * T::FIX_CHUNK + (kk & 3) * 32) >> 4;
+                const uint32_t ov = ((kk >> 2) * T::KV_CHUNK + (kk & 3) * 32) >> 4;
+                mma_ss_warp(tmem + T::DP_COL, do_lo + o, do_hi, vk_lo + voff + ov, vk_hi, id_s,
                             kk > 0 ? 1u : 0u);
             }
         };
         // dQ += dS_b·K_slot: M = 128 queries, N = D, K = 128 keys (dS packed in cols 0..63 of S_b)
         auto mma_acc = [&](int slot, int b, bool acc) {
-            const uint32_t koff = (slot * T::TILE) >> 4;
+            const uint32_t koff = (slot * T::KV_TILE) >> 4;
 #pragma unroll
             for (int kk = 0; kk < T::BS / 16; ++kk) {
                 const uint32_t bo = (kk * 16 * 128) >> 4;
-                mma_ts_warp(tmem + T::ACC_COL, tmem + T::S_COL + b * 128 + kk * 8,
+                mma_ts_warp(tmem + T::ACC_COL, tmem + T::S_COL + b * T::BS + kk * 8,
                             km_lo + koff + bo, km_hi, id_acc, (acc || kk > 0) ? 1u : 0u);
             }
         };
@@ -1078,15 +1083,15 @@ __global__ void __launch_bounds__(DqTile<D>::THREADS, 1)
                     (CAUSAL && kv0 + T::BS - 1 > row_begin + causal_off) || (kv0 + T::BS > S_k);
                 const int lim =
                     masked ? min(S_k, CAUSAL ? q_idx + 1 + causal_off : S_k) - kv0 : T::BS;
-                const uint32_t sb = lane_base + T::S_COL + b * 128;
-                // Two halves of 64 keys; dS of half h goes to columns 32h..32h+31
-                // of S_b, which have been read by then.
+                const uint32_t sb = lane_base + T::S_COL + b * T::BS;
+                // Halves of 64 keys (two for 128-key steps); dS of half h goes to
+                // columns 32h..32h+31 of S_b, which have been read by then.
 #pragma unroll 1
-                for (int h = 0; h < 2; ++h) {
+                for (int h = 0; h < T::BS / 64; ++h) {
                     uint32_t sv[64], dpv[64];
                     tmem_ld64(sb + h * 64, sv);
                     tmem_ld64(lane_base + T::DP_COL + h * 64, dpv);
-                    if (h == 1) {
+                    if (h == T::BS / 64 - 1) {
                         tc_fence_before();
                         __syncwarp();
                         if (lane == 0) mbar_arrive(dp_free);
@@ -1135,10 +1140,79 @@ __global__ void __launch_bounds__(DqTile<D>::THREADS, 1)
     }
 }
 
+}  // namespace attn
+
+#include "attn_bwd_wide.cuh"
+
+namespace attn {
+
 // ============================================================== launch
+// The key-side kernels of one backward call: attn_bwd_dkdv_kernel for
+// d <= 128; the two passes of attn_bwd_wide_kernel (dV, then dK) for d = 256.
+template <int D, bool BF16, bool CAUSAL>
+cudaError_t launch_key_side(const BwdArgs& a, cudaStream_t stream, long long op_bytes,
+                            long long group_bytes) {
+    cudaError_t err;
+    const int bh_kv = a.BH / a.kv_group;
+    const int hg_kv = static_cast<int>(
+        std::max<long long>(1, group_bytes / (op_bytes * a.S_q * a.kv_group)));
+    if constexpr (D != 256) {
+        using T = BwdTile<D>;
+        auto kdkdv = attn_bwd_dkdv_kernel<D, BF16, CAUSAL>;
+        static std::atomic<uint64_t> configured_dkdv{0};
+        err = configure_once(configured_dkdv, a.device, [&]() {
+            return cudaFuncSetAttribute(kdkdv, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                        T::SMEM_BYTES);
+        });
+        if (err != cudaSuccess) return err;
+        const int n_kt = (a.S_k + T::BU - 1) / T::BU;
+        const long long units_kv = static_cast<long long>(bh_kv) * n_kt;
+        if (units_kv > 0x7fffffffLL) return cudaErrorInvalidConfiguration;
+        // Full attention: one CTA per unit (the work queue hands the units out);
+        // causal: one persistent CTA per SM.
+        kdkdv<<<static_cast<int>(CAUSAL ? std::min<long long>(units_kv, a.num_sms) : units_kv),
+                T::THREADS, T::SMEM_BYTES,
+                stream>>>(a.tm_k_fixed, a.tm_v_fixed, a.tm_q_step, a.tm_do_step, a.lse2, a.delta,
+                          static_cast<uint16_t*>(a.dk), static_cast<uint16_t*>(a.dv), a.dk_lay,
+                          a.dv_lay, a.S_q, a.S_k, bh_kv, a.H, a.kv_group, a.S_pad, hg_kv,
+                          a.causal_off, a.scale, a.scale_log2, a.words, a.launch_dkdv,
+                          a.budget_ns);
+        return cudaGetLastError();
+    } else {
+        auto kdv = attn_bwd_wide_kernel<BF16, CAUSAL, kPassDV>;
+        auto kdk = attn_bwd_wide_kernel<BF16, CAUSAL, kPassDK>;
+        using TV = BwdWideTile<kPassDV>;
+        using TK = BwdWideTile<kPassDK>;
+        static std::atomic<uint64_t> configured_wide{0};
+        err = configure_once(configured_wide, a.device, [&]() {
+            cudaError_t e = cudaFuncSetAttribute(kdv, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                                 TV::SMEM_BYTES);
+            if (e != cudaSuccess) return e;
+            return cudaFuncSetAttribute(kdk, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                        TK::SMEM_BYTES);
+        });
+        if (err != cudaSuccess) return err;
+        const int n_kt = (a.S_k + TV::BU - 1) / TV::BU;
+        const long long units_kv = static_cast<long long>(bh_kv) * n_kt;
+        if (units_kv > 0x7fffffffLL) return cudaErrorInvalidConfiguration;
+        const int grid =
+            static_cast<int>(CAUSAL ? std::min<long long>(units_kv, a.num_sms) : units_kv);
+        kdv<<<grid, TV::THREADS, TV::SMEM_BYTES, stream>>>(
+            a.tm_k_fixed, a.tm_v_fixed, a.tm_q_step, a.tm_do_step, a.lse2, a.delta,
+            static_cast<uint16_t*>(a.dv), a.dv_lay, a.S_q, a.S_k, bh_kv, a.H, a.kv_group, a.S_pad,
+            hg_kv, a.causal_off, 1.f, a.scale_log2, a.words, a.launch_dkdv, a.budget_ns);
+        err = cudaGetLastError();
+        if (err != cudaSuccess) return err;
+        kdk<<<grid, TK::THREADS, TK::SMEM_BYTES, stream>>>(
+            a.tm_k_fixed, a.tm_v_fixed, a.tm_q_step, a.tm_do_step, a.lse2, a.delta,
+            static_cast<uint16_t*>(a.dk), a.dk_lay, a.S_q, a.S_k, bh_kv, a.H, a.kv_group, a.S_pad,
+            hg_kv, a.causal_off, a.scale, a.scale_log2, a.words, a.launch_key2, a.budget_ns);
+        return cudaGetLastError();
+    }
+}
+
 template <int D, bool BF16, bool CAUSAL>
 cudaError_t launch_attn_bwd(const BwdArgs& a, cudaStream_t stream) {
-    using T = BwdTile<D>;
     // D and LSE·log2e into the padded workspace.
     const long long rows_pad = static_cast<long long>(a.BH) * a.S_pad;
     const long long rows_per_block = 8LL * prep_rows_per_warp<D>();
@@ -1163,29 +1237,7 @@ cudaError_t launch_attn_bwd(const BwdArgs& a, cudaStream_t stream) {
     const long long op_bytes = 2LL * D * 2;   // per row of one head: two operands
     const long long group_bytes = 48LL << 20;
 
-    auto kdkdv = attn_bwd_dkdv_kernel<D, BF16, CAUSAL>;
-    static std::atomic<uint64_t> configured_dkdv{0};
-    err = configure_once(configured_dkdv, a.device, [&]() {
-        return cudaFuncSetAttribute(kdkdv, cudaFuncAttributeMaxDynamicSharedMemorySize,
-                                    T::SMEM_BYTES);
-    });
-    if (err != cudaSuccess) return err;
-    const int n_kt = (a.S_k + T::BU - 1) / T::BU;
-    const int bh_kv = a.BH / a.kv_group;
-    const long long units_kv = static_cast<long long>(bh_kv) * n_kt;
-    if (units_kv > 0x7fffffffLL) return cudaErrorInvalidConfiguration;
-    const int hg_kv = static_cast<int>(
-        std::max<long long>(1, group_bytes / (op_bytes * a.S_q * a.kv_group)));
-    // Full attention: one CTA per unit (the work queue hands the units out);
-    // causal: one persistent CTA per SM.
-    kdkdv<<<static_cast<int>(CAUSAL ? std::min<long long>(units_kv, a.num_sms) : units_kv), T::THREADS,
-            T::SMEM_BYTES,
-            stream>>>(a.tm_k_fixed, a.tm_v_fixed, a.tm_q_step, a.tm_do_step, a.lse2, a.delta,
-                      static_cast<uint16_t*>(a.dk), static_cast<uint16_t*>(a.dv), a.dk_lay,
-                      a.dv_lay, a.S_q, a.S_k, bh_kv, a.H, a.kv_group, a.S_pad, hg_kv,
-                      a.causal_off, a.scale, a.scale_log2, a.words, a.launch_dkdv,
-                      a.budget_ns);
-    err = cudaGetLastError();
+    err = launch_key_side<D, BF16, CAUSAL>(a, stream, op_bytes, group_bytes);
     if (err != cudaSuccess) return err;
 
     using TQ = DqTile<D>;
@@ -1202,7 +1254,8 @@ cudaError_t launch_attn_bwd(const BwdArgs& a, cudaStream_t stream) {
     const int hg_q = static_cast<int>(std::max<long long>(1, group_bytes / (op_bytes * a.S_k)));
     kdq<<<static_cast<int>(CAUSAL ? std::min<long long>(units_q, a.num_sms) : units_q), TQ::THREADS,
           TQ::SMEM_BYTES,
-          dq_stream>>>(a.tm_q_fixed, a.tm_do_fixed, a.tm_k_fixed, a.tm_v_fixed, a.lse2, a.delta,
+          dq_stream>>>(a.tm_q_fixed, a.tm_do_fixed, D == 256 ? a.tm_k_step : a.tm_k_fixed,
+                       D == 256 ? a.tm_v_step : a.tm_v_fixed, a.lse2, a.delta,
                     static_cast<uint16_t*>(a.dq), a.dq_lay, a.S_q, a.S_k, a.BH, a.H, a.kv_group,
                     a.S_pad, hg_q, a.causal_off, a.scale, a.scale_log2, a.words, a.launch_dq,
                     a.budget_ns);

@@ -1,5 +1,5 @@
 // One (head_dim, dtype, causal) instantiation of the attention backward per
-// object file, selected by -DATTN_D=<64|128> -DATTN_BF16=<0|1>
+// object file, selected by -DATTN_D=<64|128|256> -DATTN_BF16=<0|1>
 // -DATTN_CAUSAL=<0|1>, so the instantiations compile in parallel.
 #include "attn_bwd.cuh"
 

@@ -139,13 +139,15 @@ cudaError_t launch_attn_combine(const float* o_part, const float* lse_part, void
                                 const RowLayout& o_lay, cudaStream_t stream);
 
 // Backward launch contract (attn_bwd.cuh).  The dK/dV kernel keeps 128-row K
-// and V tiles and streams 64-row Q and dO steps; the dQ kernel keeps 128-row
-// Q and dO tiles and streams 128-row K and V steps.
+// and V tiles and streams 64-row Q and dO steps (d = 256: two passes, dV and
+// dK, attn_bwd_wide.cuh); the dQ kernel keeps 128-row Q and dO tiles and
+// streams 128-row K and V steps (64-row at d = 256).
 struct BwdArgs {
     // 4-D maps (d, S, heads, B) in each tensor's own layout
     CUtensorMap tm_k_fixed, tm_v_fixed;   // K, V: (d, S_k, H_kv, B), box 64 × 128
     CUtensorMap tm_q_step, tm_do_step;    // Q, dO: (d, S_q, H, B), box 64 × 64
     CUtensorMap tm_q_fixed, tm_do_fixed;  // Q, dO: (d, S_q, H, B), box 64 × 128
+    CUtensorMap tm_k_step, tm_v_step;     // K, V: box 64 × 64 (d = 256 only: the dQ kernel's steps)
     const void* o;                        // forward output [B, H, S_q, d]
     const void* dout;                     // dO [B, H, S_q, d]
     const float* lse;                     // forward LSE [B, H, S_q], natural log
@@ -163,8 +165,9 @@ struct BwdArgs {
     int32_t num_sms;
     int32_t device;                       // CUDA device ordinal (< 64)
     DeviceWords* words;
-    // Launch numbers of the dK/dV and dQ kernels, and the CTAs' time budget.
-    unsigned long long launch_dkdv, launch_dq, budget_ns;
+    // Launch numbers of the key-side kernel (the dV pass at d = 256), of the
+    // dK pass (d = 256) and of the dQ kernel, and the CTAs' time budget.
+    unsigned long long launch_dkdv, launch_key2, launch_dq, budget_ns;
     // When set, the dQ kernel runs on aux_stream, concurrently with the dK/dV
     // kernel on the caller's stream (they read the same inputs and write
     // disjoint outputs): ev_fork orders it after the prep kernel, ev_join

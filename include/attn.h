@@ -275,19 +275,21 @@ attn_status_t attn_fwd_splitkv(const void* q, const void* k, const void* v, void
  *
  * (the gradients of Σ O ∘ dO for the forward above; the scale follows from the
  * chain rule through scale·Q·Kᵀ).  dQ is produced by its own pass, not by
- * atomic adds, so results are deterministic.  head_dim 64 or 128.
+ * atomic adds, so results are deterministic.  head_dim 64, 128 or 256 (at
+ * 256 the key side runs as two passes, dV then dK, each recomputing Sᵀ).
  *
  * attn_bwd_workspace_size — bytes of workspace attn_bwd needs:
  * 2 · B·H · S_pad · 4 with S_pad = S_q rounded up to a multiple of 128 (the
  * page's di vector and the LSE in base 2, padded to whole tiles).  Validates
- * like attn_fwd (and head_dim ∈ {64, 128}); touches no device.
+ * like attn_fwd; touches no device.
  */
 attn_status_t attn_bwd_workspace_size(int64_t B, int64_t H, int64_t S_q, int64_t S_k, int64_t d,
                                       attn_dtype_t dtype, int64_t* workspace_bytes);
 
 /*
  * attn_bwd — enqueue the backward on `stream`: a prep kernel, then the dK/dV
- * kernel on `stream` and the dQ kernel, at the same time, on a helper stream
+ * kernel (d = 256: a dV and a dK kernel) on `stream` and the dQ kernel, at the
+ * same time, on a helper stream
  * that the library creates for the device on its first backward call (forked
  * from `stream` after the prep kernel and joined back before the call's end,
  * so `stream` sees one ordered operation).  A stream capture of `stream`
@@ -301,7 +303,7 @@ attn_status_t attn_bwd_workspace_size(int64_t B, int64_t H, int64_t S_q, int64_t
  *   dq, dk, dv outputs, [B,H,S_q,d], [B,H,S_k,d], [B,H,S_k,d] in `dtype`,
  *              16-byte aligned; every element is written (key rows that no
  *              query sees get zeros)
- *   B .. dtype as attn_fwd; d ∈ {64, 128}
+ *   B .. dtype as attn_fwd
  *   workspace  device, 16-byte aligned, at least attn_bwd_workspace_size
  *              bytes; written before it is read (nothing needs clearing);
  *              calls in flight at the same time need separate workspaces

@@ -84,7 +84,7 @@ SHAPES = [(1, 1, 1, 1), (1, 2, 17, 17), (1, 1, 64, 64), (2, 1, 127, 127), (1, 2,
 @pytest.mark.parametrize("shape", SHAPES, ids=lambda s: "x".join(map(str, s)))
 @pytest.mark.parametrize("causal", [False, True], ids=["full", "causal"])
 @pytest.mark.parametrize("dtype", ["f16", "bf16"])
-@pytest.mark.parametrize("d", [64, 128])
+@pytest.mark.parametrize("d", [64, 128, 256])
 def test_bwd_small_shapes(d, dtype, causal, shape):
     B, H, S_q, S_k = shape
     seed = S_q * 7907 + S_k * 37 + d + (1 if causal else 0)
@@ -101,7 +101,7 @@ def test_bwd_small_shapes(d, dtype, causal, shape):
 
 @pytest.mark.parametrize("causal", [False, True], ids=["full", "causal"])
 @pytest.mark.parametrize("dtype", ["f16", "bf16"])
-@pytest.mark.parametrize("d", [64, 128])
+@pytest.mark.parametrize("d", [64, 128, 256])
 def test_bwd_negative_scale(d, dtype, causal):
     """A negative scale (the page's sm_scale is any f32): forward and backward of the same
     problem, gradients within the derived bound (with |scale| in it)."""
@@ -141,9 +141,22 @@ def test_bwd_c3_sampled_heads(causal):
                     f"c3 causal={causal} head=({b},{h})")
 
 
-def test_bwd_deterministic():
-    q, k, v = make_qkv(2, 3, 500, 700, 128, "bf16", seed=31)
-    do = make_qkv(2, 3, 500, 1, 128, "bf16", seed=32)[0]
+def test_bwd_c5_sampled_heads():
+    """The d=256, S=8192 workload at full size (the two-pass key side); two heads in full."""
+    w = WORKLOADS["c5"]
+    q, k, v = workload_qkv(w)
+    do = make_qkv(w.B, w.H, w.S_q, 1, w.d, w.dtype, seed=w.seed + 100)[0]
+    dq, dk, dv = _run_bwd(q, k, v, do, False, w.scale)
+    for b, h in ((0, 0), (1, 7)):
+        got = (_f64(dq[b, h]), _f64(dk[b, h]), _f64(dv[b, h]))
+        _check_head(got, q[b, h], k[b, h], v[b, h], do[b, h], False, w.scale, w.dtype,
+                    f"c5 head=({b},{h})")
+
+
+@pytest.mark.parametrize("d", [128, 256])
+def test_bwd_deterministic(d):
+    q, k, v = make_qkv(2, 3, 500, 700, d, "bf16", seed=31)
+    do = make_qkv(2, 3, 500, 1, d, "bf16", seed=32)[0]
     for causal in (False, True):
         a = _run_bwd(q, k, v, do, causal, 0.1)
         b = _run_bwd(q, k, v, do, causal, 0.1)

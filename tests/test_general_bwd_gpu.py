@@ -86,7 +86,7 @@ def _check(got, ref, bnd, what):
                          ids=["full", "causal", "bottom_right"])
 @pytest.mark.parametrize("H,H_kv", [(4, 4), (8, 2), (6, 1)], ids=["mha", "gqa4", "mqa"])
 @pytest.mark.parametrize("dtype", ["f16", "bf16"])
-@pytest.mark.parametrize("d", [64, 128])
+@pytest.mark.parametrize("d", [64, 128, 256])
 def test_bwd_bshd_gqa_masks(d, dtype, H, H_kv, mask):
     B, S_q, S_k = 1, 200, 333
     q, _, _ = make_qkv(B, H, S_q, 1, d, dtype, seed=3 * d + H + mask)

@@ -29,9 +29,12 @@ def test_every_kernel_reported(table):
     from exact_attention_53_gb300.build import BWD_INSTANCES, INSTANCES
     fwd = [k for k in table if "attn_fwd_kernel" in k]
     bwd = [k for k in table if re.search(r"attn_bwd_(dkdv|dq|prep)_kernel", k)]
+    wide = [k for k in table if "attn_bwd_wide_kernel" in k]
     assert len(fwd) == len(INSTANCES)
-    # dK/dV and dQ per instance, prep per (d, dtype)
-    assert len(bwd) == 2 * len(BWD_INSTANCES) + len(BWD_INSTANCES) // 2
+    # per instance: dQ, and dK/dV (d <= 128) or its two d = 256 passes; prep per (d, dtype)
+    n_wide = sum(1 for d, _, _ in BWD_INSTANCES if d == 256)
+    assert len(bwd) == 2 * len(BWD_INSTANCES) - n_wide + len(BWD_INSTANCES) // 2
+    assert len(wide) == 2 * n_wide
 
 
 def test_no_kernel_spills(table):
