@@ -127,12 +127,13 @@ def replica_throughput(flops_per_step: float, steps: int, world: int, max_ms: fl
 # Source files that make up each profiled kernel: a DRAM-traffic figure is
 # used only while these files are byte-identical to the ones it was taken on.
 FWD_SOURCES = ("attn_fwd.cuh", "attn_inst.cu", "attn_launch.h", "sm100.cuh")
+BWD_SOURCES = ("attn_bwd.cuh", "attn_bwd_wide.cuh", "attn_bwd_inst.cu", "attn_launch.h", "sm100.cuh")
 KERNEL_SOURCES = {
     "attn_fwd_d128_bf16_full_c3": FWD_SOURCES,
     "attn_fwd_d128_bf16_causal_c3": FWD_SOURCES,
     "attn_fwd_splitkv_d128_bf16_decode": FWD_SOURCES + ("attn_combine.cu",),
-    "attn_bwd_d128_bf16_full_c3": ("attn_bwd.cuh", "attn_bwd_inst.cu", "attn_launch.h", "sm100.cuh"),
-    "attn_bwd_d128_bf16_causal_c3": ("attn_bwd.cuh", "attn_bwd_inst.cu", "attn_launch.h", "sm100.cuh"),
+    "attn_bwd_d128_bf16_full_c3": BWD_SOURCES,
+    "attn_bwd_d128_bf16_causal_c3": BWD_SOURCES,
 }
 
 
