@@ -278,26 +278,6 @@ unsigned long long budget_ns(double flops) {
     return ns > 1e18 ? 1000000000000000000ull : static_cast<unsigned long long>(ns);
 }
 
-attn_status_t encode_rows(CUtensorMap* map, const void* base, const Problem& p, int64_t S,
-                          const char* name) {
-    auto fn = encode_fn();
-    if (!fn) return fail(ATTN_ERR_CUDA, "cuTensorMapEncodeTiled is unavailable from the driver");
-    // Dimensions innermost first: (d, S, B·H); box 64 elements (128 bytes) × 128 rows.
-    cuuint64_t dims[3] = {static_cast<cuuint64_t>(p.d), static_cast<cuuint64_t>(S),
-                          static_cast<cuuint64_t>(p.B * p.H)};
-    cuuint64_t strides[2] = {static_cast<cuuint64_t>(p.d * 2), static_cast<cuuint64_t>(S * p.d * 2)};
-    cuuint32_t box[3] = {64, static_cast<cuuint32_t>(attn::kBlockM), 1};
-    cuuint32_t estr[3] = {1, 1, 1};
-    CUresult r = fn(map,
-                    p.dtype == ATTN_DTYPE_BF16 ? CU_TENSOR_MAP_DATA_TYPE_BFLOAT16
-                                               : CU_TENSOR_MAP_DATA_TYPE_FLOAT16,
-                    3, const_cast<void*>(base), dims, strides, box, estr,
-                    CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B,
-                    CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
-    if (r != CUDA_SUCCESS) return fail(ATTN_ERR_CUDA, "cuTensorMapEncodeTiled(%s) failed with %d", name, (int)r);
-    return ATTN_OK;
-}
-
 // Recently encoded tensor maps of this host thread.  A map is a function of
 // its encoding inputs alone (address, sizes, strides, box, element type), so a
 // repeated call on the same buffers reuses it instead of encoding it again.
@@ -363,26 +343,6 @@ attn_status_t encode_4d(CUtensorMap* map, const void* base, const Problem& p, in
     if (slot == c.next) c.next = (c.next + 1) % MapCache::kEntries;
     c.key[slot] = key;
     c.map[slot] = *map;
-    return ATTN_OK;
-}
-
-// Rows of [B·H, S, d] as a 3-D map with a box of 64 columns × box_rows rows.
-attn_status_t encode_rows_box(CUtensorMap* map, const void* base, const Problem& p, int64_t S,
-                              uint32_t box_rows, const char* name) {
-    auto fn = encode_fn();
-    if (!fn) return fail(ATTN_ERR_CUDA, "cuTensorMapEncodeTiled is unavailable from the driver");
-    cuuint64_t dims[3] = {static_cast<cuuint64_t>(p.d), static_cast<cuuint64_t>(S),
-                          static_cast<cuuint64_t>(p.B * p.H)};
-    cuuint64_t strides[2] = {static_cast<cuuint64_t>(p.d * 2), static_cast<cuuint64_t>(S * p.d * 2)};
-    cuuint32_t box[3] = {64, box_rows, 1};
-    cuuint32_t estr[3] = {1, 1, 1};
-    CUresult r = fn(map,
-                    p.dtype == ATTN_DTYPE_BF16 ? CU_TENSOR_MAP_DATA_TYPE_BFLOAT16
-                                               : CU_TENSOR_MAP_DATA_TYPE_FLOAT16,
-                    3, const_cast<void*>(base), dims, strides, box, estr,
-                    CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B,
-                    CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
-    if (r != CUDA_SUCCESS) return fail(ATTN_ERR_CUDA, "cuTensorMapEncodeTiled(%s) failed with %d", name, (int)r);
     return ATTN_OK;
 }
 

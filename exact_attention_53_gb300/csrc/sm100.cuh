@@ -193,30 +193,9 @@ __device__ __forceinline__ void tma_prefetch_desc(const CUtensorMap* map) {
     asm volatile("prefetch.tensormap [%0];" ::"l"(reinterpret_cast<uint64_t>(map)) : "memory");
 }
 
-// 3-D tiled load of one box into shared memory; completion is counted in
-// bytes on `bar`.  Coordinates are (innermost, row, head); rows past the
+// 4-D tiled load of one box into shared memory, coordinates (innermost, row,
+// head, batch); completion is counted in bytes on `bar`.  Rows past the
 // tensor's extent are filled with zeros and still counted.
-__device__ __forceinline__ void tma_load_3d(void* dst, const CUtensorMap* map, uint64_t* bar,
-                                            int32_t c0, int32_t c1, int32_t c2) {
-    asm volatile(
-        "cp.async.bulk.tensor.3d.shared::cluster.global.tile.mbarrier::complete_tx::bytes"
-        " [%0], [%1, {%3, %4, %5}], [%2];" ::"r"(smem_u32(dst)),
-        "l"(reinterpret_cast<uint64_t>(map)), "r"(smem_u32(bar)), "r"(c0), "r"(c1), "r"(c2)
-        : "memory");
-}
-
-// 3-D tiled store of one box from shared memory (rows past the tensor's
-// extent are not written), tracked by the issuing thread's bulk groups.
-__device__ __forceinline__ void tma_store_3d(const CUtensorMap* map, const void* src, int32_t c0,
-                                             int32_t c1, int32_t c2) {
-    asm volatile(
-        "cp.async.bulk.tensor.3d.global.shared::cta.tile.bulk_group [%0, {%2, %3, %4}], [%1];" ::"l"(
-            reinterpret_cast<uint64_t>(map)),
-        "r"(smem_u32(src)), "r"(c0), "r"(c1), "r"(c2)
-        : "memory");
-}
-
-// 4-D tiled load: coordinates (innermost, row, head, batch).
 __device__ __forceinline__ void tma_load_4d(void* dst, const CUtensorMap* map, uint64_t* bar,
                                             int32_t c0, int32_t c1, int32_t c2, int32_t c3) {
     asm volatile(
@@ -227,7 +206,8 @@ __device__ __forceinline__ void tma_load_4d(void* dst, const CUtensorMap* map, u
         : "memory");
 }
 
-// 4-D tiled store (rows past the tensor's extent are not written).
+// 4-D tiled store of one box from shared memory (rows past the tensor's extent
+// are not written), tracked by the issuing thread's bulk groups.
 __device__ __forceinline__ void tma_store_4d(const CUtensorMap* map, const void* src, int32_t c0,
                                              int32_t c1, int32_t c2, int32_t c3) {
     asm volatile(
