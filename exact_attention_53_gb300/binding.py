@@ -166,7 +166,7 @@ def load_debug_library() -> ctypes.CDLL:
         lib = ctypes.CDLL(path)
         i64, vp = ctypes.c_int64, ctypes.c_void_p
         lib.attn_debug_fwd.argtypes = [vp, vp, vp, vp, vp, i64, i64, i64, ctypes.c_float,
-                                       ctypes.c_int, vp]
+                                       ctypes.c_int, ctypes.c_uint64, vp]
         lib.attn_debug_fwd.restype = ctypes.c_int
         lib.attn_debug_status.argtypes = [ctypes.POINTER(ctypes.c_uint), vp]
         lib.attn_debug_status.restype = ctypes.c_int

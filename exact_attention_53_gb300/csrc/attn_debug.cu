@@ -4,9 +4,11 @@
 // The same kernel source as the release library, compiled with
 // ATTN_DEBUG_FAULTS: every bounded wait gives up after 1 ms instead of 2 s, and
 // the producer warp can be told to load nothing for one work unit and stop, so
-// the unit's consumers wait on barriers that nothing will complete.  Nothing
-// faults or hangs: the waits run out, the CTA records the role in its own
-// status word, stops the launch's other CTAs, frees tensor memory and returns.
+// the unit's consumers wait on barriers that nothing will complete; the
+// caller also sets the CTAs' time budget, so a test can make the launch pass
+// its deadline.  Nothing faults or hangs: the waits run out or the deadline
+// passes, the CTA records it in its own status word, stops the launch's other
+// CTAs, frees tensor memory and returns.
 // The release library (libattn.so) is built without this flag and has neither
 // the short limit nor the skip.
 #define ATTN_DEBUG_FAULTS 1
@@ -64,7 +66,8 @@ bool encode(CUtensorMap* map, const void* base, int64_t B, int64_t H, int64_t S)
 extern "C" {
 
 int attn_debug_fwd(const void* q, const void* k, const void* v, void* o, float* lse, int64_t B,
-                   int64_t H, int64_t S, float scale, int skip_unit, struct CUstream_st* stream) {
+                   int64_t H, int64_t S, float scale, int skip_unit, uint64_t budget_ns,
+                   struct CUstream_st* stream) {
     if (!q || !k || !v || !o || !lse || B < 1 || H < 1 || S < 1 || B * H > (1 << 20) ||
         S > (1 << 16))
         return static_cast<int>(cudaErrorInvalidValue);
@@ -95,7 +98,7 @@ int attn_debug_fwd(const void* q, const void* k, const void* v, void* o, float* 
     a.device = dev;
     a.words = static_cast<attn::DeviceWords*>(words);
     a.launch = ++g_debug_launches;
-    a.budget_ns = 5000000000ull;
+    a.budget_ns = budget_ns ? budget_ns : 5000000000ull;
     return static_cast<int>(attn::launch_attn_fwd<64, true, false, false>(a, stream));
 }
 

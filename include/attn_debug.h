@@ -8,15 +8,18 @@
  * told to issue no load for one work unit and stop.  The consumers of that
  * unit then wait on barriers nothing completes, their waits run out, the CTA
  * records which roles gave up, tells the launch's other CTAs to stop, frees its
- * tensor memory and returns; the GPU context stays usable.  Tests use it to
- * check that a wait that runs out is reported and does not hang.
+ * tensor memory and returns; the GPU context stays usable.  The CTAs' time
+ * budget is an argument too, so a launch can be made to pass its deadline.
+ * Tests use it to check that both are reported and that neither hangs.
  *
  * attn_debug_fwd — enqueue one full-attention forward on `stream` over dense
  *   bf16 q, k, v, o [B, H, S, 64] (device, 16-byte aligned) and fp32 lse
  *   [B, H, S], scaled by `scale`.  skip_unit: the work unit (one head and 256
  *   query rows, numbered head-major) whose loads the producer skips, or -1 for
- *   none (then the call computes the forward like attn_fwd).  Returns 0, or a
- *   cudaError_t value (1 for bad arguments).
+ *   none (then the call computes the forward like attn_fwd).  budget_ns: each
+ *   CTA's time budget, after which its producer stops it and the launch (0: 5 s,
+ *   far above any real duration).  Returns 0, or a cudaError_t value (1 for
+ *   bad arguments).
  * attn_debug_status — synchronise `stream`, write the debug library's status
  *   word (bit 1: producer, 2: MMA, 4: softmax, 8: epilogue, 16: drain, 512:
  *   deadline; 0 when no wait ran out) to *status and clear it.  Returns 0 or a
@@ -34,7 +37,8 @@ extern "C" {
 struct CUstream_st;
 
 int attn_debug_fwd(const void* q, const void* k, const void* v, void* o, float* lse, int64_t B,
-                   int64_t H, int64_t S, float scale, int skip_unit, struct CUstream_st* stream);
+                   int64_t H, int64_t S, float scale, int skip_unit, uint64_t budget_ns,
+                   struct CUstream_st* stream);
 int attn_debug_status(unsigned int* status, struct CUstream_st* stream);
 
 #ifdef __cplusplus

@@ -90,8 +90,8 @@ def test_libraries_export_only_their_c_abi(lib):
 
 def test_debug_entry_rejects_bad_arguments_before_device_work():
     dbg = binding.load_debug_library()
-    assert dbg.attn_debug_fwd(None, A, A, A, A, 1, 1, 128, 0.125, -1, None) == 1
-    assert dbg.attn_debug_fwd(A, A, A, A, A, 1, 1, 0, 0.125, -1, None) == 1
+    assert dbg.attn_debug_fwd(None, A, A, A, A, 1, 1, 128, 0.125, -1, 0, None) == 1
+    assert dbg.attn_debug_fwd(A, A, A, A, A, 1, 1, 0, 0.125, -1, 0, None) == 1
     assert dbg.attn_debug_status(None, None) == 1
 
 

@@ -1,12 +1,15 @@
-"""GPU failure detection: a bounded wait that runs out is reported and does not hang.
+"""GPU failure detection: a wait that runs out, or a launch past its deadline, is
+reported and does not hang.
 
 The debug build of the forward kernel (libattn_debug.so, include/attn_debug.h)
-waits at most 1 ms per barrier and can be told to load nothing for one work
-unit.  Nothing faults or hangs: that unit's consumers wait on barriers nothing
-completes, their waits run out, the kernel records the roles that gave up in
-its status word, stops the launch's other CTAs, frees tensor memory and
-returns.  These tests check that the status reports it, that the call returns
-in milliseconds, and that the same device then still computes correct results
+waits at most 1 ms per barrier, can be told to load nothing for one work unit,
+and takes its CTAs' time budget as an argument.  Nothing faults or hangs: a
+skipped unit's consumers wait on barriers nothing completes and their waits run
+out; a launch given a budget shorter than its work has its producers stop
+their CTAs at the deadline.  Either way the kernel records it in its status
+word, stops the launch's other CTAs, frees tensor memory and returns.  These
+tests check that the status reports it, that the call returns in
+milliseconds, and that the same device then still computes correct results
 with both the debug and the release library.
 """
 
@@ -39,7 +42,7 @@ def _built():
     attn_get_device_status()
 
 
-def _run_debug(q, k, v, skip_unit):
+def _run_debug(q, k, v, skip_unit, budget_ns=0):
     lib = load_debug_library()
     B, H, S, _ = q.shape
     o = torch.full_like(q, float("nan"))
@@ -48,7 +51,8 @@ def _run_debug(q, k, v, skip_unit):
     torch.cuda.synchronize()
     t0 = time.monotonic()
     rc = lib.attn_debug_fwd(q.data_ptr(), k.data_ptr(), v.data_ptr(), o.data_ptr(),
-                            lse.data_ptr(), B, H, S, 1 / math.sqrt(64), skip_unit, stream)
+                            lse.data_ptr(), B, H, S, 1 / math.sqrt(64), skip_unit, budget_ns,
+                            stream)
     assert rc == 0, f"launch returned cudaError {rc}"
     status = ctypes.c_uint(0)
     rc = lib.attn_debug_status(ctypes.byref(status), stream)
@@ -96,6 +100,18 @@ def test_one_unit_of_a_large_grid_stops_only_that_launch():
     o_cpu = o.float().cpu().numpy()
     assert np.isnan(o_cpu[0, 38, 256:]).all()
     _check_usable(host, dev_in, "grid of 256 units")
+
+
+def test_launch_past_its_deadline_stops_and_is_reported():
+    # 4 x 64 heads x 8 query blocks = 2048 units of 16 key tiles (about 0.5 ms of work); each
+    # CTA gets 30 µs, so the producers stop their CTAs and the rest of the launch stops too.
+    host, dev_in = _inputs(4, 64, 2048, seed=74)
+    o, lse, status, elapsed = _run_debug(*dev_in, skip_unit=-1, budget_ns=30_000)
+    assert status & DEADLINE, f"status {status:#x} lacks the deadline bit"
+    assert elapsed < 2.0, f"the call took {elapsed:.3f} s"
+    # Units that started late were never computed: the launch really stopped early.
+    assert torch.isnan(lse).any()
+    _check_usable(host, dev_in, "deadline")
 
 
 def test_status_is_clear_after_being_read():
