@@ -9,9 +9,9 @@ fp64 oracle at the stated tolerances (bf16 |ΔO| <= 1e-2 + 1e-2·|O|, f16
   exponentials passes a bound.  In fp16 each p must stay below 65504 (the
   packed P would round to +inf), so a later key whose logit exceeds the first
   tile's maximum by 12 or 13 nats (e^12 ≈ 1.6e5, e^13 ≈ 4.4e5: above 65504,
-  below the bf16 bound 2^20) must trigger the redo.  The first tile's keys are
-  nearly orthogonal to every query (logits within a few tenths of 0), one later
-  key has q·k = 12 or 13 at scale 1.
+  below the bf16 bound 2^20) must trigger the redo.  All keys but one are nearly
+  orthogonal to every query (logits within a few tenths of 0); one key, in the
+  second tile (or, as a control, in the first), has q·k = 12 or 13 at scale 1.
 * fp16 near its largest value.  Q, K and V of magnitude 5e4–6.5e4 (logits kept
   O(1) by the scale).  O is linear in V, so the fp16 tolerance scales with V:
   O / max|V| is compared at 4e-3.
@@ -60,17 +60,21 @@ def _growth_inputs(B, H, S_q, S_k, d, dtype, excess, specials, seed):
     return q.to(td), k.to(td), v.to(td)
 
 
+@pytest.mark.parametrize("special", [200, 100], ids=["second_tile", "first_tile"])
 @pytest.mark.parametrize("excess", [12, 13])
 @pytest.mark.parametrize("causal", [False, True], ids=["full", "causal"])
 @pytest.mark.parametrize("dtype", ["f16", "bf16"])
 @pytest.mark.parametrize("d", [64, 128, 256])
-def test_logit_growth_past_the_fp16_range(d, dtype, causal, excess):
-    # key 200 sits in the second key tile: every query tile meets it after key tile 0
-    q, k, v = _growth_inputs(1, 2, 512, 512, d, dtype, excess, [200], seed=500 + d + excess)
+def test_logit_growth_past_the_fp16_range(d, dtype, causal, excess, special):
+    # key 200 sits in the second key tile: every query tile meets it after key tile 0;
+    # key 100 sits in the first tile (rows that see it take its maximum first)
+    q, k, v = _growth_inputs(1, 2, 512, 512, d, dtype, excess, [special],
+                             seed=500 + d + excess + special)
     o, lse = fwd(q.to(DEV), k.to(DEV), v.to(DEV), causal=causal, scale=1.0)
     torch.cuda.synchronize()
     ro, rl = oracle.attention_forward(q, k, v, causal=causal, scale=1.0)
-    assert_parity(o, lse, ro, rl, dtype, f"growth {excess} d={d} {dtype} causal={causal}")
+    assert_parity(o, lse, ro, rl, dtype,
+                  f"growth {excess} at key {special} d={d} {dtype} causal={causal}")
 
 
 @pytest.mark.parametrize("excess", [12, 13])
