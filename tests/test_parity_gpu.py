@@ -119,6 +119,22 @@ def test_deterministic():
         assert torch.equal(o1, o2) and torch.equal(l1, l2)
 
 
+@pytest.mark.parametrize("name,causal", [("c3", False), ("c3", True), ("c2", True), ("c5", False)],
+                         ids=["c3-full", "c3-causal", "c2", "c5"])
+def test_repeated_launches_stay_clean_and_identical(name, causal):
+    """Twenty back-to-back launches of a workload: no bounded wait runs out in any of them (a
+    handoff race that only some launches hit would show here) and every launch gives the
+    first one's bits."""
+    w = WORKLOADS[name]
+    q, k, v = (t.to(DEV) for t in workload_qkv(w))
+    o0, l0 = fwd(q, k, v, causal=causal, scale=w.scale)
+    outs = [fwd(q, k, v, causal=causal, scale=w.scale) for _ in range(19)]
+    torch.cuda.synchronize()
+    attn_get_device_status()                 # raises AttnError on a timeout
+    for o, lse in outs:
+        assert torch.equal(o, o0) and torch.equal(lse, l0)
+
+
 def test_scale_zero_gives_mean_of_values():
     q, k, v = make_qkv(1, 2, 150, 150, 64, "f16", seed=11)
     for causal in (False, True):
