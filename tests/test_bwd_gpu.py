@@ -164,6 +164,23 @@ def test_bwd_deterministic(d):
             assert torch.equal(x, y)
 
 
+@pytest.mark.parametrize("causal", [False, True], ids=["full", "causal"])
+def test_bwd_repeated_calls_stay_clean_and_identical(causal):
+    """Eight back-to-back backward calls on c3: no bounded wait runs out (checked on the
+    device status) and every call gives the first call's bits."""
+    w = WORKLOADS["c3"]
+    q, k, v = (t.to(DEV) for t in workload_qkv(w))
+    do = make_qkv(w.B, w.H, w.S_q, 1, w.d, w.dtype, seed=w.seed + 100)[0].to(DEV)
+    o, lse = fwd(q, k, v, causal=causal, scale=w.scale)
+    first = bwd(q, k, v, o, lse, do, causal=causal, scale=w.scale)
+    rest = [bwd(q, k, v, o, lse, do, causal=causal, scale=w.scale) for _ in range(7)]
+    torch.cuda.synchronize()
+    attn_get_device_status()
+    for grads in rest:
+        for x, y in zip(grads, first):
+            assert torch.equal(x, y)
+
+
 def test_bwd_scale_zero():
     q, k, v = make_qkv(1, 2, 150, 190, 64, "f16", seed=33)
     do = make_qkv(1, 2, 150, 1, 64, "f16", seed=34)[0]
