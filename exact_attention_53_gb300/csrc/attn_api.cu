@@ -1070,11 +1070,12 @@ attn_status_t attn_get_device_status(struct CUstream_st* stream) {
     const attn::DeviceWords zero{};
     e = cudaMemcpyToSymbol(g_attn_words, &zero, sizeof(zero));
     if (e != cudaSuccess) return fail(ATTN_ERR_CUDA, "clearing status: %s", cudaGetErrorString(e));
-    return fail(ATTN_ERR_TIMEOUT, "a bounded wait ran out in:%s%s%s%s%s%s%s%s%s%s",
+    return fail(ATTN_ERR_TIMEOUT, "a bounded wait ran out in:%s%s%s%s%s%s%s%s%s%s%s",
                 (v & 1u) ? " producer" : "", (v & 2u) ? " mma" : "", (v & 4u) ? " softmax" : "",
                 (v & 8u) ? " epilogue" : "", (v & 16u) ? " drain" : "",
                 (v & 32u) ? " bwd-producer" : "", (v & 64u) ? " bwd-mma" : "",
                 (v & 128u) ? " bwd-softmax" : "", (v & 256u) ? " bwd-drain" : "",
+                (v & 1024u) ? " bwd-epilogue" : "",
                 (v & attn::sm100::kStatusDeadline) ? " (launch deadline passed)" : "");
 }
 

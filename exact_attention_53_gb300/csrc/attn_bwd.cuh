@@ -42,6 +42,7 @@ constexpr unsigned int kStatusBwdProducer = 1u << 5;
 constexpr unsigned int kStatusBwdMma = 1u << 6;
 constexpr unsigned int kStatusBwdSoftmax = 1u << 7;
 constexpr unsigned int kStatusBwdDrain = 1u << 8;
+constexpr unsigned int kStatusBwdEpilogue = 1u << 10;
 
 template <int D>
 struct BwdTile {
@@ -57,12 +58,22 @@ struct BwdTile {
     static constexpr int SLOT_BYTES = 2 * SMALL_TILE;
     static constexpr int STAT_FLOATS = 2 * BS;        // per slot: LSE·log2e and D of 64 rows
     static constexpr int CLC_SLOTS = 4;               // work-queue answers in flight
-    static constexpr int NUM_BARS = 2 + 2 * NS + 2 + 2 + 1 + 1 + 2 * CLC_SLOTS;
+    static constexpr int NUM_BARS = 2 + 2 * NS + 2 + 2 + 1 + 1 + 1 + 2 * CLC_SLOTS;
     static constexpr int TILE_BYTES = 2 * BIG_TILE + NS * SLOT_BYTES + NS * STAT_FLOATS * 4;
     static constexpr int SMEM_BYTES = 1024 + TILE_BYTES + CLC_SLOTS * 16 + NUM_BARS * 8 + 16;
-    static constexpr int THREADS = 192;               // 4 softmax warps, producer, MMA
-    static constexpr int PRODUCER_WARP = 4;
-    static constexpr int MMA_WARP = 5;
+    static constexpr int THREADS = 384;     // softmax warps 0-3, epilogue 4-7, producer, MMA, 2 idle
+    static constexpr int EPI_WARP = 4;      // first epilogue warp (warp % 4 = its lane quarter)
+    static constexpr int PRODUCER_WARP = 8;
+    static constexpr int MMA_WARP = 9;
+    // Register split: the launch grants LAUNCH_REGS a thread (65536 over 12
+    // warps, rounded down to a multiple of 8); the softmax and epilogue
+    // warpgroups grow to their budgets, the aux warpgroup (producer, MMA and
+    // two idle warps) shrinks to its own.  The sum is 3·LAUNCH_REGS.
+    static constexpr int LAUNCH_REGS = 168;
+    static constexpr int SOFTMAX_REGS = 200;
+    static constexpr int EPI_REGS = D == 64 ? 144 : 176;
+    static constexpr int AUX_REGS = D == 64 ? 160 : 128;
+    static_assert(SOFTMAX_REGS + EPI_REGS + AUX_REGS <= 3 * LAUNCH_REGS, "register split");
     static constexpr uint32_t TMEM_COLS = 512;
     static constexpr uint32_t S_COL = 0;              // S buffer b at column 64·b (fp32)
     static constexpr uint32_t DP_COL = 128;           // dP buffer b at 128 + 64·b
@@ -169,6 +180,32 @@ __device__ __forceinline__ void store_row_from_tmem(uint32_t taddr, float mul, v
     }
 }
 
+// One row of an fp32 TMEM accumulator (D columns at `taddr`) times `mul`,
+// packed as 16-bit pairs into out[D/2]: 64-column loads, one wait each.
+template <int D, bool BF16>
+__device__ __forceinline__ void read_acc_packed(uint32_t taddr, float mul, uint32_t (&out)[D / 2]) {
+    using namespace sm100;
+#pragma unroll
+    for (int c = 0; c < D; c += 64) {
+        uint32_t r[64];
+        tmem_ld64(taddr + c, r);
+#pragma unroll
+        for (int i = 0; i < 32; ++i) {
+            const float a = __uint_as_float(r[2 * i]) * mul;
+            const float b = __uint_as_float(r[2 * i + 1]) * mul;
+            out[c / 2 + i] = BF16 ? pack_bf16(a, b) : pack_f16(a, b);
+        }
+    }
+}
+
+// Store D packed 16-bit values (D/2 words) to `dst` as 16-byte pieces.
+template <int D>
+__device__ __forceinline__ void store_packed_row(const uint32_t (&w)[D / 2], void* dst) {
+    uint4* out = reinterpret_cast<uint4*>(dst);
+#pragma unroll
+    for (int i = 0; i < D / 8; ++i) out[i] = make_uint4(w[4 * i], w[4 * i + 1], w[4 * i + 2], w[4 * i + 3]);
+}
+
 // ============================================================== prep
 // delta[bh, i] = Σ_c dO[b,h,i,c]·O[b,h,i,c]; lse2[bh, i] = LSE[bh,i]·log2(e);
 // for i in [S_q, S_pad): delta = 0, lse2 = +inf.  Each lane loads 16 bytes of
@@ -251,6 +288,16 @@ __global__ void __launch_bounds__(256) attn_bwd_prep_kernel(const uint16_t* __re
     }
 }
 
+// The warpgroup register split assumes the launch grants `regs` a thread;
+// refuse to launch a build where it does not (setmaxnreg would stall).
+template <typename K>
+cudaError_t check_launch_regs(K kernel, int regs) {
+    cudaFuncAttributes fa;
+    const cudaError_t e = cudaFuncGetAttributes(&fa, kernel);
+    if (e != cudaSuccess) return e;
+    return fa.numRegs == regs ? cudaSuccess : cudaErrorInvalidConfiguration;
+}
+
 // ============================================================== dK, dV
 template <int D, bool BF16, bool CAUSAL>
 __global__ void __launch_bounds__(BwdTile<D>::THREADS, 1)
@@ -283,7 +330,8 @@ __global__ void __launch_bounds__(BwdTile<D>::THREADS, 1)
     uint64_t* s_full = slot_empty + T::NS;    // [2] Sᵀ and dPᵀ of buffer b computed
     uint64_t* p_full = s_full + 2;            // [2] Pᵀ and dSᵀ of buffer b written (per warp)
     uint64_t* acc_done = p_full + 2;          // dV and dK of the unit complete
-    uint64_t* drain = acc_done + 1;
+    uint64_t* acc_free = acc_done + 1;        // dV and dK read out (per epilogue warp)
+    uint64_t* drain = acc_free + 1;
     uint64_t* clc_full = drain + 1;           // [CLC_SLOTS] work-queue answer landed
     uint64_t* clc_empty = clc_full + T::CLC_SLOTS;
     uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(clc_empty + T::CLC_SLOTS);
@@ -345,10 +393,11 @@ __global__ void __launch_bounds__(BwdTile<D>::THREADS, 1)
             mbar_init(&p_full[b], 4);
         }
         mbar_init(acc_done, 1);
+        mbar_init(acc_free, 4);
         mbar_init(drain, 1);
         for (int s = 0; s < T::CLC_SLOTS; ++s) {
             mbar_init(&clc_full[s], 1);
-            mbar_init(&clc_empty[s], 5);         // softmax warps 0-3 and the MMA warp
+            mbar_init(&clc_empty[s], 9);         // softmax and epilogue warps, the MMA warp
         }
         *abort_flag = 0;
         fence_mbar_init();
@@ -363,7 +412,21 @@ __global__ void __launch_bounds__(BwdTile<D>::THREADS, 1)
     tc_fence_after();
     const uint32_t tmem = *tmem_slot;
 
-    if (warp == T::PRODUCER_WARP) {
+    // Each role below ends in its own copy of the teardown, so no code runs
+    // under two register budgets.
+    auto teardown = [&]() {
+        tc_fence_before();
+        __syncthreads();
+        if (warp == 0) {
+            tc_fence_after();
+            tmem_dealloc(tmem, T::TMEM_COLS);
+            if (lane == 0) publish_abort(abort_flag, words, launch);
+        }
+    };
+
+    if (warp >= T::PRODUCER_WARP) {
+      regs_set<T::AUX_REGS, T::LAUNCH_REGS>();
+      if (warp == T::PRODUCER_WARP) {
         // ------------------------------------------------------------ TMA producer
         const bool leader = elect_one();
         if (leader) {
@@ -465,7 +528,7 @@ __global__ void __launch_bounds__(BwdTile<D>::THREADS, 1)
             queue.drain(claims, status, kStatusBwdDrain);
         }
         __syncwarp();
-    } else if (warp == T::MMA_WARP) {
+      } else if (warp == T::MMA_WARP) {
         // ------------------------------------------------------------ MMA issuer
         constexpr uint32_t id_s = idesc_f16(128, T::BS, BF16, false, false);
         constexpr uint32_t id_acc = idesc_f16(128, D, BF16, false, true);
@@ -548,6 +611,10 @@ __global__ void __launch_bounds__(BwdTile<D>::THREADS, 1)
             for (int t = 0; t < n && ok; ++t) {
                 const int b = static_cast<int>((gs + t) & 1);
                 ok = mbar_wait(&p_full[b], (b ? pc1 : pc0) & 1, abort_flag, status, kStatusBwdMma);
+                // the unit's first dV/dK MMA overwrites the accumulators: the
+                // epilogue warps must have read out the previous unit's
+                if (ok && t == 0 && uk > 1)
+                    ok = mbar_wait(acc_free, (uk - 2) & 1, abort_flag, status, kStatusBwdMma);
                 ok = __all_sync(0xffffffffu, ok);
                 if (b) ++pc1; else ++pc0;
                 tc_fence_after();
@@ -582,16 +649,21 @@ __global__ void __launch_bounds__(BwdTile<D>::THREADS, 1)
             }
         }
         __syncwarp();
-    } else if (warp < 4) {
-        // ------------------------------------------------------------ softmax warps
-        const int row = warp * 32 + lane;              // key row within the tile
-        const uint32_t lane_base = tmem + (static_cast<uint32_t>(warp * 32) << 16);
+      }
+      teardown();
+    } else if (warp >= T::EPI_WARP) {
+        regs_set<T::EPI_REGS, T::LAUNCH_REGS>();
+        // ------------------------------------------------------------ epilogue warps
+        // Read dV and dK out of tensor memory as packed 16-bit rows, release
+        // the accumulators to the next unit, then store (one key row per thread).
+        const int quarter = warp & 3;
+        const int row = quarter * 32 + lane;
+        const uint32_t lane_base = tmem + (static_cast<uint32_t>(quarter * 32) << 16);
         bool ok = true;
-        uint32_t gs = 0;
-        int uk = 0;
+        int ue = 0;
         for (int r = 0; ok; ++r) {
             int L = 0;
-            const int got = unit_at(r, L, true, kStatusBwdSoftmax);
+            const int got = unit_at(r, L, true, kStatusBwdEpilogue);
             if (got < 0) ok = false;
             if (got <= 0) break;
             if (got == 2) continue;
@@ -602,18 +674,45 @@ __global__ void __launch_bounds__(BwdTile<D>::THREADS, 1)
                                                         static_cast<long long>(key) * dk_lay.row);
             uint16_t* dv_row = dv + static_cast<size_t>(b * dv_lay.batch + hk * dv_lay.head +
                                                         static_cast<long long>(key) * dv_lay.row);
+            uint32_t pv[D / 2], pk[D / 2];
             if (n == 0) {
                 // No query sees these keys: their gradients are zero.
-                if (key < S_k) {
-                    uint4* pa = reinterpret_cast<uint4*>(dk_row);
-                    uint4* pb = reinterpret_cast<uint4*>(dv_row);
-                    for (int i = 0; i < D / 8; ++i) {
-                        pa[i] = make_uint4(0, 0, 0, 0);
-                        pb[i] = make_uint4(0, 0, 0, 0);
-                    }
-                }
-                continue;
+#pragma unroll
+                for (int i = 0; i < D / 2; ++i) pv[i] = pk[i] = 0u;
+            } else {
+                ok = mbar_wait(acc_done, ue & 1, abort_flag, status, kStatusBwdEpilogue);
+                ok = __all_sync(0xffffffffu, ok);
+                ++ue;
+                if (!ok) break;
+                tc_fence_after();
+                read_acc_packed<D, BF16>(lane_base + T::ACC_COL, 1.f, pv);
+                read_acc_packed<D, BF16>(lane_base + T::ACC_COL + D, scale, pk);
+                tc_fence_before();
+                __syncwarp();
+                if (lane == 0) mbar_arrive(acc_free);
             }
+            if (key < S_k) {
+                store_packed_row<D>(pv, dv_row);
+                store_packed_row<D>(pk, dk_row);
+            }
+        }
+        teardown();
+    } else {
+        // ------------------------------------------------------------ softmax warps
+        regs_set<T::SOFTMAX_REGS, T::LAUNCH_REGS>();
+        const int row = warp * 32 + lane;              // key row within the tile
+        const uint32_t lane_base = tmem + (static_cast<uint32_t>(warp * 32) << 16);
+        bool ok = true;
+        uint32_t gs = 0;
+        for (int r = 0; ok; ++r) {
+            int L = 0;
+            const int got = unit_at(r, L, true, kStatusBwdSoftmax);
+            if (got < 0) ok = false;
+            if (got <= 0) break;
+            if (got == 2) continue;
+            int b, hk, kt, q_begin, n;
+            unit_info(L, b, hk, kt, q_begin, n);
+            const int key = kt * T::BU + row;
             int h = hk * kv_group, qi = q_begin;
             for (int t = 0; t < n; ++t, next_step(q_begin, h, qi)) {
                 const uint32_t s = gs + static_cast<uint32_t>(t);
@@ -653,22 +752,8 @@ __global__ void __launch_bounds__(BwdTile<D>::THREADS, 1)
             }
             if (!ok) break;
             gs += static_cast<uint32_t>(n);
-            ok = mbar_wait(acc_done, uk & 1, abort_flag, status, kStatusBwdSoftmax);
-            ok = __all_sync(0xffffffffu, ok);
-            ++uk;
-            if (!ok) break;
-            tc_fence_after();
-            const bool store = key < S_k;
-            store_row_from_tmem<D, BF16>(lane_base + T::ACC_COL, 1.f, dv_row, store);
-            store_row_from_tmem<D, BF16>(lane_base + T::ACC_COL + D, scale, dk_row, store);
         }
-    }
-    tc_fence_before();
-    __syncthreads();
-    if (warp == 0) {
-        tc_fence_after();
-        tmem_dealloc(tmem, T::TMEM_COLS);
-        if (lane == 0) publish_abort(abort_flag, words, launch);
+        teardown();
     }
 }
 
@@ -694,12 +779,22 @@ struct DqTile {
     static constexpr int KS = D == 64 ? 5 : (D == 128 ? 3 : 2);   // K ring slots
     static constexpr int VS = D == 64 ? 4 : (D == 128 ? 2 : 1);   // V ring slots
     static constexpr int CLC_SLOTS = 4;               // work-queue answers in flight
-    static constexpr int NUM_BARS = 2 + 2 * KS + 2 * VS + 2 + 1 + 2 + 1 + 1 + 2 * CLC_SLOTS;
+    static constexpr int NUM_BARS = 2 + 2 * KS + 2 * VS + 2 + 1 + 2 + 1 + 1 + 1 + 2 * CLC_SLOTS;
     static constexpr int TILE_BYTES = 2 * FIX_TILE + (KS + VS) * KV_TILE;
     static constexpr int SMEM_BYTES = 1024 + TILE_BYTES + CLC_SLOTS * 16 + NUM_BARS * 8 + 16;
-    static constexpr int THREADS = 192;               // 4 softmax warps, producer, MMA
-    static constexpr int PRODUCER_WARP = 4;
-    static constexpr int MMA_WARP = 5;
+    static constexpr int THREADS = 384;     // softmax warps 0-3, epilogue 4-7, producer, MMA, 2 idle
+    static constexpr int EPI_WARP = 4;      // first epilogue warp (warp % 4 = its lane quarter)
+    static constexpr int PRODUCER_WARP = 8;
+    static constexpr int MMA_WARP = 9;
+    // Register split: the launch grants LAUNCH_REGS a thread (65536 over 12
+    // warps, rounded down to a multiple of 8); the softmax and epilogue
+    // warpgroups grow to their budgets, the aux warpgroup (producer, MMA and
+    // two idle warps) shrinks to its own.  The sum is 3·LAUNCH_REGS.
+    static constexpr int LAUNCH_REGS = 168;
+    static constexpr int SOFTMAX_REGS = 176;
+    static constexpr int EPI_REGS = 192;
+    static constexpr int AUX_REGS = 136;
+    static_assert(SOFTMAX_REGS + EPI_REGS + AUX_REGS <= 3 * LAUNCH_REGS, "register split");
     static constexpr uint32_t TMEM_COLS = 512;
     static constexpr uint32_t S_COL = 0;              // S buffer b at BS·b
     static constexpr uint32_t DP_COL = 2 * BS;
@@ -741,7 +836,8 @@ __global__ void __launch_bounds__(DqTile<D>::THREADS, 1)
     uint64_t* dp_free = s_full + 2;          // the dP buffer has been read (per warp)
     uint64_t* p_full = dp_free + 1;          // [2] dS written over S_b (per warp)
     uint64_t* acc_done = p_full + 2;
-    uint64_t* drain = acc_done + 1;
+    uint64_t* acc_free = acc_done + 1;       // dQ read out (per epilogue warp)
+    uint64_t* drain = acc_free + 1;
     uint64_t* clc_full = drain + 1;          // [CLC_SLOTS] work-queue answer landed
     uint64_t* clc_empty = clc_full + T::CLC_SLOTS;
     uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(clc_empty + T::CLC_SLOTS);
@@ -796,10 +892,11 @@ __global__ void __launch_bounds__(DqTile<D>::THREADS, 1)
         }
         mbar_init(dp_free, 4);
         mbar_init(acc_done, 1);
+        mbar_init(acc_free, 4);
         mbar_init(drain, 1);
         for (int s = 0; s < T::CLC_SLOTS; ++s) {
             mbar_init(&clc_full[s], 1);
-            mbar_init(&clc_empty[s], 5);         // softmax warps 0-3 and the MMA warp
+            mbar_init(&clc_empty[s], 9);         // softmax and epilogue warps, the MMA warp
         }
         *abort_flag = 0;
         fence_mbar_init();
@@ -814,7 +911,21 @@ __global__ void __launch_bounds__(DqTile<D>::THREADS, 1)
     tc_fence_after();
     const uint32_t tmem = *tmem_slot;
 
-    if (warp == T::PRODUCER_WARP) {
+    // Each role below ends in its own copy of the teardown, so no code runs
+    // under two register budgets.
+    auto teardown = [&]() {
+        tc_fence_before();
+        __syncthreads();
+        if (warp == 0) {
+            tc_fence_after();
+            tmem_dealloc(tmem, T::TMEM_COLS);
+            if (lane == 0) publish_abort(abort_flag, words, launch);
+        }
+    };
+
+    if (warp >= T::PRODUCER_WARP) {
+      regs_set<T::AUX_REGS, T::LAUNCH_REGS>();
+      if (warp == T::PRODUCER_WARP) {
         const bool leader = elect_one();
         if (leader) {
             tma_prefetch_desc(&tm_q);
@@ -910,7 +1021,7 @@ __global__ void __launch_bounds__(DqTile<D>::THREADS, 1)
             queue.drain(claims, status, kStatusBwdDrain);
         }
         __syncwarp();
-    } else if (warp == T::MMA_WARP) {
+      } else if (warp == T::MMA_WARP) {
         constexpr uint32_t id_s = idesc_f16(128, T::BS, BF16, false, false);
         constexpr uint32_t id_acc = idesc_f16(128, D, BF16, false, true);
         const uint64_t q_desc = sdesc_sw128(smem_u32(sQ), 16, 1024);
@@ -1021,6 +1132,10 @@ __global__ void __launch_bounds__(DqTile<D>::THREADS, 1)
                     tc_commit_warp(q_empty);
                 }
                 ok = mbar_wait(&p_full[b], (b ? pc1 : pc0) & 1, abort_flag, status, kStatusBwdMma);
+                // the unit's first dQ MMA overwrites the accumulator: the
+                // epilogue warps must have read out the previous unit's
+                if (ok && t == 0 && uq > 1)
+                    ok = mbar_wait(acc_free, (uq - 2) & 1, abort_flag, status, kStatusBwdMma);
                 ok = __all_sync(0xffffffffu, ok);
                 if (b) ++pc1; else ++pc0;
                 tc_fence_after();
@@ -1053,12 +1168,50 @@ __global__ void __launch_bounds__(DqTile<D>::THREADS, 1)
             }
         }
         __syncwarp();
-    } else if (warp < 4) {
+      }
+      teardown();
+    } else if (warp >= T::EPI_WARP) {
+        regs_set<T::EPI_REGS, T::LAUNCH_REGS>();
+        // Epilogue warps: read dQ out of tensor memory as packed 16-bit rows,
+        // release the accumulator to the next unit, then store (one query row
+        // per thread).
+        const int quarter = warp & 3;
+        const int row = quarter * 32 + lane;
+        const uint32_t lane_base = tmem + (static_cast<uint32_t>(quarter * 32) << 16);
+        bool ok = true;
+        int ue = 0;
+        for (int r = 0; ok; ++r) {
+            int L = 0;
+            const int got = unit_at(r, L, true, kStatusBwdEpilogue);
+            if (got < 0) ok = false;
+            if (got <= 0) break;
+            if (got == 2) continue;
+            int bh, qt, n;
+            unit_info(L, bh, qt, n);
+            const int q_idx = qt * T::BU + row;
+            ok = mbar_wait(acc_done, ue & 1, abort_flag, status, kStatusBwdEpilogue);
+            ok = __all_sync(0xffffffffu, ok);
+            ++ue;
+            if (!ok) break;
+            tc_fence_after();
+            uint32_t pq[D / 2];
+            read_acc_packed<D, BF16>(lane_base + T::ACC_COL, scale, pq);
+            tc_fence_before();
+            __syncwarp();
+            if (lane == 0) mbar_arrive(acc_free);
+            const int b = bh / H, h = bh - b * H;
+            if (q_idx < S_q)
+                store_packed_row<D>(pq, dq + static_cast<size_t>(b * dq_lay.batch + h * dq_lay.head +
+                                                                 static_cast<long long>(q_idx) *
+                                                                     dq_lay.row));
+        }
+        teardown();
+    } else {
+        regs_set<T::SOFTMAX_REGS, T::LAUNCH_REGS>();
         const int row = warp * 32 + lane;                // query row within the tile
         const uint32_t lane_base = tmem + (static_cast<uint32_t>(warp * 32) << 16);
         bool ok = true;
         uint32_t gs = 0;
-        int uq = 0;
         for (int r = 0; ok; ++r) {
             int L = 0;
             const int got = unit_at(r, L, true, kStatusBwdSoftmax);
@@ -1118,25 +1271,8 @@ __global__ void __launch_bounds__(DqTile<D>::THREADS, 1)
             }
             if (!ok) break;
             gs += static_cast<uint32_t>(n);
-            ok = mbar_wait(acc_done, uq & 1, abort_flag, status, kStatusBwdSoftmax);
-            ok = __all_sync(0xffffffffu, ok);
-            ++uq;
-            if (!ok) break;
-            tc_fence_after();
-            const int b = bh / H, h = bh - b * H;
-            store_row_from_tmem<D, BF16>(
-                lane_base + T::ACC_COL, scale,
-                dq + static_cast<size_t>(b * dq_lay.batch + h * dq_lay.head +
-                                         static_cast<long long>(q_idx) * dq_lay.row),
-                q_idx < S_q);
         }
-    }
-    tc_fence_before();
-    __syncthreads();
-    if (warp == 0) {
-        tc_fence_after();
-        tmem_dealloc(tmem, T::TMEM_COLS);
-        if (lane == 0) publish_abort(abort_flag, words, launch);
+        teardown();
     }
 }
 
@@ -1161,8 +1297,9 @@ cudaError_t launch_key_side(const BwdArgs& a, cudaStream_t stream, long long op_
         auto kdkdv = attn_bwd_dkdv_kernel<D, BF16, CAUSAL>;
         static std::atomic<uint64_t> configured_dkdv{0};
         err = configure_once(configured_dkdv, a.device, [&]() {
-            return cudaFuncSetAttribute(kdkdv, cudaFuncAttributeMaxDynamicSharedMemorySize,
-                                        T::SMEM_BYTES);
+            const cudaError_t e = cudaFuncSetAttribute(
+                kdkdv, cudaFuncAttributeMaxDynamicSharedMemorySize, T::SMEM_BYTES);
+            return e != cudaSuccess ? e : check_launch_regs(kdkdv, T::LAUNCH_REGS);
         });
         if (err != cudaSuccess) return err;
         const int n_kt = (a.S_k + T::BU - 1) / T::BU;
@@ -1244,8 +1381,9 @@ cudaError_t launch_attn_bwd(const BwdArgs& a, cudaStream_t stream) {
     auto kdq = attn_bwd_dq_kernel<D, BF16, CAUSAL>;
     static std::atomic<uint64_t> configured_dq{0};
     err = configure_once(configured_dq, a.device, [&]() {
-        return cudaFuncSetAttribute(kdq, cudaFuncAttributeMaxDynamicSharedMemorySize,
-                                    TQ::SMEM_BYTES);
+        const cudaError_t e =
+            cudaFuncSetAttribute(kdq, cudaFuncAttributeMaxDynamicSharedMemorySize, TQ::SMEM_BYTES);
+        return e != cudaSuccess ? e : check_launch_regs(kdq, TQ::LAUNCH_REGS);
     });
     if (err != cudaSuccess) return err;
     const int n_qt = (a.S_q + TQ::BU - 1) / TQ::BU;

@@ -598,6 +598,15 @@ template <int N>
 __device__ __forceinline__ void regs_shrink() {
     asm volatile("setmaxnreg.dec.sync.aligned.u32 %0;" ::"n"(N));
 }
+// Move a warpgroup from the launch's LAUNCH registers a thread to N: grow
+// when N is larger, shrink when smaller, nothing when equal (setmaxnreg.inc
+// must not lower the count, nor .dec raise it).
+template <int N, int LAUNCH>
+__device__ __forceinline__ void regs_set() {
+    static_assert(N % 8 == 0 && N >= 24 && N <= 256, "setmaxnreg takes 24..256 in steps of 8");
+    if constexpr (N > LAUNCH) regs_grow<N>();
+    else if constexpr (N < LAUNCH) regs_shrink<N>();
+}
 
 // ---------------------------------------------------------------- math
 // Three-input maximum (one instruction on sm_100 family).
