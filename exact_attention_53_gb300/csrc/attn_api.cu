@@ -981,6 +981,11 @@ attn_status_t attn_bwd_general(const attn_bwd_params_t* a, struct CUstream_st* s
     if (p.d == 256) {
         if ((s = encode_4d(&g.tm_k_step, a->k, p, p.S_k, p.H_kv, p.lk, 64, "k")) != ATTN_OK) return s;
         if ((s = encode_4d(&g.tm_v_step, a->v, p, p.S_k, p.H_kv, p.lv, 64, "v")) != ATTN_OK) return s;
+    } else {
+        if ((s = encode_4d(&g.tm_dk_out, a->dk, p, p.S_k, p.H_kv, a->dk_layout, 32, "dk")) != ATTN_OK)
+            return s;
+        if ((s = encode_4d(&g.tm_dv_out, a->dv, p, p.S_k, p.H_kv, a->dv_layout, 32, "dv")) != ATTN_OK)
+            return s;
     }
     auto rl = [](const attn_layout_t& l) { return attn::RowLayout{l.batch, l.head, l.row}; };
     const int64_t s_pad = bwd_s_pad(p);

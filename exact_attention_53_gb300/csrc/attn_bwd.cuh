@@ -58,8 +58,13 @@ struct BwdTile {
     static constexpr int SLOT_BYTES = 2 * SMALL_TILE;
     static constexpr int STAT_FLOATS = 2 * BS;        // per slot: LSE·log2e and D of 64 rows
     static constexpr int CLC_SLOTS = 4;               // work-queue answers in flight
-    static constexpr int NUM_BARS = 2 + 2 * NS + 2 + 2 + 1 + 1 + 1 + 2 * CLC_SLOTS;
-    static constexpr int TILE_BYTES = 2 * BIG_TILE + NS * SLOT_BYTES + NS * STAT_FLOATS * 4;
+    static constexpr int NUM_BARS = 2 + 2 * NS + 2 + 2 + 1 + 2 + 1 + 2 * CLC_SLOTS;
+    // Output staging: each epilogue warp stages 64 columns of its 32 key rows
+    // in the 128-byte swizzled layout (4 KB) and stores them with one TMA
+    // tensor store.
+    static constexpr int STG_WARP = 32 * 128;
+    static constexpr int STG_OFF = 2 * BIG_TILE + NS * SLOT_BYTES + NS * STAT_FLOATS * 4;
+    static constexpr int TILE_BYTES = STG_OFF + 4 * STG_WARP;
     static constexpr int SMEM_BYTES = 1024 + TILE_BYTES + CLC_SLOTS * 16 + NUM_BARS * 8 + 16;
     static constexpr int THREADS = 384;     // softmax warps 0-3, epilogue 4-7, producer, MMA, 2 idle
     static constexpr int EPI_WARP = 4;      // first epilogue warp (warp % 4 = its lane quarter)
@@ -71,8 +76,8 @@ struct BwdTile {
     // two idle warps) shrinks to its own.  The sum is 3·LAUNCH_REGS.
     static constexpr int LAUNCH_REGS = 168;
     static constexpr int SOFTMAX_REGS = 200;
-    static constexpr int EPI_REGS = D == 64 ? 144 : 176;
-    static constexpr int AUX_REGS = D == 64 ? 160 : 128;
+    static constexpr int EPI_REGS = 152;
+    static constexpr int AUX_REGS = 152;
     static_assert(SOFTMAX_REGS + EPI_REGS + AUX_REGS <= 3 * LAUNCH_REGS, "register split");
     static constexpr uint32_t TMEM_COLS = 512;
     static constexpr uint32_t S_COL = 0;              // S buffer b at column 64·b (fp32)
@@ -181,20 +186,48 @@ __device__ __forceinline__ void store_row_from_tmem(uint32_t taddr, float mul, v
 }
 
 // One row of an fp32 TMEM accumulator (D columns at `taddr`) times `mul`,
-// packed as 16-bit pairs into out[D/2]: 64-column loads, one wait each.
-template <int D, bool BF16>
+// packed as 16-bit pairs into out[D/2]: CH-column loads (64 or 32; fewer
+// registers in flight), one wait each.
+template <int D, bool BF16, int CH = 64>
 __device__ __forceinline__ void read_acc_packed(uint32_t taddr, float mul, uint32_t (&out)[D / 2]) {
     using namespace sm100;
+    static_assert(CH == 64 || CH == 32, "64- or 32-column loads");
 #pragma unroll
-    for (int c = 0; c < D; c += 64) {
-        uint32_t r[64];
-        tmem_ld64(taddr + c, r);
+    for (int c = 0; c < D; c += CH) {
+        uint32_t r[CH];
+        if constexpr (CH == 64) tmem_ld64(taddr + c, r);
+        else tmem_ld32(taddr + c, r);
 #pragma unroll
-        for (int i = 0; i < 32; ++i) {
+        for (int i = 0; i < CH / 2; ++i) {
             const float a = __uint_as_float(r[2 * i]) * mul;
             const float b = __uint_as_float(r[2 * i + 1]) * mul;
             out[c / 2 + i] = BF16 ? pack_bf16(a, b) : pack_f16(a, b);
         }
+    }
+}
+
+// One warp stores 64 columns of its 32 rows: each lane's 32 packed words
+// (w[0..31], its row) go to the warp's 4 KB staging tile in the 128-byte
+// swizzled layout (1024-byte aligned), then lane 0 stores the tile with one
+// TMA tensor store at (col, row0, head, batch); rows past the tensor's extent
+// are not written.  Lane 0 first waits until its previous store has finished
+// reading the tile.
+__device__ __forceinline__ void store_tile_64(const uint32_t* w, uint8_t* tile, int lane,
+                                              const CUtensorMap* map, int col, int row0,
+                                              int head, int batch) {
+    using namespace sm100;
+    if (lane == 0) bulk_wait_read_all();
+    __syncwarp();
+    uint8_t* row = tile + lane * 128;
+#pragma unroll
+    for (int c = 0; c < 8; ++c)
+        *reinterpret_cast<uint4*>(row + ((c ^ (lane & 7)) << 4)) =
+            make_uint4(w[4 * c], w[4 * c + 1], w[4 * c + 2], w[4 * c + 3]);
+    fence_proxy_async_smem();
+    __syncwarp();
+    if (lane == 0) {
+        tma_store_4d(map, tile, col, row0, head, batch);
+        bulk_commit_group();
     }
 }
 
@@ -305,9 +338,10 @@ __global__ void __launch_bounds__(BwdTile<D>::THREADS, 1)
                          const __grid_constant__ CUtensorMap tm_v,    // box 64 × 128
                          const __grid_constant__ CUtensorMap tm_q,    // box 64 × 64
                          const __grid_constant__ CUtensorMap tm_do,   // box 64 × 64
+                         const __grid_constant__ CUtensorMap tm_dv,   // box 64 × 32, stores
+                         const __grid_constant__ CUtensorMap tm_dk,   // box 64 × 32, stores
                          const float* __restrict__ lse2, const float* __restrict__ delta,
-                         uint16_t* __restrict__ dk, uint16_t* __restrict__ dv, RowLayout dk_lay,
-                         RowLayout dv_lay, int S_q, int S_k, int BHkv, int H, int kv_group,
+                         int S_q, int S_k, int BHkv, int H, int kv_group,
                          int S_pad, int head_group, int causal_off, float scale,
                          float scale_log2, DeviceWords* __restrict__ words,
                          unsigned long long launch, unsigned long long budget_ns) {
@@ -330,8 +364,8 @@ __global__ void __launch_bounds__(BwdTile<D>::THREADS, 1)
     uint64_t* s_full = slot_empty + T::NS;    // [2] Sᵀ and dPᵀ of buffer b computed
     uint64_t* p_full = s_full + 2;            // [2] Pᵀ and dSᵀ of buffer b written (per warp)
     uint64_t* acc_done = p_full + 2;          // dV and dK of the unit complete
-    uint64_t* acc_free = acc_done + 1;        // dV and dK read out (per epilogue warp)
-    uint64_t* drain = acc_free + 1;
+    uint64_t* acc_free = acc_done + 1;        // [2] dV, dK read out (per epilogue warp)
+    uint64_t* drain = acc_free + 2;
     uint64_t* clc_full = drain + 1;           // [CLC_SLOTS] work-queue answer landed
     uint64_t* clc_empty = clc_full + T::CLC_SLOTS;
     uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(clc_empty + T::CLC_SLOTS);
@@ -393,7 +427,8 @@ __global__ void __launch_bounds__(BwdTile<D>::THREADS, 1)
             mbar_init(&p_full[b], 4);
         }
         mbar_init(acc_done, 1);
-        mbar_init(acc_free, 4);
+        mbar_init(&acc_free[0], 4);
+        mbar_init(&acc_free[1], 4);
         mbar_init(drain, 1);
         for (int s = 0; s < T::CLC_SLOTS; ++s) {
             mbar_init(&clc_full[s], 1);
@@ -566,17 +601,22 @@ __global__ void __launch_bounds__(BwdTile<D>::THREADS, 1)
                             id_s, kk > 0 ? 1u : 0u);
             }
         };
-        // dV += Pᵀ_b·dO_slot, dK += dSᵀ_b·Q_slot: M = 128 keys, N = D, K = 64 queries
-        auto mma_acc = [&](int slot, int b, bool acc) {
+        // dV += Pᵀ_b·dO_slot (g = 0) and dK += dSᵀ_b·Q_slot (g = 1): M = 128
+        // keys, N = D, K = 64 queries.  mask bit g selects the products; with
+        // both, the two accumulators' MMAs alternate.
+        auto mma_acc = [&](int slot, int b, bool acc, int mask) {
             const uint32_t qoff = (slot * T::SLOT_BYTES) >> 4;
             const uint32_t dooff = (slot * T::SLOT_BYTES + T::SMALL_TILE) >> 4;
 #pragma unroll
             for (int kk = 0; kk < T::BS / 16; ++kk) {
                 const uint32_t bo = (kk * 16 * 128) >> 4;
-                mma_ts_warp(tmem + T::ACC_COL, tmem + T::S_COL + b * 64 + T::PK_OFF + kk * 8,
-                            rm_lo + dooff + bo, rm_hi, id_acc, (acc || kk > 0) ? 1u : 0u);
-                mma_ts_warp(tmem + T::ACC_COL + D, tmem + T::DP_COL + b * 64 + T::PK_OFF + kk * 8,
-                            rm_lo + qoff + bo, rm_hi, id_acc, (acc || kk > 0) ? 1u : 0u);
+                if (mask & 1)
+                    mma_ts_warp(tmem + T::ACC_COL, tmem + T::S_COL + b * 64 + T::PK_OFF + kk * 8,
+                                rm_lo + dooff + bo, rm_hi, id_acc, (acc || kk > 0) ? 1u : 0u);
+                if (mask & 2)
+                    mma_ts_warp(tmem + T::ACC_COL + D,
+                                tmem + T::DP_COL + b * 64 + T::PK_OFF + kk * 8, rm_lo + qoff + bo,
+                                rm_hi, id_acc, (acc || kk > 0) ? 1u : 0u);
             }
         };
         uint32_t pc0 = 0, pc1 = 0;
@@ -611,15 +651,24 @@ __global__ void __launch_bounds__(BwdTile<D>::THREADS, 1)
             for (int t = 0; t < n && ok; ++t) {
                 const int b = static_cast<int>((gs + t) & 1);
                 ok = mbar_wait(&p_full[b], (b ? pc1 : pc0) & 1, abort_flag, status, kStatusBwdMma);
-                // the unit's first dV/dK MMA overwrites the accumulators: the
-                // epilogue warps must have read out the previous unit's
-                if (ok && t == 0 && uk > 1)
-                    ok = mbar_wait(acc_free, (uk - 2) & 1, abort_flag, status, kStatusBwdMma);
                 ok = __all_sync(0xffffffffu, ok);
                 if (b) ++pc1; else ++pc0;
                 tc_fence_after();
                 if (!ok) break;
-                mma_acc(cur, b, t > 0);
+                if (t == 0 && uk > 1) {
+                    // A unit's first dV (dK) MMA overwrites that accumulator:
+                    // the epilogue warps must have read out the previous unit's.
+                    for (int g = 0; g < 2 && ok; ++g) {
+                        ok = mbar_wait(&acc_free[g], (uk - 2) & 1, abort_flag, status,
+                                       kStatusBwdMma);
+                        ok = __all_sync(0xffffffffu, ok);
+                        tc_fence_after();
+                        if (ok) mma_acc(cur, b, false, 1 << g);
+                    }
+                    if (!ok) break;
+                } else {
+                    mma_acc(cur, b, t > 0, 3);
+                }
                 tc_commit_warp(&slot_empty[cur]);
                 int nn = 0;
                 if (t + 2 < n) {
@@ -654,11 +703,13 @@ __global__ void __launch_bounds__(BwdTile<D>::THREADS, 1)
     } else if (warp >= T::EPI_WARP) {
         regs_set<T::EPI_REGS, T::LAUNCH_REGS>();
         // ------------------------------------------------------------ epilogue warps
-        // Read dV and dK out of tensor memory as packed 16-bit rows, release
-        // the accumulators to the next unit, then store (one key row per thread).
+        // Read dV out of tensor memory as packed 16-bit rows (one key row per
+        // thread), release it to the next unit and store it, then the same
+        // for dK: 64 columns of the warp's 32 rows at a time, through its
+        // staging tile.
         const int quarter = warp & 3;
-        const int row = quarter * 32 + lane;
         const uint32_t lane_base = tmem + (static_cast<uint32_t>(quarter * 32) << 16);
+        uint8_t* tile = smem + T::STG_OFF + quarter * T::STG_WARP;
         bool ok = true;
         int ue = 0;
         for (int r = 0; ok; ++r) {
@@ -669,33 +720,40 @@ __global__ void __launch_bounds__(BwdTile<D>::THREADS, 1)
             if (got == 2) continue;
             int b, hk, kt, q_begin, n;
             unit_info(L, b, hk, kt, q_begin, n);
-            const int key = kt * T::BU + row;
-            uint16_t* dk_row = dk + static_cast<size_t>(b * dk_lay.batch + hk * dk_lay.head +
-                                                        static_cast<long long>(key) * dk_lay.row);
-            uint16_t* dv_row = dv + static_cast<size_t>(b * dv_lay.batch + hk * dv_lay.head +
-                                                        static_cast<long long>(key) * dv_lay.row);
-            uint32_t pv[D / 2], pk[D / 2];
-            if (n == 0) {
-                // No query sees these keys: their gradients are zero.
-#pragma unroll
-                for (int i = 0; i < D / 2; ++i) pv[i] = pk[i] = 0u;
-            } else {
-                ok = mbar_wait(acc_done, ue & 1, abort_flag, status, kStatusBwdEpilogue);
+            const int row0 = kt * T::BU + quarter * 32;
+            // Keys no query sees (n = 0) get zero gradients.
+            uint32_t wv[D / 2], wk[D / 2];
+            if (n > 0) {
+                ok = mbar_wait_idle(acc_done, ue & 1, abort_flag, status, kStatusBwdEpilogue);
                 ok = __all_sync(0xffffffffu, ok);
                 ++ue;
                 if (!ok) break;
                 tc_fence_after();
-                read_acc_packed<D, BF16>(lane_base + T::ACC_COL, 1.f, pv);
-                read_acc_packed<D, BF16>(lane_base + T::ACC_COL + D, scale, pk);
+                read_acc_packed<D, BF16>(lane_base + T::ACC_COL, 1.f, wv);
                 tc_fence_before();
                 __syncwarp();
-                if (lane == 0) mbar_arrive(acc_free);
+                if (lane == 0) mbar_arrive(&acc_free[0]);
+            } else {
+#pragma unroll
+                for (int i = 0; i < D / 2; ++i) wv[i] = 0u;
             }
-            if (key < S_k) {
-                store_packed_row<D>(pv, dv_row);
-                store_packed_row<D>(pk, dk_row);
+#pragma unroll
+            for (int c = 0; c < D; c += 64)
+                store_tile_64(wv + c / 2, tile, lane, &tm_dv, c, row0, hk, b);
+            if (n > 0) {
+                read_acc_packed<D, BF16>(lane_base + T::ACC_COL + D, scale, wk);
+                tc_fence_before();
+                __syncwarp();
+                if (lane == 0) mbar_arrive(&acc_free[1]);
+            } else {
+#pragma unroll
+                for (int i = 0; i < D / 2; ++i) wk[i] = 0u;
             }
+#pragma unroll
+            for (int c = 0; c < D; c += 64)
+                store_tile_64(wk + c / 2, tile, lane, &tm_dk, c, row0, hk, b);
         }
+        bulk_wait_all();       // every tile store has landed before the CTA exits
         teardown();
     } else {
         // ------------------------------------------------------------ softmax warps
@@ -1189,7 +1247,7 @@ __global__ void __launch_bounds__(DqTile<D>::THREADS, 1)
             int bh, qt, n;
             unit_info(L, bh, qt, n);
             const int q_idx = qt * T::BU + row;
-            ok = mbar_wait(acc_done, ue & 1, abort_flag, status, kStatusBwdEpilogue);
+            ok = mbar_wait_idle(acc_done, ue & 1, abort_flag, status, kStatusBwdEpilogue);
             ok = __all_sync(0xffffffffu, ok);
             ++ue;
             if (!ok) break;
@@ -1309,9 +1367,9 @@ cudaError_t launch_key_side(const BwdArgs& a, cudaStream_t stream, long long op_
         // causal: one persistent CTA per SM.
         kdkdv<<<static_cast<int>(CAUSAL ? std::min<long long>(units_kv, a.num_sms) : units_kv),
                 T::THREADS, T::SMEM_BYTES,
-                stream>>>(a.tm_k_fixed, a.tm_v_fixed, a.tm_q_step, a.tm_do_step, a.lse2, a.delta,
-                          static_cast<uint16_t*>(a.dk), static_cast<uint16_t*>(a.dv), a.dk_lay,
-                          a.dv_lay, a.S_q, a.S_k, bh_kv, a.H, a.kv_group, a.S_pad, hg_kv,
+                stream>>>(a.tm_k_fixed, a.tm_v_fixed, a.tm_q_step, a.tm_do_step, a.tm_dv_out,
+                          a.tm_dk_out, a.lse2, a.delta, a.S_q, a.S_k, bh_kv, a.H, a.kv_group,
+                          a.S_pad, hg_kv,
                           a.causal_off, a.scale, a.scale_log2, a.words, a.launch_dkdv,
                           a.budget_ns);
         return cudaGetLastError();

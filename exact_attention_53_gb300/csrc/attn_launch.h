@@ -148,6 +148,7 @@ struct BwdArgs {
     CUtensorMap tm_q_step, tm_do_step;    // Q, dO: (d, S_q, H, B), box 64 × 64
     CUtensorMap tm_q_fixed, tm_do_fixed;  // Q, dO: (d, S_q, H, B), box 64 × 128
     CUtensorMap tm_k_step, tm_v_step;     // K, V: box 64 × 64 (d = 256 only: the dQ kernel's steps)
+    CUtensorMap tm_dk_out, tm_dv_out;     // dK, dV: (d, S_k, H_kv, B), box 64 × 32, stores (d <= 128)
     const void* o;                        // forward output [B, H, S_q, d]
     const void* dout;                     // dO [B, H, S_q, d]
     const float* lse;                     // forward LSE [B, H, S_q], natural log

@@ -103,6 +103,23 @@ __device__ __forceinline__ bool mbar_wait(uint64_t* bar, uint32_t parity,
     }
 }
 
+// mbar_wait for a role that idles for a long time (a whole work unit) and is
+// not on the critical path: it first polls with a kIdleSleepNs sleep between
+// tries (at most kIdleTries of them, about a millisecond), leaving its issue
+// slots to the warps of the same SM sub-partition that do the unit's work
+// (polling without the sleep slowed those warps measurably), then waits as
+// mbar_wait does, with the same limit and abort behaviour.
+constexpr unsigned int kIdleSleepNs = 128;
+constexpr int kIdleTries = 4096;
+
+__device__ __forceinline__ bool mbar_wait_idle(uint64_t* bar, uint32_t parity,
+                                               volatile int* abort_flag, unsigned int* status,
+                                               unsigned int code) {
+    const uint32_t a = smem_u32(bar);
+    for (int i = 0; i < kIdleTries && !mbar_try_wait(a, parity); ++i) __nanosleep(kIdleSleepNs);
+    return mbar_wait(bar, parity, abort_flag, status, code);
+}
+
 // Launch-wide bounds, kept in registers by each CTA's TMA producer warp (the
 // one role that runs ahead of the others and is never on the critical path).
 // Together with the bounded waits they make every launch end in bounded time:
@@ -226,6 +243,15 @@ __device__ __forceinline__ void bulk_load(void* dst, const void* src, uint32_t b
             smem_u32(dst)),
         "l"(reinterpret_cast<uint64_t>(src)), "r"(bytes), "r"(smem_u32(bar))
         : "memory");
+}
+
+// 1-D bulk copy shared -> global of `bytes` (a multiple of 16; both addresses
+// 16-byte aligned), tracked by the issuing thread's bulk groups.
+__device__ __forceinline__ void bulk_store(void* dst, const void* src, uint32_t bytes) {
+    asm volatile("cp.async.bulk.global.shared::cta.bulk_group [%0], [%1], %2;" ::"l"(
+                     reinterpret_cast<uint64_t>(dst)),
+                 "r"(smem_u32(src)), "r"(bytes)
+                 : "memory");
 }
 
 __device__ __forceinline__ void bulk_commit_group() {
