@@ -19,10 +19,16 @@
 //                          steps, S = Q·Kᵀ and dP = dO·Vᵀ, dS by the softmax
 //                          warps (one query row per thread), dQ += dS·K.
 //
+// In both main kernels four epilogue warps read the finished accumulators of
+// a unit out of TMEM, release them (the next unit's first accumulating MMA
+// waits for that) and store them while the next unit's steps run; the dK/dV
+// kernel stages them in shared memory for TMA tensor stores.
+//
 // dQ gets its own pass (it recomputes S and dP) instead of the page's f32
 // atomics, so every result is deterministic: no two CTAs ever add into the
 // same output.  Tensor memory holds two S buffers, two dP buffers and the
-// accumulators (dV and dK: 2·d columns; dQ: d), so head_dim is 64 or 128.
+// accumulators (dV and dK: 2·d columns; dQ: d), so this file's dK/dV kernel
+// takes head_dim 64 or 128 (256: attn_bwd_wide.cuh).
 #pragma once
 
 #include <cuda.h>

@@ -1,9 +1,9 @@
 """Build-time resource checks (CPU only; needs nvcc).
 
 Every kernel instantiation is compiled with ``-Xptxas -v`` (the build's own flags) and must not
-spill, and the two-tile forward kernels must launch with exactly the 168 registers per thread
-that their warpgroup register split assumes (the host refuses to launch them otherwise, so a
-drift here would only show up on a GPU).
+spill, and the two-tile forward kernels and the dK/dV and dQ backward kernels must launch with
+exactly the 168 registers per thread that their warpgroup register splits assume (the host
+refuses to launch them otherwise, so a drift here would only show up on a GPU).
 """
 
 import re
@@ -48,3 +48,13 @@ def test_two_tile_forward_launch_registers(table):
         m = re.match(r"attn::attn_fwd_kernel<\(int\)(\d+), \(bool\)\d, \(bool\)\d, \(bool\)(\d)>", name)
         if m and int(m.group(1)) in (64, 128) and m.group(2) == "0":
             assert regs == 168, f"{name}: {regs} registers at launch, the split expects 168"
+
+
+def test_backward_launch_registers(table):
+    # the dK/dV and dQ kernels (d = 64, 128 and the d = 256 dQ) run 384 threads re-split from 168
+    found = 0
+    for name, (regs, *_rest) in table.items():
+        if re.match(r"attn::attn_bwd_(dkdv|dq)_kernel<", name):
+            found += 1
+            assert regs == 168, f"{name}: {regs} registers at launch, the split expects 168"
+    assert found > 0
