@@ -558,6 +558,13 @@ attn_status_t validate_bwd_head_dim(const Problem& p) {
 // device's first attn_fwd_host call and kept for the life of the process.
 struct HostPipe {
     static constexpr int kChunks = 8;
+    // Chunk sizes in proportion to these weights (when there are at least
+    // kWeightSum heads): the first and last chunks are a third of the others,
+    // so the pipeline fills (first upload, nothing to overlap it) and drains
+    // (last forward and download) sooner.  Measured on c3: 1.186 ms per call
+    // against 1.227 ms with equal chunks; 10 or 12 chunks were slower.
+    static constexpr int kWeight[kChunks] = {1, 3, 3, 3, 3, 3, 3, 1};
+    static constexpr int kWeightSum = 20;
     std::mutex mu;
     bool ready = false;
     cudaStream_t in = nullptr, out = nullptr;
@@ -664,6 +671,13 @@ attn_status_t attn_fwd_host(const void* q_host, const void* k_host, const void* 
     const int64_t BH = B * H;
     const size_t total = p.q_bytes + 2 * p.kv_bytes + p.o_bytes;
     const int64_t chunks = total < (size_t(32) << 20) ? 1 : std::min<int64_t>(HostPipe::kChunks, BH);
+    const bool weighted = chunks == HostPipe::kChunks && BH >= HostPipe::kWeightSum;
+    auto bound = [&](int64_t c) -> int64_t {      // first (b, h) of chunk c
+        if (!weighted) return BH * c / chunks;
+        int64_t w = 0;
+        for (int64_t i = 0; i < c; ++i) w += HostPipe::kWeight[i];
+        return BH * w / HostPipe::kWeightSum;
+    };
     const size_t q_head = static_cast<size_t>(S_q * d * 2), kv_head = static_cast<size_t>(S_k * d * 2);
     const size_t l_head = static_cast<size_t>(S_q * 4);
     cudaError_t e;
@@ -676,7 +690,7 @@ attn_status_t attn_fwd_host(const void* q_host, const void* k_host, const void* 
         (e = cudaStreamWaitEvent(pipe->out, pipe->start, 0)) != cudaSuccess)
         return cuda_fail("ordering the copy streams");
     for (int64_t c = 0; c < chunks; ++c) {
-        const int64_t h0 = BH * c / chunks, h1 = BH * (c + 1) / chunks;
+        const int64_t h0 = bound(c), h1 = bound(c + 1);
         const size_t n = static_cast<size_t>(h1 - h0);
         auto at = [&](const void* base, size_t per_head) {
             return static_cast<const char*>(base) + static_cast<size_t>(h0) * per_head;
@@ -691,7 +705,7 @@ attn_status_t attn_fwd_host(const void* q_host, const void* k_host, const void* 
             return cuda_fail("host-to-device copy");
     }
     for (int64_t c = 0; c < chunks; ++c) {
-        const int64_t h0 = BH * c / chunks, h1 = BH * (c + 1) / chunks;
+        const int64_t h0 = bound(c), h1 = bound(c + 1);
         const size_t n = static_cast<size_t>(h1 - h0);
         auto at = [&](const void* base, size_t per_head) {
             return const_cast<char*>(static_cast<const char*>(base) + static_cast<size_t>(h0) * per_head);

@@ -212,10 +212,14 @@ def test_host_buffers_entry_point():
     assert torch.equal(o2.cpu(), oh) and torch.equal(l2.cpu(), lh)
 
 
+@pytest.mark.parametrize("B,H,S", [(2, 16, 2048), (1, 12, 4096), (1, 5, 8192)],
+                         ids=["32-heads-weighted", "12-heads-equal", "5-heads-one-each"])
 @pytest.mark.parametrize("causal", [False, True], ids=["full", "causal"])
-def test_host_entry_point_pipelined_chunks(causal):
-    """Above 32 MB the host entry point overlaps chunks of heads; results match the device path."""
-    B, H, S, d = 2, 16, 2048, 128
+def test_host_entry_point_pipelined_chunks(causal, B, H, S):
+    """Above 32 MB the host entry point overlaps chunks of heads (8 chunks weighted
+    1:3:...:3:1 from 20 heads on, 8 equal ones below that, one per head below 8);
+    results match the device path."""
+    d = 128
     q, k, v = make_qkv(B, H, S, S, d, "bf16", seed=18)
     qh, kh, vh = q.pin_memory(), k.pin_memory(), v.pin_memory()
     oh = torch.full_like(qh, 3.0).pin_memory()
