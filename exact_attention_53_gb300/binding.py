@@ -148,7 +148,7 @@ def load_library() -> ctypes.CDLL:
         return lib
 
 
-DEBUG_EXPORTS = ("attn_debug_fwd", "attn_debug_status")   # declared in include/attn_debug.h
+DEBUG_EXPORTS = ("attn_debug_fwd", "attn_debug_bwd", "attn_debug_status")   # include/attn_debug.h
 _debug_lib = None
 
 
@@ -168,6 +168,9 @@ def load_debug_library() -> ctypes.CDLL:
         lib.attn_debug_fwd.argtypes = [vp, vp, vp, vp, vp, i64, i64, i64, ctypes.c_float,
                                        ctypes.c_int, ctypes.c_uint64, vp]
         lib.attn_debug_fwd.restype = ctypes.c_int
+        lib.attn_debug_bwd.argtypes = [vp] * 10 + [i64, i64, i64, ctypes.c_float, ctypes.c_int,
+                                                   ctypes.c_uint64, vp]
+        lib.attn_debug_bwd.restype = ctypes.c_int
         lib.attn_debug_status.argtypes = [ctypes.POINTER(ctypes.c_uint), vp]
         lib.attn_debug_status.restype = ctypes.c_int
         _debug_lib = lib

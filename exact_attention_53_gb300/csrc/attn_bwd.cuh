@@ -494,6 +494,11 @@ __global__ void __launch_bounds__(BwdTile<D>::THREADS, 1)
             if (got == 2) continue;
             int b, hk, kt, q_begin, n;
             unit_info(L, b, hk, kt, q_begin, n);
+#ifdef ATTN_DEBUG_FAULTS
+            // Debug builds only: load nothing for the chosen unit and stop, so
+            // its consumers' waits run out.
+            if (L == g_attn_debug_skip_unit) break;
+#endif
             if (n == 0) {
                 claim_next();
                 continue;

@@ -62,12 +62,6 @@ __host__ __device__ constexpr float rescale_sum() {
 }
 constexpr float kLn2 = 0.693147180559945309f;
 
-#ifdef ATTN_DEBUG_FAULTS
-// Debug builds only (never the release library): the producer loads nothing
-// for this work unit and stops, so the unit's consumers wait until their limit
-// runs out.  -1: no unit is skipped.
-__device__ int g_attn_debug_skip_unit = -1;
-#endif
 
 
 // Number of key tiles query tile t of a block starting at row q0 visits.

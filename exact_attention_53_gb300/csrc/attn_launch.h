@@ -181,6 +181,13 @@ struct BwdArgs {
 template <int D, bool BF16, bool CAUSAL>
 cudaError_t launch_attn_bwd(const BwdArgs& args, cudaStream_t stream);
 
+#ifdef ATTN_DEBUG_FAULTS
+// Debug builds only (never the release library): the forward's producer, and
+// the backward's dK/dV producer, load nothing for this work unit and stop, so
+// the unit's consumers wait until their limit runs out.  -1: no unit skipped.
+__device__ int g_attn_debug_skip_unit = -1;
+#endif
+
 // Device address of the built-in split-KV scratch (ATTN_NOALLOC_SCRATCH_BYTES
 // bytes, 256-byte aligned) on the current device.
 cudaError_t noalloc_scratch_address(void** ptr);

@@ -92,6 +92,9 @@ def test_debug_entry_rejects_bad_arguments_before_device_work():
     dbg = binding.load_debug_library()
     assert dbg.attn_debug_fwd(None, A, A, A, A, 1, 1, 128, 0.125, -1, 0, None) == 1
     assert dbg.attn_debug_fwd(A, A, A, A, A, 1, 1, 0, 0.125, -1, 0, None) == 1
+    assert dbg.attn_debug_bwd(None, *[A] * 9, 1, 1, 128, 0.125, -1, 0, None) == 1
+    assert dbg.attn_debug_bwd(*[A] * 9, None, 1, 1, 128, 0.125, -1, 0, None) == 1
+    assert dbg.attn_debug_bwd(*[A] * 10, 1, 1, 0, 0.125, -1, 0, None) == 1
     assert dbg.attn_debug_status(None, None) == 1
 
 
