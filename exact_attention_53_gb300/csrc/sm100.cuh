@@ -245,15 +245,6 @@ __device__ __forceinline__ void bulk_load(void* dst, const void* src, uint32_t b
         : "memory");
 }
 
-// 1-D bulk copy shared -> global of `bytes` (a multiple of 16; both addresses
-// 16-byte aligned), tracked by the issuing thread's bulk groups.
-__device__ __forceinline__ void bulk_store(void* dst, const void* src, uint32_t bytes) {
-    asm volatile("cp.async.bulk.global.shared::cta.bulk_group [%0], [%1], %2;" ::"l"(
-                     reinterpret_cast<uint64_t>(dst)),
-                 "r"(smem_u32(src)), "r"(bytes)
-                 : "memory");
-}
-
 __device__ __forceinline__ void bulk_commit_group() {
     asm volatile("cp.async.bulk.commit_group;" ::: "memory");
 }
