@@ -131,3 +131,28 @@ def test_bwd_general_matches_dense_bitwise():
         torch.cuda.synchronize()
         for x, y in zip(a, b):
             assert torch.equal(x, y.contiguous())
+
+
+@pytest.mark.parametrize("d", [64, 128, 256])
+@pytest.mark.parametrize("causal", [False, True], ids=["full", "causal"])
+def test_bwd_writes_only_inside_the_gradient_views(d, causal):
+    """dQ, dK, dV as slices of larger buffers (64 more columns per row, 7 more rows per head):
+    the padding keeps its sentinel, so the tile stores never write past a view's columns or
+    its S rows, and the gradients equal the dense entry point's bit for bit."""
+    B, H, S = 1, 3, 333
+    q, k, v = make_qkv(B, H, S, S, d, "bf16", seed=60 + d)
+    do = make_qkv(B, H, S, 1, d, "bf16", seed=61 + d)[0]
+    qd, kd, vd, dod = q.to(DEV), k.to(DEV), v.to(DEV), do.to(DEV)
+    o, lse = fwd(qd, kd, vd, causal=causal)
+    ref = bwd(qd, kd, vd, o, lse, dod, causal=causal)
+    sentinel = -123.0
+    bufs = [torch.full((B, H, S + 7, d + 64), sentinel, dtype=torch.bfloat16, device=DEV)
+            for _ in range(3)]
+    views = [bb[:, :, :S, :d] for bb in bufs]
+    bwd_general(qd, kd, vd, o, lse, dod, mask=ATTN_MASK_CAUSAL if causal else ATTN_MASK_NONE,
+                dq=views[0], dk=views[1], dv=views[2])
+    torch.cuda.synchronize()
+    for name, bb, view, want in zip(("dq", "dk", "dv"), bufs, views, ref):
+        assert torch.equal(view, want), f"{name}: differs from the dense call"
+        assert (bb[:, :, :, d:] == sentinel).all(), f"{name}: written past its columns"
+        assert (bb[:, :, S:, :] == sentinel).all(), f"{name}: written past its rows"
