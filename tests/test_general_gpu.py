@@ -115,3 +115,30 @@ def test_bottom_right_rejects_longer_queries_on_gpu():
     q, k, v = make_qkv(1, 1, 300, 200, 64, "bf16", seed=44)
     with pytest.raises(AttnError, match="S_q <= S_k"):
         fwd_general(q.to(DEV), k.to(DEV), v.to(DEV), mask=ATTN_MASK_CAUSAL_BOTTOM_RIGHT)
+
+
+@pytest.mark.parametrize("d", [64, 128, 256])
+@pytest.mark.parametrize("mode", ["full", "causal", "split"])
+def test_forward_writes_only_inside_the_output_view(d, mode):
+    """O as a slice of a larger buffer (64 more columns per row, 7 more rows per head): the
+    padding keeps its sentinel, and O and LSE equal the dense entry point's bit for bit."""
+    from exact_attention_53_gb300 import fwd_splitkv, fwd_splitkv_general
+    B, H = 1, 3
+    S_q, S_k = (5, 3000) if mode == "split" else (333, 333)
+    q, k, v = make_qkv(B, H, S_q, S_k, d, "bf16", seed=80 + d)
+    qd, kd, vd = q.to(DEV), k.to(DEV), v.to(DEV)
+    sentinel = -123.0
+    buf = torch.full((B, H, S_q + 7, d + 64), sentinel, dtype=torch.bfloat16, device=DEV)
+    view = buf[:, :, :S_q, :d]
+    if mode == "split":
+        ro, rl = fwd_splitkv(qd, kd, vd, n_split=3)
+        o, lse = fwd_splitkv_general(qd, kd, vd, n_split=3, out=view)
+    else:
+        causal = mode == "causal"
+        ro, rl = fwd(qd, kd, vd, causal=causal)
+        o, lse = fwd_general(qd, kd, vd, mask=ATTN_MASK_CAUSAL if causal else ATTN_MASK_NONE,
+                             out=view)
+    torch.cuda.synchronize()
+    assert torch.equal(view, ro) and torch.equal(lse, rl)
+    assert (buf[:, :, :, d:] == sentinel).all(), "written past the view's columns"
+    assert (buf[:, :, S_q:, :] == sentinel).all(), "written past the view's rows"
