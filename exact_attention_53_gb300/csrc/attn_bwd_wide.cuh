@@ -39,7 +39,8 @@ struct BwdWideTile {
     // Q ring slots: a Q slot is held from its step's Sᵀ (issued two steps
     // ahead) until the softmax warps have read its statistics, so with two
     // slots every Sᵀ waited for its Q to arrive; the dV pass has room for a
-    // third (dV pass on c5: 1.40 → 0.84 ms), the dK pass (K and V fixed) not.
+    // third (dV pass at B=2, H=8, S=8192: 1.40 → 0.84 ms), the dK pass (K and
+    // V fixed) not.
     static constexpr int NQ = PASS == kPassDK ? 2 : 3;
     static constexpr int NO = PASS == kPassDK ? 1 : 2;           // dO ring slots
     static constexpr int STAT_FLOATS = 2 * BS;        // per Q slot: LSE·log2e and D of 64 rows
